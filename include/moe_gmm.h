@@ -1,0 +1,233 @@
+/*
+ * moe_gmm.h -- C ABI of the routed-expert MoE hot path on GB300 (sm_103a).
+ *
+ * The library computes the routed-expert part of a Mixture-of-Experts layer:
+ *
+ *   topk ids --permute--> expert-contiguous rows --GMM(gate_up)--> SwiGLU
+ *            --GMM(down)--> weighted top-k combine --> y
+ *
+ * plus every gradient of it.  Sources, cited by page title and section:
+ *
+ *  [GMM]         "NPU Training Operators - GMM", section "算子语义" (operator
+ *                semantics: x[sum(group_list), K], weight[E, K, N],
+ *                group_list, the eager per-group loop, the worked example,
+ *                grad_input_e = dY_e W_e^T, grad_weight_e = X_e^T dY_e) and
+ *                section "Qwen3.5 MoE 路径" (permute -> histc -> GMM gate_up ->
+ *                swiglu -> GMM down -> unpermute with probs).
+ *  [MegaMoE]     "MegaMoE" operator doc, "计算公式" (topkIds INT32 [T, topK],
+ *                topkWeights [T, topK], SiLU, the clip value c, swiglu) and
+ *                "A16W16 非量化场景" (dispatch row(i,k), Linear1, activation,
+ *                Linear2, Token Combine).
+ *  [PermuteGrad] "CANN ops-transformer 算子详解 MoeTokenPermuteWithRoutingMapGrad",
+ *                sections 2.2-2.3 (probs and token gradients), 3 (two-phase
+ *                workspace-size + execute API), 4.2-4.3 (null / invalid
+ *                argument errors), 5 (empty tensors need no workspace),
+ *                6.2 (per token: walk topK slots, skip -1, fp32 accumulate).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, and
+ *    must be 16-byte aligned.  The caller allocates and owns every buffer,
+ *    including the workspace; the library allocates nothing.
+ *  - bf16 tensors are raw bfloat16 bits (moe_bf16).  Matmuls accumulate in
+ *    fp32 and round to bf16 (nearest even) once.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and never synchronises the host, except moe_read_status.
+ *  - Host-side argument checks return an error before anything is launched.
+ *    Errors the device finds (an expert id outside [-1, E), a negative
+ *    group count, sum(group_list) larger than the rows given, a row id out of
+ *    range, a pipeline wait that timed out) are written to the status word
+ *    at the start of the workspace; the first error sticks until
+ *    moe_workspace_init clears it.  Read it with moe_read_status.
+ *  - Every workspace must be zero-initialised once (moe_workspace_init)
+ *    before its first use.  Calls that share a workspace must be ordered on
+ *    one stream.
+ *  - Empty problems (T == 0 or M == 0) are a successful no-op.
+ *  - Sizes: E <= 1024; K, N, H and I multiples of 64 for the matmuls; k <= 64.
+ */
+#ifndef MOE_GMM_H
+#define MOE_GMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;                 /* raw bfloat16 bits */
+typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULLPTR = 1,      /* a required pointer is NULL */
+  MOE_ERR_INVALID = 2,      /* bad size, k > E, misaligned pointer, workspace too small */
+  MOE_ERR_UNSUPPORTED = 3,  /* sizes outside what the kernels handle (see above) */
+  MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+  MOE_ERR_DEVICE = 5,       /* the device found bad data (ids, counts, row ids) */
+  MOE_ERR_TIMEOUT = 6       /* a bounded pipeline wait expired inside a kernel */
+} moe_status_t;
+
+enum { MOE_EPILOGUE_NONE = 0, MOE_EPILOGUE_SWIGLU = 1 };
+
+/* Bytes at the start of every workspace that hold the device status word. */
+#define MOE_STATUS_BYTES 256
+
+/* ---------------------------------------------------------------- status */
+
+/* Zero the status block of a workspace (asynchronous on stream). */
+MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream` and return the sticky device status of `ws`
+ * (MOE_OK, MOE_ERR_DEVICE or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the stream
+ * itself reports an error. */
+MOE_API moe_status_t moe_read_status(const void* ws, moe_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+/* ---------------------------------------------------------------- dispatch */
+
+/* Workspace bytes for moe_permute. */
+MOE_API size_t moe_permute_workspace_size(int64_t T, int64_t k, int64_t E);
+
+/* Token permute (dispatch): [GMM] "Qwen3.5 MoE 路径" (permute + histc) and the
+ * worked example of "算子语义"; [MegaMoE] EP Dispatch (row(i,k)).
+ *
+ *   x          [T, H] bf16 tokens (may be NULL together with x_perm: index-only)
+ *   topk_ids   [T, k] int32 expert ids in [-1, E); -1 marks an unused slot
+ *   x_perm     [T*k, H] bf16 out: rows grouped by expert; within an expert,
+ *              rows follow ascending flat slot index f = t*k + j (a stable
+ *              counting sort).  Only the first R = sum(group_list) rows are
+ *              written.
+ *   group_list [E] int64 out: rows per expert (a histogram of topk_ids)
+ *   row_id_map [T*k] int32 out: flat slot -> row, -1 for unused slots
+ *   sorted_flat[T*k] int32 out: row -> flat slot for rows < R, -1 after R
+ */
+MOE_API moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids,
+                         int64_t T, int64_t H, int64_t k, int64_t E,
+                         moe_bf16* x_perm, int64_t* group_list,
+                         int32_t* row_id_map, int32_t* sorted_flat,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- grouped matmul */
+
+/* Workspace bytes for gmm_forward / gmm_backward. */
+MOE_API size_t gmm_workspace_size(int64_t M, int64_t K, int64_t N, int64_t E);
+
+/* Grouped matmul forward: [GMM] "算子语义", y[s:e] = x[s:e] @ w[g] for group g
+ * owning rows [s, e) = [cumsum before g, cumsum through g) of group_list.
+ *
+ *   x          [M, K] bf16, rows grouped by expert (M = rows of the buffer)
+ *   w          [E, K, N] bf16
+ *   group_list [E] int64 counts (device); sum must be <= M, rows at and past
+ *              the sum are neither read for any group nor written
+ *   epilogue   MOE_EPILOGUE_NONE:   y [M, N] = the product
+ *              MOE_EPILOGUE_SWIGLU: N = 2I (gate = first I columns, up = last
+ *                I), y [M, I] = SiLU(min(G,c)) * clip(U,-c,c) with G, U the
+ *                bf16-rounded product ([MegaMoE] 激活函数公式); h_save, if not
+ *                NULL, receives the bf16 product [M, N]
+ *   clip       c; 0 means no clip (+inf); must be >= 0
+ */
+MOE_API moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
+                         int64_t M, int64_t K, int64_t N, int64_t E,
+                         int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Grouped matmul backward: [GMM] "算子语义" backward formulas
+ *   dx[s:e] = dy[s:e] @ w[g]^T            (dx [M, K], NULL to skip)
+ *   dw[g]   = x[s:e]^T @ dy[s:e]          (dw [E, K, N], NULL to skip;
+ *                                          an empty group gets zeros)
+ *   dy [M, N] bf16 upstream gradient. */
+MOE_API moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
+                          const moe_bf16* dy, int64_t M, int64_t K, int64_t N, int64_t E,
+                          moe_bf16* dx, moe_bf16* dw,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- combine and gradients */
+
+/* Workspace bytes for the combine-side entry points (just the status block). */
+MOE_API size_t moe_unpermute_workspace_size(void);
+
+/* Weighted combine: [MegaMoE] Token Combine, y[t] = sum_j w[t,j] * y_perm[row(t,j)],
+ * fp32 accumulation in j order, one bf16 rounding; unused slots add nothing.
+ *   y_perm [T*k, H] bf16, row_id_map [T*k] int32 (from moe_permute),
+ *   topk_w [T, k] fp32 (NULL means every weight is 1), y [T, H] bf16 out. */
+MOE_API moe_status_t moe_unpermute(const moe_bf16* y_perm, const int32_t* row_id_map, const float* topk_w,
+                           int64_t T, int64_t H, int64_t k, moe_bf16* y,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gradients of the combine: [PermuteGrad] 2.2 (probs) with the combine of
+ * [MegaMoE] Token Combine differentiated:
+ *   dy_perm[row(t,j)] = w[t,j] * dy[t]          ([T*k, H] bf16, rows >= R untouched)
+ *   dprobs[t,j]       = <dy[t], y_perm[row(t,j)]> ([T, k] fp32; 0 for unused slots) */
+MOE_API moe_status_t moe_unpermute_backward(const moe_bf16* dy, const moe_bf16* y_perm,
+                                    const int32_t* row_id_map, const float* topk_w,
+                                    int64_t T, int64_t H, int64_t k,
+                                    moe_bf16* dy_perm, float* dprobs,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Token gradient of the permute: [PermuteGrad] 2.3 and 6.2, index-add of the
+ * permuted rows back onto their tokens, deterministic (fixed j order, fp32):
+ *   dx[t] = sum_j dx_perm[row(t,j)]   (dx [T, H] bf16) */
+MOE_API moe_status_t moe_permute_backward(const moe_bf16* dx_perm, const int32_t* row_id_map,
+                                  int64_t T, int64_t H, int64_t k, moe_bf16* dx,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* SwiGLU gradient with clip: [MegaMoE] 激活函数公式 differentiated.
+ *   h [rows, 2I] bf16 pre-activation (gate | up), da [rows, I] bf16,
+ *   dh [rows, 2I] bf16 out:
+ *   dG = dA * U_c * SiLU'(G_c) * [G <= c],  dU = dA * SiLU(G_c) * [-c <= U <= c] */
+MOE_API moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I,
+                                 float clip, moe_bf16* dh,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- whole layer */
+
+/* Tensors the forward keeps for the backward (all device pointers, caller-owned). */
+typedef struct moe_layer_saved {
+  moe_bf16* x_perm;      /* [T*k, H]  permuted tokens */
+  moe_bf16* h;           /* [T*k, 2I] gate_up product (pre-activation) */
+  moe_bf16* a;           /* [T*k, I]  SwiGLU output */
+  moe_bf16* y2;          /* [T*k, H]  down product */
+  int32_t* row_id_map;   /* [T*k] */
+  int32_t* sorted_flat;  /* [T*k] */
+  int64_t* group_list;   /* [E] */
+} moe_layer_saved_t;
+
+/* Workspace bytes for moe_layer_forward and moe_layer_backward with these
+ * sizes (one size serves both calls, with or without `saved`). */
+MOE_API size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
+
+/* Routed-expert layer forward ([GMM] "Qwen3.5 MoE 路径"; [MegaMoE] A16W16):
+ * permute -> GMM(w1 [E, H, 2I]) with SwiGLU(clip) -> GMM(w2 [E, I, H]) -> combine.
+ *   x [T, H] bf16, topk_ids [T, k] int32, topk_w [T, k] fp32, y [T, H] bf16 out.
+ *   saved: NULL for inference (intermediates live in ws), or the buffers that
+ *   moe_layer_backward will read. */
+MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
+                               const moe_bf16* w1, const moe_bf16* w2,
+                               int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
+                               moe_bf16* y, const moe_layer_saved_t* saved,
+                               void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Backward of moe_layer_forward (saved must be what the forward filled):
+ *   dy [T, H] bf16 in; dx [T, H], dw1 [E, H, 2I], dw2 [E, I, H] bf16 and
+ *   dprobs [T, k] fp32 out (any of them may be NULL except dx). */
+MOE_API moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w,
+                                const moe_bf16* w1, const moe_bf16* w2,
+                                const moe_layer_saved_t* saved,
+                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
+                                moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MOE_GMM_H */

@@ -1,0 +1,75 @@
+"""ctypes view of the C ABI declared in include/moe_gmm.h (signatures only)."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import build as _build
+
+P = C.c_void_p
+I64 = C.c_int64
+SZ = C.c_size_t
+F32 = C.c_float
+INT = C.c_int
+ST = C.c_int  # moe_status_t
+
+MOE_STATUS_BYTES = 256
+MOE_EPILOGUE_NONE = 0
+MOE_EPILOGUE_SWIGLU = 1
+
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_NULLPTR", 2: "MOE_ERR_INVALID", 3: "MOE_ERR_UNSUPPORTED",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT",
+}
+
+
+class MoeLayerSaved(C.Structure):
+    _fields_ = [("x_perm", P), ("h", P), ("a", P), ("y2", P),
+                ("row_id_map", P), ("sorted_flat", P), ("group_list", P)]
+
+
+SIGNATURES = {
+    "moe_workspace_init": (ST, [P, SZ, P]),
+    "moe_read_status": (ST, [P, P]),
+    "moe_status_string": (C.c_char_p, [ST]),
+    "moe_permute_workspace_size": (SZ, [I64, I64, I64]),
+    "moe_permute": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, SZ, P]),
+    "gmm_workspace_size": (SZ, [I64, I64, I64, I64]),
+    "gmm_forward": (ST, [P, P, P, I64, I64, I64, I64, INT, F32, P, P, P, SZ, P]),
+    "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
+    "moe_unpermute_workspace_size": (SZ, []),
+    "moe_unpermute": (ST, [P, P, P, I64, I64, I64, P, P, SZ, P]),
+    "moe_unpermute_backward": (ST, [P, P, P, P, I64, I64, I64, P, P, P, SZ, P]),
+    "moe_permute_backward": (ST, [P, P, I64, I64, I64, P, P, SZ, P]),
+    "moe_swiglu_backward": (ST, [P, P, I64, I64, F32, P, P, SZ, P]),
+    "moe_layer_workspace_size": (SZ, [I64, I64, I64, I64, I64]),
+    "moe_layer_forward": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, F32, P, C.POINTER(MoeLayerSaved),
+                               P, SZ, P]),
+    "moe_layer_backward": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64, F32,
+                                P, P, P, P, P, SZ, P]),
+}
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError("moe_routed_expert_gb300: CUDA library not built (%s); run build()" % path)
+        _build.build()
+    lib = C.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

@@ -1,0 +1,282 @@
+"""Python binding of the C ABI: same names as include/moe_gmm.h, torch tensors in
+and out.  Argument marshalling only -- every step runs in the CUDA library;
+there is no CPU or PyTorch fallback, and a missing library raises.
+
+Tensors must be CUDA, contiguous, and of the dtypes the header states (bf16
+for activations and weights, int32 ids / row maps, int64 group_list, fp32
+routing weights and dprobs).  Outputs are allocated here with torch (device
+memory is torch's job) unless passed in.  Calls run on torch's current
+stream unless ``stream`` is given.  Each call checks the host-side status;
+device-side errors are sticky in the workspace and are read by
+``read_status`` (which synchronises).
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import torch
+
+from . import _abi
+
+BF16 = torch.bfloat16
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, _abi.STATUS_NAMES.get(status, str(status))))
+
+
+def _lib():
+    return _abi.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def _dtype(t, dt, name):
+    if t is not None and t.dtype != dt:
+        raise ValueError("%s must be %s, got %s" % (name, dt, t.dtype))
+
+
+class Workspace:
+    """Caller-owned device workspace: zero-initialised status block + scratch."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.nbytes = int(max(nbytes, _abi.MOE_STATUS_BYTES))
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+    def ensure(self, nbytes: int) -> "Workspace":
+        if nbytes > self.nbytes:
+            self.__init__(nbytes, self.buf.device)
+        return self
+
+    @property
+    def ptr(self):
+        return C.c_void_p(self.buf.data_ptr())
+
+    def reset(self, stream=None):
+        _check(_lib().moe_workspace_init(self.ptr, self.nbytes, _stream(stream)), "moe_workspace_init")
+
+
+def _ws(ws: Optional[Workspace], nbytes: int, device) -> Workspace:
+    return Workspace(nbytes, device) if ws is None else ws.ensure(nbytes)
+
+
+def read_status(ws: Workspace, stream=None) -> int:
+    """Synchronise and return the workspace's sticky device status (0 = OK)."""
+    return int(_lib().moe_read_status(ws.ptr, _stream(stream)))
+
+
+def status_string(status: int) -> str:
+    return _lib().moe_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ sizes
+def moe_permute_workspace_size(T, k, E) -> int:
+    return int(_lib().moe_permute_workspace_size(T, k, E))
+
+
+def gmm_workspace_size(M, K, N, E) -> int:
+    return int(_lib().gmm_workspace_size(M, K, N, E))
+
+
+def moe_unpermute_workspace_size() -> int:
+    return int(_lib().moe_unpermute_workspace_size())
+
+
+def moe_layer_workspace_size(T, H, I, E, k) -> int:
+    return int(_lib().moe_layer_workspace_size(T, H, I, E, k))
+
+
+# ------------------------------------------------------------------ dispatch
+def moe_permute(x: Optional[torch.Tensor], topk_ids: torch.Tensor, E: int, *, out=None,
+                ws: Optional[Workspace] = None, stream=None):
+    """Returns (x_perm [T*k, H] or None, group_list [E] int64, row_id_map [T*k] int32,
+    sorted_flat [T*k] int32)."""
+    _dtype(x, BF16, "x")
+    _dtype(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    H = x.shape[1] if x is not None else 0
+    dev = topk_ids.device
+    if out is None:
+        x_perm = torch.empty(T * k, H, dtype=BF16, device=dev) if x is not None else None
+        group_list = torch.empty(E, dtype=torch.int64, device=dev)
+        row_id_map = torch.empty(T * k, dtype=torch.int32, device=dev)
+        sorted_flat = torch.empty(T * k, dtype=torch.int32, device=dev)
+    else:
+        x_perm, group_list, row_id_map, sorted_flat = out
+    w = _ws(ws, moe_permute_workspace_size(T, k, E), dev)
+    _check(_lib().moe_permute(_ptr(x), _ptr(topk_ids), T, H, k, E, _ptr(x_perm), _ptr(group_list),
+                              _ptr(row_id_map), _ptr(sorted_flat), w.ptr, w.nbytes, _stream(stream)),
+           "moe_permute")
+    return x_perm, group_list, row_id_map, sorted_flat
+
+
+# ------------------------------------------------------------------ grouped matmul
+def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, epilogue: int = 0,
+                clip: float = 0.0, y: Optional[torch.Tensor] = None, h_save: Optional[torch.Tensor] = None,
+                ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """y = grouped x @ w (epilogue 1: SwiGLU over the [gate | up] halves)."""
+    _dtype(x, BF16, "x")
+    _dtype(w, BF16, "w")
+    _dtype(group_list, torch.int64, "group_list")
+    M, K = x.shape
+    E, K2, N = w.shape
+    if K2 != K:
+        raise ValueError("x and w disagree on K")
+    out_cols = N // 2 if epilogue == _abi.MOE_EPILOGUE_SWIGLU else N
+    if y is None:
+        y = torch.empty(M, out_cols, dtype=BF16, device=x.device)
+    wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
+    _check(_lib().gmm_forward(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, int(epilogue), float(clip),
+                              _ptr(y), _ptr(h_save), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_forward")
+    return y
+
+
+def gmm_backward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, dy: torch.Tensor, *,
+                 need_dx: bool = True, need_dw: bool = True, dx=None, dw=None,
+                 ws: Optional[Workspace] = None, stream=None):
+    """Returns (dx [M, K] or None, dw [E, K, N] or None)."""
+    _dtype(x, BF16, "x")
+    _dtype(w, BF16, "w")
+    _dtype(dy, BF16, "dy")
+    M, K = x.shape
+    E, _, N = w.shape
+    if need_dx and dx is None:
+        dx = torch.empty(M, K, dtype=BF16, device=x.device)
+    if need_dw and dw is None:
+        dw = torch.empty(E, K, N, dtype=BF16, device=x.device)
+    wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
+    _check(_lib().gmm_backward(_ptr(x), _ptr(w), _ptr(group_list), _ptr(dy), M, K, N, E,
+                               _ptr(dx if need_dx else None), _ptr(dw if need_dw else None),
+                               wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward")
+    return (dx if need_dx else None), (dw if need_dw else None)
+
+
+# ------------------------------------------------------------------ combine side
+def moe_unpermute(y_perm, row_id_map, topk_w, T: int, k: int, *, y=None, ws=None, stream=None):
+    H = y_perm.shape[1]
+    _dtype(y_perm, BF16, "y_perm")
+    _dtype(topk_w, torch.float32, "topk_w")
+    if y is None:
+        y = torch.empty(T, H, dtype=BF16, device=y_perm.device)
+    wsp = _ws(ws, moe_unpermute_workspace_size(), y_perm.device)
+    _check(_lib().moe_unpermute(_ptr(y_perm), _ptr(row_id_map), _ptr(topk_w), T, H, k, _ptr(y),
+                                wsp.ptr, wsp.nbytes, _stream(stream)), "moe_unpermute")
+    return y
+
+
+def moe_unpermute_backward(dy, y_perm, row_id_map, topk_w, k: int, *, dy_perm=None, dprobs=None,
+                           need_dprobs: bool = True, ws=None, stream=None):
+    T, H = dy.shape
+    _dtype(dy, BF16, "dy")
+    _dtype(y_perm, BF16, "y_perm")
+    if dy_perm is None:
+        dy_perm = torch.empty(T * k, H, dtype=BF16, device=dy.device)
+    if need_dprobs and dprobs is None:
+        dprobs = torch.empty(T, k, dtype=torch.float32, device=dy.device)
+    wsp = _ws(ws, moe_unpermute_workspace_size(), dy.device)
+    _check(_lib().moe_unpermute_backward(_ptr(dy), _ptr(y_perm), _ptr(row_id_map), _ptr(topk_w), T, H, k,
+                                         _ptr(dy_perm), _ptr(dprobs if need_dprobs else None),
+                                         wsp.ptr, wsp.nbytes, _stream(stream)), "moe_unpermute_backward")
+    return dy_perm, (dprobs if need_dprobs else None)
+
+
+def moe_permute_backward(dx_perm, row_id_map, T: int, k: int, *, dx=None, ws=None, stream=None):
+    H = dx_perm.shape[1]
+    _dtype(dx_perm, BF16, "dx_perm")
+    if dx is None:
+        dx = torch.empty(T, H, dtype=BF16, device=dx_perm.device)
+    wsp = _ws(ws, moe_unpermute_workspace_size(), dx_perm.device)
+    _check(_lib().moe_permute_backward(_ptr(dx_perm), _ptr(row_id_map), T, H, k, _ptr(dx),
+                                       wsp.ptr, wsp.nbytes, _stream(stream)), "moe_permute_backward")
+    return dx
+
+
+def moe_swiglu_backward(h, da, clip: float = 0.0, *, dh=None, ws=None, stream=None):
+    rows, I2 = h.shape
+    _dtype(h, BF16, "h")
+    _dtype(da, BF16, "da")
+    if dh is None:
+        dh = torch.empty_like(h)
+    wsp = _ws(ws, moe_unpermute_workspace_size(), h.device)
+    _check(_lib().moe_swiglu_backward(_ptr(h), _ptr(da), rows, I2 // 2, float(clip), _ptr(dh),
+                                      wsp.ptr, wsp.nbytes, _stream(stream)), "moe_swiglu_backward")
+    return dh
+
+
+# ------------------------------------------------------------------ whole layer
+class LayerSaved:
+    """Device buffers the layer forward fills for the backward."""
+
+    def __init__(self, T, H, I, E, k, device="cuda"):
+        R = T * k
+        self.x_perm = torch.empty(R, H, dtype=BF16, device=device)
+        self.h = torch.empty(R, 2 * I, dtype=BF16, device=device)
+        self.a = torch.empty(R, I, dtype=BF16, device=device)
+        self.y2 = torch.empty(R, H, dtype=BF16, device=device)
+        self.row_id_map = torch.empty(R, dtype=torch.int32, device=device)
+        self.sorted_flat = torch.empty(R, dtype=torch.int32, device=device)
+        self.group_list = torch.empty(E, dtype=torch.int64, device=device)
+
+    def struct(self) -> _abi.MoeLayerSaved:
+        return _abi.MoeLayerSaved(*(t.data_ptr() for t in (self.x_perm, self.h, self.a, self.y2, self.row_id_map,
+                                                             self.sorted_flat, self.group_list)))
+
+
+def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: Optional[LayerSaved] = None,
+                      y=None, ws: Optional[Workspace] = None, stream=None):
+    T, H = x.shape
+    E, _, I2 = w1.shape
+    I = I2 // 2
+    k = topk_ids.shape[1]
+    for t, n in ((x, "x"), (w1, "w1"), (w2, "w2")):
+        _dtype(t, BF16, n)
+    _dtype(topk_ids, torch.int32, "topk_ids")
+    _dtype(topk_w, torch.float32, "topk_w")
+    if y is None:
+        y = torch.empty(T, H, dtype=BF16, device=x.device)
+    wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), x.device)
+    sv = C.byref(saved.struct()) if saved is not None else None
+    _check(_lib().moe_layer_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2), T, H, I, E, k,
+                                    float(clip), _ptr(y), sv, wsp.ptr, wsp.nbytes, _stream(stream)),
+           "moe_layer_forward")
+    return y
+
+
+def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0, *, dx=None, dw1=None, dw2=None,
+                       dprobs=None, ws: Optional[Workspace] = None, stream=None):
+    T, H = dy.shape
+    E, _, I2 = w1.shape
+    I = I2 // 2
+    k = topk_w.shape[1]
+    dev = dy.device
+    dx = torch.empty(T, H, dtype=BF16, device=dev) if dx is None else dx
+    dw1 = torch.empty_like(w1) if dw1 is None else dw1
+    dw2 = torch.empty_like(w2) if dw2 is None else dw2
+    dprobs = torch.empty(T, k, dtype=torch.float32, device=dev) if dprobs is None else dprobs
+    wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), dev)
+    _check(_lib().moe_layer_backward(_ptr(dy), _ptr(topk_w), _ptr(w1), _ptr(w2), C.byref(saved.struct()),
+                                     T, H, I, E, k, float(clip), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprobs),
+                                     wsp.ptr, wsp.nbytes, _stream(stream)), "moe_layer_backward")
+    return dx, dw1, dw2, dprobs

@@ -1,0 +1,335 @@
+// The C ABI (include/moe_gmm.h): argument checks, workspace carving and the
+// launch sequence of each entry point.  Host code only; kernels live in
+// permute.cu, gmm.cu and combine.cu.
+//
+// The two-phase convention (size query, then execute with a caller-owned
+// workspace on a stream) and the null / invalid argument split follow
+// "CANN ops-transformer 算子详解 MoeTokenPermuteWithRoutingMapGrad", sections 3
+// and 4.2-4.3; empty inputs are a no-op needing no workspace (section 5).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "moe_gmm.h"
+
+namespace moe {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline uint32_t* status_of(void* ws) { return static_cast<uint32_t*>(ws); }
+inline uint8_t* after_status(void* ws) { return static_cast<uint8_t*>(ws) + MOE_STATUS_BYTES; }
+
+moe_status_t check_ws(const void* ws, size_t have, size_t need) {
+  if (ws == nullptr) return MOE_ERR_NULLPTR;
+  if (!aligned16(ws) || have < need) return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+bool bad_clip(float clip) { return !(clip >= 0.0f) || isinf(clip); }  // NaN fails the first test
+
+size_t layer_acts_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  const size_t R = static_cast<size_t>(T * k);
+  const size_t fwd = align256(R * H * 2) + align256(R * I * 2) + align256(R * H * 2) + 2 * align256(R * 4) +
+                     align256(static_cast<size_t>(E) * 8);
+  const size_t bwd = align256(R * H * 2) + align256(R * I * 2) + align256(R * 2 * I * 2);
+  return fwd > bwd ? fwd : bwd;
+}
+
+moe_status_t check_gmm_dims(int64_t M, int64_t K, int64_t N, int64_t E) {
+  if (M < 0 || K <= 0 || N <= 0 || E <= 0) return MOE_ERR_INVALID;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (K % 64 || N % 64) return MOE_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || K > INT32_MAX / 2 || N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_tokens(int64_t T, int64_t H, int64_t k) {
+  if (T < 0 || H <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (k > kMaxTopK || H % 8) return MOE_ERR_UNSUPPORTED;
+  if (T * k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_NULLPTR: return "MOE_ERR_NULLPTR";
+    case MOE_ERR_INVALID: return "MOE_ERR_INVALID";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_NULLPTR;
+  if (ws_bytes < MOE_STATUS_BYTES || !aligned16(ws)) return MOE_ERR_INVALID;
+  return cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_read_status(const void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_NULLPTR;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(v);
+}
+
+// ------------------------------------------------------------------ dispatch
+size_t moe_permute_workspace_size(int64_t T, int64_t k, int64_t E) {
+  if (T <= 0 || k <= 0 || E <= 0) return MOE_STATUS_BYTES;
+  return MOE_STATUS_BYTES + permute_scratch_bytes(T, k, E);
+}
+
+moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k, int64_t E,
+                         moe_bf16* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!topk_ids || !group_list || !row_id_map || !sorted_flat) return MOE_ERR_NULLPTR;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_NULLPTR;
+  if (E <= 0 || k > E) return MOE_ERR_INVALID;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = check_tokens(T, x ? H : 8, k);
+  if (st != MOE_OK) return st;
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_permute_workspace_size(T, k, E))) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0)
+    return cudaMemsetAsync(group_list, 0, E * sizeof(int64_t), s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_permute(x, topk_ids, T, H, k, E, x_perm, group_list, row_id_map, sorted_flat, status_of(ws),
+                        after_status(ws), s);
+}
+
+// ------------------------------------------------------------------ grouped matmul
+size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES; }
+
+moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
+                         int64_t N, int64_t E, int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_gmm_dims(M, K, N, E);
+  if (st != MOE_OK) return st;
+  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPILOGUE_SWIGLU && N % 256) return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPILOGUE_NONE && h_save) return MOE_ERR_INVALID;
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (h_save && !aligned16(h_save)) ||
+      (reinterpret_cast<uintptr_t>(group_list) & 7u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  return launch_gmm(GMM_FWD, epilogue, x, w, group_list, M, K, N, E, clip, y, h_save, status_of(ws),
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
+                          int64_t M, int64_t K, int64_t N, int64_t E, moe_bf16* dx, moe_bf16* dw,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !w || !group_list || !dy) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_gmm_dims(M, K, N, E);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || (dx && !aligned16(dx)) || (dw && !aligned16(dw)) ||
+      (reinterpret_cast<uintptr_t>(group_list) & 7u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    // no rows: every group is empty, so dW is zero
+    if (dw && cudaMemsetAsync(dw, 0, static_cast<size_t>(E * K * N) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (dx && (st = launch_gmm(GMM_DX, 0, dy, w, group_list, M, K, N, E, 0.f, dx, nullptr, status_of(ws), s)) != MOE_OK)
+    return st;
+  if (dw && (st = launch_gmm(GMM_DW, 0, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status_of(ws), s)) != MOE_OK)
+    return st;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ combine side
+size_t moe_unpermute_workspace_size(void) { return MOE_STATUS_BYTES; }
+
+moe_status_t moe_unpermute(const moe_bf16* y_perm, const int32_t* row_id_map, const float* topk_w, int64_t T,
+                           int64_t H, int64_t k, moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!y_perm || !row_id_map || !y) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_tokens(T, H, k);
+  if (st != MOE_OK) return st;
+  if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  return launch_unpermute(y_perm, row_id_map, topk_w, T, H, k, y, status_of(ws),
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_unpermute_backward(const moe_bf16* dy, const moe_bf16* y_perm, const int32_t* row_id_map,
+                                    const float* topk_w, int64_t T, int64_t H, int64_t k, moe_bf16* dy_perm,
+                                    float* dprobs, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!dy || !y_perm || !row_id_map || !topk_w || !dy_perm) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_tokens(T, H, k);
+  if (st != MOE_OK) return st;
+  if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm)) return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  return launch_unpermute_backward(dy, y_perm, row_id_map, topk_w, T, H, k, dy_perm, dprobs, status_of(ws),
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute_backward(const moe_bf16* dx_perm, const int32_t* row_id_map, int64_t T, int64_t H,
+                                  int64_t k, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!dx_perm || !row_id_map || !dx) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_tokens(T, H, k);
+  if (st != MOE_OK) return st;
+  if (!aligned16(dx_perm) || !aligned16(dx)) return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  return launch_unpermute(dx_perm, row_id_map, nullptr, T, H, k, dx, status_of(ws),
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I, float clip,
+                                 moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!h || !da || !dh) return MOE_ERR_NULLPTR;
+  if (rows < 0 || I <= 0 || bad_clip(clip)) return MOE_ERR_INVALID;
+  if (I % 8) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(da) || !aligned16(dh)) return MOE_ERR_INVALID;
+  moe_status_t st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  return launch_swiglu_backward(h, da, rows, I, clip, dh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ whole layer
+size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_STATUS_BYTES;
+  return MOE_STATUS_BYTES + permute_scratch_bytes(T, k, E) + layer_acts_bytes(T, H, I, E, k);
+}
+
+namespace {
+moe_status_t check_layer(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip) {
+  if (E <= 0 || I <= 0 || k > E || bad_clip(clip)) return MOE_ERR_INVALID;
+  moe_status_t st = check_tokens(T, H, k);
+  if (st != MOE_OK) return st;
+  if (E > kMaxExperts || H % 64 || I % 128) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+bool saved_ok(const moe_layer_saved_t* sv) {
+  return sv->x_perm && sv->h && sv->a && sv->y2 && sv->row_id_map && sv->sorted_flat && sv->group_list;
+}
+bool saved_aligned(const moe_layer_saved_t* sv) {
+  return aligned16(sv->x_perm) && aligned16(sv->h) && aligned16(sv->a) && aligned16(sv->y2) &&
+         (reinterpret_cast<uintptr_t>(sv->group_list) & 7u) == 0;
+}
+}  // namespace
+
+moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w, const moe_bf16* w1,
+                               const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
+                               moe_bf16* y, const moe_layer_saved_t* saved, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  if (!x || !topk_ids || !topk_w || !w1 || !w2 || !y) return MOE_ERR_NULLPTR;
+  if (saved && !saved_ok(saved)) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_layer(T, H, I, E, k, clip);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) || (saved && !saved_aligned(saved)))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_layer_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = status_of(ws);
+  uint8_t* scratch = after_status(ws);
+  uint8_t* acts = scratch + permute_scratch_bytes(T, k, E);
+  const int64_t R = T * k;
+  moe_bf16 *x_perm, *h, *a, *y2;
+  int32_t *rmap, *sflat;
+  int64_t* gl;
+  if (saved) {
+    x_perm = saved->x_perm; h = saved->h; a = saved->a; y2 = saved->y2;
+    rmap = saved->row_id_map; sflat = saved->sorted_flat; gl = saved->group_list;
+  } else {
+    uint8_t* p = acts;
+    x_perm = reinterpret_cast<moe_bf16*>(p); p += align256(R * H * 2);
+    a = reinterpret_cast<moe_bf16*>(p);      p += align256(R * I * 2);
+    y2 = reinterpret_cast<moe_bf16*>(p);     p += align256(R * H * 2);
+    rmap = reinterpret_cast<int32_t*>(p);    p += align256(R * 4);
+    sflat = reinterpret_cast<int32_t*>(p);   p += align256(R * 4);
+    gl = reinterpret_cast<int64_t*>(p);
+    h = nullptr;
+  }
+  if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
+  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, clip, a, h, status, s)) != MOE_OK)
+    return st;
+  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_NONE, a, w2, gl, R, I, H, E, 0.f, y2, nullptr, status, s)) != MOE_OK)
+    return st;
+  return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
+}
+
+moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const moe_bf16* w1, const moe_bf16* w2,
+                                const moe_layer_saved_t* saved, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                                float clip, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  if (!dy || !topk_w || !w1 || !w2 || !saved || !dx) return MOE_ERR_NULLPTR;
+  if (!saved_ok(saved)) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_layer(T, H, I, E, k, clip);
+  if (st != MOE_OK) return st;
+  if (!aligned16(dy) || !aligned16(w1) || !aligned16(w2) || !aligned16(dx) || (dw1 && !aligned16(dw1)) ||
+      (dw2 && !aligned16(dw2)) || !saved_aligned(saved))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_layer_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (dw1 && cudaMemsetAsync(dw1, 0, static_cast<size_t>(E * H * 2 * I) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dw2 && cudaMemsetAsync(dw2, 0, static_cast<size_t>(E * I * H) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  uint32_t* status = status_of(ws);
+  uint8_t* acts = after_status(ws) + permute_scratch_bytes(T, k, E);
+  const int64_t R = T * k;
+  moe_bf16* dy2 = reinterpret_cast<moe_bf16*>(acts);
+  moe_bf16* da = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2));
+  moe_bf16* dh = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2) + align256(R * I * 2));
+  moe_bf16* dx_perm = dy2;  // dy2 is dead once dA and dW2 are done
+  if ((st = launch_unpermute_backward(dy, saved->y2, saved->row_id_map, topk_w, T, H, k, dy2, dprobs, status, s)) !=
+      MOE_OK)
+    return st;
+  if ((st = launch_gmm(GMM_DX, 0, dy2, w2, saved->group_list, R, I, H, E, 0.f, da, nullptr, status, s)) != MOE_OK)
+    return st;
+  if (dw2 && (st = launch_gmm(GMM_DW, 0, saved->a, dy2, saved->group_list, R, I, H, E, 0.f, dw2, nullptr, status, s)) !=
+                 MOE_OK)
+    return st;
+  if ((st = launch_swiglu_backward(saved->h, da, R, I, clip, dh, s)) != MOE_OK) return st;
+  if ((st = launch_gmm(GMM_DX, 0, dh, w1, saved->group_list, R, H, 2 * I, E, 0.f, dx_perm, nullptr, status, s)) !=
+      MOE_OK)
+    return st;
+  if (dw1 &&
+      (st = launch_gmm(GMM_DW, 0, saved->x_perm, dh, saved->group_list, R, H, 2 * I, E, 0.f, dw1, nullptr, status, s)) !=
+          MOE_OK)
+    return st;
+  return launch_unpermute(dx_perm, saved->row_id_map, nullptr, T, H, k, dx, status, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// Combine side of the routed-expert path: weighted top-k combine (unpermute),
+// its gradients, and the SwiGLU gradient.  All are HBM-bound row streams:
+// 16-byte vector loads through the read-only path, fp32 accumulation in a
+// fixed order (so results are deterministic), one bf16 rounding at the end.
+//
+//   combine       "MegaMoE", Token Combine: y_i = sum_k w_k Y_{e_ik}[row(i,k)].
+//   token grad    "CANN ops-transformer 算子详解 MoeTokenPermuteWithRoutingMapGrad",
+//                 2.3 and 6.2: per output token, walk its topK slots, skip -1,
+//                 accumulate in fp32, cast back -- the same kernel with unit
+//                 weights.
+//   probs grad    the same article, 2.2, in the [T, topK] shape of its 6.3:
+//                 dprobs[t,j] = <dy[t], Y[row(t,j)]>, with dY[row(t,j)] = w dy[t].
+//   SwiGLU grad   "MegaMoE", 激活函数公式 (swiglu with clip c) differentiated.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int COLS_PER_BLOCK = THREADS * 8;  // 2048 bf16 per block row segment
+constexpr int JB = 8;                         // slots loaded together
+
+__device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
+  acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+  acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+  acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+  acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+  acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
+  acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
+  acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
+  acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+  uint4 q;
+  q.x = pack_bf16x2(a[0], a[1]);
+  q.y = pack_bf16x2(a[2], a[3]);
+  q.z = pack_bf16x2(a[4], a[5]);
+  q.w = pack_bf16x2(a[6], a[7]);
+  return q;
+}
+
+// grid (T, ceil(H / 2048)); each thread owns 8 consecutive columns of one token.
+template <bool HAS_W>
+__global__ void __launch_bounds__(THREADS) unpermute_kernel(const uint16_t* __restrict__ y_perm,
+                                                            const int32_t* __restrict__ row_id_map,
+                                                            const float* __restrict__ topk_w, int64_t H, int k,
+                                                            int64_t rows_cap, uint16_t* __restrict__ y,
+                                                            uint32_t* status) {
+  const int64_t t = blockIdx.x;
+  const int64_t col = static_cast<int64_t>(blockIdx.y) * COLS_PER_BLOCK + threadIdx.x * 8;
+  if (col >= H) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j0 = 0; j0 < k; j0 += JB) {
+    int32_t r[JB];
+    uint4 v[JB];
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
+      const int j = j0 + jj;
+      r[jj] = j < k ? row_id_map[t * k + j] : -1;
+      if (r[jj] < -1 || r[jj] >= rows_cap) {
+        set_status(status, MOE_ERR_DEVICE);
+        r[jj] = -1;
+      }
+      if (r[jj] >= 0) v[jj] = ld_nc_v4(y_perm + static_cast<int64_t>(r[jj]) * H + col);
+    }
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
+      if (r[jj] >= 0) add8(acc, v[jj], HAS_W ? topk_w[t * k + j0 + jj] : 1.0f);
+    }
+  }
+  *reinterpret_cast<uint4*>(y + t * H + col) = pack8(acc);
+}
+
+// One block per token: writes dy_perm rows and reduces the k dot products.
+__global__ void __launch_bounds__(THREADS) unpermute_backward_kernel(
+    const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y_perm, const int32_t* __restrict__ row_id_map,
+    const float* __restrict__ topk_w, int64_t H, int k, int64_t rows_cap, uint16_t* __restrict__ dy_perm,
+    float* __restrict__ dprobs, uint32_t* status) {
+  __shared__ float red[THREADS / 32][JB];
+  const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j0 = 0; j0 < k; j0 += JB) {
+    int32_t r[JB];
+    float w[JB], dot[JB];
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
+      const int j = j0 + jj;
+      r[jj] = j < k ? row_id_map[t * k + j] : -1;
+      if (r[jj] < -1 || r[jj] >= rows_cap) {
+        if (threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE);
+        r[jj] = -1;
+      }
+      w[jj] = (j < k && topk_w) ? topk_w[t * k + j] : 0.f;
+      dot[jj] = 0.f;
+    }
+    for (int64_t col = threadIdx.x * 8; col < H; col += COLS_PER_BLOCK) {
+      const uint4 g = ld_nc_v4(dy + t * H + col);
+      float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                     bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+      uint4 v[JB];
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj)
+        if (r[jj] >= 0) v[jj] = ld_nc_v4(y_perm + static_cast<int64_t>(r[jj]) * H + col);
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        if (r[jj] < 0) continue;
+        float d = 0.f;
+        d = fmaf(gf[0], bf16_lo(v[jj].x), d);
+        d = fmaf(gf[1], bf16_hi(v[jj].x), d);
+        d = fmaf(gf[2], bf16_lo(v[jj].y), d);
+        d = fmaf(gf[3], bf16_hi(v[jj].y), d);
+        d = fmaf(gf[4], bf16_lo(v[jj].z), d);
+        d = fmaf(gf[5], bf16_hi(v[jj].z), d);
+        d = fmaf(gf[6], bf16_lo(v[jj].w), d);
+        d = fmaf(gf[7], bf16_hi(v[jj].w), d);
+        dot[jj] += d;
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = w[jj] * gf[i];
+        *reinterpret_cast<uint4*>(dy_perm + static_cast<int64_t>(r[jj]) * H + col) = pack8(o);
+      }
+    }
+    if (dprobs) {
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        float d = dot[jj];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (lane == 0) red[warp][jj] = d;
+      }
+      __syncthreads();
+      if (threadIdx.x < JB) {
+        const int j = j0 + threadIdx.x;
+        float d = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < THREADS / 32; ++w8) d += red[w8][threadIdx.x];
+        if (j < k) dprobs[t * k + j] = (r[threadIdx.x] >= 0) ? d : 0.f;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Elementwise over rows x I: 8 columns per thread (gate at c, up at I + c).
+__global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t* __restrict__ h,
+                                                                  const uint16_t* __restrict__ da, int64_t rows,
+                                                                  int64_t I, float c, uint16_t* __restrict__ dh) {
+  const int64_t per_row = I / 8;
+  const int64_t items = rows * per_row;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x; it < items;
+       it += static_cast<int64_t>(gridDim.x) * THREADS) {
+    const int64_t r = it / per_row;
+    const int64_t col = (it - r * per_row) * 8;
+    const uint4 gv = ld_nc_v4(h + r * 2 * I + col);
+    const uint4 uv = ld_nc_v4(h + r * 2 * I + I + col);
+    const uint4 dv = ld_nc_v4(da + r * I + col);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    float dg[8], du[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+      const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
+      const float d = (i & 1) ? bf16_hi(dw[i >> 1]) : bf16_lo(dw[i >> 1]);
+      const float gc = fminf(g, c);
+      const float uc = fminf(fmaxf(u, -c), c);
+      const float s = 1.0f / (1.0f + __expf(-gc));
+      const float silu = gc * s;
+      const float dsilu = s * (1.0f + gc * (1.0f - s));
+      dg[i] = (g <= c) ? d * uc * dsilu : 0.0f;
+      du[i] = (u >= -c && u <= c) ? d * silu : 0.0f;
+    }
+    *reinterpret_cast<uint4*>(dh + r * 2 * I + col) = pack8(dg);
+    *reinterpret_cast<uint4*>(dh + r * 2 * I + I + col) = pack8(du);
+  }
+}
+
+}  // namespace
+
+moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
+                              int64_t T, int64_t H, int64_t k, uint16_t* y, uint32_t* status, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H + COLS_PER_BLOCK - 1) / COLS_PER_BLOCK));
+  if (topk_w)
+    unpermute_kernel<true><<<grid, THREADS, 0, s>>>(y_perm, row_id_map, topk_w, H, static_cast<int>(k), T * k, y,
+                                                    status);
+  else
+    unpermute_kernel<false><<<grid, THREADS, 0, s>>>(y_perm, row_id_map, nullptr, H, static_cast<int>(k), T * k, y,
+                                                     status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_id_map,
+                                       const float* topk_w, int64_t T, int64_t H, int64_t k,
+                                       uint16_t* dy_perm, float* dprobs, uint32_t* status, cudaStream_t s) {
+  unpermute_backward_kernel<<<static_cast<unsigned>(T), THREADS, 0, s>>>(dy, y_perm, row_id_map, topk_w, H,
+                                                                         static_cast<int>(k), T * k, dy_perm,
+                                                                         dprobs, status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
+                                    uint16_t* dh, cudaStream_t s) {
+  const float c = clip > 0.0f ? clip : INFINITY;
+  const int64_t items = rows * (I / 8);
+  int64_t blocks = (items + THREADS - 1) / THREADS;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  swiglu_backward_kernel<<<static_cast<unsigned>(blocks), THREADS, 0, s>>>(h, da, rows, I, c, dh);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

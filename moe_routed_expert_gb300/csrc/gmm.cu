@@ -1,0 +1,543 @@
+// Grouped matmul (GMM) on the 5th-generation tensor cores: a persistent,
+// warp-specialised tcgen05 kernel with TMA-fed shared-memory stages and a
+// double-buffered fp32 accumulator in TMEM.
+//
+// What it computes follows "NPU Training Operators - GMM", section "算子语义":
+// rows of x are grouped by expert (group g owns rows [cumsum before g,
+// cumsum through g) of group_list) and
+//   forward   y_g  = x_g  @ W_g                 (GMM_FWD)
+//   input grad dx_g = dy_g @ W_g^T              (GMM_DX)
+//   weight grad dW_g = x_g^T @ dy_g, 0 if empty (GMM_DW)
+// The gate_up forward can finish with the clipped SwiGLU of "MegaMoE",
+// "激活函数公式" (gate = first I columns, up = last I), in the epilogue.
+//
+// Design (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
+//               (64 x 256) into a 4-stage ring, one mbarrier pair per stage.
+//   warp 1      TMEM allocator + MMA issuer: 4 x tcgen05.mma (M=128, N=256,
+//               K=16) per stage into one of two 256-column fp32 accumulators;
+//               tcgen05.commit frees the stage and, after the last stage,
+//               hands the accumulator to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld (32 lanes x 32 columns) -> bf16 ->
+//               row-masked global stores; then release the accumulator.
+// The group structure is read on the device (no host sync): every CTA scans
+// group_list into row offsets and a tile prefix in shared memory and maps a
+// linear tile id to (group, row tile, column tile) by binary search.  Tiles
+// are visited column-tile fastest so concurrent CTAs share A rows and W
+// columns in L2.  For dW the contraction runs over the group's own rows: the
+// last 64-row block of a group is zero-filled past the group end in shared
+// memory before the MMA, and groups are visited largest-first.
+// Every wait is bounded; on a timeout the kernel drains its own copies and
+// MMAs, writes MOE_ERR_TIMEOUT to the status word and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BN * BK * 2;        // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BOX_BYTES = 64 * 64 * 2;      // one 64 x 64 bf16 box = 8 KB
+constexpr int TMEM_COLS = 2 * BN;           // two accumulators
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t kTimeoutNs = 4000000000ull;   // 4 s: far above any legal wait
+
+struct GmmParams {
+  const int64_t* group_list;
+  int E;
+  int64_t rows_cap;    // rows of the grouped operand (M)
+  int out_rows;        // GMM_DW: rows of one expert's dW (K)
+  int out_cols;        // columns of the output (FWD: N, or I with SwiGLU; DX: K; DW: N)
+  int tile_cols;       // column tiles per row tile
+  int kblocks;         // FWD / DX: contraction blocks of 64 (K/64 or N/64)
+  uint16_t* out;
+  int64_t ld_out;
+  uint16_t* h_save;    // SwiGLU: bf16 pre-activation [M, 2I]
+  int act_cols;        // SwiGLU: I
+  float clip;          // SwiGLU: c (+inf: none)
+  uint32_t* status;
+};
+
+struct __align__(16) GmmSmem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+  int32_t bad;
+  int32_t ntiles;
+  int64_t grp_off[kMaxExperts + 1];   // row offset of each expert (by id)
+  int32_t grp_cnt[kMaxExperts];       // rows of each expert (by id)
+  int32_t order[kMaxExperts];         // visiting order: position -> expert id
+  int32_t tile_start[kMaxExperts + 1];  // tile prefix over visiting positions
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(GmmSmem);
+
+struct TileInfo {
+  int g;          // expert id
+  int64_t row0;   // FWD/DX: first row of x/dy; DW: first output row (k)
+  int rows_valid; // rows of the tile that belong to the output
+  int col0;       // first output column (SwiGLU: first activation column)
+  int kblocks;    // contraction blocks of 64
+  int64_t m0;     // DW: first contraction row (group start)
+  int depth;      // DW: contraction rows of the group
+};
+
+template <int MODE, bool SWIGLU>
+__device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmParams& p, int t) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  const int g = sm->order[lo];
+  const int local = t - sm->tile_start[lo];
+  const int rt = local / p.tile_cols;
+  const int ct = local - rt * p.tile_cols;
+  ti.g = g;
+  ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
+  if (MODE == GMM_DW) {
+    ti.row0 = static_cast<int64_t>(rt) * BM;
+    ti.rows_valid = min(BM, p.out_rows - rt * BM);
+    ti.m0 = sm->grp_off[g];
+    ti.depth = sm->grp_cnt[g];
+    ti.kblocks = (ti.depth + BK - 1) / BK;
+  } else {
+    ti.row0 = sm->grp_off[g] + static_cast<int64_t>(rt) * BM;
+    ti.rows_valid = min(BM, sm->grp_cnt[g] - rt * BM);
+    ti.m0 = 0;
+    ti.depth = 0;
+    ti.kblocks = p.kblocks;
+  }
+  return ti;
+}
+
+// Lane 0 waits, the whole warp learns the outcome (keeps the warp converged
+// for the .sync.aligned tcgen05 instructions that follow).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Wait that ignores the abort flag: used only to drain in-flight work on the abort path.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  uint32_t dummy = 0;
+  mbar_wait_bounded(bar, parity, &dummy, 200000000ull);
+}
+
+__device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&r)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 q;
+    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+    d[v] = q;
+  }
+}
+
+template <int MODE, bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
+  constexpr bool A_MN = (MODE == GMM_DW);
+  constexpr bool B_MN = (MODE != GMM_DX);
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GmmSmem* sm = reinterpret_cast<GmmSmem*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t stage_base = smem_u32(smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    sm->bad = 0;
+    sm->abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sm->tmem_full[a]), 1);
+      mbar_init(smem_u32(&sm->tmem_empty[a]), 4);
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += NUM_THREADS) {
+    const int64_t c = p.group_list[e];
+    if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
+    sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
+  }
+  __syncthreads();
+  if (MODE == GMM_DW) {
+    // largest group first (ties: lower id first)
+    for (int e = tid; e < E; e += NUM_THREADS) {
+      const int ce = sm->grp_cnt[e];
+      int r = 0;
+      for (int e2 = 0; e2 < E; ++e2) {
+        const int c2 = sm->grp_cnt[e2];
+        r += (c2 > ce) || (c2 == ce && e2 < e);
+      }
+      sm->order[r] = e;
+    }
+  } else {
+    for (int e = tid; e < E; e += NUM_THREADS) sm->order[e] = e;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int64_t rows = 0;
+    int32_t tiles = 0;
+    const int row_tiles_dw = (p.out_rows + BM - 1) / BM;
+    for (int e = lo; e < hi; ++e) {
+      rows += sm->grp_cnt[e];
+      const int g = sm->order[e];
+      tiles += (MODE == GMM_DW) ? row_tiles_dw * p.tile_cols
+                                : ((sm->grp_cnt[g] + BM - 1) / BM) * p.tile_cols;
+    }
+    int64_t rows_incl = rows;
+    int32_t tiles_incl = tiles;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t r2 = __shfl_up_sync(0xffffffffu, rows_incl, d);
+      const int32_t t2 = __shfl_up_sync(0xffffffffu, tiles_incl, d);
+      if (lane >= d) { rows_incl += r2; tiles_incl += t2; }
+    }
+    int64_t rb = rows_incl - rows;
+    int32_t tb = tiles_incl - tiles;
+    for (int e = lo; e < hi; ++e) {
+      sm->grp_off[e] = rb;
+      rb += sm->grp_cnt[e];
+      const int g = sm->order[e];
+      sm->tile_start[e] = tb;
+      tb += (MODE == GMM_DW) ? row_tiles_dw * p.tile_cols
+                             : ((sm->grp_cnt[g] + BM - 1) / BM) * p.tile_cols;
+    }
+    if (lane == 31) {
+      sm->grp_off[E] = rows_incl;
+      sm->tile_start[E] = tiles_incl;
+      sm->ntiles = tiles_incl;
+      if (rows_incl > p.rows_cap) sm->bad = 1;
+    }
+  }
+  __syncthreads();
+  if (sm->bad) {
+    if (tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm->tmem_base;
+  const int ntiles = sm->ntiles;
+  volatile uint32_t* abort_flag = &sm->abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+          const uint32_t bar = smem_u32(&sm->full[s]);
+          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          mbar_expect_tx(bar, STAGE_BYTES);
+          if (MODE == GMM_FWD) {
+            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              const int col = SWIGLU ? ((j < 2) ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * (j - 2))
+                                     : ti.col0 + 64 * j;
+              tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
+            }
+          } else if (MODE == GMM_DX) {
+            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
+          } else {
+            const int32_t mrow = static_cast<int32_t>(ti.m0 + static_cast<int64_t>(kb) * BK);
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(a_dst + i * BOX_BYTES, &tmA, bar, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * BOX_BYTES, &tmB, bar, ti.col0 + 64 * j, mrow);
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA can exit
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    uint32_t it = 0, local = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+      if (ti.kblocks == 0) continue;
+      const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+      if (!warp_wait(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, lane)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!warp_wait(smem_u32(&sm->full[s]), ph, abort_flag, lane)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = stage_base + s * STAGE_BYTES;
+        const uint32_t b_addr = a_addr + A_BYTES;
+        if (MODE == GMM_DW) {
+          const int valid = ti.depth - kb * BK;
+          if (valid < BK) {
+            // rows past the group end belong to the next group: zero them in
+            // every box of this stage (a swizzled row stays inside its 128 bytes)
+            const int nbox = (A_BYTES + B_BYTES) / BOX_BYTES;
+            const int nchunk = (BK - valid) * 8;  // 16-byte chunks per box
+            uint8_t* base = smem + s * STAGE_BYTES;
+            for (int i = lane; i < nbox * nchunk; i += 32) {
+              const int box = i / nchunk, c = i - box * nchunk;
+              *reinterpret_cast<uint4*>(base + box * BOX_BYTES + valid * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, BOX_BYTES, 1024)
+                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
+                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm->empty[s]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(smem_u32(&sm->tmem_full[acc]));
+      __syncwarp();
+      ++local;
+    }
+    if (!ok && lane == 0) {
+      tc_commit(smem_u32(&sm->drain));
+      drain_wait(smem_u32(&sm->drain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane;
+    uint32_t local = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+      const bool row_ok = row_in_tile < ti.rows_valid;
+      const int64_t row = ti.row0 + row_in_tile;
+      if (MODE == GMM_DW && ti.kblocks == 0) {
+        if (row_ok) {
+          uint16_t* dst = p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out + row * p.ld_out + ti.col0;
+          const int ncols = min(BN, p.out_cols - ti.col0);
+          for (int c = 0; c < ncols; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+      if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (SWIGLU) {
+        const float c = p.clip;
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 2; cc += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + cc, g);
+          tmem_ld32(taddr + BN / 2 + cc, u);
+          tmem_ld_wait();
+          if (row_ok) {
+            // H is stored in bf16; the activation is taken on those stored values
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __float_as_uint(round_bf16(__uint_as_float(g[i])));
+              u[i] = __float_as_uint(round_bf16(__uint_as_float(u[i])));
+            }
+            if (p.h_save) {
+              store_row32(p.h_save + row * (2 * p.act_cols) + ti.col0 + cc, g);
+              store_row32(p.h_save + row * (2 * p.act_cols) + p.act_cols + ti.col0 + cc, u);
+            }
+            uint32_t a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gc = fminf(__uint_as_float(g[i]), c);
+              const float uc = fminf(fmaxf(__uint_as_float(u[i]), -c), c);
+              const float sg = 1.0f / (1.0f + __expf(-gc));
+              a[i] = __float_as_uint(gc * sg * uc);
+            }
+            store_row32(p.out + row * p.ld_out + ti.col0 + cc, a);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 32) {
+          if (ti.col0 + cc >= p.out_cols) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(taddr + cc, r);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint16_t* dst = (MODE == GMM_DW)
+                ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out + row * p.ld_out + ti.col0 + cc
+                : p.out + row * p.ld_out + ti.col0 + cc;
+            store_row32(dst, r);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty[acc]));
+      ++local;
+    }
+  }
+
+  __syncthreads();
+  if (sm->abort && tid == 0) set_status(p.status, MOE_ERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor [rows, cols] row-major; box = 64 columns x box_rows rows, 128B swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 tensor [E, K, N] row-major; box = 64 (n) x box_k (k) x 1 (e), 128B swizzle.
+bool make_map_3d(CUtensorMap* m, const void* base, int64_t E, int64_t K, int64_t N, int box_k) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(K) * N * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_k), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, bool SWIGLU>
+moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s) {
+  auto kern = gmm_kernel<MODE, SWIGLU>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured_dev = dev;
+  }
+  kern<<<num_sms(), NUM_THREADS, kSmemBytes, s>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
+                        int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s) {
+  // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
+  GmmParams p{};
+  p.group_list = group_list;
+  p.E = static_cast<int>(E);
+  p.rows_cap = M;
+  p.status = status;
+  p.out = out;
+  p.h_save = h_save;
+  p.clip = clip > 0.0f ? clip : INFINITY;
+  CUtensorMap ta, tb;
+  if (mode == GMM_FWD) {
+    const bool sw = (epilogue == MOE_EPILOGUE_SWIGLU);
+    p.out_cols = static_cast<int>(sw ? N / 2 : N);
+    p.ld_out = p.out_cols;
+    p.act_cols = static_cast<int>(N / 2);
+    p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
+    p.kblocks = static_cast<int>(K / BK);
+    if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
+    return sw ? launch_mode<GMM_FWD, true>(ta, tb, p, s) : launch_mode<GMM_FWD, false>(ta, tb, p, s);
+  }
+  if (mode == GMM_DX) {
+    p.out_cols = static_cast<int>(K);
+    p.ld_out = K;
+    p.tile_cols = static_cast<int>((K + BN - 1) / BN);
+    p.kblocks = static_cast<int>(N / BK);
+    if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
+    return launch_mode<GMM_DX, false>(ta, tb, p, s);
+  }
+  p.out_rows = static_cast<int>(K);
+  p.out_cols = static_cast<int>(N);
+  p.ld_out = N;
+  p.tile_cols = static_cast<int>((N + BN - 1) / BN);
+  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64)) return MOE_ERR_CUDA;
+  return launch_mode<GMM_DW, false>(ta, tb, p, s);
+}
+
+}  // namespace moe

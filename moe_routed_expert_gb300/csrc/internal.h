@@ -1,0 +1,41 @@
+// Internal launchers shared by the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe_gmm.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 64;
+
+// Workspace layout: [status block | op scratch ...], every piece 256-byte aligned.
+inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+int num_sms();  // SM count of the current device (cached per device)
+
+// ---- dispatch (permute.cu)
+size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E);
+moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
+                            uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
+                            uint32_t* status, void* scratch, cudaStream_t s);
+
+// ---- combine side (combine.cu)
+moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
+                              int64_t T, int64_t H, int64_t k, uint16_t* y, uint32_t* status, cudaStream_t s);
+moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_id_map,
+                                       const float* topk_w, int64_t T, int64_t H, int64_t k,
+                                       uint16_t* dy_perm, float* dprobs, uint32_t* status, cudaStream_t s);
+moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
+                                    uint16_t* dh, cudaStream_t s);
+
+// ---- grouped matmul (gmm.cu)
+enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
+moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
+                        int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,242 @@
+// Token permute (dispatch): device histogram, exclusive scan and stable
+// counting-sort scatter, then a row gather.
+//
+// "NPU Training Operators - GMM", section "算子语义": tokens must be laid out
+// expert-contiguous with group_list holding the rows per expert (permute +
+// histc in "Qwen3.5 MoE 路径"); "MegaMoE", EP Dispatch: each (token i, slot k)
+// owns one row row(i,k) of its expert's block, rows stacked in a fixed order.
+// The order used here is ascending flat slot f = t*k + j within an expert.
+//
+// Kernels (four launches, no host sync):
+//   count   one block per chunk of 1024 slots: shared-memory histogram,
+//           written as chunk_counts[e][chunk]; ids outside [-1, E) raise
+//           MOE_ERR_DEVICE and are skipped.
+//   scan    one block: per expert (one warp each) exclusive scan over chunks,
+//           block scan over experts -> group_list and each chunk's first row.
+//   rank    one block per chunk; each of its 8 warps owns 128 consecutive
+//           slots.  Per-warp expert counts -> per-warp base rows; then every
+//           32-slot step ranks equal ids with __match_any_sync, which keeps
+//           the flat order (stable).  Writes row_id_map and sorted_flat.
+//   gather  warp per (slot, 2 KB segment of the row), in slot order so the k
+//           copies of one token read it once from HBM: x_perm[row] = x[t].
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int CHUNK = 1024;          // slots per block (count and rank)
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;  // 8
+constexpr int SUB = CHUNK / WARPS;   // 128 slots per warp in the rank kernel
+
+__global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* __restrict__ ids, int64_t nslots,
+                                                                int E, int nchunks, int32_t* __restrict__ chunk_counts,
+                                                                uint32_t* status) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += THREADS) hist[e] = 0;
+  __syncthreads();
+  const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
+  for (int i = threadIdx.x; i < CHUNK; i += THREADS) {
+    const int64_t f = f0 + i;
+    if (f < nslots) {
+      const int e = ids[f];
+      if (e < -1 || e >= E) set_status(status, MOE_ERR_DEVICE);
+      else if (e >= 0) atomicAdd(&hist[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += THREADS)
+    chunk_counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
+}
+
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int E, int nchunks, int64_t nslots,
+                                                            int32_t* __restrict__ chunk_counts,
+                                                            int64_t* __restrict__ group_list,
+                                                            int32_t* __restrict__ sorted_flat) {
+  __shared__ int32_t total[kMaxExperts];
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t R_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 1) per expert: exclusive scan of its chunk counts (in place), total rows
+  for (int e = warp; e < E; e += 32) {
+    int32_t* row = chunk_counts + static_cast<int64_t>(e) * nchunks;
+    int32_t run = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int32_t v = c < nchunks ? row[c] : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      if (c < nchunks) row[c] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) total[e] = run;
+  }
+  __syncthreads();
+  // 2) exclusive scan over experts (E <= 1024 = one element per thread)
+  const int e = threadIdx.x;
+  const int32_t v = e < E ? total[e] : 0;
+  int32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t w = warp_sum[lane];
+    int32_t wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += o;
+    }
+    warp_sum[lane] = wi - w;
+    if (lane == 31) R_sh = wi;
+  }
+  __syncthreads();
+  const int32_t off = warp_sum[warp] + incl - v;
+  if (e < E) {
+    group_list[e] = v;
+    total[e] = off;
+  }
+  __syncthreads();
+  // 3) chunk bases become absolute first rows
+  for (int ee = warp; ee < E; ee += 32) {
+    int32_t* row = chunk_counts + static_cast<int64_t>(ee) * nchunks;
+    const int32_t base = total[ee];
+    for (int c = lane; c < nchunks; c += 32) row[c] += base;
+  }
+  // 4) rows past R own no slot
+  for (int64_t r = R_sh + threadIdx.x; r < nslots; r += 1024) sorted_flat[r] = -1;
+}
+
+__global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __restrict__ ids, int64_t nslots,
+                                                               int E, int nchunks,
+                                                               const int32_t* __restrict__ chunk_base,
+                                                               int32_t* __restrict__ row_id_map,
+                                                               int32_t* __restrict__ sorted_flat) {
+  extern __shared__ int32_t wbase[];  // [WARPS][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < WARPS * E; i += THREADS) wbase[i] = 0;
+  __syncthreads();
+  const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK + warp * SUB;
+  int32_t* mine = wbase + warp * E;
+  // per-warp counts
+#pragma unroll 1
+  for (int step = 0; step < SUB / 32; ++step) {
+    const int64_t f = f0 + step * 32 + lane;
+    int e = f < nslots ? ids[f] : -1;
+    if (e < -1 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+  }
+  __syncthreads();
+  // per-expert scan over the warps of this chunk, starting at the chunk's first row
+  for (int e = threadIdx.x; e < E; e += THREADS) {
+    int32_t run = chunk_base[static_cast<int64_t>(e) * nchunks + blockIdx.x];
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const int32_t c = wbase[w * E + e];
+      wbase[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int step = 0; step < SUB / 32; ++step) {
+    const int64_t f = f0 + step * 32 + lane;
+    int e = f < nslots ? ids[f] : -1;
+    if (e < -1 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int32_t row = mine[e] + __popc(peers & lt);
+      row_id_map[f] = row;
+      sorted_flat[row] = static_cast<int32_t>(f);
+    } else if (f < nslots) {
+      row_id_map[f] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+constexpr int SEG = 1024;  // bf16 elements per warp item (2 KB)
+
+__global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t* __restrict__ x, int64_t nslots,
+                                                                 int64_t H, int k,
+                                                                 const int32_t* __restrict__ row_id_map,
+                                                                 uint16_t* __restrict__ x_perm) {
+  const int64_t nseg = (H + SEG - 1) / SEG;
+  const int64_t items = nslots * nseg;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
+  for (int64_t item = gw; item < items; item += nw) {
+    const int64_t f = item / nseg;
+    const int64_t seg = item - f * nseg;
+    const int32_t row = row_id_map[f];
+    if (row < 0) continue;
+    const int64_t t = f / k;
+    const uint16_t* src = x + t * H + seg * SEG;
+    uint16_t* dst = x_perm + static_cast<int64_t>(row) * H + seg * SEG;
+    const int64_t n = (H - seg * SEG) < SEG ? (H - seg * SEG) : static_cast<int64_t>(SEG);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = (u * 32 + lane) * 8;
+      if (c < n) v[u] = ld_nc_v4(src + c);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = (u * 32 + lane) * 8;
+      if (c < n) *reinterpret_cast<uint4*>(dst + c) = v[u];
+    }
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E) {
+  const int64_t nslots = T * k;
+  const int64_t nchunks = (nslots + CHUNK - 1) / CHUNK;
+  return align256(static_cast<size_t>(nchunks * E) * sizeof(int32_t));
+}
+
+moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
+                            uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
+                            uint32_t* status, void* scratch, cudaStream_t s) {
+  const int64_t nslots = T * k;
+  const int nchunks = static_cast<int>((nslots + CHUNK - 1) / CHUNK);
+  int32_t* chunk_counts = static_cast<int32_t*>(scratch);
+  const int e = static_cast<int>(E);
+  permute_count_kernel<<<nchunks, THREADS, e * sizeof(int32_t), s>>>(ids, nslots, e, nchunks, chunk_counts, status);
+  permute_scan_kernel<<<1, 1024, 0, s>>>(e, nchunks, nslots, chunk_counts, group_list, sorted_flat);
+  const size_t rank_smem = static_cast<size_t>(WARPS) * e * sizeof(int32_t);
+  permute_rank_kernel<<<nchunks, THREADS, rank_smem, s>>>(ids, nslots, e, nchunks, chunk_counts, row_id_map,
+                                                          sorted_flat);
+  if (x != nullptr && x_perm != nullptr && H > 0) {
+    const int64_t items = nslots * ((H + SEG - 1) / SEG);
+    const int64_t warps_needed = items;
+    int64_t blocks = (warps_needed + WARPS - 1) / WARPS;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    permute_gather_kernel<<<static_cast<unsigned>(blocks), THREADS, 0, s>>>(x, nslots, H, static_cast<int>(k),
+                                                                           row_id_map, x_perm);
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,107 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+entry point include/moe_gmm.h declares, and rejects bad arguments on the host
+before anything reaches a GPU (no call here launches a kernel)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    import moe_routed_expert_gb300 as M
+    return M.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for n in ("gmm_forward", "gmm_backward", "moe_permute", "moe_unpermute", "moe_layer_forward",
+              "moe_layer_backward", "moe_unpermute_backward", "moe_permute_backward", "moe_swiglu_backward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import subprocess
+    from moe_routed_expert_gb300 import _abi
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.lib_path()], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+    # nothing else leaks out of the library's C++ internals
+    assert all(not e.startswith("_ZN3moe") for e in exported)
+    assert set(_abi.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in {0: "MOE_OK", 1: "MOE_ERR_NULLPTR", 2: "MOE_ERR_INVALID", 3: "MOE_ERR_UNSUPPORTED",
+                       4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT"}.items():
+        assert lib.moe_status_string(code).decode() == name
+
+
+def test_workspace_sizes(lib):
+    assert lib.gmm_workspace_size(8192, 1024, 2048, 8) == 256
+    assert lib.moe_unpermute_workspace_size() == 256
+    # permute: status block + per-chunk counts (1024 slots per chunk, int32 per expert)
+    assert lib.moe_permute_workspace_size(4096, 8, 256) == 256 + 32 * 256 * 4
+    assert lib.moe_permute_workspace_size(0, 8, 256) == 256
+    T, H, I, E, k = 4096, 2048, 512, 256, 8
+    n = lib.moe_layer_workspace_size(T, H, I, E, k)
+    R = T * k
+    assert n >= 256 + R * H * 2 * 2 + R * I * 2 + 2 * R * 4 + E * 8
+    assert n % 256 == 0
+
+
+FAKE = C.c_void_p(0x10000)   # never dereferenced: every call below fails its host checks first
+MIS = C.c_void_p(0x10008)    # 8-byte aligned, not 16
+
+
+def test_null_and_invalid_arguments_fail_on_the_host(lib):
+    ws, nws = FAKE, 1 << 20
+    # required pointer missing
+    assert lib.gmm_forward(None, FAKE, FAKE, 64, 128, 256, 4, 0, 0.0, FAKE, None, ws, nws, None) == 1
+    assert lib.moe_permute(FAKE, None, 4, 64, 2, 4, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 1
+    assert lib.moe_permute(None, FAKE, 4, 64, 2, 4, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 1  # x without x_perm
+    assert lib.moe_unpermute(FAKE, None, FAKE, 4, 64, 2, FAKE, ws, nws, None) == 1
+    assert lib.moe_layer_backward(FAKE, FAKE, FAKE, FAKE, None, 4, 64, 128, 4, 2, 0.0, FAKE, FAKE, FAKE, FAKE,
+                                  ws, nws, None) == 1
+    # sizes
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 100, 256, 4, 0, 0.0, FAKE, None, ws, nws, None) == 3  # K % 64
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 2000, 0, 0.0, FAKE, None, ws, nws, None) == 3  # E
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, -1, 128, 256, 4, 0, 0.0, FAKE, None, ws, nws, None) == 2
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 192, 4, 1, 0.0, FAKE, None, ws, nws, None) == 3  # SwiGLU N
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 4, 7, 0.0, FAKE, None, ws, nws, None) == 3  # epilogue
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 4, 1, -1.0, FAKE, None, ws, nws, None) == 2  # clip < 0
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 4, 1, float("nan"), FAKE, None, ws, nws, None) == 2
+    assert lib.moe_permute(FAKE, FAKE, 4, 64, 5, 4, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2  # k > E
+    assert lib.moe_permute(FAKE, FAKE, 4, 64, 65, 100, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 3  # k > 64
+    assert lib.moe_layer_forward(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 96, 4, 2, 0.0, FAKE, None, ws, nws,
+                                 None) == 3  # I % 128
+    # alignment and workspace size
+    assert lib.gmm_forward(MIS, FAKE, FAKE, 64, 128, 256, 4, 0, 0.0, FAKE, None, ws, nws, None) == 2
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 4, 0, 0.0, FAKE, None, ws, 16, None) == 2
+    assert lib.gmm_forward(FAKE, FAKE, FAKE, 64, 128, 256, 4, 0, 0.0, FAKE, None, None, nws, None) == 1
+    assert lib.moe_permute(FAKE, FAKE, 4096, 64, 8, 256, FAKE, FAKE, FAKE, FAKE, ws, 256, None) == 2
+    assert lib.moe_workspace_init(None, 256, None) == 1
+    assert lib.moe_workspace_init(FAKE, 16, None) == 2
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    import moe_routed_expert_gb300 as M
+    x = torch.zeros(64, 128, dtype=torch.bfloat16)
+    w = torch.zeros(4, 128, 256, dtype=torch.bfloat16)
+    gl = torch.tensor([16, 16, 0, 32])
+    with pytest.raises((ValueError, RuntimeError)):
+        M.gmm_forward(x, w, gl)

@@ -1,0 +1,145 @@
+"""Parity of the tcgen05 grouped matmul (forward, SwiGLU epilogue, dX, dW)
+with the oracle, elementwise within the pages' bf16 tolerance, over ragged
+groups (empty groups, groups shorter than a tile, rows past the group sum),
+sizes that span several tiles with partial edges, and the workload shapes."""
+import numpy as np
+import pytest
+
+import oracle as O
+from tests._util import assert_close, dev, dev_bf16, f64, host_f64
+from workloads import WORKLOADS, gmm_inputs, normal_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def counts_with_empties(rng, E, M, n_empty):
+    c = np.zeros(E, np.int64)
+    live = rng.permutation(E)[n_empty:]
+    cuts = np.sort(rng.integers(0, M + 1, size=len(live) - 1))
+    c[live] = np.diff(np.concatenate([[0], cuts, [M]]))
+    return c
+
+
+def gpu_forward(x, w, gl, epilogue=0, clip=0.0, want_h=False):
+    import torch
+    import moe_routed_expert_gb300 as M
+    ws = M.Workspace(256)
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    h = torch.empty(x.shape[0], w.shape[2], dtype=torch.bfloat16, device="cuda") if want_h else None
+    y = M.gmm_forward(xd, wd, dev(gl), epilogue=epilogue, clip=clip, h_save=h, ws=ws)
+    assert M.read_status(ws) == 0
+    return y, h
+
+
+@pytest.mark.parametrize("M_,K,N,E,n_empty,seed", [
+    (64, 128, 256, 4, 1, 0),       # one tile, one empty group
+    (300, 192, 320, 5, 2, 1),      # partial row tiles, N not a multiple of 256, K = 3 blocks
+    (1000, 256, 512, 9, 3, 2),     # many short groups
+    (2500, 512, 768, 3, 0, 3),     # long groups, 3 column tiles
+    (129, 64, 64, 1, 0, 4),        # single expert, one row past a tile
+])
+def test_forward_ragged(M_, K, N, E, n_empty, seed):
+    rng = np.random.default_rng(seed)
+    gl = counts_with_empties(rng, E, M_, n_empty)
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (E, K, N), 1 / np.sqrt(K))
+    y, _ = gpu_forward(x, w, gl)
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+
+
+def test_forward_rows_past_the_group_sum_are_untouched():
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(9)
+    E, K, N, M_ = 3, 128, 256, 200
+    gl = np.array([50, 0, 90], np.int64)     # sum 140 < 200 rows in the buffer
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (E, K, N), 1 / np.sqrt(K))
+    y = torch.full((M_, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = M.Workspace(256)
+    M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), y=y, ws=ws)
+    assert M.read_status(ws) == 0
+    assert_close("y", y[:140], O.gmm_forward(f64(x[:140]), f64(w), gl))
+    assert torch.all(y[140:] == 7.0)
+
+
+@pytest.mark.parametrize("clip", [0.0, 1.5])
+def test_forward_swiglu_epilogue(clip):
+    rng = np.random.default_rng(11)
+    E, K, I, M_ = 6, 256, 384, 777
+    gl = counts_with_empties(rng, E, M_, 2)
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (E, K, 2 * I), 2 / np.sqrt(K))
+    a, h = gpu_forward(x, w, gl, epilogue=1, clip=clip, want_h=True)
+    h_o = O.gmm_forward(f64(x), f64(w), gl)
+    assert_close("h", h, h_o)
+    # the activation is taken on the stored bf16 H: compare on the GPU's own H too
+    assert_close("a(own h)", a, O.swiglu(host_f64(h), clip))
+    assert_close("a", a, O.swiglu(h_o, clip))
+
+
+def test_workload_gmm_tiny_e4():
+    wl = WORKLOADS["gmm_tiny_e4"]
+    inp = gmm_inputs(wl)
+    assert inp["group_list"][2] == 0 and inp["group_list"].sum() == wl.M
+    y, _ = gpu_forward(inp["x"], inp["w"], inp["group_list"])
+    assert_close("y", y, O.gmm_forward(f64(inp["x"]), f64(inp["w"]), inp["group_list"]))
+
+
+def gpu_backward(x, w, gl, dy):
+    import moe_routed_expert_gb300 as M
+    ws = M.Workspace(256)
+    dx, dw = M.gmm_backward(dev_bf16(x), dev_bf16(w), dev(gl), dev_bf16(dy), ws=ws)
+    assert M.read_status(ws) == 0
+    return dx, dw
+
+
+@pytest.mark.parametrize("M_,K,N,E,n_empty,seed", [
+    (64, 128, 256, 4, 1, 20),
+    (300, 192, 320, 5, 2, 21),     # dW row tile past K, columns past N, partial 64-row blocks
+    (1000, 256, 512, 9, 3, 22),
+    (2500, 512, 768, 3, 0, 23),
+])
+def test_backward_ragged(M_, K, N, E, n_empty, seed):
+    rng = np.random.default_rng(seed)
+    gl = counts_with_empties(rng, E, M_, n_empty)
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (E, K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    dx, dw = gpu_backward(x, w, gl, dy)
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw", dw, dw_o)
+    for e in np.flatnonzero(gl == 0):
+        assert np.all(host_f64(dw[e]) == 0)
+
+
+def test_workload_gmm_zipf_e8():
+    wl = WORKLOADS["gmm_zipf_e8"]
+    inp = gmm_inputs(wl)
+    gl = inp["group_list"]
+    assert (gl == 0).sum() == 2 and gl.sum() == wl.M
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    y, _ = gpu_forward(x, w, gl)
+    dx, dw = gpu_backward(x, w, gl, dy)
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw", dw, dw_o)
+
+
+@pytest.mark.parametrize("bad", ["negative", "too_many_rows"])
+def test_bad_group_list_raises_device_status(bad):
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(3)
+    x = normal_bf16(rng, (64, 128))
+    w = normal_bf16(rng, (4, 128, 256))
+    gl = np.array([32, -1, 16, 16]) if bad == "negative" else np.array([32, 32, 16, 16])
+    ws = M.Workspace(256)
+    y = torch.zeros(64, 256, dtype=torch.bfloat16, device="cuda")
+    M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), y=y, ws=ws)
+    assert M.read_status(ws) == 5
+    assert torch.all(y == 0)   # nothing was computed
+    ws.reset()
+    assert M.read_status(ws) == 0

@@ -1,0 +1,589 @@
+"""Benchmark of the routed-expert MoE hot path on GB300.
+
+Default workload: the MoE layer training step (T=16384 tokens, hidden 4096,
+64 experts, top-8, intermediate 1024, SwiGLU clip 7, one hot expert): permute,
+gate_up GMM with the SwiGLU epilogue, down GMM, weighted combine, then the
+whole backward (combine gradients, dX and dW of both GMMs, SwiGLU gradient,
+token gradient).  One step = one forward + backward over one batch.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                        [--impl reference]
+
+Prints one JSON line.  ``value`` is tokens/s of the whole job with inputs
+resident in HBM, timed with CUDA events on the launching stream between a
+barrier + synchronize on both sides (max over ranks); ``e2e`` is the same
+metric through the public layer entry points with host (pinned) inputs and
+outputs copied inside the timed region.  Under torchrun every rank runs its
+own replica (the layer shards by batch with no data-path exchange), so the
+scaling is weak.  ``--impl reference`` times the CPU oracle on a bounded
+token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import WORKLOADS, gmm_inputs, layer_inputs  # noqa: E402
+
+METRIC = "GMM fwd+bwd TFLOP/s and MoE-layer tokens/s on 1 GB300; % of bf16 peak / HBM BW"
+DEFAULT_WORKLOAD = "layer_train_t16384"
+
+
+# ---------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % self.gpu)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def bf16_dev(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+# ---------------------------------------------------------------------------- GPU steps
+class LayerTrainStep:
+    """Forward + backward of the routed-expert layer, as the sequence of C-ABI
+    calls the layer entry points make (so each GMM launch can be timed)."""
+
+    def __init__(self, wl, dev, inp):
+        import torch
+        import moe_routed_expert_gb300 as M
+        self.M, self.wl, self.dev = M, wl, dev
+        T, H, E, k, I = wl.T, wl.H, wl.E, wl.k, wl.I
+        R = T * k
+        self.x = bf16_dev(inp["x"], dev)
+        self.w1 = bf16_dev(inp["w1"], dev)
+        self.w2 = bf16_dev(inp["w2"], dev)
+        self.dy = bf16_dev(inp["dy"], dev)
+        self.ids = torch.from_numpy(inp["topk_ids"]).to(dev)
+        self.tw = torch.from_numpy(inp["topk_w"]).to(dev)
+        self.saved = M.LayerSaved(T, H, I, E, k, dev)
+        bf = torch.bfloat16
+        self.y = torch.empty(T, H, dtype=bf, device=dev)
+        self.dy2 = torch.empty(R, H, dtype=bf, device=dev)
+        self.da = torch.empty(R, I, dtype=bf, device=dev)
+        self.dh = torch.empty(R, 2 * I, dtype=bf, device=dev)
+        self.dx = torch.empty(T, H, dtype=bf, device=dev)
+        self.dw1 = torch.empty_like(self.w1)
+        self.dw2 = torch.empty_like(self.w2)
+        self.dprobs = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.ws = M.Workspace(max(M.moe_permute_workspace_size(T, k, E), M.moe_layer_workspace_size(T, H, I, E, k)),
+                              dev)
+        gl = inp["topk_ids"]
+        counts = np.bincount(gl[gl >= 0].ravel(), minlength=E)
+        Rr = int(counts.sum())
+        f_up, f_dn = 2.0 * Rr * H * 2 * I, 2.0 * Rr * I * H
+        self.stages = [
+            ("permute", self.permute, 0.0, 4),
+            ("gmm_fwd_gate_up_swiglu", self.gmm1, f_up, 1),
+            ("gmm_fwd_down", self.gmm2, f_dn, 1),
+            ("combine", self.combine, 0.0, 1),
+            ("combine_bwd", self.combine_bwd, 0.0, 1),
+            ("gmm_dx_down", self.dx_down, f_dn, 1),
+            ("gmm_dw_down", self.dw_down, f_dn, 1),
+            ("swiglu_bwd", self.swiglu_bwd, 0.0, 1),
+            ("gmm_dx_gate_up", self.dx_up, f_up, 1),
+            ("gmm_dw_gate_up", self.dw_up, f_up, 1),
+            ("permute_bwd", self.permute_bwd, 0.0, 1),
+        ]
+        self.units = T  # tokens per step
+        self.unit = "tokens/s"
+
+    def permute(self):
+        s = self.saved
+        self.M.moe_permute(self.x, self.ids, self.wl.E, out=(s.x_perm, s.group_list, s.row_id_map, s.sorted_flat),
+                           ws=self.ws)
+
+    def gmm1(self):
+        s = self.saved
+        self.M.gmm_forward(s.x_perm, self.w1, s.group_list, epilogue=1, clip=self.wl.clip, y=s.a, h_save=s.h,
+                           ws=self.ws)
+
+    def gmm2(self):
+        s = self.saved
+        self.M.gmm_forward(s.a, self.w2, s.group_list, y=s.y2, ws=self.ws)
+
+    def combine(self):
+        s = self.saved
+        self.M.moe_unpermute(s.y2, s.row_id_map, self.tw, self.wl.T, self.wl.k, y=self.y, ws=self.ws)
+
+    def combine_bwd(self):
+        s = self.saved
+        self.M.moe_unpermute_backward(self.dy, s.y2, s.row_id_map, self.tw, self.wl.k, dy_perm=self.dy2,
+                                      dprobs=self.dprobs, ws=self.ws)
+
+    def dx_down(self):
+        s = self.saved
+        self.M.gmm_backward(s.a, self.w2, s.group_list, self.dy2, need_dw=False, dx=self.da, ws=self.ws)
+
+    def dw_down(self):
+        s = self.saved
+        self.M.gmm_backward(s.a, self.w2, s.group_list, self.dy2, need_dx=False, dw=self.dw2, ws=self.ws)
+
+    def swiglu_bwd(self):
+        self.M.moe_swiglu_backward(self.saved.h, self.da, self.wl.clip, dh=self.dh, ws=self.ws)
+
+    def dx_up(self):
+        s = self.saved
+        # dx_perm reuses the dY2 buffer, as the layer entry point does
+        self.M.gmm_backward(s.x_perm, self.w1, s.group_list, self.dh, need_dw=False, dx=self.dy2, ws=self.ws)
+
+    def dw_up(self):
+        s = self.saved
+        self.M.gmm_backward(s.x_perm, self.w1, s.group_list, self.dh, need_dx=False, dw=self.dw1, ws=self.ws)
+
+    def permute_bwd(self):
+        self.M.moe_permute_backward(self.dy2, self.saved.row_id_map, self.wl.T, self.wl.k, dx=self.dx, ws=self.ws)
+
+    # public-API step with host buffers, for e2e
+    def e2e_setup(self, inp):
+        import torch
+        self.h_x = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.h_dy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.h_ids = torch.from_numpy(inp["topk_ids"]).pin_memory()
+        self.h_tw = torch.from_numpy(inp["topk_w"]).pin_memory()
+        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+        self.h_dx = torch.empty(self.dx.shape, dtype=self.dx.dtype).pin_memory()
+        self.h_dprobs = torch.empty(self.dprobs.shape, dtype=self.dprobs.dtype).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_dy, self.h_ids, self.h_tw))
+        self.d2h = sum(t.numel() * t.element_size() for t in (self.h_y, self.h_dx, self.h_dprobs))
+        self.e2e_launches = 4 + 2 + 1 + 1 + 4 + 1 + 1
+
+    def e2e_step(self):
+        M, wl = self.M, self.wl
+        self.x.copy_(self.h_x, non_blocking=True)
+        self.dy.copy_(self.h_dy, non_blocking=True)
+        self.ids.copy_(self.h_ids, non_blocking=True)
+        self.tw.copy_(self.h_tw, non_blocking=True)
+        M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, wl.clip, saved=self.saved, y=self.y,
+                            ws=self.ws)
+        M.moe_layer_backward(self.dy, self.tw, self.w1, self.w2, self.saved, wl.clip, dx=self.dx, dw1=self.dw1,
+                             dw2=self.dw2, dprobs=self.dprobs, ws=self.ws)
+        self.h_y.copy_(self.y, non_blocking=True)
+        self.h_dx.copy_(self.dx, non_blocking=True)
+        self.h_dprobs.copy_(self.dprobs, non_blocking=True)
+
+
+class LayerFwdStep(LayerTrainStep):
+    """Forward only (prefill / decode layer workloads)."""
+
+    def __init__(self, wl, dev, inp):
+        inp = dict(inp)
+        inp["dy"] = inp["x"]
+        super().__init__(wl, dev, inp)
+        self.stages = self.stages[:4]
+        # algorithmic bytes of the GMMs: weights of non-empty experts + activations in/out once
+        ids = inp["topk_ids"]
+        counts = np.bincount(ids[ids >= 0].ravel(), minlength=wl.E)
+        live = int((counts > 0).sum())
+        R = int(counts.sum())
+        H, I = wl.H, wl.I
+        self.gmm_bytes = {"gmm_fwd_gate_up_swiglu": live * H * 2 * I * 2 + R * H * 2 + R * I * 2,
+                          "gmm_fwd_down": live * I * H * 2 + R * I * 2 + R * H * 2}
+
+    def e2e_step(self):
+        M, wl = self.M, self.wl
+        self.x.copy_(self.h_x, non_blocking=True)
+        self.ids.copy_(self.h_ids, non_blocking=True)
+        self.tw.copy_(self.h_tw, non_blocking=True)
+        M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, wl.clip, y=self.y, ws=self.ws)
+        self.h_y.copy_(self.y, non_blocking=True)
+
+    def e2e_setup(self, inp):
+        super().e2e_setup(inp)
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_ids, self.h_tw))
+        self.d2h = self.h_y.numel() * self.h_y.element_size()
+        self.e2e_launches = 4 + 2 + 1
+
+
+class GmmStep:
+    """Standalone grouped matmul forward + dX + dW (the Zipf GMM workload)."""
+
+    def __init__(self, wl, dev, inp):
+        import torch
+        import moe_routed_expert_gb300 as M
+        self.M, self.wl = M, wl
+        self.x = bf16_dev(inp["x"], dev)
+        self.w = bf16_dev(inp["w"], dev)
+        self.dyv = bf16_dev(inp["dy"], dev) if "dy" in inp else None
+        self.gl = torch.from_numpy(inp["group_list"]).to(dev)
+        self.y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty_like(self.x)
+        self.dw = torch.empty_like(self.w)
+        self.ws = M.Workspace(256, dev)
+        f = 2.0 * wl.M * wl.K * wl.N
+        self.stages = [("gmm_fwd", self.fwd, f, 1)]
+        if wl.backward:
+            self.stages += [("gmm_dx", self.bdx, f, 1), ("gmm_dw", self.bdw, f, 1)]
+        self.units = sum(s[2] for s in self.stages) / 1e12
+        self.unit = "TFLOP/s"
+
+    def fwd(self):
+        self.M.gmm_forward(self.x, self.w, self.gl, y=self.y, ws=self.ws)
+
+    def bdx(self):
+        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, need_dw=False, dx=self.dx, ws=self.ws)
+
+    def bdw(self):
+        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, need_dx=False, dw=self.dw, ws=self.ws)
+
+    def e2e_setup(self, inp):
+        import torch
+        self.h_x = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.h_dy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.h_y = torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory()
+        self.h_dx = torch.empty(self.dx.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d = 2 * (self.h_x.numel() + self.h_dy.numel())
+        self.d2h = 2 * (self.h_y.numel() + self.h_dx.numel())
+        self.e2e_launches = 3
+
+    def e2e_step(self):
+        self.x.copy_(self.h_x, non_blocking=True)
+        self.dyv.copy_(self.h_dy, non_blocking=True)
+        self.M.gmm_forward(self.x, self.w, self.gl, y=self.y, ws=self.ws)
+        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, dx=self.dx, dw=self.dw, ws=self.ws)
+        self.h_y.copy_(self.y, non_blocking=True)
+        self.h_dx.copy_(self.dx, non_blocking=True)
+
+
+def make_step(name, dev, tokens=None):
+    wl = WORKLOADS[name]
+    if name.startswith("gmm"):
+        inp = gmm_inputs(wl)
+        return GmmStep(wl, dev, inp), inp
+    inp = layer_inputs(wl, tokens=tokens)
+    if tokens is not None:   # a smaller batch of the same workload (profiling captures)
+        wl = wl.with_tokens(tokens)
+    return (LayerTrainStep(wl, dev, inp) if wl.backward else LayerFwdStep(wl, dev, inp)), inp
+
+
+# ---------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_layer_step(wl, inp_sub):
+    import oracle as O
+    f = O.bf16_bits_to_f64
+    x, w1, w2 = f(inp_sub["x"]), f(inp_sub["w1"]), f(inp_sub["w2"])
+    y, sv = O.moe_layer_forward(x, inp_sub["topk_ids"], inp_sub["topk_w"], w1, w2, wl.clip)
+    if wl.backward:
+        O.moe_layer_backward(f(inp_sub["dy"]), sv, inp_sub["topk_w"], w1, w2, wl.clip)
+
+
+def layer_sample(inp, T, E):
+    """The first T tokens, with only the slots routed to experts 0..E-1 kept (the
+    rest marked unused) and only those experts' weights: every kept expert does
+    exactly the work it does in the full problem over those tokens."""
+    d = {}
+    ids = np.ascontiguousarray(inp["topk_ids"][:T]).copy()
+    ids[ids >= E] = -1
+    d["topk_ids"] = ids
+    for key in ("x", "topk_w", "dy"):
+        if key in inp:
+            d[key] = np.ascontiguousarray(inp[key][:T])
+    d["w1"], d["w2"] = inp["w1"][:E], inp["w2"][:E]
+    return d, int((ids >= 0).sum())
+
+
+def oracle_gmm_step(wl, inp, rows):
+    import oracle as O
+    f = O.bf16_bits_to_f64
+    gl = inp["group_list"].copy()
+    # keep the first `rows` rows: trim the groups from the end
+    left = rows
+    for e in range(len(gl)):
+        take = min(gl[e], left)
+        gl[e] = take
+        left -= take
+    x, w = f(inp["x"][:rows]), f(inp["w"])
+    O.gmm_forward(x, w, gl)
+    if wl.backward:
+        O.gmm_backward(x, w, gl, f(inp["dy"][:rows]))
+
+
+def cpu_sample(name, inp, target_s=15.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload.
+    Returns (value, unit, sample description, seconds, runner) where runner()
+    repeats the same sample and value is the sample's work per second."""
+    wl = WORKLOADS[name]
+    if name.startswith("gmm"):
+        per_row = (3 if wl.backward else 1) * 2.0 * wl.K * wl.N / 1e12
+        rows = min(wl.M, 512)
+        t0 = time.perf_counter(); oracle_gmm_step(wl, inp, rows); dt = time.perf_counter() - t0
+        if dt < target_s / 3 and rows < wl.M:
+            rows = int(min(wl.M, rows * max(1.0, target_s / max(dt, 1e-3))))
+            t0 = time.perf_counter(); oracle_gmm_step(wl, inp, rows); dt = time.perf_counter() - t0
+        desc = "first %d of %d rows (groups trimmed from the end), fwd%s" % (rows, wl.M, "+dX+dW" if wl.backward else "")
+        return rows * per_row / dt, "TFLOP/s", desc, dt, (lambda: oracle_gmm_step(wl, inp, rows)), rows * per_row
+    # token-equivalents: a token owns k routed rows
+    E_s = max(1, wl.E // 8)
+    T_s = max(1, wl.T // 8)
+    sub, rows = layer_sample(inp, T_s, E_s)
+    t0 = time.perf_counter(); oracle_layer_step(wl, sub); dt = time.perf_counter() - t0
+    if dt < target_s / 3 and T_s < wl.T:
+        T_s = int(min(wl.T, T_s * max(1.0, target_s / max(dt, 1e-3))))
+        sub, rows = layer_sample(inp, T_s, E_s)
+        t0 = time.perf_counter(); oracle_layer_step(wl, sub); dt = time.perf_counter() - t0
+    tok_eq = rows / wl.k
+    desc = ("first %d of %d tokens, slots of experts 0..%d of %d kept (%d routed rows = %.0f token-equivalents "
+            "at k=%d), layer fwd%s in float64" % (T_s, wl.T, E_s - 1, wl.E, rows, tok_eq, wl.k,
+                                                  "+bwd" if wl.backward else ""))
+    return tok_eq / dt, "tokens/s", desc, dt, (lambda: oracle_layer_step(wl, sub)), tok_eq
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name = args.workload
+    wl = WORKLOADS[name]
+    inp = gmm_inputs(wl) if name.startswith("gmm") else layer_inputs(wl)
+    # one bounded sample per step, sized so the whole run stays within a few minutes
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    _, unit, sample, _, fn, units = cpu_sample(name, inp, target_s=per_step)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        fn()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    v = units * len(times) / total
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the first T tokens of the layer workload (smaller captures; not a bench line)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import moe_routed_expert_gb300 as M
+
+    step, inp = make_step(args.workload, dev, args.tokens)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # the sampler starts before the warm-up: nvidia-smi's start-up must not land in the timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        for _, fn, _, _ in step.stages:
+            fn()
+    assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
+
+    ns = len(step.stages)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        ev = events[s]
+        ev[0].record(stream)
+        for i, (_, fn, _, _) in enumerate(step.stages):
+            fn()
+            ev[i + 1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
+
+    stage_ms = [0.0] * ns
+    for s in range(args.steps):
+        for i in range(ns):
+            stage_ms[i] += events[s][i].elapsed_time(events[s][i + 1])
+    stage_ms = [v / args.steps for v in stage_ms]
+    ms_per_step = elapsed_ms / args.steps
+    value = step.units * world / (ms_per_step / 1e3)
+
+    kernels = {}
+    gmm_flops, gmm_ms, gmm_launches = 0.0, 0.0, 0
+    launches = 0
+    for (name, _, flops, nl), ms in zip(step.stages, stage_ms):
+        entry = {"ms": round(ms, 4), "launches": nl}
+        if flops:
+            entry["tflops"] = round(flops / (ms / 1e3) / 1e12, 1)
+            gmm_flops += flops
+            gmm_ms += ms
+            gmm_launches += nl
+        launches += nl
+        kernels[name] = entry
+
+    hbm_bound = hasattr(step, "gmm_bytes")
+    if hbm_bound:
+        gbytes = sum(step.gmm_bytes.values())
+        achieved = gbytes / (gmm_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "gmm_kernel (all GMM launches of a step)", "peak_kind": "hbm copy, %s" % peaks["source"]}
+    else:
+        achieved = gmm_flops / (gmm_ms / 1e3) / 1e12
+        long_step = ms_per_step * args.steps > 500.0
+        peak = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "gmm_kernel (all %d GMM launches of a step)" % gmm_launches,
+                "peak_kind": "bf16 dense %s, %s" % ("sustained" if long_step else "burst", peaks["source"])}
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": step.unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, **{k_: v_ for k_, v_ in vars(step.wl).items() if k_ != "name"},
+                       "l2": "inputs larger than L2" if args.workload != "layer_decode_t64"
+                       else "weights (1.4 GB touched) larger than L2", "parallelism": "replicas" if world > 1 else "1 GPU"},
+            "roofline": roof, "kernels": kernels, "gpu_launches": launches * args.steps,
+            "gmm_tflops": round(gmm_flops / (gmm_ms / 1e3) / 1e12, 1) if gmm_ms else None}
+    if clock_info is not None:
+        line["clocks"] = clock_info
+
+    # end to end through the public entry points, host buffers, copies inside the timed region
+    if not args.no_e2e:
+        step.e2e_setup(inp)
+        for _ in range(2):
+            step.e2e_step()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step.e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        line["e2e"] = {"value": round(step.units * world / (e_ms / args.steps / 1e3), 3), "unit": step.unit,
+                       "h2d_bytes_per_step": int(step.h2d), "d2h_bytes_per_step": int(step.d2h),
+                       "ms_per_step": round(e_ms / args.steps, 4), "api": "moe_layer_forward/backward"
+                       if not args.workload.startswith("gmm") else "gmm_forward/gmm_backward"}
+        assert M.read_status(step.ws) == 0
+
+    if args.tokens is not None:
+        line["config"]["note"] = "first %d tokens only: a profiling run, not the workload's bench line" % args.tokens
+    if rank == 0 and not args.no_cpu_baseline:
+        v, unit, sample, secs, _, _ = cpu_sample(args.workload, inp)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample, "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

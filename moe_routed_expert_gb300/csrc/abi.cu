@@ -112,8 +112,9 @@ size_t moe_permute_workspace_size(int64_t T, int64_t k, int64_t E) {
 moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k, int64_t E,
                          moe_bf16* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!topk_ids || !group_list || !row_id_map || !sorted_flat) return MOE_ERR_NULLPTR;
-  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_NULLPTR;
+  if (!group_list) return MOE_ERR_NULLPTR;
+  if (T != 0 && (!topk_ids || !row_id_map || !sorted_flat)) return MOE_ERR_NULLPTR;  // T == 0: nothing to read or write
+  if (T != 0 && (x == nullptr) != (x_perm == nullptr)) return MOE_ERR_NULLPTR;
   if (E <= 0 || k > E) return MOE_ERR_INVALID;
   if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   moe_status_t st = check_tokens(T, x ? H : 8, k);

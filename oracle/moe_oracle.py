@@ -83,26 +83,32 @@ def round_to_bf16(v):
     bfloat16 has float32's 8-bit exponent and 8 significant bits.  A value
     v = m * 2**e (0.5 <= |m| < 1) lies on a grid of spacing 2**(e-8); below the
     normal range (2**-126) the grid spacing stays 2**-133 (subnormals).
-    Results of magnitude 2**128 or more overflow to +-inf.
+    Results of magnitude 2**128 or more overflow to +-inf; inf and nan pass
+    through unchanged.  Works through the array in chunks of 2**20 values.
     """
     v = np.asarray(v, dtype=np.float64)
-    out = v.copy()
-    fin = np.isfinite(v)
-    if not np.any(fin):
-        return out
-    vf = v[fin]
-    _, e = np.frexp(vf)
-    q = np.maximum(e.astype(np.int64) - 8, -133)
-    r = np.ldexp(np.round(np.ldexp(vf, -q)), q)  # np.round: half to even
-    r = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, vf), r)
-    out[fin] = r
-    return out
+    out = np.empty_like(v)
+    src, dst = v.reshape(-1), out.reshape(-1)
+    step = 1 << 20
+    with np.errstate(invalid="ignore", over="ignore"):
+        for s in range(0, src.size, step):
+            c = src[s:s + step]
+            _, e = np.frexp(c)
+            q = np.maximum(e - 8, -133)
+            r = np.ldexp(np.round(np.ldexp(c, -q)), q)  # np.round: half to even
+            dst[s:s + step] = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, c), r)
+    return out if v.ndim else out[()]
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:
-    """Raw bfloat16 bits (uint16) -> float64 values."""
-    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    """Raw bfloat16 bits (uint16) -> float64 values (exact)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, np.float64)
+    src, dst = b.reshape(-1), out.reshape(-1)
+    step = 1 << 22
+    for s in range(0, src.size, step):
+        dst[s:s + step] = (src[s:s + step].astype(np.uint32) << 16).view(np.float32)
+    return out
 
 
 def f64_to_bf16_bits(v) -> np.ndarray:
@@ -217,8 +223,8 @@ def gmm_forward(x, w, group_list, store=round_to_bf16):
     for g in range(w.shape[0]):
         s, e = off[g], off[g + 1]
         if e > s:
-            y[s:e] = x[s:e] @ w[g]
-    return _store(store, y)
+            y[s:e] = _store(store, x[s:e] @ w[g])
+    return y
 
 
 def gmm_backward(x, w, group_list, dy, store=round_to_bf16):
@@ -233,9 +239,9 @@ def gmm_backward(x, w, group_list, dy, store=round_to_bf16):
     for g in range(w.shape[0]):
         s, e = off[g], off[g + 1]
         if e > s:
-            dx[s:e] = dy[s:e] @ w[g].T
-            dw[g] = x[s:e].T @ dy[s:e]
-    return _store(store, dx), _store(store, dw)
+            dx[s:e] = _store(store, dy[s:e] @ w[g].T)
+            dw[g] = _store(store, x[s:e].T @ dy[s:e])
+    return dx, dw
 
 
 # --------------------------------------------------------------------------

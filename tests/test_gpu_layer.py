@@ -35,7 +35,15 @@ def gpu_layer(inp, wl, backward, want_saved=False):
     return out
 
 
-def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None):
+def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None, gpu_saved=None, steps=True):
+    """Oracle on the whole problem, on a token subset, or on the sub-problem that
+    keeps only expert ``keep_expert``'s slots.
+
+    With ``gpu_saved`` (host copies of the GPU's saved x_perm, h, a, y2 and its
+    row_id_map) the backward starts from the GPU's stored forward tensors: a
+    bf16 store is a rounding decision, and each side must take it in the same
+    precision (the kernel's fp32 accumulation).  Every forward step is checked
+    separately against the oracle on the GPU's own input to that step."""
     ids = inp["topk_ids"]
     sel = slice(None) if tokens is None else tokens
     ids = ids[sel].copy()
@@ -45,10 +53,104 @@ def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None):
     w1, w2 = wf if wf is not None else (f64(inp["w1"]), f64(inp["w2"]))
     y, sv = O.moe_layer_forward(x, ids, tw, w1, w2, wl.clip)
     out = {"y": y, "saved": sv}
+    if gpu_saved is not None:
+        # rows of this (sub-)problem -> rows of the GPU's full problem
+        T, k = ids.shape
+        orig_tok = np.arange(inp["topk_ids"].shape[0])[sel]
+        flat_sub = sv["sorted_flat"].astype(np.int64)
+        flat_full = orig_tok[flat_sub // k] * k + flat_sub % k
+        grow = gpu_saved["row_id_map"][flat_full].astype(np.int64)
+        sv = dict(sv)
+        for key in ("h", "a", "y2"):
+            sv[key] = f64(gpu_saved[key][grow])
+        out["gpu_rows"] = grow
+        out["steps"] = {} if not steps else {
+            "h": (sv["h"], O.gmm_forward(sv["x_perm"], w1, sv["group_list"])),
+            "a": (sv["a"], O.swiglu(sv["h"], wl.clip)),
+            "y2": (sv["y2"], O.gmm_forward(sv["a"], w2, sv["group_list"])),
+        }
+        out["y_steps"] = O.moe_unpermute(sv["y2"], sv["row_id_map"], tw, T, k)
     if backward:
         dx, dw1, dw2, dpr = O.moe_layer_backward(f64(inp["dy"][sel]), sv, tw, w1, w2, wl.clip)
         out.update(dx=dx, dw1=dw1, dw2=dw2, dprobs=dpr)
     return out
+
+
+def saved_to_host(saved):
+    import torch
+    bits = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return {"h": bits(saved.h), "a": bits(saved.a), "y2": bits(saved.y2), "x_perm": bits(saved.x_perm),
+            "row_id_map": saved.row_id_map.cpu().numpy(), "sorted_flat": saved.sorted_flat.cpu().numpy(),
+            "group_list": saved.group_list.cpu().numpy()}
+
+
+def check_steps(o):
+    for key, (got, want) in o["steps"].items():
+        assert_close(key, got, want)
+
+
+def gpu_chain_backward(saved, dy, tw, w1, w2, clip, T, k):
+    """The backward as the chain of individual C-ABI calls on the saved tensors."""
+    import moe_routed_expert_gb300 as M
+    ws = M.Workspace(256)
+    c = {}
+    c["dy2"], c["dprobs"] = M.moe_unpermute_backward(dy, saved.y2, saved.row_id_map, tw, k, ws=ws)
+    c["da"], c["dw2"] = M.gmm_backward(saved.a, w2, saved.group_list, c["dy2"], ws=ws)
+    c["dh"] = M.moe_swiglu_backward(saved.h, c["da"], clip, ws=ws)
+    c["dxp"], c["dw1"] = M.gmm_backward(saved.x_perm, w1, saved.group_list, c["dh"], ws=ws)
+    c["dx"] = M.moe_permute_backward(c["dxp"], saved.row_id_map, T, k, ws=ws)
+    assert M.read_status(ws) == 0
+    return c
+
+
+def check_layer_equals_chain(g, chain):
+    """The layer entry point launches the same kernels in the same order: bit-identical."""
+    import torch
+    for key in ("dx", "dw1", "dw2", "dprobs"):
+        assert torch.equal(g[key], chain[key]), key
+
+
+def check_chain_ops(inp, wl, gs, chain, experts=None, tokens=None):
+    """Each op of the backward chain against the oracle on that op's own inputs
+    (the GPU's previous-step output).  Whole problem by default; at full size,
+    the given experts (every row and the whole dW) and tokens."""
+    T, k = wl.T, wl.k
+    gl = gs["group_list"]
+    off = np.concatenate([[0], np.cumsum(gl)])
+    w1_bits, w2_bits = inp["w1"], inp["w2"]
+    hb = {key: chain[key].cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+          for key in ("dy2", "da", "dh", "dxp")}
+    hb.update({"h": gs["h"], "a": gs["a"], "y2": gs["y2"], "x_perm": gs["x_perm"]})
+    exps = range(wl.E) if experts is None else experts
+    dw1, dw2 = host_f64(chain["dw1"]), host_f64(chain["dw2"])
+    for e in exps:
+        s, t = int(off[e]), int(off[e + 1])
+        if t == s:
+            assert np.all(dw1[e] == 0) and np.all(dw2[e] == 0)
+            continue
+        W1, W2 = f64(w1_bits[e:e + 1]), f64(w2_bits[e:e + 1])
+        n = [t - s]
+        da_o, dw2_o = O.gmm_backward(f64(hb["a"][s:t]), W2, n, f64(hb["dy2"][s:t]))
+        assert_close("da[e=%d]" % e, f64(hb["da"][s:t]), da_o)
+        assert_close("dw2[e=%d]" % e, dw2[e], dw2_o[0])
+        assert_close("dh[e=%d]" % e, f64(hb["dh"][s:t]), O.swiglu_backward(f64(hb["h"][s:t]), f64(hb["da"][s:t]), wl.clip))
+        dxp_o, dw1_o = O.gmm_backward(f64(hb["x_perm"][s:t]), W1, n, f64(hb["dh"][s:t]))
+        assert_close("dx_perm[e=%d]" % e, f64(hb["dxp"][s:t]), dxp_o)
+        assert_close("dw1[e=%d]" % e, dw1[e], dw1_o[0])
+    # per-token ops: combine gradients and the token gradient
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    rmap = gs["row_id_map"].reshape(T, k)[toks]
+    sub = rmap.reshape(-1)
+    used = sub[sub >= 0]
+    # rows of the selected tokens, renumbered 0..n-1 in slot order
+    local = np.full(sub.shape, -1, np.int32)
+    local[sub >= 0] = np.arange(len(used), dtype=np.int32)
+    dy = f64(inp["dy"][toks])
+    dy2_o, dpr_o = O.moe_unpermute_backward(dy, f64(hb["y2"][used]), local, inp["topk_w"][toks], len(toks), k)
+    assert_close("dy2[tokens]", f64(hb["dy2"][used]), dy2_o)
+    assert_close("dprobs[tokens]", host_f64(chain["dprobs"])[toks], dpr_o)
+    assert_close("dx[tokens]", host_f64(chain["dx"])[toks],
+                 O.moe_permute_backward(f64(hb["dxp"][used]), local, len(toks), k))
 
 
 SMALL = [
@@ -65,16 +167,24 @@ def test_layer_small_every_output(wl):
         inp["topk_ids"][::5, -1] = -1
         inp["topk_ids"][inp["topk_ids"] == 3] = -1
     g = gpu_layer(inp, wl, backward=True)
-    o = oracle_layer(inp, wl, backward=True)
-    sv, so = g["saved"], o["saved"]
+    gs = saved_to_host(g["saved"])
+    o = oracle_layer(inp, wl, backward=True, gpu_saved=gs)
+    so = o["saved"]
     R = int(so["group_list"].sum())
-    np.testing.assert_array_equal(sv.group_list.cpu().numpy(), so["group_list"])
-    np.testing.assert_array_equal(sv.row_id_map.cpu().numpy(), so["row_id_map"])
-    assert_close("h", host_f64(sv.h)[:R], so["h"])
-    assert_close("a", host_f64(sv.a)[:R], so["a"])
-    assert_close("y2", host_f64(sv.y2)[:R], so["y2"])
-    for key in ("y", "dx", "dw1", "dw2", "dprobs"):
-        assert_close(key, g[key], o[key])
+    np.testing.assert_array_equal(gs["group_list"], so["group_list"])
+    np.testing.assert_array_equal(gs["row_id_map"], so["row_id_map"])
+    np.testing.assert_array_equal(gs["sorted_flat"][:R], so["sorted_flat"])
+    np.testing.assert_array_equal(f64(gs["x_perm"][:R]), so["x_perm"])
+    check_steps(o)
+    assert_close("y", g["y"], o["y_steps"])
+    # shallow outputs (sums over the k slots of a token) also end to end
+    o_pure = oracle_layer(inp, wl, backward=True)
+    for key in ("y", "dx", "dprobs"):
+        assert_close(key + " (end to end)", g[key], o_pure[key])
+    chain = gpu_chain_backward(g["saved"], dev_bf16(inp["dy"]), dev(inp["topk_w"]), dev_bf16(inp["w1"]),
+                               dev_bf16(inp["w2"]), wl.clip, wl.T, wl.k)
+    check_layer_equals_chain(g, chain)
+    check_chain_ops(inp, wl, gs, chain)
 
 
 @pytest.mark.parametrize("name", ["layer_decode_t64", "layer_prefill_t4096"])
@@ -82,34 +192,48 @@ def test_layer_forward_workloads_every_output(name):
     wl = WORKLOADS[name]
     inp = layer_inputs(wl)
     g = gpu_layer(inp, wl, backward=False, want_saved=True)
-    o = oracle_layer(inp, wl, backward=False)
-    np.testing.assert_array_equal(g["saved"].group_list.cpu().numpy(), o["saved"]["group_list"])
-    assert_close("y", g["y"], o["y"])
+    gs = saved_to_host(g["saved"])
+    o = oracle_layer(inp, wl, backward=False, gpu_saved=gs)
+    np.testing.assert_array_equal(gs["group_list"], o["saved"]["group_list"])
+    np.testing.assert_array_equal(gs["row_id_map"], o["saved"]["row_id_map"])
+    check_steps(o)
+    assert_close("y", g["y"], o["y_steps"])
+    # inference mode (nothing saved) gives the same y bit for bit
+    g2 = gpu_layer(inp, wl, backward=False)
+    assert np.array_equal(host_f64(g2["y"]), host_f64(g["y"]))
 
 
 def test_layer_train_t16384_sampled():
     wl = WORKLOADS["layer_train_t16384"]
     inp = layer_inputs(wl)
     g = gpu_layer(inp, wl, backward=True)
-    sv = g["saved"]
+    gs = saved_to_host(g["saved"])
     # integer outputs: exact, whole problem
     rmap_o, sflat_o, counts_o, _ = O.stable_counting_sort(inp["topk_ids"], wl.E)
-    np.testing.assert_array_equal(sv.group_list.cpu().numpy(), counts_o)
-    np.testing.assert_array_equal(sv.row_id_map.cpu().numpy(), rmap_o)
-    np.testing.assert_array_equal(sv.sorted_flat.cpu().numpy(), sflat_o)
+    np.testing.assert_array_equal(gs["group_list"], counts_o)
+    np.testing.assert_array_equal(gs["row_id_map"], rmap_o)
+    np.testing.assert_array_equal(gs["sorted_flat"], sflat_o)
     # sampled tokens
     rng = np.random.default_rng(123)
     toks = np.sort(rng.choice(wl.T, size=48, replace=False))
-    toks = np.concatenate([[0, wl.T - 1], toks])
+    toks = np.unique(np.concatenate([[0, wl.T - 1], toks]))
     wf = (f64(inp["w1"]), f64(inp["w2"]))
-    o = oracle_layer(inp, wl, backward=True, tokens=toks, wf=wf)
-    for key in ("y", "dx", "dprobs"):
+    o = oracle_layer(inp, wl, backward=True, tokens=toks, wf=wf, gpu_saved=gs)
+    np.testing.assert_array_equal(f64(gs["x_perm"][o["gpu_rows"]]), o["saved"]["x_perm"])
+    check_steps(o)
+    assert_close("y[tokens]", host_f64(g["y"])[toks], o["y_steps"])
+    for key in ("dx", "dprobs"):
         assert_close(key + "[tokens]", host_f64(g[key])[toks], o[key])
-    # sampled experts: the hot one, and two others
+    # end to end (oracle from the inputs alone) for the outputs that only sum a
+    # token's k slots; dprobs is a 4096-long dot product with dy and is checked
+    # on the GPU's own y2 above
+    o_pure = oracle_layer(inp, wl, backward=True, tokens=toks, wf=wf)
+    for key in ("y", "dx"):
+        assert_close(key + "[tokens] (end to end)", host_f64(g[key])[toks], o_pure[key])
+    # backward: the layer equals the chain of single ops, each op checked on its own inputs
+    chain = gpu_chain_backward(g["saved"], dev_bf16(inp["dy"]), dev(inp["topk_w"]), dev_bf16(inp["w1"]),
+                               dev_bf16(inp["w2"]), wl.clip, wl.T, wl.k)
+    check_layer_equals_chain(g, chain)
     hot = inp["hot_expert"]
-    others = [e for e in rng.permutation(wl.E) if e != hot][:2]
-    dw1, dw2 = host_f64(g["dw1"]), host_f64(g["dw2"])
-    for e in [hot] + others:
-        oe = oracle_layer(inp, wl, backward=True, keep_expert=e, wf=wf)
-        assert_close("dw1[%d]" % e, dw1[e], oe["dw1"][e])
-        assert_close("dw2[%d]" % e, dw2[e], oe["dw2"][e])
+    others = [int(e) for e in rng.permutation(wl.E) if e != hot][:2]
+    check_chain_ops(inp, wl, gs, chain, experts=[hot] + others, tokens=toks)

@@ -116,6 +116,29 @@ MOE_API moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids,
                          int32_t* row_id_map, int32_t* sorted_flat,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The same permute for callers that cannot allocate device memory, and so
+ * cannot supply a workspace: code running where cudaMalloc is not allowed
+ * (a host framework whose allocator owns all device memory, a plugin or
+ * embedded runtime with a fixed memory budget, a path that must not wait on
+ * the driver's allocator).  The pages have no counterpart to this entry point;
+ * it exists for those callers.
+ *
+ * Same arguments, outputs and results as moe_permute, with no workspace:
+ *   device_status  NULL, or a device word the caller owns and zeroes; bad ids
+ *                  set it to MOE_ERR_DEVICE (sticky, like the workspace word).
+ * Scratch: one fixed device array inside the library, 512 KiB of int32
+ * counters, held by every device that loads the library until the process
+ * exits.  Sizes with ceil(T*k / 1024) * E > 131072 return MOE_ERR_UNSUPPORTED.
+ * The first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture.  It calls
+ * no allocator.  All calls share the array, so calls whose kernels overlap on
+ * the GPU race: order them on one stream. */
+MOE_API moe_status_t moe_permute_no_alloc(const moe_bf16* x, const int32_t* topk_ids,
+                         int64_t T, int64_t H, int64_t k, int64_t E,
+                         moe_bf16* x_perm, int64_t* group_list,
+                         int32_t* row_id_map, int32_t* sorted_flat,
+                         uint32_t* device_status, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- grouped matmul */
 
 /* Workspace bytes for gmm_forward / gmm_backward. */

@@ -34,6 +34,7 @@ SIGNATURES = {
     "moe_status_string": (C.c_char_p, [ST]),
     "moe_permute_workspace_size": (SZ, [I64, I64, I64]),
     "moe_permute": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, SZ, P]),
+    "moe_permute_no_alloc": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, P]),
     "gmm_workspace_size": (SZ, [I64, I64, I64, I64]),
     "gmm_forward": (ST, [P, P, P, I64, I64, I64, I64, INT, F32, P, P, P, SZ, P]),
     "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),

@@ -132,6 +132,29 @@ def moe_permute(x: Optional[torch.Tensor], topk_ids: torch.Tensor, E: int, *, ou
     return x_perm, group_list, row_id_map, sorted_flat
 
 
+def moe_permute_no_alloc(x: Optional[torch.Tensor], topk_ids: torch.Tensor, E: int, *, out=None,
+                         device_status: Optional[torch.Tensor] = None, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory (the library's fixed internal scratch is used instead; see the C
+    header for its size limit and for the rule that overlapping calls race).
+    Outputs are allocated here only when ``out`` is not given."""
+    _dtype(x, BF16, "x")
+    _dtype(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    H = x.shape[1] if x is not None else 0
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(T * k, H, dtype=BF16, device=dev) if x is not None else None,
+               torch.empty(E, dtype=torch.int64, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev))
+    x_perm, group_list, row_id_map, sorted_flat = out
+    _check(_lib().moe_permute_no_alloc(_ptr(x), _ptr(topk_ids), T, H, k, E, _ptr(x_perm), _ptr(group_list),
+                                       _ptr(row_id_map), _ptr(sorted_flat), _ptr(device_status), _stream(stream)),
+           "moe_permute_no_alloc")
+    return x_perm, group_list, row_id_map, sorted_flat
+
+
 # ------------------------------------------------------------------ grouped matmul
 def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, epilogue: int = 0,
                 clip: float = 0.0, y: Optional[torch.Tensor] = None, h_save: Optional[torch.Tensor] = None,

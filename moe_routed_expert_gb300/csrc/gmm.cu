@@ -35,8 +35,6 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -307,8 +305,43 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
       }
     }
+  } else if (warp == 1 && MODE != GMM_DW) {
+    // ---------------------------------------------------------------- MMA issuer (one thread)
+    if (lane == 0) {
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+        const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = stage_base + s * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
+                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm->empty[s]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm->tmem_full[acc]));
+        ++local;
+      }
+      if (!ok) {
+        tc_commit(smem_u32(&sm->drain));
+        drain_wait(smem_u32(&sm->drain), 0);
+      }
+    }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- MMA issuer for dW (whole warp: it zeroes rows)
     uint32_t it = 0, local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -445,45 +478,6 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 2D bf16 tensor [rows, cols] row-major; box = 64 columns x box_rows rows, 128B swizzle.
-bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3D bf16 tensor [E, K, N] row-major; box = 64 (n) x box_k (k) x 1 (e), 128B swizzle.
-bool make_map_3d(CUtensorMap* m, const void* base, int64_t E, int64_t K, int64_t N, int box_k) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(K) * N * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_k), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int MODE, bool SWIGLU>
 moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s) {
   auto kern = gmm_kernel<MODE, SWIGLU>;
@@ -505,6 +499,11 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s) {
   // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
+  // Forward and dX go to CTA pairs (256-row tiles) when groups average at
+  // least 512 rows; below that the extra padding of a 256-row tile costs more
+  // than the pair saves, and the 128-row kernel here runs instead.
+  if (mode != GMM_DW && M >= kPairMinRowsPerGroup * E)
+    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, s);
   GmmParams p{};
   p.group_list = group_list;
   p.E = static_cast<int>(E);

@@ -1,0 +1,482 @@
+// Grouped matmul forward and input gradient on CTA pairs (tcgen05 cta_group::2).
+//
+// Same operation as gmm.cu ("NPU Training Operators - GMM", section "算子语义":
+// y_g = x_g @ W_g and dx_g = dy_g @ W_g^T over the rows of each group, with the
+// optional clipped SwiGLU of "MegaMoE", "激活函数公式", in the gate_up epilogue),
+// laid out for GB300's paired SMs:
+//
+//   * a cluster of two CTAs owns a 256 x 256 output tile; CTA r loads rows
+//     [128r, 128r+128) of A and columns [128r, 128r+128) of B (32 KB per 64-deep
+//     stage instead of 48 KB), and one thread of the even CTA issues
+//     tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads both CTAs'
+//     shared memory and writes each CTA's 128 rows into its own TMEM;
+//   * both CTAs' TMA copies complete on the even CTA's stage barrier;
+//     tcgen05.commit multicasts the stage release and the accumulator-ready
+//     signal to both CTAs; both epilogues release the accumulator on the even
+//     CTA's barrier;
+//   * 5 stages of 32 KB; two 256-column fp32 accumulators (all 512 TMEM columns);
+//   * the epilogue stages each warp's 32 rows x 128 columns as bf16 in
+//     shared memory (XOR-swizzled 16-byte chunks, conflict-free) and writes
+//     them back two full rows per warp instruction (coalesced), masking rows
+//     past the group end and columns past N.
+// Group offsets are read on the device as in gmm.cu; tiles are visited column
+// tile fastest.  Every mbarrier wait is bounded; a timeout stops all roles,
+// waits for copies in flight, frees TMEM and writes MOE_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                         // rows per CTA (256 per pair)
+constexpr int BN = 256;                         // accumulator columns
+constexpr int BNH = 128;                        // B columns held by each CTA
+constexpr int BK = 64;
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BNH * BK * 2;           // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
+constexpr int BOX_BYTES = 64 * 64 * 2;
+constexpr int EPI_ROW_BYTES = 256;              // 128 bf16 columns
+constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;   // 32 KB
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+
+struct PairParams {
+  const int64_t* group_list;
+  int E;
+  int64_t rows_cap;
+  int out_cols;     // output columns (FWD: N or I; DX: K)
+  int tile_cols;    // column tiles
+  int kblocks;      // contraction blocks of 64
+  uint16_t* out;
+  int64_t ld_out;
+  uint16_t* h_save;
+  int act_cols;     // SwiGLU: I
+  float clip;
+  uint32_t* status;
+};
+
+struct __align__(16) PairSmem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+  int32_t bad;
+  int32_t ntiles;
+  int64_t grp_off[kMaxExperts + 1];
+  int32_t grp_cnt[kMaxExperts];
+  int32_t tile_start[kMaxExperts + 1];
+};
+
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + sizeof(PairSmem);
+
+struct PairTile {
+  int g;
+  int64_t row0;     // first row of this CTA's half
+  int rows_valid;   // rows of this CTA's half inside the group (may be <= 0)
+  int col0;         // first output column (SwiGLU: first activation column)
+};
+
+template <bool SWIGLU>
+__device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int t, uint32_t rank) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int local = t - sm->tile_start[lo];
+  const int rt = local / p.tile_cols;
+  const int ct = local - rt * p.tile_cols;
+  PairTile ti;
+  ti.g = lo;
+  const int first = rt * (2 * BM) + static_cast<int>(rank) * BM;
+  ti.row0 = sm->grp_off[lo] + first;
+  ti.rows_valid = min(BM, sm->grp_cnt[lo] - first);
+  ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
+  return ti;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  uint32_t dummy = 0;
+  mbar_wait_bounded(bar, parity, &dummy, 200000000ull);
+}
+
+// 32 fp32 accumulator columns of this thread's row -> bf16 -> 4 swizzled
+// 16-byte chunks (chunk index c0 .. c0+3) of this thread's staging row.
+__device__ __forceinline__ void stage_chunk(uint8_t* ebuf, int lane, int c0, const uint32_t (&r)[32]) {
+  uint8_t* row = ebuf + lane * EPI_ROW_BYTES;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 q;
+    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+    const int c = (c0 + v) ^ (lane & 7);
+    *reinterpret_cast<uint4*>(row + c * 16) = q;
+  }
+}
+
+// Write the warp's staged 32 rows x 128 columns: two rows per instruction,
+// 16 lanes x 16 bytes per row.  Rows >= rows_valid and columns >= ncols are skipped.
+__device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16_t* base, int64_t ld, int rows_valid,
+                                           int ncols) {
+  const int j = lane & 15;
+  const int half = lane >> 4;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int row = 2 * i + half;
+    const uint4 v = *reinterpret_cast<const uint4*>(ebuf + row * EPI_ROW_BYTES + ((j ^ (row & 7)) * 16));
+    if (row < rows_valid && j * 8 < ncols) *reinterpret_cast<uint4*>(base + row * ld + j * 8) = v;
+  }
+}
+
+template <int MODE, bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PairParams p) {
+  constexpr bool B_MN = (MODE == GMM_FWD);
+  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, false, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ebuf_all = smem + STAGES * STAGE_BYTES;
+  PairSmem* sm = reinterpret_cast<PairSmem*>(ebuf_all + EPI_BYTES);
+  const uint32_t stage_base = smem_u32(smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(nclusters_x());
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    sm->bad = 0;
+    sm->abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sm->tmem_full[a]), 1);
+      mbar_init(smem_u32(&sm->tmem_empty[a]), 8);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += NUM_THREADS) {
+    const int64_t c = p.group_list[e];
+    if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
+    sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int64_t rows = 0;
+    int32_t tiles = 0;
+    for (int e = lo; e < hi; ++e) {
+      rows += sm->grp_cnt[e];
+      tiles += ((sm->grp_cnt[e] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+    }
+    int64_t rows_incl = rows;
+    int32_t tiles_incl = tiles;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t r2 = __shfl_up_sync(0xffffffffu, rows_incl, d);
+      const int32_t t2 = __shfl_up_sync(0xffffffffu, tiles_incl, d);
+      if (lane >= d) { rows_incl += r2; tiles_incl += t2; }
+    }
+    int64_t rb = rows_incl - rows;
+    int32_t tb = tiles_incl - tiles;
+    for (int e = lo; e < hi; ++e) {
+      sm->grp_off[e] = rb;
+      sm->tile_start[e] = tb;
+      rb += sm->grp_cnt[e];
+      tb += ((sm->grp_cnt[e] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+    }
+    if (lane == 31) {
+      sm->grp_off[E] = rows_incl;
+      sm->tile_start[E] = tiles_incl;
+      sm->ntiles = tiles_incl;
+      if (rows_incl > p.rows_cap) sm->bad = 1;
+    }
+  }
+  __syncthreads();
+  if (sm->bad) {  // both CTAs of the pair read the same group_list and leave here together
+    if (tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy completion
+
+  const uint32_t tmem_base = sm->tmem_base;
+  const int ntiles = sm->ntiles;
+  volatile uint32_t* abort_flag = &sm->abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cid; t < ntiles && ok; t += ncl) {
+        const PairTile ti = decode_pair_tile<SWIGLU>(sm, p, t, rank);
+        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+          const uint32_t bar_local = smem_u32(&sm->full[s]);
+          const uint32_t bar = mapa_shared(bar_local, 0);  // the even CTA's stage barrier
+          if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
+          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          if (MODE == GMM_FWD) {
+#pragma unroll
+            for (int j = 0; j < BNH / 64; ++j) {
+              const int col = SWIGLU ? (rank == 0 ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * j)
+                                     : ti.col0 + static_cast<int>(rank) * BNH + 64 * j;
+              tma_load_3d_pair(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
+            }
+          } else {
+            tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, ti.col0 + static_cast<int>(rank) * BNH, ti.g);
+          }
+        }
+      }
+      // every stage this CTA filled must be released before the CTA may exit:
+      // the release is an arrival sent from the even CTA
+      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      for (uint32_t i = first; i < it; ++i) {
+        if (*abort_flag) break;
+        mbar_wait_bounded(smem_u32(&sm->empty[i % STAGES]), (i / STAGES) & 1u, abort_flag, kTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA, one thread)
+    // A single thread waits and issues: warp-wide shuffles and syncs per stage
+    // measurably delay the MMA stream.
+    if (rank == 0 && lane == 0) {
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int t = cid; t < ntiles && ok; t += ncl) {
+        const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = stage_base + s * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
+                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(smem_u32(&sm->empty[s]), 0x3);
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(smem_u32(&sm->tmem_full[acc]), 0x3);
+        ++local;
+      }
+      if (!ok) {
+        tc_commit_pair_multicast(smem_u32(&sm->drain), 0x1);
+        drain_wait(smem_u32(&sm->drain), 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    uint8_t* ebuf = ebuf_all + q * EPI_WARP_BYTES;
+    uint32_t local = 0;
+    for (int t = cid; t < ntiles; t += ncl) {
+      const PairTile ti = decode_pair_tile<SWIGLU>(sm, p, t, rank);
+      const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+      if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int rows_valid = ti.rows_valid - q * 32;  // rows of this warp's 32 that are in the group
+      const int64_t wrow0 = ti.row0 + q * 32;
+      const uint32_t release = mapa_shared(smem_u32(&sm->tmem_empty[acc]), 0);
+      auto release_tmem = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(release);
+      };
+      if (SWIGLU) {
+        const float c = p.clip;
+        const int64_t ldh = 2 * static_cast<int64_t>(p.act_cols);
+        // pass 1: the activation
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 2; cc += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + cc, g);
+          tmem_ld32(taddr + BN / 2 + cc, u);
+          tmem_ld_wait();
+          uint32_t a[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gv = round_bf16(__uint_as_float(g[i]));  // H is stored in bf16
+            const float uv = round_bf16(__uint_as_float(u[i]));
+            const float gc = fminf(gv, c);
+            const float uc = fminf(fmaxf(uv, -c), c);
+            a[i] = __float_as_uint(gc * (1.0f / (1.0f + __expf(-gc))) * uc);
+          }
+          stage_chunk(ebuf, lane, cc / 8, a);
+        }
+        if (!p.h_save) release_tmem();
+        __syncwarp();
+        flush_rows(ebuf, lane, p.out + wrow0 * p.ld_out + ti.col0, p.ld_out, rows_valid, BN / 2);
+        __syncwarp();
+        if (p.h_save) {
+          // passes 2 and 3: the bf16 pre-activation, gate then up
+#pragma unroll 1
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 2; cc += 32) {
+              uint32_t r[32];
+              tmem_ld32(taddr + part * (BN / 2) + cc, r);
+              tmem_ld_wait();
+              stage_chunk(ebuf, lane, cc / 8, r);
+            }
+            if (part == 1) release_tmem();
+            __syncwarp();
+            flush_rows(ebuf, lane, p.h_save + wrow0 * ldh + part * p.act_cols + ti.col0, ldh, rows_valid, BN / 2);
+            __syncwarp();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 2; cc += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + half * (BN / 2) + cc, r);
+            tmem_ld_wait();
+            stage_chunk(ebuf, lane, cc / 8, r);
+          }
+          if (half == 1) release_tmem();
+          __syncwarp();
+          const int col = ti.col0 + half * (BN / 2);
+          flush_rows(ebuf, lane, p.out + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
+          __syncwarp();
+        }
+      }
+      ++local;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // a timed-out pipeline may still have copies landing: give them time
+    if (tid == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+    }
+    __syncthreads();
+  }
+  cluster_sync_all();  // no arrival or copy targets either CTA past this point
+  if (*abort_flag && tid == 0) set_status(p.status, MOE_ERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE, bool SWIGLU>
+moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairParams& p, cudaStream_t s) {
+  auto kern = gmm_pair_kernel<MODE, SWIGLU>;
+  static int configured_dev = -1;
+  static int grid = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (configured_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return MOE_ERR_CUDA;
+    grid = 2 * clusters;
+    configured_dev = dev;
+  }
+  cfg.gridDim = dim3(grid, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+// FWD (optionally with the SwiGLU epilogue) and DX on CTA pairs.
+moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
+                             int64_t M, int64_t K, int64_t N, int64_t E, float clip, uint16_t* out, uint16_t* h_save,
+                             uint32_t* status, cudaStream_t s) {
+  PairParams p{};
+  p.group_list = group_list;
+  p.E = static_cast<int>(E);
+  p.rows_cap = M;
+  p.status = status;
+  p.out = out;
+  p.h_save = h_save;
+  p.clip = clip > 0.0f ? clip : INFINITY;
+  CUtensorMap ta, tb;
+  if (mode == GMM_FWD) {
+    const bool sw = (epilogue == MOE_EPILOGUE_SWIGLU);
+    p.out_cols = static_cast<int>(sw ? N / 2 : N);
+    p.ld_out = p.out_cols;
+    p.act_cols = static_cast<int>(N / 2);
+    p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
+    p.kblocks = static_cast<int>(K / BK);
+    if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
+    return sw ? launch_pair<GMM_FWD, true>(ta, tb, p, s) : launch_pair<GMM_FWD, false>(ta, tb, p, s);
+  }
+  p.out_cols = static_cast<int>(K);
+  p.ld_out = K;
+  p.tile_cols = static_cast<int>((K + BN - 1) / BN);
+  p.kblocks = static_cast<int>(N / BK);
+  if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
+  return launch_pair<GMM_DX, false>(ta, tb, p, s);
+}
+
+}  // namespace moe

@@ -7,6 +7,8 @@
 
 #include "moe_gmm.h"
 
+struct CUtensorMap_st;  // cuda.h
+
 namespace moe {
 
 constexpr int kMaxExperts = 1024;
@@ -32,8 +34,16 @@ moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_per
 moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
                                     uint16_t* dh, cudaStream_t s);
 
-// ---- grouped matmul (gmm.cu)
+// ---- TMA descriptors (tmap.cu): bf16, 128B swizzle, 64-element inner box
+bool make_map_2d(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+bool make_map_3d(::CUtensorMap_st* m, const void* base, int64_t E, int64_t K, int64_t N, int box_k);
+
+// ---- grouped matmul (gmm.cu, gmm_pair.cu)
 enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
+constexpr int64_t kPairMinRowsPerGroup = 512;
+moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
+                             int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                             uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s);
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s);

@@ -47,20 +47,67 @@ def test_forward_ragged(M_, K, N, E, n_empty, seed):
     assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
 
 
-def test_forward_rows_past_the_group_sum_are_untouched():
+# Shapes whose groups average >= 512 rows take the CTA-pair kernel (256-row
+# tiles) for forward and dX; these cases put a 1-row group, a group shorter than
+# one CTA's 128 rows, empty groups and partial column tiles on that path.
+PAIR_CASES = [
+    ([1700, 1, 130, 300], 192, 320),
+    ([2048, 0, 0, 1], 256, 512),
+    ([700, 900, 0, 600, 520], 128, 768),
+    ([4096], 1024, 256),
+]
+
+
+@pytest.mark.parametrize("counts,K,N", PAIR_CASES)
+def test_forward_and_dx_pair_path(counts, K, N):
+    rng = np.random.default_rng(sum(counts) + K)
+    gl = np.array(counts, np.int64)
+    M_ = int(gl.sum())
+    assert M_ >= 512 * len(gl)
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    y, _ = gpu_forward(x, w, gl)
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+    dx, dw = gpu_backward(x, w, gl, dy)
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw", dw, dw_o)
+
+
+@pytest.mark.parametrize("clip", [0.0, 2.0])
+def test_swiglu_epilogue_pair_path(clip):
+    rng = np.random.default_rng(17)
+    gl = np.array([1500, 3, 0, 1100], np.int64)
+    K, I = 256, 384
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, 2 * I), 2 / np.sqrt(K))
+    a, h = gpu_forward(x, w, gl, epilogue=1, clip=clip, want_h=True)
+    h_o = O.gmm_forward(f64(x), f64(w), gl)
+    assert_close("h", h, h_o)
+    assert_close("a(own h)", a, O.swiglu(host_f64(h), clip))
+    # without h_save the activation is the same, bit for bit
+    a2, _ = gpu_forward(x, w, gl, epilogue=1, clip=clip, want_h=False)
+    assert np.array_equal(host_f64(a2), host_f64(a))
+
+
+@pytest.mark.parametrize("M_,gl", [(200, [50, 0, 90]), (4000, [1500, 0, 600])])   # 128-row and pair kernels
+def test_forward_rows_past_the_group_sum_are_untouched(M_, gl):
     import torch
     import moe_routed_expert_gb300 as M
     rng = np.random.default_rng(9)
-    E, K, N, M_ = 3, 128, 256, 200
-    gl = np.array([50, 0, 90], np.int64)     # sum 140 < 200 rows in the buffer
+    E, K, N = 3, 128, 256
+    gl = np.array(gl, np.int64)     # sum below the rows in the buffer
     x = normal_bf16(rng, (M_, K))
     w = normal_bf16(rng, (E, K, N), 1 / np.sqrt(K))
     y = torch.full((M_, N), 7.0, dtype=torch.bfloat16, device="cuda")
     ws = M.Workspace(256)
     M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), y=y, ws=ws)
     assert M.read_status(ws) == 0
-    assert_close("y", y[:140], O.gmm_forward(f64(x[:140]), f64(w), gl))
-    assert torch.all(y[140:] == 7.0)
+    S = int(gl.sum())
+    assert_close("y", y[:S], O.gmm_forward(f64(x[:S]), f64(w), gl))
+    assert torch.all(y[S:] == 7.0)
 
 
 @pytest.mark.parametrize("clip", [0.0, 1.5])
@@ -128,16 +175,18 @@ def test_workload_gmm_zipf_e8():
     assert_close("dw", dw, dw_o)
 
 
-@pytest.mark.parametrize("bad", ["negative", "too_many_rows"])
-def test_bad_group_list_raises_device_status(bad):
+@pytest.mark.parametrize("bad,M_", [("negative", 64), ("too_many_rows", 64), ("negative", 4096),
+                                     ("too_many_rows", 4096)])   # 128-row kernel, then CTA pairs
+def test_bad_group_list_raises_device_status(bad, M_):
     import torch
     import moe_routed_expert_gb300 as M
     rng = np.random.default_rng(3)
-    x = normal_bf16(rng, (64, 128))
+    x = normal_bf16(rng, (M_, 128))
     w = normal_bf16(rng, (4, 128, 256))
-    gl = np.array([32, -1, 16, 16]) if bad == "negative" else np.array([32, 32, 16, 16])
+    q = M_ // 4
+    gl = np.array([2 * q, -1, q, q]) if bad == "negative" else np.array([2 * q, 2 * q, q, q])
     ws = M.Workspace(256)
-    y = torch.zeros(64, 256, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(M_, 256, dtype=torch.bfloat16, device="cuda")
     M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), y=y, ws=ws)
     assert M.read_status(ws) == 5
     assert torch.all(y == 0)   # nothing was computed

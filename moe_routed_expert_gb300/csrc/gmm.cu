@@ -499,10 +499,11 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s) {
   // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
-  // Forward and dX go to CTA pairs (256-row tiles) when groups average at
-  // least 512 rows; below that the extra padding of a 256-row tile costs more
-  // than the pair saves, and the 128-row kernel here runs instead.
-  if (mode != GMM_DW && M >= kPairMinRowsPerGroup * E)
+  // CTA pairs (256 x 256 tiles) when groups average at least 512 rows; below
+  // that the extra padding of a 256-row tile (forward, dX) and the short
+  // contractions (dW) cost more than the pair saves, and the 128-row kernel
+  // here runs instead.
+  if (M >= kPairMinRowsPerGroup * E)
     return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, s);
   GmmParams p{};
   p.group_list = group_list;

@@ -1,9 +1,11 @@
-// Grouped matmul forward and input gradient on CTA pairs (tcgen05 cta_group::2).
+// Grouped matmul on CTA pairs (tcgen05 cta_group::2): forward, input gradient
+// and weight gradient.
 //
-// Same operation as gmm.cu ("NPU Training Operators - GMM", section "算子语义":
-// y_g = x_g @ W_g and dx_g = dy_g @ W_g^T over the rows of each group, with the
-// optional clipped SwiGLU of "MegaMoE", "激活函数公式", in the gate_up epilogue),
-// laid out for GB300's paired SMs:
+// Same operations as gmm.cu ("NPU Training Operators - GMM", section "算子语义":
+// y_g = x_g @ W_g, dx_g = dy_g @ W_g^T over the rows of each group, and
+// dW_g = x_g^T @ dy_g contracted over the group's own rows, zero for an empty
+// group; the gate_up forward can end with the clipped SwiGLU of "MegaMoE",
+// "激活函数公式"), laid out for GB300's paired SMs:
 //
 //   * a cluster of two CTAs owns a 256 x 256 output tile; CTA r loads rows
 //     [128r, 128r+128) of A and columns [128r, 128r+128) of B (32 KB per 64-deep
@@ -19,6 +21,12 @@
 //     shared memory (XOR-swizzled 16-byte chunks, conflict-free) and writes
 //     them back two full rows per warp instruction (coalesced), masking rows
 //     past the group end and columns past N.
+//   * dW: a stage whose 64 contraction rows cross the group end has its copies
+//     complete on a local barrier of each CTA instead; a fixup warp in each CTA
+//     zeroes the rows past the group end (a swizzled row stays inside its own
+//     128 bytes), fences them for the tensor core, and the even CTA's fixup
+//     warp, once the odd one has reported, marks the stage full.  Groups are
+//     visited largest first so the long contractions start early.
 // Group offsets are read on the device as in gmm.cu; tiles are visited column
 // tile fastest.  Every mbarrier wait is bounded; a timeout stops all roles,
 // waits for copies in flight, frees TMEM and writes MOE_ERR_TIMEOUT.
@@ -46,14 +54,15 @@ constexpr int EPI_ROW_BYTES = 256;              // 128 bf16 columns
 constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;   // 32 KB
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;   // producer, MMA, 4 epilogue warps, dW fixup warp
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 struct PairParams {
   const int64_t* group_list;
   int E;
   int64_t rows_cap;
-  int out_cols;     // output columns (FWD: N or I; DX: K)
+  int out_rows;     // dW: rows of one expert's gradient (K)
+  int out_cols;     // output columns (FWD: N or I; DX: K; DW: N)
   int tile_cols;    // column tiles
   int kblocks;      // contraction blocks of 64
   uint16_t* out;
@@ -70,40 +79,58 @@ struct __align__(16) PairSmem {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
+  uint64_t aux[STAGES];        // dW: copies of a stage that crosses the group end
+  uint64_t peer_done[STAGES];  // dW: the odd CTA has zeroed its half of that stage
   uint32_t tmem_base;
   uint32_t abort;
   int32_t bad;
   int32_t ntiles;
   int64_t grp_off[kMaxExperts + 1];
   int32_t grp_cnt[kMaxExperts];
-  int32_t tile_start[kMaxExperts + 1];
+  int32_t order[kMaxExperts];          // visiting position -> expert id
+  int32_t tile_start[kMaxExperts + 1]; // tile prefix over visiting positions
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + sizeof(PairSmem);
 
 struct PairTile {
   int g;
-  int64_t row0;     // first row of this CTA's half
-  int rows_valid;   // rows of this CTA's half inside the group (may be <= 0)
-  int col0;         // first output column (SwiGLU: first activation column)
+  int64_t row0;     // FWD/DX: first row of this CTA's half; DW: first output row of it
+  int rows_valid;   // rows of this CTA's half that belong to the output (may be <= 0)
+  int col0;         // first output column of the pair tile (SwiGLU: first activation column)
+  int kblocks;      // contraction blocks of 64
+  int64_t m0;       // DW: first contraction row (the group's first row)
+  int depth;        // DW: contraction rows of the group
 };
 
-template <bool SWIGLU>
+template <int MODE, bool SWIGLU>
 __device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int t, uint32_t rank) {
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
   }
+  const int g = sm->order[lo];
   const int local = t - sm->tile_start[lo];
   const int rt = local / p.tile_cols;
   const int ct = local - rt * p.tile_cols;
   PairTile ti;
-  ti.g = lo;
+  ti.g = g;
   const int first = rt * (2 * BM) + static_cast<int>(rank) * BM;
-  ti.row0 = sm->grp_off[lo] + first;
-  ti.rows_valid = min(BM, sm->grp_cnt[lo] - first);
   ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
+  if (MODE == GMM_DW) {
+    ti.row0 = first;
+    ti.rows_valid = min(BM, p.out_rows - first);
+    ti.m0 = sm->grp_off[g];
+    ti.depth = sm->grp_cnt[g];
+    ti.kblocks = (ti.depth + BK - 1) / BK;
+  } else {
+    ti.row0 = sm->grp_off[g] + first;
+    ti.rows_valid = min(BM, sm->grp_cnt[g] - first);
+    ti.m0 = 0;
+    ti.depth = 0;
+    ti.kblocks = p.kblocks;
+  }
   return ti;
 }
 
@@ -111,6 +138,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   int ok = 1;
   if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Bounded wait with cluster-scope acquire: for a barrier the peer CTA arrives on.
+__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *abort = 1u;
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -151,8 +197,9 @@ __device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16
 template <int MODE, bool SWIGLU>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PairParams p) {
-  constexpr bool B_MN = (MODE == GMM_FWD);
-  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, false, B_MN);
+  constexpr bool A_MN = (MODE == GMM_DW);
+  constexpr bool B_MN = (MODE != GMM_DX);
+  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -181,6 +228,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(smem_u32(&sm->tmem_empty[a]), 8);  // 4 epilogue warps in each CTA
     }
     mbar_init(smem_u32(&sm->drain), 1);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(smem_u32(&sm->aux[st]), 1);
+      mbar_init(smem_u32(&sm->peer_done[st]), 1);
+    }
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -192,6 +243,22 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
   }
   __syncthreads();
+  if (MODE == GMM_DW) {
+    // largest group first (ties: lower id first)
+    for (int e = tid; e < E; e += NUM_THREADS) {
+      const int ce = sm->grp_cnt[e];
+      int r = 0;
+      for (int e2 = 0; e2 < E; ++e2) {
+        const int c2 = sm->grp_cnt[e2];
+        r += (c2 > ce) || (c2 == ce && e2 < e);
+      }
+      sm->order[r] = e;
+    }
+  } else {
+    for (int e = tid; e < E; e += NUM_THREADS) sm->order[e] = e;
+  }
+  __syncthreads();
+  const int dw_tiles = ((p.out_rows + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
@@ -199,7 +266,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int32_t tiles = 0;
     for (int e = lo; e < hi; ++e) {
       rows += sm->grp_cnt[e];
-      tiles += ((sm->grp_cnt[e] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+      tiles += (MODE == GMM_DW) ? dw_tiles : ((sm->grp_cnt[sm->order[e]] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
     }
     int64_t rows_incl = rows;
     int32_t tiles_incl = tiles;
@@ -215,7 +282,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       sm->grp_off[e] = rb;
       sm->tile_start[e] = tb;
       rb += sm->grp_cnt[e];
-      tb += ((sm->grp_cnt[e] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+      tb += (MODE == GMM_DW) ? dw_tiles : ((sm->grp_cnt[sm->order[e]] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
@@ -248,15 +315,39 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t it = 0;
       bool ok = true;
       for (int t = cid; t < ntiles && ok; t += ncl) {
-        const PairTile ti = decode_pair_tile<SWIGLU>(sm, p, t, rank);
-        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+        const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          if (MODE == GMM_DW) {
+            const int32_t mrow = static_cast<int32_t>(ti.m0 + static_cast<int64_t>(kb) * BK);
+            const int bcol = ti.col0 + static_cast<int>(rank) * BNH;
+            if (ti.depth - kb * BK < BK) {
+              // crosses the group end: each CTA counts its own copies, the fixup warp takes over
+              const uint32_t aux = smem_u32(&sm->aux[s]);
+              mbar_expect_tx(aux, STAGE_BYTES);
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(a_dst + i * BOX_BYTES, &tmA, aux, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
+#pragma unroll
+              for (int j = 0; j < BNH / 64; ++j) tma_load_2d(b_dst + j * BOX_BYTES, &tmB, aux, bcol + 64 * j, mrow);
+            } else {
+              const uint32_t bar_local = smem_u32(&sm->full[s]);
+              const uint32_t bar = mapa_shared(bar_local, 0);
+              if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d_pair(a_dst + i * BOX_BYTES, &tmA, bar, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
+#pragma unroll
+              for (int j = 0; j < BNH / 64; ++j) tma_load_2d_pair(b_dst + j * BOX_BYTES, &tmB, bar, bcol + 64 * j, mrow);
+            }
+            continue;
+          }
           const uint32_t bar_local = smem_u32(&sm->full[s]);
           const uint32_t bar = mapa_shared(bar_local, 0);  // the even CTA's stage barrier
           if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
-          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
-          const uint32_t b_dst = a_dst + A_BYTES;
           tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
           if (MODE == GMM_FWD) {
 #pragma unroll
@@ -286,11 +377,13 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int t = cid; t < ntiles && ok; t += ncl) {
+        const int kblocks = decode_pair_tile<MODE, SWIGLU>(sm, p, t, 0).kblocks;
+        if (kblocks == 0) continue;  // dW of an empty group: the epilogue writes zeros
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
           tc_fence_after();
@@ -298,7 +391,8 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, BOX_BYTES, 1024)
+                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
                                      : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
             tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
@@ -314,13 +408,24 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         drain_wait(smem_u32(&sm->drain), 0);
       }
     }
-  } else {
+  } else if (warp <= 5) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     uint8_t* ebuf = ebuf_all + q * EPI_WARP_BYTES;
     uint32_t local = 0;
     for (int t = cid; t < ntiles; t += ncl) {
-      const PairTile ti = decode_pair_tile<SWIGLU>(sm, p, t, rank);
+      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+      uint16_t* obase = (MODE == GMM_DW) ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out : p.out;
+      if (MODE == GMM_DW && ti.kblocks == 0) {
+        // an empty group's weight gradient is zero: one 512-byte row per instruction
+        const int rows_valid = ti.rows_valid - q * 32;
+        const int ncols = min(BN, p.out_cols - ti.col0);
+        for (int r = 0; r < 32 && r < rows_valid; ++r)
+          if (lane * 8 < ncols)
+            *reinterpret_cast<uint4*>(obase + (ti.row0 + q * 32 + r) * p.ld_out + ti.col0 + lane * 8) =
+                make_uint4(0, 0, 0, 0);
+        continue;
+      }
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
@@ -388,11 +493,48 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (half == 1) release_tmem();
           __syncwarp();
           const int col = ti.col0 + half * (BN / 2);
-          flush_rows(ebuf, lane, p.out + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
+          flush_rows(ebuf, lane, obase + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
           __syncwarp();
         }
       }
       ++local;
+    }
+  } else if (MODE == GMM_DW) {
+    // ---------------------------------------------------------------- dW fixup warp (both CTAs)
+    // For each stage that crosses a group end: wait for this CTA's copies,
+    // zero the rows past the group end, make them visible to the tensor core;
+    // the odd CTA reports to the even one, the even CTA then marks the stage full.
+    uint32_t it = 0, aux_ph = 0, peer_ph = 0;
+    bool ok = true;
+    for (int t = cid; t < ntiles && ok; t += ncl) {
+      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+        const int valid = ti.depth - kb * BK;
+        if (valid >= BK) continue;
+        const uint32_t s = it % STAGES;
+        if (!warp_wait(smem_u32(&sm->aux[s]), (aux_ph >> s) & 1u, abort_flag, lane)) { ok = false; break; }
+        aux_ph ^= 1u << s;
+        uint8_t* stage = smem + s * STAGE_BYTES;
+        constexpr int nbox = STAGE_BYTES / BOX_BYTES;
+        const int nchunk = (BK - valid) * 8;  // 16-byte chunks past the group end, per box
+        for (int i = lane; i < nbox * nchunk; i += 32) {
+          const int box = i / nchunk, c = i - box * nchunk;
+          *reinterpret_cast<uint4*>(stage + box * BOX_BYTES + valid * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (rank == 1) {
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm->peer_done[s]), 0));
+        } else {
+          int good = 1;
+          if (lane == 0) good = wait_cluster_bounded(smem_u32(&sm->peer_done[s]), (peer_ph >> s) & 1u, abort_flag);
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) { ok = false; break; }
+          peer_ph ^= 1u << s;
+          if (lane == 0) mbar_arrive(smem_u32(&sm->full[s]));
+        }
+        __syncwarp();
+      }
     }
   }
 
@@ -448,7 +590,7 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pai
 
 }  // namespace
 
-// FWD (optionally with the SwiGLU epilogue) and DX on CTA pairs.
+// FWD (optionally with the SwiGLU epilogue), DX and DW on CTA pairs.
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip, uint16_t* out, uint16_t* h_save,
                              uint32_t* status, cudaStream_t s) {
@@ -471,12 +613,21 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
     return sw ? launch_pair<GMM_FWD, true>(ta, tb, p, s) : launch_pair<GMM_FWD, false>(ta, tb, p, s);
   }
-  p.out_cols = static_cast<int>(K);
-  p.ld_out = K;
-  p.tile_cols = static_cast<int>((K + BN - 1) / BN);
-  p.kblocks = static_cast<int>(N / BK);
-  if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
-  return launch_pair<GMM_DX, false>(ta, tb, p, s);
+  if (mode == GMM_DX) {
+    p.out_cols = static_cast<int>(K);
+    p.ld_out = K;
+    p.tile_cols = static_cast<int>((K + BN - 1) / BN);
+    p.kblocks = static_cast<int>(N / BK);
+    if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
+    return launch_pair<GMM_DX, false>(ta, tb, p, s);
+  }
+  // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
+  p.out_rows = static_cast<int>(K);
+  p.out_cols = static_cast<int>(N);
+  p.ld_out = N;
+  p.tile_cols = static_cast<int>((N + BN - 1) / BN);
+  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64)) return MOE_ERR_CUDA;
+  return launch_pair<GMM_DW, false>(ta, tb, p, s);
 }
 
 }  // namespace moe

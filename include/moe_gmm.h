@@ -141,7 +141,9 @@ MOE_API moe_status_t moe_permute_no_alloc(const moe_bf16* x, const int32_t* topk
 
 /* ---------------------------------------------------------------- grouped matmul */
 
-/* Workspace bytes for gmm_forward / gmm_backward. */
+/* Workspace bytes for gmm_forward / gmm_backward: the status block plus
+ * 384 KiB in which the weight-gradient kernel rewrites its TMA descriptors
+ * for each group (six 256-byte slots for each of up to 256 CTAs). */
 MOE_API size_t gmm_workspace_size(int64_t M, int64_t K, int64_t N, int64_t E);
 
 /* Grouped matmul forward: [GMM] "算子语义", y[s:e] = x[s:e] @ w[g] for group g

@@ -129,7 +129,7 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, 
 }
 
 // ------------------------------------------------------------------ grouped matmul
-size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES; }
+size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES + kGmmScratchBytes; }
 
 moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
                          int64_t N, int64_t E, int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
@@ -147,7 +147,7 @@ moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* gr
   if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
   if (M == 0) return MOE_OK;
   return launch_gmm(GMM_FWD, epilogue, x, w, group_list, M, K, N, E, clip, y, h_save, status_of(ws),
-                    reinterpret_cast<cudaStream_t>(stream));
+                    after_status(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
@@ -166,9 +166,11 @@ moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* g
     if (dw && cudaMemsetAsync(dw, 0, static_cast<size_t>(E * K * N) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (dx && (st = launch_gmm(GMM_DX, 0, dy, w, group_list, M, K, N, E, 0.f, dx, nullptr, status_of(ws), s)) != MOE_OK)
+  if (dx && (st = launch_gmm(GMM_DX, 0, dy, w, group_list, M, K, N, E, 0.f, dx, nullptr, status_of(ws),
+                             after_status(ws), s)) != MOE_OK)
     return st;
-  if (dw && (st = launch_gmm(GMM_DW, 0, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status_of(ws), s)) != MOE_OK)
+  if (dw && (st = launch_gmm(GMM_DW, 0, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status_of(ws),
+                             after_status(ws), s)) != MOE_OK)
     return st;
   return MOE_OK;
 }
@@ -228,7 +230,7 @@ moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t 
 // ------------------------------------------------------------------ whole layer
 size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_STATUS_BYTES;
-  return MOE_STATUS_BYTES + permute_scratch_bytes(T, k, E) + layer_acts_bytes(T, H, I, E, k);
+  return MOE_STATUS_BYTES + kGmmScratchBytes + permute_scratch_bytes(T, k, E) + layer_acts_bytes(T, H, I, E, k);
 }
 
 namespace {
@@ -262,7 +264,8 @@ moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t* status = status_of(ws);
-  uint8_t* scratch = after_status(ws);
+  uint8_t* gmm_scratch = after_status(ws);
+  uint8_t* scratch = gmm_scratch + kGmmScratchBytes;
   uint8_t* acts = scratch + permute_scratch_bytes(T, k, E);
   const int64_t R = T * k;
   moe_bf16 *x_perm, *h, *a, *y2;
@@ -282,9 +285,11 @@ moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const
     h = nullptr;
   }
   if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
-  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, clip, a, h, status, s)) != MOE_OK)
+  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, clip, a, h, status, gmm_scratch,
+                       s)) != MOE_OK)
     return st;
-  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_NONE, a, w2, gl, R, I, H, E, 0.f, y2, nullptr, status, s)) != MOE_OK)
+  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_NONE, a, w2, gl, R, I, H, E, 0.f, y2, nullptr, status, gmm_scratch, s)) !=
+      MOE_OK)
     return st;
   return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
 }
@@ -308,7 +313,8 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
     return MOE_OK;
   }
   uint32_t* status = status_of(ws);
-  uint8_t* acts = after_status(ws) + permute_scratch_bytes(T, k, E);
+  uint8_t* gmm_scratch = after_status(ws);
+  uint8_t* acts = gmm_scratch + kGmmScratchBytes + permute_scratch_bytes(T, k, E);
   const int64_t R = T * k;
   moe_bf16* dy2 = reinterpret_cast<moe_bf16*>(acts);
   moe_bf16* da = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2));
@@ -317,18 +323,18 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
   if ((st = launch_unpermute_backward(dy, saved->y2, saved->row_id_map, topk_w, T, H, k, dy2, dprobs, status, s)) !=
       MOE_OK)
     return st;
-  if ((st = launch_gmm(GMM_DX, 0, dy2, w2, saved->group_list, R, I, H, E, 0.f, da, nullptr, status, s)) != MOE_OK)
-    return st;
-  if (dw2 && (st = launch_gmm(GMM_DW, 0, saved->a, dy2, saved->group_list, R, I, H, E, 0.f, dw2, nullptr, status, s)) !=
-                 MOE_OK)
-    return st;
-  if ((st = launch_swiglu_backward(saved->h, da, R, I, clip, dh, s)) != MOE_OK) return st;
-  if ((st = launch_gmm(GMM_DX, 0, dh, w1, saved->group_list, R, H, 2 * I, E, 0.f, dx_perm, nullptr, status, s)) !=
+  if ((st = launch_gmm(GMM_DX, 0, dy2, w2, saved->group_list, R, I, H, E, 0.f, da, nullptr, status, gmm_scratch, s)) !=
       MOE_OK)
     return st;
-  if (dw1 &&
-      (st = launch_gmm(GMM_DW, 0, saved->x_perm, dh, saved->group_list, R, H, 2 * I, E, 0.f, dw1, nullptr, status, s)) !=
-          MOE_OK)
+  if (dw2 && (st = launch_gmm(GMM_DW, 0, saved->a, dy2, saved->group_list, R, I, H, E, 0.f, dw2, nullptr, status,
+                              gmm_scratch, s)) != MOE_OK)
+    return st;
+  if ((st = launch_swiglu_backward(saved->h, da, R, I, clip, dh, s)) != MOE_OK) return st;
+  if ((st = launch_gmm(GMM_DX, 0, dh, w1, saved->group_list, R, H, 2 * I, E, 0.f, dx_perm, nullptr, status,
+                       gmm_scratch, s)) != MOE_OK)
+    return st;
+  if (dw1 && (st = launch_gmm(GMM_DW, 0, saved->x_perm, dh, saved->group_list, R, H, 2 * I, E, 0.f, dw1, nullptr, status,
+                              gmm_scratch, s)) != MOE_OK)
     return st;
   return launch_unpermute(dx_perm, saved->row_id_map, nullptr, T, H, k, dx, status, s);
 }

@@ -120,6 +120,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// ----------------------------------------------------------------- TMA descriptors edited on the device
+// Field edits of a 128-byte tensor map held in shared memory.
+__device__ __forceinline__ void tmap_set_address(uint32_t smem_map, uint64_t addr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" :: "r"(smem_map), "l"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void tmap_set_rows(uint32_t smem_map, uint32_t rows) {  // extent of dimension 1
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" :: "r"(smem_map), "r"(rows)
+               : "memory");
+}
+// Copy an edited map to global memory for the TMA unit (whole warp), then make
+// it visible to this thread's later copies.
+__device__ __forceinline__ void tmap_publish(void* gmem_map, uint32_t smem_map) {
+  asm volatile("tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.cta.sync.aligned [%0], [%1], 128;"
+               :: "l"(gmem_map), "r"(smem_map) : "memory");
+}
+__device__ __forceinline__ void tmap_acquire(const void* gmem_map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.cta [%0], 128;" :: "l"(gmem_map) : "memory");
+}
+
 // ----------------------------------------------------------------- clusters (CTA pairs)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -7,26 +7,25 @@
 // cumsum through g) of group_list) and
 //   forward   y_g  = x_g  @ W_g                 (GMM_FWD)
 //   input grad dx_g = dy_g @ W_g^T              (GMM_DX)
-//   weight grad dW_g = x_g^T @ dy_g, 0 if empty (GMM_DW)
 // The gate_up forward can finish with the clipped SwiGLU of "MegaMoE",
 // "激活函数公式" (gate = first I columns, up = last I), in the epilogue.
+// This 128-row kernel serves groups that average under 512 rows; larger ones,
+// and every weight gradient, run on CTA pairs (gmm_pair.cu).
 //
 // Design (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //               (64 x 256) into a 4-stage ring, one mbarrier pair per stage.
-//   warp 1      TMEM allocator + MMA issuer: 4 x tcgen05.mma (M=128, N=256,
-//               K=16) per stage into one of two 256-column fp32 accumulators;
-//               tcgen05.commit frees the stage and, after the last stage,
-//               hands the accumulator to the epilogue.
+//   warp 1      TMEM allocator; one thread issues 4 x tcgen05.mma (M=128,
+//               N=256, K=16) per stage into one of two 256-column fp32
+//               accumulators; tcgen05.commit frees the stage and, after the
+//               last stage, hands the accumulator to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld (32 lanes x 32 columns) -> bf16 ->
 //               row-masked global stores; then release the accumulator.
 // The group structure is read on the device (no host sync): every CTA scans
 // group_list into row offsets and a tile prefix in shared memory and maps a
 // linear tile id to (group, row tile, column tile) by binary search.  Tiles
 // are visited column-tile fastest so concurrent CTAs share A rows and W
-// columns in L2.  For dW the contraction runs over the group's own rows: the
-// last 64-row block of a group is zero-filled past the group end in shared
-// memory before the MMA, and groups are visited largest-first.
+// columns in L2.
 // Every wait is bounded; on a timeout the kernel drains its own copies and
 // MMAs, writes MOE_ERR_TIMEOUT to the status word and returns.
 #include <cuda.h>
@@ -57,10 +56,9 @@ struct GmmParams {
   const int64_t* group_list;
   int E;
   int64_t rows_cap;    // rows of the grouped operand (M)
-  int out_rows;        // GMM_DW: rows of one expert's dW (K)
-  int out_cols;        // columns of the output (FWD: N, or I with SwiGLU; DX: K; DW: N)
+  int out_cols;        // columns of the output (FWD: N, or I with SwiGLU; DX: K)
   int tile_cols;       // column tiles per row tile
-  int kblocks;         // FWD / DX: contraction blocks of 64 (K/64 or N/64)
+  int kblocks;         // contraction blocks of 64 (FWD: K/64, DX: N/64)
   uint16_t* out;
   int64_t ld_out;
   uint16_t* h_save;    // SwiGLU: bf16 pre-activation [M, 2I]
@@ -81,20 +79,16 @@ struct __align__(16) GmmSmem {
   int32_t ntiles;
   int64_t grp_off[kMaxExperts + 1];   // row offset of each expert (by id)
   int32_t grp_cnt[kMaxExperts];       // rows of each expert (by id)
-  int32_t order[kMaxExperts];         // visiting order: position -> expert id
-  int32_t tile_start[kMaxExperts + 1];  // tile prefix over visiting positions
+  int32_t tile_start[kMaxExperts + 1];  // tile prefix over experts
 };
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(GmmSmem);
 
 struct TileInfo {
   int g;          // expert id
-  int64_t row0;   // FWD/DX: first row of x/dy; DW: first output row (k)
-  int rows_valid; // rows of the tile that belong to the output
+  int64_t row0;   // first row of x / dy
+  int rows_valid; // rows of the tile inside the group
   int col0;       // first output column (SwiGLU: first activation column)
-  int kblocks;    // contraction blocks of 64
-  int64_t m0;     // DW: first contraction row (group start)
-  int depth;      // DW: contraction rows of the group
 };
 
 template <int MODE, bool SWIGLU>
@@ -105,25 +99,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmPara
     if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
   }
   TileInfo ti;
-  const int g = sm->order[lo];
+  const int g = lo;
   const int local = t - sm->tile_start[lo];
   const int rt = local / p.tile_cols;
   const int ct = local - rt * p.tile_cols;
   ti.g = g;
   ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
-  if (MODE == GMM_DW) {
-    ti.row0 = static_cast<int64_t>(rt) * BM;
-    ti.rows_valid = min(BM, p.out_rows - rt * BM);
-    ti.m0 = sm->grp_off[g];
-    ti.depth = sm->grp_cnt[g];
-    ti.kblocks = (ti.depth + BK - 1) / BK;
-  } else {
-    ti.row0 = sm->grp_off[g] + static_cast<int64_t>(rt) * BM;
-    ti.rows_valid = min(BM, sm->grp_cnt[g] - rt * BM);
-    ti.m0 = 0;
-    ti.depth = 0;
-    ti.kblocks = p.kblocks;
-  }
+  ti.row0 = sm->grp_off[g] + static_cast<int64_t>(rt) * BM;
+  ti.rows_valid = min(BM, sm->grp_cnt[g] - rt * BM);
   return ti;
 }
 
@@ -157,9 +140,9 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&r)[3
 template <int MODE, bool SWIGLU>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
-  constexpr bool A_MN = (MODE == GMM_DW);
-  constexpr bool B_MN = (MODE != GMM_DX);
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static_assert(MODE == GMM_FWD || MODE == GMM_DX, "dW runs on CTA pairs");
+  constexpr bool B_MN = (MODE == GMM_FWD);
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,32 +178,14 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
   }
   __syncthreads();
-  if (MODE == GMM_DW) {
-    // largest group first (ties: lower id first)
-    for (int e = tid; e < E; e += NUM_THREADS) {
-      const int ce = sm->grp_cnt[e];
-      int r = 0;
-      for (int e2 = 0; e2 < E; ++e2) {
-        const int c2 = sm->grp_cnt[e2];
-        r += (c2 > ce) || (c2 == ce && e2 < e);
-      }
-      sm->order[r] = e;
-    }
-  } else {
-    for (int e = tid; e < E; e += NUM_THREADS) sm->order[e] = e;
-  }
-  __syncthreads();
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int64_t rows = 0;
     int32_t tiles = 0;
-    const int row_tiles_dw = (p.out_rows + BM - 1) / BM;
     for (int e = lo; e < hi; ++e) {
       rows += sm->grp_cnt[e];
-      const int g = sm->order[e];
-      tiles += (MODE == GMM_DW) ? row_tiles_dw * p.tile_cols
-                                : ((sm->grp_cnt[g] + BM - 1) / BM) * p.tile_cols;
+      tiles += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
     }
     int64_t rows_incl = rows;
     int32_t tiles_incl = tiles;
@@ -234,11 +199,9 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     int32_t tb = tiles_incl - tiles;
     for (int e = lo; e < hi; ++e) {
       sm->grp_off[e] = rb;
-      rb += sm->grp_cnt[e];
-      const int g = sm->order[e];
       sm->tile_start[e] = tb;
-      tb += (MODE == GMM_DW) ? row_tiles_dw * p.tile_cols
-                             : ((sm->grp_cnt[g] + BM - 1) / BM) * p.tile_cols;
+      rb += sm->grp_cnt[e];
+      tb += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
@@ -270,7 +233,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
           const uint32_t bar = smem_u32(&sm->full[s]);
@@ -285,17 +248,9 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                                      : ti.col0 + 64 * j;
               tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
             }
-          } else if (MODE == GMM_DX) {
+          } else {
             tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
             tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
-          } else {
-            const int32_t mrow = static_cast<int32_t>(ti.m0 + static_cast<int64_t>(kb) * BK);
-#pragma unroll
-            for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(a_dst + i * BOX_BYTES, &tmA, bar, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * BOX_BYTES, &tmB, bar, ti.col0 + 64 * j, mrow);
           }
         }
       }
@@ -305,18 +260,17 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
       }
     }
-  } else if (warp == 1 && MODE != GMM_DW) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
     if (lane == 0) {
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
           tc_fence_after();
@@ -340,62 +294,6 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         drain_wait(smem_u32(&sm->drain), 0);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer for dW (whole warp: it zeroes rows)
-    uint32_t it = 0, local = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
-      if (ti.kblocks == 0) continue;
-      const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
-      if (!warp_wait(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, lane)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!warp_wait(smem_u32(&sm->full[s]), ph, abort_flag, lane)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a_addr = stage_base + s * STAGE_BYTES;
-        const uint32_t b_addr = a_addr + A_BYTES;
-        if (MODE == GMM_DW) {
-          const int valid = ti.depth - kb * BK;
-          if (valid < BK) {
-            // rows past the group end belong to the next group: zero them in
-            // every box of this stage (a swizzled row stays inside its 128 bytes)
-            const int nbox = (A_BYTES + B_BYTES) / BOX_BYTES;
-            const int nchunk = (BK - valid) * 8;  // 16-byte chunks per box
-            uint8_t* base = smem + s * STAGE_BYTES;
-            for (int i = lane; i < nbox * nchunk; i += 32) {
-              const int box = i / nchunk, c = i - box * nchunk;
-              *reinterpret_cast<uint4*>(base + box * BOX_BYTES + valid * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, BOX_BYTES, 1024)
-                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
-                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&sm->empty[s]));
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(smem_u32(&sm->tmem_full[acc]));
-      __syncwarp();
-      ++local;
-    }
-    if (!ok && lane == 0) {
-      tc_commit(smem_u32(&sm->drain));
-      drain_wait(smem_u32(&sm->drain), 0);
-    }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quarter of this warp
@@ -405,14 +303,6 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
       const bool row_ok = row_in_tile < ti.rows_valid;
       const int64_t row = ti.row0 + row_in_tile;
-      if (MODE == GMM_DW && ti.kblocks == 0) {
-        if (row_ok) {
-          uint16_t* dst = p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out + row * p.ld_out + ti.col0;
-          const int ncols = min(BN, p.out_cols - ti.col0);
-          for (int c = 0; c < ncols; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
@@ -455,9 +345,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           tmem_ld32(taddr + cc, r);
           tmem_ld_wait();
           if (row_ok) {
-            uint16_t* dst = (MODE == GMM_DW)
-                ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out + row * p.ld_out + ti.col0 + cc
-                : p.out + row * p.ld_out + ti.col0 + cc;
+            uint16_t* dst = p.out + row * p.ld_out + ti.col0 + cc;
             store_row32(dst, r);
           }
         }
@@ -497,14 +385,14 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
 
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                        uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s) {
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s) {
   // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
-  // CTA pairs (256 x 256 tiles) when groups average at least 512 rows; below
-  // that the extra padding of a 256-row tile (forward, dX) and the short
-  // contractions (dW) cost more than the pair saves, and the 128-row kernel
-  // here runs instead.
-  if (M >= kPairMinRowsPerGroup * E)
-    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, s);
+  // CTA pairs (256 x 256 tiles) for every weight gradient, and for forward and
+  // dX when groups average at least 512 rows; below that the extra padding of
+  // a 256-row tile costs more than the pair saves, and the 128-row kernel here
+  // runs instead.
+  if (mode == GMM_DW || M >= kPairMinRowsPerGroup * E)
+    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, gmm_scratch, s);
   GmmParams p{};
   p.group_list = group_list;
   p.E = static_cast<int>(E);
@@ -524,20 +412,12 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
     return sw ? launch_mode<GMM_FWD, true>(ta, tb, p, s) : launch_mode<GMM_FWD, false>(ta, tb, p, s);
   }
-  if (mode == GMM_DX) {
-    p.out_cols = static_cast<int>(K);
-    p.ld_out = K;
-    p.tile_cols = static_cast<int>((K + BN - 1) / BN);
-    p.kblocks = static_cast<int>(N / BK);
-    if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
-    return launch_mode<GMM_DX, false>(ta, tb, p, s);
-  }
-  p.out_rows = static_cast<int>(K);
-  p.out_cols = static_cast<int>(N);
-  p.ld_out = N;
-  p.tile_cols = static_cast<int>((N + BN - 1) / BN);
-  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64)) return MOE_ERR_CUDA;
-  return launch_mode<GMM_DW, false>(ta, tb, p, s);
+  p.out_cols = static_cast<int>(K);
+  p.ld_out = K;
+  p.tile_cols = static_cast<int>((K + BN - 1) / BN);
+  p.kblocks = static_cast<int>(N / BK);
+  if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
+  return launch_mode<GMM_DX, false>(ta, tb, p, s);
 }
 
 }  // namespace moe

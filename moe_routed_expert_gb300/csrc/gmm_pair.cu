@@ -21,12 +21,12 @@
 //     shared memory (XOR-swizzled 16-byte chunks, conflict-free) and writes
 //     them back two full rows per warp instruction (coalesced), masking rows
 //     past the group end and columns past N.
-//   * dW: a stage whose 64 contraction rows cross the group end has its copies
-//     complete on a local barrier of each CTA instead; a fixup warp in each CTA
-//     zeroes the rows past the group end (a swizzled row stays inside its own
-//     128 bytes), fences them for the tensor core, and the even CTA's fixup
-//     warp, once the odd one has reported, marks the stage full.  Groups are
-//     visited largest first so the long contractions start early.
+//   * dW contracts over each group's own rows.  For every group it starts, the
+//     producer warp rewrites a copy of each TMA descriptor (base address = the
+//     group's first row, row extent = the group's row count) and publishes it
+//     to a per-CTA slot in the workspace, so rows past the group end arrive as
+//     zeros from the TMA unit itself.  Groups are visited largest first so the
+//     long contractions start early.
 // Group offsets are read on the device as in gmm.cu; tiles are visited column
 // tile fastest.  Every mbarrier wait is bounded; a timeout stops all roles,
 // waits for copies in flight, frees TMEM and writes MOE_ERR_TIMEOUT.
@@ -54,7 +54,7 @@ constexpr int EPI_ROW_BYTES = 256;              // 128 bf16 columns
 constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;   // 32 KB
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_THREADS = 224;   // producer, MMA, 4 epilogue warps, dW fixup warp
+constexpr int NUM_THREADS = 192;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 struct PairParams {
@@ -71,16 +71,21 @@ struct PairParams {
   int act_cols;     // SwiGLU: I
   float clip;
   uint32_t* status;
+  // dW: the operands' bases and row pitches, and kMapSlots descriptor pairs per CTA
+  const uint8_t* a_base;
+  const uint8_t* b_base;
+  int64_t a_pitch;
+  int64_t b_pitch;
+  uint8_t* map_slots;
 };
 
-struct __align__(16) PairSmem {
+struct __align__(128) PairSmem {
+  uint8_t map_edit[2][128];    // dW: descriptors being rewritten (A, B)
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
-  uint64_t aux[STAGES];        // dW: copies of a stage that crosses the group end
-  uint64_t peer_done[STAGES];  // dW: the odd CTA has zeroed its half of that stage
   uint32_t tmem_base;
   uint32_t abort;
   int32_t bad;
@@ -138,25 +143,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   int ok = 1;
   if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Bounded wait with cluster-scope acquire: for a barrier the peer CTA arrives on.
-__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    if (ok) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
-      *abort = 1u;
-      return false;
-    }
-  }
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -228,10 +214,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(smem_u32(&sm->tmem_empty[a]), 8);  // 4 epilogue warps in each CTA
     }
     mbar_init(smem_u32(&sm->drain), 1);
-    for (int st = 0; st < STAGES; ++st) {
-      mbar_init(smem_u32(&sm->aux[st]), 1);
-      mbar_init(smem_u32(&sm->peer_done[st]), 1);
-    }
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -309,7 +291,73 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const int ntiles = sm->ntiles;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (warp == 0) {
+  if (warp == 0 && MODE == GMM_DW) {
+    // ---------------------------------------------------------------- dW TMA producer (both CTAs)
+    // The whole warp walks the tiles (it rewrites descriptors together); lane 0 copies.
+    uint8_t* slots = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlots * 256;
+    const uint32_t edit_a = smem_u32(sm->map_edit[0]), edit_b = smem_u32(sm->map_edit[1]);
+    uint32_t it = 0;
+    int ok = 1, cur_g = -1, slot = -1;
+    const void* map_a = nullptr;
+    const void* map_b = nullptr;
+    for (int t = cid; t < ntiles && ok; t += ncl) {
+      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+      if (ti.kblocks == 0) continue;
+      if (ti.g != cur_g) {
+        // a new group: descriptors whose row 0 is the group's first row and
+        // whose row extent is the group's row count
+        cur_g = ti.g;
+        slot = (slot + 1) % kMapSlots;  // a slot is rewritten only after its copies have all landed
+        uint8_t* ga = slots + slot * 256;
+        uint8_t* gb = ga + 128;
+        if (lane < 8) {
+          reinterpret_cast<uint4*>(sm->map_edit[0])[lane] = reinterpret_cast<const uint4*>(&tmA)[lane];
+          reinterpret_cast<uint4*>(sm->map_edit[1])[lane] = reinterpret_cast<const uint4*>(&tmB)[lane];
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tmap_set_address(edit_a, reinterpret_cast<uint64_t>(p.a_base + ti.m0 * p.a_pitch));
+          tmap_set_rows(edit_a, static_cast<uint32_t>(ti.depth));
+          tmap_set_address(edit_b, reinterpret_cast<uint64_t>(p.b_base + ti.m0 * p.b_pitch));
+          tmap_set_rows(edit_b, static_cast<uint32_t>(ti.depth));
+        }
+        __syncwarp();
+        tmap_publish(ga, edit_a);
+        tmap_publish(gb, edit_b);
+        if (lane == 0) {
+          tmap_acquire(ga);
+          tmap_acquire(gb);
+        }
+        map_a = ga;
+        map_b = gb;
+      }
+      if (lane == 0) {
+        const int bcol = ti.col0 + static_cast<int>(rank) * BNH;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = 0; break; }
+          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const uint32_t bar_local = smem_u32(&sm->full[s]);
+          const uint32_t bar = mapa_shared(bar_local, 0);
+          if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
+#pragma unroll
+          for (int i2 = 0; i2 < BM / 64; ++i2)
+            tma_load_2d_pair(a_dst + i2 * BOX_BYTES, map_a, bar, static_cast<int32_t>(ti.row0) + 64 * i2, kb * BK);
+#pragma unroll
+          for (int j = 0; j < BNH / 64; ++j) tma_load_2d_pair(b_dst + j * BOX_BYTES, map_b, bar, bcol + 64 * j, kb * BK);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (lane == 0) {  // every stage filled here must be released before the CTA may exit
+      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      for (uint32_t i2 = first; i2 < it; ++i2) {
+        if (*abort_flag) break;
+        mbar_wait_bounded(smem_u32(&sm->empty[i2 % STAGES]), (i2 / STAGES) & 1u, abort_flag, kTimeoutNs);
+      }
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t it = 0;
@@ -321,30 +369,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
           const uint32_t a_dst = stage_base + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
-          if (MODE == GMM_DW) {
-            const int32_t mrow = static_cast<int32_t>(ti.m0 + static_cast<int64_t>(kb) * BK);
-            const int bcol = ti.col0 + static_cast<int>(rank) * BNH;
-            if (ti.depth - kb * BK < BK) {
-              // crosses the group end: each CTA counts its own copies, the fixup warp takes over
-              const uint32_t aux = smem_u32(&sm->aux[s]);
-              mbar_expect_tx(aux, STAGE_BYTES);
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d(a_dst + i * BOX_BYTES, &tmA, aux, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
-#pragma unroll
-              for (int j = 0; j < BNH / 64; ++j) tma_load_2d(b_dst + j * BOX_BYTES, &tmB, aux, bcol + 64 * j, mrow);
-            } else {
-              const uint32_t bar_local = smem_u32(&sm->full[s]);
-              const uint32_t bar = mapa_shared(bar_local, 0);
-              if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d_pair(a_dst + i * BOX_BYTES, &tmA, bar, static_cast<int32_t>(ti.row0) + 64 * i, mrow);
-#pragma unroll
-              for (int j = 0; j < BNH / 64; ++j) tma_load_2d_pair(b_dst + j * BOX_BYTES, &tmB, bar, bcol + 64 * j, mrow);
-            }
-            continue;
-          }
           const uint32_t bar_local = smem_u32(&sm->full[s]);
           const uint32_t bar = mapa_shared(bar_local, 0);  // the even CTA's stage barrier
           if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
@@ -499,43 +523,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
       ++local;
     }
-  } else if (MODE == GMM_DW) {
-    // ---------------------------------------------------------------- dW fixup warp (both CTAs)
-    // For each stage that crosses a group end: wait for this CTA's copies,
-    // zero the rows past the group end, make them visible to the tensor core;
-    // the odd CTA reports to the even one, the even CTA then marks the stage full.
-    uint32_t it = 0, aux_ph = 0, peer_ph = 0;
-    bool ok = true;
-    for (int t = cid; t < ntiles && ok; t += ncl) {
-      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
-      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
-        const int valid = ti.depth - kb * BK;
-        if (valid >= BK) continue;
-        const uint32_t s = it % STAGES;
-        if (!warp_wait(smem_u32(&sm->aux[s]), (aux_ph >> s) & 1u, abort_flag, lane)) { ok = false; break; }
-        aux_ph ^= 1u << s;
-        uint8_t* stage = smem + s * STAGE_BYTES;
-        constexpr int nbox = STAGE_BYTES / BOX_BYTES;
-        const int nchunk = (BK - valid) * 8;  // 16-byte chunks past the group end, per box
-        for (int i = lane; i < nbox * nchunk; i += 32) {
-          const int box = i / nchunk, c = i - box * nchunk;
-          *reinterpret_cast<uint4*>(stage + box * BOX_BYTES + valid * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (rank == 1) {
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm->peer_done[s]), 0));
-        } else {
-          int good = 1;
-          if (lane == 0) good = wait_cluster_bounded(smem_u32(&sm->peer_done[s]), (peer_ph >> s) & 1u, abort_flag);
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) { ok = false; break; }
-          peer_ph ^= 1u << s;
-          if (lane == 0) mbar_arrive(smem_u32(&sm->full[s]));
-        }
-        __syncwarp();
-      }
-    }
   }
 
   __syncthreads();
@@ -581,6 +568,7 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pai
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return MOE_ERR_CUDA;
     grid = 2 * clusters;
+    if (grid > kMaxGmmCtas) grid = kMaxGmmCtas;  // the descriptor slots cover this many CTAs
     configured_dev = dev;
   }
   cfg.gridDim = dim3(grid, 1, 1);
@@ -593,7 +581,7 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pai
 // FWD (optionally with the SwiGLU epilogue), DX and DW on CTA pairs.
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip, uint16_t* out, uint16_t* h_save,
-                             uint32_t* status, cudaStream_t s) {
+                             uint32_t* status, void* gmm_scratch, cudaStream_t s) {
   PairParams p{};
   p.group_list = group_list;
   p.E = static_cast<int>(E);
@@ -622,6 +610,12 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     return launch_pair<GMM_DX, false>(ta, tb, p, s);
   }
   // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
+  if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
+  p.a_base = reinterpret_cast<const uint8_t*>(a);
+  p.b_base = reinterpret_cast<const uint8_t*>(b);
+  p.a_pitch = K * 2;
+  p.b_pitch = N * 2;
+  p.map_slots = static_cast<uint8_t*>(gmm_scratch);
   p.out_rows = static_cast<int>(K);
   p.out_cols = static_cast<int>(N);
   p.ld_out = N;

@@ -41,11 +41,17 @@ bool make_map_3d(::CUtensorMap_st* m, const void* base, int64_t E, int64_t K, in
 // ---- grouped matmul (gmm.cu, gmm_pair.cu)
 enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
 constexpr int64_t kPairMinRowsPerGroup = 512;
+// GMM scratch in the workspace: per CTA, kMapSlots pairs of 128-byte TMA
+// descriptors that the dW kernel rewrites for each group.
+constexpr int kMapSlots = 6;
+constexpr int kMaxGmmCtas = 256;
+constexpr size_t kGmmScratchBytes = static_cast<size_t>(kMaxGmmCtas) * kMapSlots * 256;
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                             uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s);
+                             uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);
+// gmm_scratch: kGmmScratchBytes of workspace (used by dW).
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                        uint16_t* out, uint16_t* h_save, uint32_t* status, cudaStream_t s);
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);
 
 }  // namespace moe

@@ -51,7 +51,7 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert lib.gmm_workspace_size(8192, 1024, 2048, 8) == 256
+    assert lib.gmm_workspace_size(8192, 1024, 2048, 8) == 256 + 256 * 6 * 256  # status + descriptor slots
     assert lib.moe_unpermute_workspace_size() == 256
     # permute: status block + per-chunk counts (1024 slots per chunk, int32 per expert)
     assert lib.moe_permute_workspace_size(4096, 8, 256) == 256 + 32 * 256 * 4
@@ -59,7 +59,7 @@ def test_workspace_sizes(lib):
     T, H, I, E, k = 4096, 2048, 512, 256, 8
     n = lib.moe_layer_workspace_size(T, H, I, E, k)
     R = T * k
-    assert n >= 256 + R * H * 2 * 2 + R * I * 2 + 2 * R * 4 + E * 8
+    assert n >= 256 + 256 * 6 * 256 + R * H * 2 * 2 + R * I * 2 + 2 * R * 4 + E * 8
     assert n % 256 == 0
 
 

@@ -130,7 +130,6 @@ class LayerTrainStep:
         bf = torch.bfloat16
         self.y = torch.empty(T, H, dtype=bf, device=dev)
         self.dy2 = torch.empty(R, H, dtype=bf, device=dev)
-        self.da = torch.empty(R, I, dtype=bf, device=dev)
         self.dh = torch.empty(R, 2 * I, dtype=bf, device=dev)
         self.dx = torch.empty(T, H, dtype=bf, device=dev)
         self.dw1 = torch.empty_like(self.w1)
@@ -148,9 +147,8 @@ class LayerTrainStep:
             ("gmm_fwd_down", self.gmm2, f_dn, 1),
             ("combine", self.combine, 0.0, 1),
             ("combine_bwd", self.combine_bwd, 0.0, 1),
-            ("gmm_dx_down", self.dx_down, f_dn, 1),
+            ("gmm_dx_down_swiglu_bwd", self.dx_down_swiglu, f_dn, 1),
             ("gmm_dw_down", self.dw_down, f_dn, 1),
-            ("swiglu_bwd", self.swiglu_bwd, 0.0, 1),
             ("gmm_dx_gate_up", self.dx_up, f_up, 1),
             ("gmm_dw_gate_up", self.dw_up, f_up, 1),
             ("permute_bwd", self.permute_bwd, 0.0, 1),
@@ -181,16 +179,14 @@ class LayerTrainStep:
         self.M.moe_unpermute_backward(self.dy, s.y2, s.row_id_map, self.tw, self.wl.k, dy_perm=self.dy2,
                                       dprobs=self.dprobs, ws=self.ws)
 
-    def dx_down(self):
+    def dx_down_swiglu(self):
+        # dH = SwiGLU'(H, dY2 @ W2^T) in one grouped matmul, as the layer backward does
         s = self.saved
-        self.M.gmm_backward(s.a, self.w2, s.group_list, self.dy2, need_dw=False, dx=self.da, ws=self.ws)
+        self.M.gmm_backward_dx_swiglu(self.dy2, self.w2, s.group_list, s.h, self.wl.clip, dh=self.dh, ws=self.ws)
 
     def dw_down(self):
         s = self.saved
         self.M.gmm_backward(s.a, self.w2, s.group_list, self.dy2, need_dx=False, dw=self.dw2, ws=self.ws)
-
-    def swiglu_bwd(self):
-        self.M.moe_swiglu_backward(self.saved.h, self.da, self.wl.clip, dh=self.dh, ws=self.ws)
 
     def dx_up(self):
         s = self.saved
@@ -204,33 +200,27 @@ class LayerTrainStep:
     def permute_bwd(self):
         self.M.moe_permute_backward(self.dy2, self.saved.row_id_map, self.wl.T, self.wl.k, dx=self.dx, ws=self.ws)
 
-    # public-API step with host buffers, for e2e
-    def e2e_setup(self, inp):
-        import torch
-        self.h_x = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-        self.h_dy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-        self.h_ids = torch.from_numpy(inp["topk_ids"]).pin_memory()
-        self.h_tw = torch.from_numpy(inp["topk_w"]).pin_memory()
-        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
-        self.h_dx = torch.empty(self.dx.shape, dtype=self.dx.dtype).pin_memory()
-        self.h_dprobs = torch.empty(self.dprobs.shape, dtype=self.dprobs.dtype).pin_memory()
-        self.h2d = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_dy, self.h_ids, self.h_tw))
-        self.d2h = sum(t.numel() * t.element_size() for t in (self.h_y, self.h_dx, self.h_dprobs))
-        self.e2e_launches = 4 + 2 + 1 + 1 + 4 + 1 + 1
+    # public entry points with host buffers, for e2e
+    def e2e_host_inputs(self, inp):
+        return {"x": pinned_bf16(inp["x"]), "dy": pinned_bf16(inp["dy"]), "topk_ids": pinned(inp["topk_ids"]),
+                "topk_w": pinned(inp["topk_w"])}
 
-    def e2e_step(self):
+    def e2e_outputs(self):
+        import torch
+        T, H, k = self.wl.T, self.wl.H, self.wl.k
+        return {"y": torch.empty(T, H, dtype=torch.bfloat16, device=self.dev),
+                "dx": torch.empty(T, H, dtype=torch.bfloat16, device=self.dev),
+                "dprobs": torch.empty(T, k, dtype=torch.float32, device=self.dev)}
+
+    def e2e_compute(self, i, o):
         M, wl = self.M, self.wl
-        self.x.copy_(self.h_x, non_blocking=True)
-        self.dy.copy_(self.h_dy, non_blocking=True)
-        self.ids.copy_(self.h_ids, non_blocking=True)
-        self.tw.copy_(self.h_tw, non_blocking=True)
-        M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, wl.clip, saved=self.saved, y=self.y,
+        M.moe_layer_forward(i["x"], i["topk_ids"], i["topk_w"], self.w1, self.w2, wl.clip, saved=self.saved, y=o["y"],
                             ws=self.ws)
-        M.moe_layer_backward(self.dy, self.tw, self.w1, self.w2, self.saved, wl.clip, dx=self.dx, dw1=self.dw1,
-                             dw2=self.dw2, dprobs=self.dprobs, ws=self.ws)
-        self.h_y.copy_(self.y, non_blocking=True)
-        self.h_dx.copy_(self.dx, non_blocking=True)
-        self.h_dprobs.copy_(self.dprobs, non_blocking=True)
+        M.moe_layer_backward(i["dy"], i["topk_w"], self.w1, self.w2, self.saved, wl.clip, dx=o["dx"], dw1=self.dw1,
+                             dw2=self.dw2, dprobs=o["dprobs"], ws=self.ws)
+
+    e2e_launches = 4 + 2 + 1 + 1 + 4 + 1
+    e2e_api = "moe_layer_forward/moe_layer_backward"
 
 
 class LayerFwdStep(LayerTrainStep):
@@ -250,19 +240,19 @@ class LayerFwdStep(LayerTrainStep):
         self.gmm_bytes = {"gmm_fwd_gate_up_swiglu": live * H * 2 * I * 2 + R * H * 2 + R * I * 2,
                           "gmm_fwd_down": live * I * H * 2 + R * I * 2 + R * H * 2}
 
-    def e2e_step(self):
-        M, wl = self.M, self.wl
-        self.x.copy_(self.h_x, non_blocking=True)
-        self.ids.copy_(self.h_ids, non_blocking=True)
-        self.tw.copy_(self.h_tw, non_blocking=True)
-        M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, wl.clip, y=self.y, ws=self.ws)
-        self.h_y.copy_(self.y, non_blocking=True)
+    def e2e_host_inputs(self, inp):
+        return {"x": pinned_bf16(inp["x"]), "topk_ids": pinned(inp["topk_ids"]), "topk_w": pinned(inp["topk_w"])}
 
-    def e2e_setup(self, inp):
-        super().e2e_setup(inp)
-        self.h2d = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_ids, self.h_tw))
-        self.d2h = self.h_y.numel() * self.h_y.element_size()
-        self.e2e_launches = 4 + 2 + 1
+    def e2e_outputs(self):
+        import torch
+        return {"y": torch.empty(self.wl.T, self.wl.H, dtype=torch.bfloat16, device=self.dev)}
+
+    def e2e_compute(self, i, o):
+        self.M.moe_layer_forward(i["x"], i["topk_ids"], i["topk_w"], self.w1, self.w2, self.wl.clip, y=o["y"],
+                                 ws=self.ws)
+
+    e2e_launches = 4 + 2 + 1
+    e2e_api = "moe_layer_forward"
 
 
 class GmmStep:
@@ -271,7 +261,7 @@ class GmmStep:
     def __init__(self, wl, dev, inp):
         import torch
         import moe_routed_expert_gb300 as M
-        self.M, self.wl = M, wl
+        self.M, self.wl, self.dev = M, wl, dev
         self.x = bf16_dev(inp["x"], dev)
         self.w = bf16_dev(inp["w"], dev)
         self.dyv = bf16_dev(inp["dy"], dev) if "dy" in inp else None
@@ -296,23 +286,74 @@ class GmmStep:
     def bdw(self):
         self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, need_dx=False, dw=self.dw, ws=self.ws)
 
-    def e2e_setup(self, inp):
-        import torch
-        self.h_x = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-        self.h_dy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-        self.h_y = torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory()
-        self.h_dx = torch.empty(self.dx.shape, dtype=torch.bfloat16).pin_memory()
-        self.h2d = 2 * (self.h_x.numel() + self.h_dy.numel())
-        self.d2h = 2 * (self.h_y.numel() + self.h_dx.numel())
-        self.e2e_launches = 3
+    def e2e_host_inputs(self, inp):
+        return {"x": pinned_bf16(inp["x"]), "dy": pinned_bf16(inp["dy"])}
 
-    def e2e_step(self):
-        self.x.copy_(self.h_x, non_blocking=True)
-        self.dyv.copy_(self.h_dy, non_blocking=True)
-        self.M.gmm_forward(self.x, self.w, self.gl, y=self.y, ws=self.ws)
-        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, dx=self.dx, dw=self.dw, ws=self.ws)
-        self.h_y.copy_(self.y, non_blocking=True)
-        self.h_dx.copy_(self.dx, non_blocking=True)
+    def e2e_outputs(self):
+        import torch
+        return {"y": torch.empty_like(self.y), "dx": torch.empty_like(self.dx)}
+
+    def e2e_compute(self, i, o):
+        self.M.gmm_forward(i["x"], self.w, self.gl, y=o["y"], ws=self.ws)
+        self.M.gmm_backward(i["x"], self.w, self.gl, i["dy"], dx=o["dx"], dw=self.dw, ws=self.ws)
+
+    e2e_launches = 3
+    e2e_api = "gmm_forward/gmm_backward"
+
+
+def pinned(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
+def pinned_bf16(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+class E2EPipeline:
+    """Every step copies its inputs host->device and its results device->host
+    (pinned buffers).  Two buffer sets let the copies of neighbouring steps run
+    on their own streams while a step computes; each step still waits for its
+    own inputs, and the timed region ends when the last results are on the host."""
+
+    def __init__(self, step, inp, nbuf=2):
+        import torch
+        self.step, self.nbuf = step, nbuf
+        self.h_in = step.e2e_host_inputs(inp)
+        self.d_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=step.dev) for k, v in self.h_in.items()}
+                     for _ in range(nbuf)]
+        self.d_out = [step.e2e_outputs() for _ in range(nbuf)]
+        self.h_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in d.items()} for d in self.d_out]
+        self.h2d = torch.cuda.Stream(device=step.dev)
+        self.d2h = torch.cuda.Stream(device=step.dev)
+        ev = lambda: [torch.cuda.Event() for _ in range(nbuf)]
+        self.in_ready, self.in_free, self.done, self.out_free = ev(), ev(), ev(), ev()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h_in.values())
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.h_out[0].values())
+
+    def run(self, steps):
+        import torch
+        comp = torch.cuda.current_stream()
+        for i in range(steps):
+            b = i % self.nbuf
+            self.h2d.wait_event(self.in_free[b])
+            with torch.cuda.stream(self.h2d):
+                for k, v in self.h_in.items():
+                    self.d_in[b][k].copy_(v, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+            comp.wait_event(self.in_ready[b])
+            comp.wait_event(self.out_free[b])
+            self.step.e2e_compute(self.d_in[b], self.d_out[b])
+            self.in_free[b].record(comp)
+            self.done[b].record(comp)
+            self.d2h.wait_event(self.done[b])
+            with torch.cuda.stream(self.d2h):
+                for k, v in self.d_out[b].items():
+                    self.h_out[b][k].copy_(v, non_blocking=True)
+            self.out_free[b].record(self.d2h)
+        for b in range(self.nbuf):
+            comp.wait_event(self.out_free[b])
 
 
 def make_step(name, dev, tokens=None):
@@ -550,15 +591,15 @@ def main():
 
     # end to end through the public entry points, host buffers, copies inside the timed region
     if not args.no_e2e:
-        step.e2e_setup(inp)
-        for _ in range(2):
-            step.e2e_step()
+        pipe = E2EPipeline(step, inp)
+        pipe.run(2)
         barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            step.e2e_step()
+        pipe.h2d.wait_stream(stream)
+        pipe.d2h.wait_stream(stream)
+        pipe.run(args.steps)
         b.record(stream)
         barrier()
         e_ms = a.elapsed_time(b)
@@ -567,9 +608,9 @@ def main():
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         line["e2e"] = {"value": round(step.units * world / (e_ms / args.steps / 1e3), 3), "unit": step.unit,
-                       "h2d_bytes_per_step": int(step.h2d), "d2h_bytes_per_step": int(step.d2h),
-                       "ms_per_step": round(e_ms / args.steps, 4), "api": "moe_layer_forward/backward"
-                       if not args.workload.startswith("gmm") else "gmm_forward/gmm_backward"}
+                       "h2d_bytes_per_step": int(pipe.h2d_bytes), "d2h_bytes_per_step": int(pipe.d2h_bytes),
+                       "ms_per_step": round(e_ms / args.steps, 4), "api": step.e2e_api,
+                       "copies": "pinned host buffers; two buffer sets, H2D and D2H on their own streams"}
         assert M.read_status(step.ws) == 0
 
     if args.tokens is not None:

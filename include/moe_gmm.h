@@ -175,6 +175,19 @@ MOE_API moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const in
                           moe_bf16* dx, moe_bf16* dw,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The input gradient of a grouped matmul followed by the SwiGLU gradient, in
+ * one pass: the memory-saving backward of "03 · grouped GEMM path" (MegaBlocks),
+ * section 4.3 -- the activation gradient is taken from the saved GMM output, and
+ * here inside the dX epilogue, so dA is never stored:
+ *   dA[s:e] = bf16(dy[s:e] @ w[g]^T)      (not written)
+ *   dh[s:e] = SwiGLU'(h[s:e], dA[s:e])    ([MegaMoE] 激活函数公式 differentiated,
+ *                                           clip c as in moe_swiglu_backward)
+ *   dy [M, N], w [E, K, N], h [M, 2K] (gate | up) bf16 in; dh [M, 2K] bf16 out.
+ * Equal, bit for bit, to gmm_backward's dx followed by moe_swiglu_backward. */
+MOE_API moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
+                          const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                          moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- combine and gradients */
 
 /* Workspace bytes for the combine-side entry points (just the status block). */

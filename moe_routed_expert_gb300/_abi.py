@@ -38,6 +38,7 @@ SIGNATURES = {
     "gmm_workspace_size": (SZ, [I64, I64, I64, I64]),
     "gmm_forward": (ST, [P, P, P, I64, I64, I64, I64, INT, F32, P, P, P, SZ, P]),
     "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
+    "gmm_backward_dx_swiglu": (ST, [P, P, P, P, I64, I64, I64, I64, F32, P, P, SZ, P]),
     "moe_unpermute_workspace_size": (SZ, []),
     "moe_unpermute": (ST, [P, P, P, I64, I64, I64, P, P, SZ, P]),
     "moe_unpermute_backward": (ST, [P, P, P, P, I64, I64, I64, P, P, P, SZ, P]),

@@ -196,6 +196,21 @@ def gmm_backward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, dy:
     return (dx if need_dx else None), (dw if need_dw else None)
 
 
+def gmm_backward_dx_swiglu(dy: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, h: torch.Tensor,
+                           clip: float = 0.0, *, dh=None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """dh = SwiGLU gradient of h given dA = grouped dy @ w^T, in one pass (dA is not stored)."""
+    for t, n in ((dy, "dy"), (w, "w"), (h, "h")):
+        _dtype(t, BF16, n)
+    M, N = dy.shape
+    E, K, _ = w.shape
+    if dh is None:
+        dh = torch.empty(M, 2 * K, dtype=BF16, device=dy.device)
+    wsp = _ws(ws, gmm_workspace_size(M, K, N, E), dy.device)
+    _check(_lib().gmm_backward_dx_swiglu(_ptr(dy), _ptr(w), _ptr(group_list), _ptr(h), M, K, N, E, float(clip),
+                                         _ptr(dh), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward_dx_swiglu")
+    return dh
+
+
 # ------------------------------------------------------------------ combine side
 def moe_unpermute(y_perm, row_id_map, topk_w, T: int, k: int, *, y=None, ws=None, stream=None):
     H = y_perm.shape[1]

@@ -48,7 +48,7 @@ size_t layer_acts_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const size_t R = static_cast<size_t>(T * k);
   const size_t fwd = align256(R * H * 2) + align256(R * I * 2) + align256(R * H * 2) + 2 * align256(R * 4) +
                      align256(static_cast<size_t>(E) * 8);
-  const size_t bwd = align256(R * H * 2) + align256(R * I * 2) + align256(R * 2 * I * 2);
+  const size_t bwd = align256(R * H * 2) + align256(R * 2 * I * 2);
   return fwd > bwd ? fwd : bwd;
 }
 
@@ -173,6 +173,22 @@ moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* g
                              after_status(ws), s)) != MOE_OK)
     return st;
   return MOE_OK;
+}
+
+moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
+                                    const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                                    moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!dy || !w || !group_list || !h || !dh) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_gmm_dims(M, K, N, E);
+  if (st != MOE_OK) return st;
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  if (!aligned16(dy) || !aligned16(w) || !aligned16(h) || !aligned16(dh) ||
+      (reinterpret_cast<uintptr_t>(group_list) & 7u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  return launch_gmm(GMM_DX, EPI_DSWIGLU, dy, w, group_list, M, K, N, E, clip, dh, const_cast<moe_bf16*>(h),
+                    status_of(ws), after_status(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ combine side
@@ -317,19 +333,18 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
   uint8_t* acts = gmm_scratch + kGmmScratchBytes + permute_scratch_bytes(T, k, E);
   const int64_t R = T * k;
   moe_bf16* dy2 = reinterpret_cast<moe_bf16*>(acts);
-  moe_bf16* da = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2));
-  moe_bf16* dh = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2) + align256(R * I * 2));
-  moe_bf16* dx_perm = dy2;  // dy2 is dead once dA and dW2 are done
+  moe_bf16* dh = reinterpret_cast<moe_bf16*>(acts + align256(R * H * 2));
+  moe_bf16* dx_perm = dy2;  // dy2 is dead once dH and dW2 are done
   if ((st = launch_unpermute_backward(dy, saved->y2, saved->row_id_map, topk_w, T, H, k, dy2, dprobs, status, s)) !=
       MOE_OK)
     return st;
-  if ((st = launch_gmm(GMM_DX, 0, dy2, w2, saved->group_list, R, I, H, E, 0.f, da, nullptr, status, gmm_scratch, s)) !=
-      MOE_OK)
+  // dH = SwiGLU'(H, dY2 @ W2^T) in one grouped matmul (dA is never stored)
+  if ((st = launch_gmm(GMM_DX, EPI_DSWIGLU, dy2, w2, saved->group_list, R, I, H, E, clip, dh, saved->h, status,
+                       gmm_scratch, s)) != MOE_OK)
     return st;
   if (dw2 && (st = launch_gmm(GMM_DW, 0, saved->a, dy2, saved->group_list, R, I, H, E, 0.f, dw2, nullptr, status,
                               gmm_scratch, s)) != MOE_OK)
     return st;
-  if ((st = launch_swiglu_backward(saved->h, da, R, I, clip, dh, s)) != MOE_OK) return st;
   if ((st = launch_gmm(GMM_DX, 0, dh, w1, saved->group_list, R, H, 2 * I, E, 0.f, dx_perm, nullptr, status,
                        gmm_scratch, s)) != MOE_OK)
     return st;

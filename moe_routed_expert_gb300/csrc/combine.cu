@@ -169,13 +169,7 @@ __global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t
       const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
       const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
       const float d = (i & 1) ? bf16_hi(dw[i >> 1]) : bf16_lo(dw[i >> 1]);
-      const float gc = fminf(g, c);
-      const float uc = fminf(fmaxf(u, -c), c);
-      const float s = 1.0f / (1.0f + __expf(-gc));
-      const float silu = gc * s;
-      const float dsilu = s * (1.0f + gc * (1.0f - s));
-      dg[i] = (g <= c) ? d * uc * dsilu : 0.0f;
-      du[i] = (u >= -c && u <= c) ? d * silu : 0.0f;
+      swiglu_grad(g, u, d, c, dg[i], du[i]);
     }
     *reinterpret_cast<uint4*>(dh + r * 2 * I + col) = pack8(dg);
     *reinterpret_cast<uint4*>(dh + r * 2 * I + I + col) = pack8(du);

@@ -31,6 +31,24 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// sigma(z) = 1 / (1 + e^-z) with the hardware exponential and an approximate
+// reciprocal (2 ulp): every use rounds its result to bf16 (8 significant bits).
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+
+// SwiGLU gradient ("MegaMoE", 激活函数公式, differentiated) for one element:
+// g, u = bf16 gate / up pre-activation, d = dA (already bf16-valued), clip c
+// (+inf: none).  dG = d * U_c * SiLU'(G_c) * [G <= c], dU = d * SiLU(G_c) * [-c <= U <= c].
+// One definition, shared by the standalone kernel and the dX epilogues.
+__device__ __forceinline__ void swiglu_grad(float g, float u, float d, float c, float& dg, float& du) {
+  const float gc = fminf(g, c);
+  const float uc = fminf(fmaxf(u, -c), c);
+  const float s = sigmoid_fast(gc);
+  const float silu = gc * s;
+  const float dsilu = s * (1.0f + gc * (1.0f - s));
+  dg = (g <= c) ? d * uc * dsilu : 0.0f;
+  du = (u >= -c && u <= c) ? d * silu : 0.0f;
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -61,7 +61,8 @@ struct GmmParams {
   int kblocks;         // contraction blocks of 64 (FWD: K/64, DX: N/64)
   uint16_t* out;
   int64_t ld_out;
-  uint16_t* h_save;    // SwiGLU: bf16 pre-activation [M, 2I]
+  uint16_t* h_save;    // SwiGLU: bf16 pre-activation [M, 2I] out
+  const uint16_t* h_in;  // SwiGLU gradient: saved pre-activation [M, 2I] in
   int act_cols;        // SwiGLU: I
   float clip;          // SwiGLU: c (+inf: none)
   uint32_t* status;
@@ -91,7 +92,7 @@ struct TileInfo {
   int col0;       // first output column (SwiGLU: first activation column)
 };
 
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 __device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmParams& p, int t) {
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
@@ -104,7 +105,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmPara
   const int rt = local / p.tile_cols;
   const int ct = local - rt * p.tile_cols;
   ti.g = g;
-  ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
+  ti.col0 = ct * (EPI == EPI_SWIGLU ? BN / 2 : BN);
   ti.row0 = sm->grp_off[g] + static_cast<int64_t>(rt) * BM;
   ti.rows_valid = min(BM, sm->grp_cnt[g] - rt * BM);
   return ti;
@@ -137,7 +138,7 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&r)[3
   }
 }
 
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
   static_assert(MODE == GMM_FWD || MODE == GMM_DX, "dW runs on CTA pairs");
@@ -232,7 +233,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+        const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
         for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
@@ -244,7 +245,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j) {
-              const int col = SWIGLU ? ((j < 2) ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * (j - 2))
+              const int col = EPI == EPI_SWIGLU ? ((j < 2) ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * (j - 2))
                                      : ti.col0 + 64 * j;
               tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
             }
@@ -300,14 +301,14 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const int row_in_tile = q * 32 + lane;
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE, SWIGLU>(sm, p, t);
+      const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
       const bool row_ok = row_in_tile < ti.rows_valid;
       const int64_t row = ti.row0 + row_in_tile;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (SWIGLU) {
+      if (EPI == EPI_SWIGLU) {
         const float c = p.clip;
 #pragma unroll 1
         for (int cc = 0; cc < BN / 2; cc += 32) {
@@ -331,10 +332,48 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             for (int i = 0; i < 32; ++i) {
               const float gc = fminf(__uint_as_float(g[i]), c);
               const float uc = fminf(fmaxf(__uint_as_float(u[i]), -c), c);
-              const float sg = 1.0f / (1.0f + __expf(-gc));
+              const float sg = sigmoid_fast(gc);
               a[i] = __float_as_uint(gc * sg * uc);
             }
             store_row32(p.out + row * p.ld_out + ti.col0 + cc, a);
+          }
+        }
+      } else if (EPI == EPI_DSWIGLU) {
+        // dH from dA (this accumulator, rounded to bf16) and the saved H, row by row
+        const float c = p.clip;
+        const int I = p.act_cols;
+        const int64_t ldh = 2 * static_cast<int64_t>(I);
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 32) {
+          if (ti.col0 + cc >= p.out_cols) break;  // warp-uniform
+          uint32_t d[32];
+          tmem_ld32(taddr + cc, d);
+          tmem_ld_wait();
+          if (row_ok) {
+            const uint16_t* hg = p.h_in + row * ldh + ti.col0 + cc;
+            uint16_t* out = p.out + row * ldh + ti.col0 + cc;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 gv = ld_nc_v4(hg + 8 * v);
+              const uint4 uv = ld_nc_v4(hg + I + 8 * v);
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+              const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+              float dg[8], du[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float g = (e & 1) ? bf16_hi(gw[e >> 1]) : bf16_lo(gw[e >> 1]);
+                const float u = (e & 1) ? bf16_hi(uw[e >> 1]) : bf16_lo(uw[e >> 1]);
+                const float da = round_bf16(__uint_as_float(d[8 * v + e]));
+                swiglu_grad(g, u, da, c, dg[e], du[e]);
+              }
+              uint4 og, ou;
+              og.x = pack_bf16x2(dg[0], dg[1]); og.y = pack_bf16x2(dg[2], dg[3]);
+              og.z = pack_bf16x2(dg[4], dg[5]); og.w = pack_bf16x2(dg[6], dg[7]);
+              ou.x = pack_bf16x2(du[0], du[1]); ou.y = pack_bf16x2(du[2], du[3]);
+              ou.z = pack_bf16x2(du[4], du[5]); ou.w = pack_bf16x2(du[6], du[7]);
+              *reinterpret_cast<uint4*>(out + 8 * v) = og;
+              *reinterpret_cast<uint4*>(out + I + 8 * v) = ou;
+            }
           }
         }
       } else {
@@ -366,9 +405,9 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 }
 
 // ------------------------------------------------------------------ host side
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s) {
-  auto kern = gmm_kernel<MODE, SWIGLU>;
+  auto kern = gmm_kernel<MODE, EPI>;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -403,21 +442,24 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.clip = clip > 0.0f ? clip : INFINITY;
   CUtensorMap ta, tb;
   if (mode == GMM_FWD) {
-    const bool sw = (epilogue == MOE_EPILOGUE_SWIGLU);
+    const bool sw = (epilogue == EPI_SWIGLU);
     p.out_cols = static_cast<int>(sw ? N / 2 : N);
     p.ld_out = p.out_cols;
     p.act_cols = static_cast<int>(N / 2);
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
-    return sw ? launch_mode<GMM_FWD, true>(ta, tb, p, s) : launch_mode<GMM_FWD, false>(ta, tb, p, s);
+    return sw ? launch_mode<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s) : launch_mode<GMM_FWD, EPI_PLAIN>(ta, tb, p, s);
   }
+  const bool dsw = (epilogue == EPI_DSWIGLU);
   p.out_cols = static_cast<int>(K);
-  p.ld_out = K;
+  p.ld_out = dsw ? 2 * K : K;
+  p.act_cols = static_cast<int>(K);
+  p.h_in = h_save;
   p.tile_cols = static_cast<int>((K + BN - 1) / BN);
   p.kblocks = static_cast<int>(N / BK);
   if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
-  return launch_mode<GMM_DX, false>(ta, tb, p, s);
+  return dsw ? launch_mode<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s) : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s);
 }
 
 }  // namespace moe

@@ -68,6 +68,7 @@ struct PairParams {
   uint16_t* out;
   int64_t ld_out;
   uint16_t* h_save;
+  const uint16_t* h_in;   // SwiGLU gradient: saved pre-activation [rows, 2I]
   int act_cols;     // SwiGLU: I
   float clip;
   uint32_t* status;
@@ -108,7 +109,7 @@ struct PairTile {
   int depth;        // DW: contraction rows of the group
 };
 
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 __device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int t, uint32_t rank) {
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
@@ -122,7 +123,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const P
   PairTile ti;
   ti.g = g;
   const int first = rt * (2 * BM) + static_cast<int>(rank) * BM;
-  ti.col0 = ct * (SWIGLU ? BN / 2 : BN);
+  ti.col0 = ct * (EPI == EPI_SWIGLU ? BN / 2 : BN);
   if (MODE == GMM_DW) {
     ti.row0 = first;
     ti.rows_valid = min(BM, p.out_rows - first);
@@ -180,7 +181,7 @@ __device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16
   }
 }
 
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PairParams p) {
   constexpr bool A_MN = (MODE == GMM_DW);
@@ -301,7 +302,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const void* map_a = nullptr;
     const void* map_b = nullptr;
     for (int t = cid; t < ntiles && ok; t += ncl) {
-      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
       if (ti.kblocks == 0) continue;
       if (ti.g != cur_g) {
         // a new group: descriptors whose row 0 is the group's first row and
@@ -363,7 +364,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t it = 0;
       bool ok = true;
       for (int t = cid; t < ntiles && ok; t += ncl) {
-        const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
@@ -376,7 +377,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (MODE == GMM_FWD) {
 #pragma unroll
             for (int j = 0; j < BNH / 64; ++j) {
-              const int col = SWIGLU ? (rank == 0 ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * j)
+              const int col = EPI == EPI_SWIGLU ? (rank == 0 ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * j)
                                      : ti.col0 + static_cast<int>(rank) * BNH + 64 * j;
               tma_load_3d_pair(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
             }
@@ -401,7 +402,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int t = cid; t < ntiles && ok; t += ncl) {
-        const int kblocks = decode_pair_tile<MODE, SWIGLU>(sm, p, t, 0).kblocks;
+        const int kblocks = decode_pair_tile<MODE, EPI>(sm, p, t, 0).kblocks;
         if (kblocks == 0) continue;  // dW of an empty group: the epilogue writes zeros
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
@@ -438,7 +439,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* ebuf = ebuf_all + q * EPI_WARP_BYTES;
     uint32_t local = 0;
     for (int t = cid; t < ntiles; t += ncl) {
-      const PairTile ti = decode_pair_tile<MODE, SWIGLU>(sm, p, t, rank);
+      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
       uint16_t* obase = (MODE == GMM_DW) ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out : p.out;
       if (MODE == GMM_DW && ti.kblocks == 0) {
         // an empty group's weight gradient is zero: one 512-byte row per instruction
@@ -462,7 +463,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(release);
       };
-      if (SWIGLU) {
+      if (EPI == EPI_SWIGLU) {
         const float c = p.clip;
         const int64_t ldh = 2 * static_cast<int64_t>(p.act_cols);
         // pass 1: the activation
@@ -479,7 +480,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const float uv = round_bf16(__uint_as_float(u[i]));
             const float gc = fminf(gv, c);
             const float uc = fminf(fmaxf(uv, -c), c);
-            a[i] = __float_as_uint(gc * (1.0f / (1.0f + __expf(-gc))) * uc);
+            a[i] = __float_as_uint(gc * sigmoid_fast(gc) * uc);
           }
           stage_chunk(ebuf, lane, cc / 8, a);
         }
@@ -503,6 +504,78 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             flush_rows(ebuf, lane, p.h_save + wrow0 * ldh + part * p.act_cols + ti.col0, ldh, rows_valid, BN / 2);
             __syncwarp();
           }
+        }
+      } else if (EPI == EPI_DSWIGLU) {
+        // dH from dA (this accumulator, rounded to bf16 as a stored dA would be)
+        // and the saved H: per 64 columns, the warp loads its 32 rows of gate and
+        // up into shared memory (coalesced), each thread turns its row into dG
+        // and dU in place, and the warp writes them back (coalesced).
+        const float c = p.clip;
+        const int I = p.act_cols;
+        const int64_t ldh = 2 * static_cast<int64_t>(I);
+        uint8_t* gbuf = ebuf;                 // 32 rows x 128 bytes
+        uint8_t* ubuf = ebuf + 32 * 128;
+        const int lr = lane >> 3, lc = lane & 7;  // coalesced: 4 rows x 8 chunks per instruction
+#pragma unroll 1
+        for (int c64 = 0; c64 < BN / 64; ++c64) {
+          const int col = ti.col0 + c64 * 64;
+          const bool cols_ok = col < p.out_cols;   // warp-uniform
+          if (cols_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + lr;
+              if (r < rows_valid) {
+                const uint16_t* src = p.h_in + (wrow0 + r) * ldh + col + lc * 8;
+                const int off = r * 128 + ((lc ^ (r & 7)) * 16);
+                *reinterpret_cast<uint4*>(gbuf + off) = ld_nc_v4(src);
+                *reinterpret_cast<uint4*>(ubuf + off) = ld_nc_v4(src + I);
+              }
+            }
+          }
+          __syncwarp();
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t d[32];
+            tmem_ld32(taddr + c64 * 64 + half * 32, d);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int off = lane * 128 + (((half * 4 + q4) ^ (lane & 7)) * 16);
+              uint4 gv = *reinterpret_cast<const uint4*>(gbuf + off);
+              uint4 uv = *reinterpret_cast<const uint4*>(ubuf + off);
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+              const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+              float dg[8], du[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float g = (e & 1) ? bf16_hi(gw[e >> 1]) : bf16_lo(gw[e >> 1]);
+                const float u = (e & 1) ? bf16_hi(uw[e >> 1]) : bf16_lo(uw[e >> 1]);
+                const float da = round_bf16(__uint_as_float(d[q4 * 8 + e]));
+                swiglu_grad(g, u, da, c, dg[e], du[e]);
+              }
+              gv.x = pack_bf16x2(dg[0], dg[1]); gv.y = pack_bf16x2(dg[2], dg[3]);
+              gv.z = pack_bf16x2(dg[4], dg[5]); gv.w = pack_bf16x2(dg[6], dg[7]);
+              uv.x = pack_bf16x2(du[0], du[1]); uv.y = pack_bf16x2(du[2], du[3]);
+              uv.z = pack_bf16x2(du[4], du[5]); uv.w = pack_bf16x2(du[6], du[7]);
+              *reinterpret_cast<uint4*>(gbuf + off) = gv;
+              *reinterpret_cast<uint4*>(ubuf + off) = uv;
+            }
+          }
+          if (c64 == BN / 64 - 1) release_tmem();
+          __syncwarp();
+          if (cols_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + lr;
+              if (r < rows_valid) {
+                uint16_t* dst = obase + (wrow0 + r) * ldh + col + lc * 8;
+                const int off = r * 128 + ((lc ^ (r & 7)) * 16);
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(gbuf + off);
+                *reinterpret_cast<uint4*>(dst + I) = *reinterpret_cast<const uint4*>(ubuf + off);
+              }
+            }
+          }
+          __syncwarp();
         }
       } else {
 #pragma unroll 1
@@ -542,9 +615,9 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
-template <int MODE, bool SWIGLU>
+template <int MODE, int EPI>
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairParams& p, cudaStream_t s) {
-  auto kern = gmm_pair_kernel<MODE, SWIGLU>;
+  auto kern = gmm_pair_kernel<MODE, EPI>;
   static int configured_dev = -1;
   static int grid = 0;
   int dev = 0;
@@ -592,22 +665,25 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.clip = clip > 0.0f ? clip : INFINITY;
   CUtensorMap ta, tb;
   if (mode == GMM_FWD) {
-    const bool sw = (epilogue == MOE_EPILOGUE_SWIGLU);
+    const bool sw = (epilogue == EPI_SWIGLU);
     p.out_cols = static_cast<int>(sw ? N / 2 : N);
     p.ld_out = p.out_cols;
     p.act_cols = static_cast<int>(N / 2);
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
-    return sw ? launch_pair<GMM_FWD, true>(ta, tb, p, s) : launch_pair<GMM_FWD, false>(ta, tb, p, s);
+    return sw ? launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s) : launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, p, s);
   }
   if (mode == GMM_DX) {
+    const bool dsw = (epilogue == EPI_DSWIGLU);
     p.out_cols = static_cast<int>(K);
-    p.ld_out = K;
+    p.ld_out = dsw ? 2 * K : K;
+    p.act_cols = static_cast<int>(K);
+    p.h_in = h_save;
     p.tile_cols = static_cast<int>((K + BN - 1) / BN);
     p.kblocks = static_cast<int>(N / BK);
     if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
-    return launch_pair<GMM_DX, false>(ta, tb, p, s);
+    return dsw ? launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s) : launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, p, s);
   }
   // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
   if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
@@ -621,7 +697,7 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.ld_out = N;
   p.tile_cols = static_cast<int>((N + BN - 1) / BN);
   if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64)) return MOE_ERR_CUDA;
-  return launch_pair<GMM_DW, false>(ta, tb, p, s);
+  return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, p, s);
 }
 
 }  // namespace moe

@@ -40,6 +40,10 @@ bool make_map_3d(::CUtensorMap_st* m, const void* base, int64_t E, int64_t K, in
 
 // ---- grouped matmul (gmm.cu, gmm_pair.cu)
 enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
+// Epilogues: 0 plain store; 1 (forward) SwiGLU of the [gate | up] product, H
+// saved to h; 2 (dX) SwiGLU gradient: out = dH from dA = this product and the
+// saved pre-activation passed in h.
+enum GmmEpilogue { EPI_PLAIN = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
 constexpr int64_t kPairMinRowsPerGroup = 512;
 // GMM scratch in the workspace: per CTA, kMapSlots pairs of 128-byte TMA
 // descriptors that the dW kernel rewrites for each group.
@@ -49,7 +53,8 @@ constexpr size_t kGmmScratchBytes = static_cast<size_t>(kMaxGmmCtas) * kMapSlots
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                              uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);
-// gmm_scratch: kGmmScratchBytes of workspace (used by dW).
+// gmm_scratch: kGmmScratchBytes of workspace (used by dW).  h: SwiGLU forward
+// output of H, or the saved H read by the SwiGLU-gradient epilogue.
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);

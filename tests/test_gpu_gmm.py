@@ -192,3 +192,30 @@ def test_bad_group_list_raises_device_status(bad, M_):
     assert torch.all(y == 0)   # nothing was computed
     ws.reset()
     assert M.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("counts,K,N,clip", [
+    ([300, 0, 211, 90], 256, 512, 0.0),          # 128-row kernel
+    ([1700, 1, 130, 300], 128, 320, 0.0),        # CTA pairs, partial column tiles
+    ([2048, 0, 900, 1200], 384, 256, 1.0),       # CTA pairs, clip
+])
+def test_dx_swiglu_fused_equals_dx_then_swiglu_backward(counts, K, N, clip):
+    """gmm_backward_dx_swiglu == gmm_backward's dx followed by moe_swiglu_backward,
+    bit for bit, and both match the oracle's SwiGLU gradient on the same dA."""
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(K + N + len(counts))
+    gl = np.array(counts, np.int64)
+    M_ = int(gl.sum())
+    dy = normal_bf16(rng, (M_, N))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(N))
+    h = normal_bf16(rng, (M_, 2 * K), 1.5)
+    ws = M.Workspace(256)
+    dyd, wd, hd, gld = dev_bf16(dy), dev_bf16(w), dev_bf16(h), dev(gl)
+    dh = M.gmm_backward_dx_swiglu(dyd, wd, gld, hd, clip, ws=ws)
+    da, _ = M.gmm_backward(dev_bf16(np.zeros((M_, K), np.uint16)), wd, gld, dyd, need_dw=False, ws=ws)
+    dh_ref = M.moe_swiglu_backward(hd, da, clip, ws=ws)
+    assert M.read_status(ws) == 0
+    assert np.array_equal(host_f64(dh), host_f64(dh_ref))
+    assert_close("dh", dh, O.swiglu_backward(f64(h), host_f64(da), clip))
+    da_o, _ = O.gmm_backward(np.zeros((M_, K)), f64(w), gl, f64(dy))
+    assert_close("da", da, da_o)

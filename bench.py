@@ -38,6 +38,31 @@ from workloads import WORKLOADS, gmm_inputs, layer_inputs  # noqa: E402
 METRIC = "GMM fwd+bwd TFLOP/s and MoE-layer tokens/s on 1 GB300; % of bf16 peak / HBM BW"
 DEFAULT_WORKLOAD = "layer_train_t16384"
 
+# DRAM bytes per GMM launch (mean of the six launches of one training step),
+# from one ncu capture of the GMM sources with these hashes
+# (profiles/gmm_traffic_layer_train_t16384.md); reported only while they match.
+GMM_TRAFFIC = {
+    "workload": "layer_train_t16384",
+    "bytes_per_launch": 2.714e9,
+    "sources": {
+        "gmm.cu": "6b20128de24b671f426a8e30e793213d5e70900cf071cb434dea9bf710756605",
+        "gmm_pair.cu": "85e7139c308b823f2e8c23dda6d38d5b4e5b96101dad05d60a521930ba309b76",
+        "common.cuh": "16fca4e890f126fb8eb439df36d919c3fac0b23cf79361f65c0cd30b0f4bc4fd",
+    },
+}
+
+
+def measured_gmm_traffic(workload):
+    import hashlib
+    if workload != GMM_TRAFFIC["workload"]:
+        return None
+    csrc = os.path.join(ROOT, "moe_routed_expert_gb300", "csrc")
+    for name, digest in GMM_TRAFFIC["sources"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return GMM_TRAFFIC["bytes_per_launch"]
+
 
 # ---------------------------------------------------------------------------- helpers
 def load_peaks():
@@ -573,8 +598,9 @@ def main():
         achieved = gmm_flops / (gmm_ms / 1e3) / 1e12
         long_step = ms_per_step * args.steps > 500.0
         peak = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
+        traffic = measured_gmm_traffic(args.workload) if args.tokens is None else None
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": "gmm_kernel (all %d GMM launches of a step)" % gmm_launches,
                 "peak_kind": "bf16 dense %s, %s" % ("sustained" if long_step else "burst", peaks["source"])}
 

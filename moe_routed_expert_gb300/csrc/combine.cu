@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -52,6 +53,8 @@ __global__ void __launch_bounds__(THREADS) unpermute_kernel(const uint16_t* __re
                                                             const float* __restrict__ topk_w, int64_t H, int k,
                                                             int64_t rows_cap, uint16_t* __restrict__ y,
                                                             uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   const int64_t col = static_cast<int64_t>(blockIdx.y) * COLS_PER_BLOCK + threadIdx.x * 8;
   if (col >= H) return;
@@ -83,6 +86,8 @@ __global__ void __launch_bounds__(THREADS) unpermute_backward_kernel(
     const float* __restrict__ topk_w, int64_t H, int k, int64_t rows_cap, uint16_t* __restrict__ dy_perm,
     float* __restrict__ dprobs, uint32_t* status) {
   __shared__ float red[THREADS / 32][JB];
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j0 = 0; j0 < k; j0 += JB) {
@@ -151,6 +156,8 @@ __global__ void __launch_bounds__(THREADS) unpermute_backward_kernel(
 __global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t* __restrict__ h,
                                                                   const uint16_t* __restrict__ da, int64_t rows,
                                                                   int64_t I, float c, uint16_t* __restrict__ dh) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t per_row = I / 8;
   const int64_t items = rows * per_row;
   for (int64_t it = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x; it < items;
@@ -181,22 +188,20 @@ __global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t
 moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
                               int64_t T, int64_t H, int64_t k, uint16_t* y, uint32_t* status, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H + COLS_PER_BLOCK - 1) / COLS_PER_BLOCK));
-  if (topk_w)
-    unpermute_kernel<true><<<grid, THREADS, 0, s>>>(y_perm, row_id_map, topk_w, H, static_cast<int>(k), T * k, y,
-                                                    status);
-  else
-    unpermute_kernel<false><<<grid, THREADS, 0, s>>>(y_perm, row_id_map, nullptr, H, static_cast<int>(k), T * k, y,
-                                                     status);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t e =
+      topk_w ? launch_pdl(unpermute_kernel<true>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map, topk_w, H,
+                          static_cast<int>(k), T * k, y, status)
+             : launch_pdl(unpermute_kernel<false>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map,
+                          static_cast<const float*>(nullptr), H, static_cast<int>(k), T * k, y, status);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_id_map,
                                        const float* topk_w, int64_t T, int64_t H, int64_t k,
                                        uint16_t* dy_perm, float* dprobs, uint32_t* status, cudaStream_t s) {
-  unpermute_backward_kernel<<<static_cast<unsigned>(T), THREADS, 0, s>>>(dy, y_perm, row_id_map, topk_w, H,
-                                                                         static_cast<int>(k), T * k, dy_perm,
-                                                                         dprobs, status);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(unpermute_backward_kernel, dim3(static_cast<unsigned>(T)), dim3(THREADS), 0, s, 1, dy, y_perm,
+                    row_id_map, topk_w, H, static_cast<int>(k), T * k, dy_perm, dprobs, status) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
@@ -207,8 +212,9 @@ moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  swiglu_backward_kernel<<<static_cast<unsigned>(blocks), THREADS, 0, s>>>(h, da, rows, I, c, dh);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(swiglu_backward_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, h, da, rows, I,
+                    c, dh) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -173,6 +174,10 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     tma_prefetch_desc(&tmB);
   }
   __syncthreads();
+  // Everything above touches only shared memory and the kernel parameters, so
+  // it overlaps the tail of the previous kernel on the stream.
+  pdl_wait();
+  pdl_trigger();
   for (int e = tid; e < E; e += NUM_THREADS) {
     const int64_t c = p.group_list[e];
     if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
@@ -416,8 +421,9 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
       return MOE_ERR_CUDA;
     configured_dev = dev;
   }
-  kern<<<num_sms(), NUM_THREADS, kSmemBytes, s>>>(ta, tb, p);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_pdl(kern, dim3(num_sms()), dim3(NUM_THREADS), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace

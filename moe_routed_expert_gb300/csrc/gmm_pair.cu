@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -220,6 +221,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tma_prefetch_desc(&tmB);
   }
   __syncthreads();
+  // Everything above touches only shared memory and the kernel parameters, so
+  // it overlaps the tail of the previous kernel on the stream.
+  pdl_wait();
+  pdl_trigger();
   for (int e = tid; e < E; e += NUM_THREADS) {
     const int64_t c = p.group_list[e];
     if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
@@ -644,9 +649,9 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pai
     if (grid > kMaxGmmCtas) grid = kMaxGmmCtas;  // the descriptor slots cover this many CTAs
     configured_dev = dev;
   }
-  cfg.gridDim = dim3(grid, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return MOE_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace

@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -36,6 +37,8 @@ constexpr int SUB = CHUNK / WARPS;   // 128 slots per warp in the rank kernel
 __global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* __restrict__ ids, int64_t nslots,
                                                                 int E, int nchunks, int32_t* __restrict__ chunk_counts,
                                                                 uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += THREADS) hist[e] = 0;
   __syncthreads();
@@ -61,6 +64,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int E, int nchunks, 
   __shared__ int32_t total[kMaxExperts];
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t R_sh;
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 1) per expert: exclusive scan of its chunk counts (in place), total rows
   for (int e = warp; e < E; e += 32) {
@@ -126,6 +131,8 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
                                                                int32_t* __restrict__ row_id_map,
                                                                int32_t* __restrict__ sorted_flat) {
   extern __shared__ int32_t wbase[];  // [WARPS][E]
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < WARPS * E; i += THREADS) wbase[i] = 0;
   __syncthreads();
@@ -178,6 +185,8 @@ __global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t*
                                                                  int64_t H, int k,
                                                                  const int32_t* __restrict__ row_id_map,
                                                                  uint16_t* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nseg = (H + SEG - 1) / SEG;
   const int64_t items = nslots * nseg;
   const int lane = threadIdx.x & 31;
@@ -221,11 +230,16 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
   const int nchunks = static_cast<int>((nslots + CHUNK - 1) / CHUNK);
   int32_t* chunk_counts = static_cast<int32_t*>(scratch);
   const int e = static_cast<int>(E);
-  permute_count_kernel<<<nchunks, THREADS, e * sizeof(int32_t), s>>>(ids, nslots, e, nchunks, chunk_counts, status);
-  permute_scan_kernel<<<1, 1024, 0, s>>>(e, nchunks, nslots, chunk_counts, group_list, sorted_flat);
+  if (launch_pdl(permute_count_kernel, dim3(nchunks), dim3(THREADS), e * sizeof(int32_t), s, 1, ids, nslots, e,
+                 nchunks, chunk_counts, status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, 1, e, nchunks, nslots, chunk_counts, group_list,
+                 sorted_flat) != cudaSuccess)
+    return MOE_ERR_CUDA;
   const size_t rank_smem = static_cast<size_t>(WARPS) * e * sizeof(int32_t);
-  permute_rank_kernel<<<nchunks, THREADS, rank_smem, s>>>(ids, nslots, e, nchunks, chunk_counts, row_id_map,
-                                                          sorted_flat);
+  if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
+                 static_cast<const int32_t*>(chunk_counts), row_id_map, sorted_flat) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (x != nullptr && x_perm != nullptr && H > 0) {
     const int64_t items = nslots * ((H + SEG - 1) / SEG);
     const int64_t warps_needed = items;
@@ -233,8 +247,9 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
     const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    permute_gather_kernel<<<static_cast<unsigned>(blocks), THREADS, 0, s>>>(x, nslots, H, static_cast<int>(k),
-                                                                           row_id_map, x_perm);
+    if (launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, x, nslots, H,
+                   static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -18,18 +18,25 @@
 //     CTA's barrier;
 //   * 5 stages of 32 KB; two 256-column fp32 accumulators (all 512 TMEM columns);
 //   * the epilogue stages each warp's 32 rows x 128 columns as bf16 in
-//     shared memory (XOR-swizzled 16-byte chunks, conflict-free) and writes
-//     them back two full rows per warp instruction (coalesced), masking rows
-//     past the group end and columns past N.
+//     shared memory (XOR-swizzled 16-byte chunks, conflict-free).  A plain
+//     product leaves through TMA tile stores (two 64-column boxes per warp
+//     and half tile; the map clips columns past N); the rows of a group's last
+//     tile that end inside a warp's 32, and the SwiGLU epilogues, are written
+//     two full rows per warp instruction (coalesced), masking rows past the
+//     group end and columns past N.
 //   * dW contracts over each group's own rows.  For every group it starts, the
 //     producer warp rewrites a copy of each TMA descriptor (base address = the
 //     group's first row, row extent = the group's row count) and publishes it
 //     to a per-CTA slot in the workspace, so rows past the group end arrive as
-//     zeros from the TMA unit itself.  Groups are visited largest first so the
-//     long contractions start early.
-// Group offsets are read on the device as in gmm.cu; tiles are visited column
-// tile fastest.  Every mbarrier wait is bounded; a timeout stops all roles,
-// waits for copies in flight, frees TMEM and writes MOE_ERR_TIMEOUT.
+//     zeros from the TMA unit itself.
+//   * tiles go to the clusters as sched.cuh describes: strided over all tiles
+//     (group by group, column tile fastest), or, for a weight gradient whose
+//     operands fit in L2, a run of clusters per group sized to even out the
+//     groups' different contraction depths.  dW visits the groups largest
+//     first: the deepest tiles start together and share their operands in L2.
+// Group offsets are read on the device as in gmm.cu.  Every mbarrier wait is
+// bounded; a timeout stops all roles, waits for copies in flight, frees TMEM
+// and writes MOE_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -38,6 +45,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
+#include "sched.cuh"
 
 namespace moe {
 namespace {
@@ -54,9 +62,14 @@ constexpr int BOX_BYTES = 64 * 64 * 2;
 constexpr int EPI_ROW_BYTES = 256;              // 128 bf16 columns
 constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;   // 32 KB
+constexpr int BOX_STAGE = 32 * 128;             // one warp's 32 rows x 64 columns, bf16
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
+// dW is scheduled by group when its operands (x and dy rows of every group)
+// take at most this many bytes and at most this many groups have rows.
+constexpr int64_t kByGroupMaxBytes = 64ll << 20;
+constexpr int kByGroupMaxGroups = 32;
 
 struct PairParams {
   const int64_t* group_list;
@@ -91,14 +104,24 @@ struct __align__(128) PairSmem {
   uint32_t tmem_base;
   uint32_t abort;
   int32_t bad;
-  int32_t ntiles;
+  int32_t n_empty;                     // groups without rows
+  int32_t n_live;                      // groups with rows
+  int32_t kb_max;                      // dW: deepest contraction of a tile, in blocks of 64
+  int32_t by_group;                    // dW: tiles scheduled by group
+  uint32_t best_load;                  // dW: smallest feasible per-cluster load of the search
+  int64_t units;                       // dW: contraction blocks of all tiles
   int64_t grp_off[kMaxExperts + 1];
   int32_t grp_cnt[kMaxExperts];
-  int32_t order[kMaxExperts];          // visiting position -> expert id
-  int32_t tile_start[kMaxExperts + 1]; // tile prefix over visiting positions
+  int32_t order[kMaxExperts];          // visiting position -> group (dW: largest first)
+  int32_t tile_start[kMaxExperts + 1]; // tile prefix over visiting positions (dW: groups with rows only)
+  int32_t run_start[kMaxExperts + 1];  // dW by group: prefix over visiting positions of the cluster runs
+  int32_t empty_ids[kMaxExperts];      // dW: the groups without rows
+  int32_t live_ids[kByGroupMaxGroups]; // dW: the groups with rows, when few
+  int32_t strided_load[kMaxGmmCtas / 2];  // dW: blocks per cluster of the strided schedule
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + sizeof(PairSmem);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct PairTile {
   int g;
@@ -110,15 +133,10 @@ struct PairTile {
   int depth;        // DW: contraction rows of the group
 };
 
+// Tile `local` of group g (row tile major, column tile fastest).
 template <int MODE, int EPI>
-__device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int t, uint32_t rank) {
-  int lo = 0, hi = p.E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
-  }
-  const int g = sm->order[lo];
-  const int local = t - sm->tile_start[lo];
+__device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int g, int local,
+                                                     uint32_t rank) {
   const int rt = local / p.tile_cols;
   const int ct = local - rt * p.tile_cols;
   PairTile ti;
@@ -140,6 +158,22 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const P
   }
   return ti;
 }
+
+// The tiles of one cluster, in the order every role of the kernel visits them.
+struct ClusterTiles {
+  const PairSmem* sm;
+  int E, ncl;
+  TileWalk w;
+  __device__ __forceinline__ ClusterTiles(const PairSmem* sm_, int E_, int ncl_, int cid, bool none)
+      : sm(sm_), E(E_), ncl(ncl_) {
+    if (sm->by_group) walk_group_init(w, cid, sm->run_start, E);
+    else walk_strided_init(w, cid);
+    if (none) w.t = INT64_MAX, w.g = -1;
+  }
+  __device__ __forceinline__ bool next(TileRef& r) {
+    return sm->by_group ? walk_group_next(w, sm->tile_start, r) : walk_strided_next(w, sm->tile_start, E, ncl, r);
+  }
+};
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int lane) {
   int ok = 1;
@@ -168,6 +202,36 @@ __device__ __forceinline__ void stage_chunk(uint8_t* ebuf, int lane, int c0, con
   }
 }
 
+// The same 32 columns into the TMA store layout: two 64-column boxes of 32
+// rows x 128 bytes, 16-byte chunk j of row r at (j ^ (r & 7)) (128B swizzle).
+__device__ __forceinline__ void stage_box(uint8_t* ebuf, int lane, int cc, const uint32_t (&r)[32]) {
+  uint8_t* row = ebuf + (cc >> 6) * BOX_STAGE + lane * 128;
+  const int j0 = (cc & 63) >> 3;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 q;
+    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+    *reinterpret_cast<uint4*>(row + (((j0 + v) ^ (lane & 7)) * 16)) = q;
+  }
+}
+
+// flush_rows for the box layout.
+__device__ __forceinline__ void flush_rows_box(const uint8_t* ebuf, int lane, uint16_t* base, int64_t ld,
+                                               int rows_valid, int ncols) {
+  const int j = lane & 15;
+  const int half = lane >> 4;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int row = 2 * i + half;
+    const uint4 v = *reinterpret_cast<const uint4*>(ebuf + (j >> 3) * BOX_STAGE + row * 128 +
+                                                    (((j & 7) ^ (row & 7)) * 16));
+    if (row < rows_valid && j * 8 < ncols) *reinterpret_cast<uint4*>(base + row * ld + j * 8) = v;
+  }
+}
+
 // Write the warp's staged 32 rows x 128 columns: two rows per instruction,
 // 16 lanes x 16 bytes per row.  Rows >= rows_valid and columns >= ncols are skipped.
 __device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16_t* base, int64_t ld, int rows_valid,
@@ -184,7 +248,8 @@ __device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16
 
 template <int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PairParams p) {
+gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const PairParams p) {
   constexpr bool A_MN = (MODE == GMM_DW);
   constexpr bool B_MN = (MODE != GMM_DX);
   constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
@@ -207,6 +272,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (tid == 0) {
     sm->bad = 0;
     sm->abort = 0;
+    sm->best_load = ~0u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&sm->full[s]), 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
@@ -219,10 +285,19 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI == EPI_PLAIN) tma_prefetch_desc(&tmC);
   }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  for (int c = tid; c < kMaxGmmCtas / 2; c += NUM_THREADS) sm->strided_load[c] = 0;
+  tc_fence_before();
   __syncthreads();
-  // Everything above touches only shared memory and the kernel parameters, so
-  // it overlaps the tail of the previous kernel on the stream.
+  tc_fence_after();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy completion
+  // Everything above touches only shared memory, TMEM and the kernel
+  // parameters, so it overlaps the tail of the previous kernel on the stream.
   pdl_wait();
   pdl_trigger();
   for (int e = tid; e < E; e += NUM_THREADS) {
@@ -246,55 +321,122 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int e = tid; e < E; e += NUM_THREADS) sm->order[e] = e;
   }
   __syncthreads();
+  // Prefix over the groups of rows, over visiting positions of tiles (dW:
+  // groups with rows only), and the lists of the groups with and without rows.
   const int dw_tiles = ((p.out_rows + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+  auto tiles_of = [&](int c) -> int {
+    return (MODE == GMM_DW) ? (c > 0 ? dw_tiles : 0) : ((c + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+  };
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
-    int64_t rows = 0;
-    int32_t tiles = 0;
+    int64_t rows = 0, units = 0;
+    int32_t tiles = 0, empties = 0, kbm = 0;
     for (int e = lo; e < hi; ++e) {
-      rows += sm->grp_cnt[e];
-      tiles += (MODE == GMM_DW) ? dw_tiles : ((sm->grp_cnt[sm->order[e]] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+      const int c = sm->grp_cnt[e];
+      const int kb = (c + BK - 1) / BK;
+      rows += c;
+      tiles += tiles_of(sm->grp_cnt[sm->order[e]]);
+      units += static_cast<int64_t>(tiles_of(c)) * kb;
+      empties += (c == 0);
+      kbm = max(kbm, kb);
     }
-    int64_t rows_incl = rows;
-    int32_t tiles_incl = tiles;
+    int64_t rows_incl = rows, units_incl = units;
+    int32_t tiles_incl = tiles, empties_incl = empties;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int64_t r2 = __shfl_up_sync(0xffffffffu, rows_incl, d);
+      const int64_t u2 = __shfl_up_sync(0xffffffffu, units_incl, d);
       const int32_t t2 = __shfl_up_sync(0xffffffffu, tiles_incl, d);
-      if (lane >= d) { rows_incl += r2; tiles_incl += t2; }
+      const int32_t e2 = __shfl_up_sync(0xffffffffu, empties_incl, d);
+      if (lane >= d) { rows_incl += r2; units_incl += u2; tiles_incl += t2; empties_incl += e2; }
     }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) kbm = max(kbm, __shfl_xor_sync(0xffffffffu, kbm, d));
     int64_t rb = rows_incl - rows;
-    int32_t tb = tiles_incl - tiles;
+    int32_t tb = tiles_incl - tiles, eb = empties_incl - empties;
     for (int e = lo; e < hi; ++e) {
+      const int c = sm->grp_cnt[e];
       sm->grp_off[e] = rb;
       sm->tile_start[e] = tb;
-      rb += sm->grp_cnt[e];
-      tb += (MODE == GMM_DW) ? dw_tiles : ((sm->grp_cnt[sm->order[e]] + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+      rb += c;
+      tb += tiles_of(sm->grp_cnt[sm->order[e]]);
+      if (c == 0) sm->empty_ids[eb++] = e;
+      else if (e - eb < kByGroupMaxGroups) sm->live_ids[e - eb] = e;
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
       sm->tile_start[E] = tiles_incl;
-      sm->ntiles = tiles_incl;
+      sm->n_empty = empties_incl;
+      sm->n_live = E - empties_incl;
+      sm->kb_max = kbm;
+      sm->units = units_incl;
+      sm->by_group = 0;
       if (rows_incl > p.rows_cap) sm->bad = 1;
     }
   }
   __syncthreads();
-  if (sm->bad) {  // both CTAs of the pair read the same group_list and leave here together
-    if (tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
-    return;
+  if (MODE == GMM_DW) {
+    // Few groups whose operands fit in L2: the smallest per-cluster load L
+    // (in blocks of 64) among NUM_THREADS candidates in [lb, 2 lb), lb the
+    // larger of the deepest tile and the average; group j then gets
+    // ceil(tiles / floor(L / kb_j)) clusters.  Taken only if L is below the
+    // largest load of the strided schedule.  32-bit arithmetic: the blocks of
+    // all tiles are below 2^30 here.
+    const int nl = sm->n_live;
+    const int64_t bytes = sm->grp_off[E] * (static_cast<int64_t>(p.out_rows) + p.out_cols) * 2;
+    if (!sm->bad && nl >= 1 && nl <= kByGroupMaxGroups && nl <= ncl && bytes <= kByGroupMaxBytes &&
+        sm->units < (1ll << 30)) {
+      const uint32_t lb = max(static_cast<uint32_t>(sm->kb_max),
+                              static_cast<uint32_t>((sm->units + ncl - 1) / ncl));
+      const uint32_t L = lb + static_cast<uint32_t>((static_cast<uint64_t>(lb) * tid) / NUM_THREADS);
+      uint32_t need = 0;
+      for (int i = 0; i < nl; ++i) need += group_clusters(dw_tiles, (sm->grp_cnt[sm->live_ids[i]] + BK - 1) / BK, L, ncl);
+      const uint32_t cand = __reduce_min_sync(0xffffffffu, need <= static_cast<uint32_t>(ncl) ? L : ~0u);
+      if (lane == 0) atomicMin(&sm->best_load, cand);
+      for (int t = tid; t < sm->tile_start[E]; t += NUM_THREADS) {
+        const int g = sm->order[prefix_find(sm->tile_start, E, t)];
+        atomicAdd(&sm->strided_load[t % ncl], (sm->grp_cnt[g] + BK - 1) / BK);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t smax = 0;
+        for (int c = lane; c < ncl; c += 32) smax = max(smax, static_cast<uint32_t>(sm->strided_load[c]));
+        smax = __reduce_max_sync(0xffffffffu, smax);
+        const uint32_t best = sm->best_load;
+        if (best < smax) {
+          const int per = (E + 31) / 32;
+          const int lo = min(E, lane * per), hi = min(E, lo + per);
+          auto runs_of = [&](int j) -> int32_t {  // visiting position j
+            return static_cast<int32_t>(
+                group_clusters(dw_tiles, (sm->grp_cnt[sm->order[j]] + BK - 1) / BK, best, ncl));
+          };
+          int32_t runs = 0;
+          for (int e = lo; e < hi; ++e) runs += runs_of(e);
+          int32_t incl = runs;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const int32_t r2 = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += r2;
+          }
+          int32_t rb = incl - runs;
+          for (int e = lo; e < hi; ++e) {
+            sm->run_start[e] = rb;
+            rb += runs_of(e);
+          }
+          if (lane == 31) {
+            sm->run_start[E] = incl;
+            sm->by_group = 1;
+          }
+        }
+      }
+      __syncthreads();
+    }
   }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy completion
+  if (sm->bad && tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+  const bool no_work = sm->bad != 0;  // both CTAs of the pair read the same group_list: no tiles for either
 
   const uint32_t tmem_base = sm->tmem_base;
-  const int ntiles = sm->ntiles;
   volatile uint32_t* abort_flag = &sm->abort;
 
   if (warp == 0 && MODE == GMM_DW) {
@@ -306,9 +448,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int ok = 1, cur_g = -1, slot = -1;
     const void* map_a = nullptr;
     const void* map_b = nullptr;
-    for (int t = cid; t < ntiles && ok; t += ncl) {
-      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
-      if (ti.kblocks == 0) continue;
+    ClusterTiles tiles(sm, E, ncl, cid, no_work);
+    TileRef tr;
+    while (ok && tiles.next(tr)) {
+      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
       if (ti.g != cur_g) {
         // a new group: descriptors whose row 0 is the group's first row and
         // whose row extent is the group's row count
@@ -368,8 +511,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = cid; t < ntiles && ok; t += ncl) {
-        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
+      ClusterTiles tiles(sm, E, ncl, cid, no_work);
+      TileRef tr;
+      while (ok && tiles.next(tr)) {
+        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
@@ -406,9 +551,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (rank == 0 && lane == 0) {
       uint32_t it = 0, local = 0;
       bool ok = true;
-      for (int t = cid; t < ntiles && ok; t += ncl) {
-        const int kblocks = decode_pair_tile<MODE, EPI>(sm, p, t, 0).kblocks;
-        if (kblocks == 0) continue;  // dW of an empty group: the epilogue writes zeros
+      ClusterTiles tiles(sm, E, ncl, cid, no_work);
+      TileRef tr;
+      while (ok && tiles.next(tr)) {
+        const int kblocks = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, 0).kblocks;
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
         tc_fence_after();
@@ -442,20 +588,26 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     uint8_t* ebuf = ebuf_all + q * EPI_WARP_BYTES;
-    uint32_t local = 0;
-    for (int t = cid; t < ntiles; t += ncl) {
-      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, t, rank);
-      uint16_t* obase = (MODE == GMM_DW) ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out : p.out;
-      if (MODE == GMM_DW && ti.kblocks == 0) {
-        // an empty group's weight gradient is zero: one 512-byte row per instruction
+    if (MODE == GMM_DW && !no_work) {
+      // an empty group's weight gradient is zero: one 512-byte row per instruction
+      const int nz = sm->n_empty * dw_tiles;
+      for (int z = cid; z < nz; z += ncl) {
+        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->empty_ids[z / dw_tiles], z % dw_tiles, rank);
+        uint16_t* obase = p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out;
         const int rows_valid = ti.rows_valid - q * 32;
         const int ncols = min(BN, p.out_cols - ti.col0);
         for (int r = 0; r < 32 && r < rows_valid; ++r)
           if (lane * 8 < ncols)
             *reinterpret_cast<uint4*>(obase + (ti.row0 + q * 32 + r) * p.ld_out + ti.col0 + lane * 8) =
                 make_uint4(0, 0, 0, 0);
-        continue;
       }
+    }
+    uint32_t local = 0;
+    ClusterTiles tiles(sm, E, ncl, cid, no_work);
+    TileRef tr;
+    while (tiles.next(tr)) {
+      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
+      uint16_t* obase = (MODE == GMM_DW) ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out : p.out;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
@@ -583,24 +735,42 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           __syncwarp();
         }
       } else {
+        // dW rows come in whole warps (K is a multiple of 64); forward and dX
+        // rows past the group end can fall inside a warp's 32.
+        const int64_t grow0 = (MODE == GMM_DW) ? static_cast<int64_t>(ti.g) * p.out_rows + wrow0 : wrow0;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
+          if (lane == 0) bulk_wait_read();  // the previous stores have read the staging buffer
+          __syncwarp();
 #pragma unroll 1
           for (int cc = 0; cc < BN / 2; cc += 32) {
             uint32_t r[32];
             tmem_ld32(taddr + half * (BN / 2) + cc, r);
             tmem_ld_wait();
-            stage_chunk(ebuf, lane, cc / 8, r);
+            stage_box(ebuf, lane, cc, r);
           }
           if (half == 1) release_tmem();
-          __syncwarp();
           const int col = ti.col0 + half * (BN / 2);
-          flush_rows(ebuf, lane, obase + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
+          if (rows_valid >= 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              for (int b = 0; b < 2; ++b)
+                if (col + 64 * b < p.out_cols)
+                  tma_store_2d(&tmC, smem_u32(ebuf + b * BOX_STAGE), col + 64 * b, static_cast<int32_t>(grow0));
+              bulk_commit();
+            }
+          } else if (rows_valid > 0) {
+            __syncwarp();
+            flush_rows_box(ebuf, lane, obase + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
+          }
           __syncwarp();
         }
       }
       ++local;
     }
+    if (EPI == EPI_PLAIN && lane == 0) bulk_wait_all();  // every tile store has landed
+    __syncwarp();
   }
 
   __syncthreads();
@@ -621,7 +791,8 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 }
 
 template <int MODE, int EPI>
-moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairParams& p, cudaStream_t s) {
+moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const PairParams& p,
+                         cudaStream_t s) {
   auto kern = gmm_pair_kernel<MODE, EPI>;
   static int configured_dev = -1;
   static int grid = 0;
@@ -649,7 +820,7 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pai
     if (grid > kMaxGmmCtas) grid = kMaxGmmCtas;  // the descriptor slots cover this many CTAs
     configured_dev = dev;
   }
-  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, tc, p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -668,7 +839,7 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.out = out;
   p.h_save = h_save;
   p.clip = clip > 0.0f ? clip : INFINITY;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (mode == GMM_FWD) {
     const bool sw = (epilogue == EPI_SWIGLU);
     p.out_cols = static_cast<int>(sw ? N / 2 : N);
@@ -677,7 +848,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
-    return sw ? launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s) : launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, p, s);
+    if (sw) return launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, tb, p, s);
+    if (!make_map_2d(&tc, out, M, N, 32)) return MOE_ERR_CUDA;
+    return launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, tc, p, s);
   }
   if (mode == GMM_DX) {
     const bool dsw = (epilogue == EPI_DSWIGLU);
@@ -688,7 +861,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.tile_cols = static_cast<int>((K + BN - 1) / BN);
     p.kblocks = static_cast<int>(N / BK);
     if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
-    return dsw ? launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s) : launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, p, s);
+    if (dsw) return launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, tb, p, s);
+    if (!make_map_2d(&tc, out, M, K, 32)) return MOE_ERR_CUDA;
+    return launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, tc, p, s);
   }
   // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
   if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
@@ -701,8 +876,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.out_cols = static_cast<int>(N);
   p.ld_out = N;
   p.tile_cols = static_cast<int>((N + BN - 1) / BN);
-  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64)) return MOE_ERR_CUDA;
-  return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, p, s);
+  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64) || !make_map_2d(&tc, out, E * K, N, 32))
+    return MOE_ERR_CUDA;
+  return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, tc, p, s);
 }
 
 }  // namespace moe

@@ -75,6 +75,45 @@ def test_forward_and_dx_pair_path(counts, K, N):
     assert_close("dw", dw, dw_o)
 
 
+# Weight gradients whose groups have unequal depths, small enough for the
+# CTA-pair kernel to give each group its own run of clusters, and a single
+# group of deep tiles; one workspace serves every call, a permute included.
+BALANCE_CASES = [
+    ([512], 4096, 256),
+    ([3803, 2000, 1000, 0], 1024, 2048),
+    ([551, 443, 1656, 1018, 721, 0, 0, 3803], 1024, 2048),
+]
+
+
+@pytest.mark.parametrize("counts,K,N", BALANCE_CASES)
+def test_weight_gradient_schedules(counts, K, N):
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(sum(counts) + 7 * K)
+    gl = np.array(counts, np.int64)
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    xd, wd, gld, dyd = dev_bf16(x), dev_bf16(w), dev(gl), dev_bf16(dy)
+    ws = M.Workspace(max(M.gmm_workspace_size(M_, K, N, len(gl)), M.moe_permute_workspace_size(4096, 8, 64)))
+    ids = torch.from_numpy(rng.integers(0, 64, size=(4096, 8)).astype(np.int32)).cuda()
+    outs = []
+    for _ in range(2):
+        M.moe_permute(None, ids, 64, ws=ws)
+        y = M.gmm_forward(xd, wd, gld, ws=ws)
+        dx, dw = M.gmm_backward(xd, wd, gld, dyd, ws=ws)
+        outs.append((y, dx, dw))
+    assert M.read_status(ws) == 0
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    y, dx, dw = outs[0]
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw", dw, dw_o)
+
+
 @pytest.mark.parametrize("clip", [0.0, 2.0])
 def test_swiglu_epilogue_pair_path(clip):
     rng = np.random.default_rng(17)

@@ -298,18 +298,16 @@ class GmmStep:
         f = 2.0 * wl.M * wl.K * wl.N
         self.stages = [("gmm_fwd", self.fwd, f, 1)]
         if wl.backward:
-            self.stages += [("gmm_dx", self.bdx, f, 1), ("gmm_dw", self.bdw, f, 1)]
+            # one gmm_backward call: dX and dW (two launches, side by side when small)
+            self.stages += [("gmm_bwd_dx_dw", self.bwd, 2 * f, 2)]
         self.units = sum(s[2] for s in self.stages) / 1e12
         self.unit = "TFLOP/s"
 
     def fwd(self):
         self.M.gmm_forward(self.x, self.w, self.gl, y=self.y, ws=self.ws)
 
-    def bdx(self):
-        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, need_dw=False, dx=self.dx, ws=self.ws)
-
-    def bdw(self):
-        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, need_dx=False, dw=self.dw, ws=self.ws)
+    def bwd(self):
+        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, dx=self.dx, dw=self.dw, ws=self.ws)
 
     def e2e_host_inputs(self, inp):
         return {"x": pinned_bf16(inp["x"]), "dy": pinned_bf16(inp["dy"])}

@@ -166,13 +166,8 @@ moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* g
     if (dw && cudaMemsetAsync(dw, 0, static_cast<size_t>(E * K * N) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (dx && (st = launch_gmm(GMM_DX, 0, dy, w, group_list, M, K, N, E, 0.f, dx, nullptr, status_of(ws),
-                             after_status(ws), s)) != MOE_OK)
-    return st;
-  if (dw && (st = launch_gmm(GMM_DW, 0, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status_of(ws),
-                             after_status(ws), s)) != MOE_OK)
-    return st;
-  return MOE_OK;
+  return launch_gmm_backward(x, w, group_list, dy, M, K, N, E, EPI_PLAIN, 0.f, nullptr, dx, dw, status_of(ws),
+                             after_status(ws), s);
 }
 
 moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
@@ -339,17 +334,11 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
       MOE_OK)
     return st;
   // dH = SwiGLU'(H, dY2 @ W2^T) in one grouped matmul (dA is never stored)
-  if ((st = launch_gmm(GMM_DX, EPI_DSWIGLU, dy2, w2, saved->group_list, R, I, H, E, clip, dh, saved->h, status,
-                       gmm_scratch, s)) != MOE_OK)
+  if ((st = launch_gmm_backward(saved->a, w2, saved->group_list, dy2, R, I, H, E, EPI_DSWIGLU, clip, saved->h, dh,
+                                dw2, status, gmm_scratch, s)) != MOE_OK)
     return st;
-  if (dw2 && (st = launch_gmm(GMM_DW, 0, saved->a, dy2, saved->group_list, R, I, H, E, 0.f, dw2, nullptr, status,
-                              gmm_scratch, s)) != MOE_OK)
-    return st;
-  if ((st = launch_gmm(GMM_DX, 0, dh, w1, saved->group_list, R, H, 2 * I, E, 0.f, dx_perm, nullptr, status,
-                       gmm_scratch, s)) != MOE_OK)
-    return st;
-  if (dw1 && (st = launch_gmm(GMM_DW, 0, saved->x_perm, dh, saved->group_list, R, H, 2 * I, E, 0.f, dw1, nullptr, status,
-                              gmm_scratch, s)) != MOE_OK)
+  if ((st = launch_gmm_backward(saved->x_perm, w1, saved->group_list, dh, R, H, 2 * I, E, EPI_PLAIN, 0.f, nullptr,
+                                dx_perm, dw1, status, gmm_scratch, s)) != MOE_OK)
     return st;
   return launch_unpermute(dx_perm, saved->row_id_map, nullptr, T, H, k, dx, status, s);
 }

@@ -67,6 +67,7 @@ struct GmmParams {
   int act_cols;        // SwiGLU: I
   float clip;          // SwiGLU: c (+inf: none)
   uint32_t* status;
+  int concurrent;      // see GmmLaunch
 };
 
 struct __align__(16) GmmSmem {
@@ -176,7 +177,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   // Everything above touches only shared memory and the kernel parameters, so
   // it overlaps the tail of the previous kernel on the stream.
-  pdl_wait();
+  if (!p.concurrent) pdl_wait();
   pdl_trigger();
   for (int e = tid; e < E; e += NUM_THREADS) {
     const int64_t c = p.group_list[e];
@@ -219,6 +220,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   if (sm->bad) {
     if (tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+    if (p.concurrent && tid == 0) pdl_wait();
     return;
   }
   if (warp == 1) {
@@ -407,11 +409,13 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if (p.concurrent && tid == 0) pdl_wait();  // finish no earlier than the launch before this one
 }
 
 // ------------------------------------------------------------------ host side
 template <int MODE, int EPI>
-moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s) {
+moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s,
+                         int max_ctas) {
   auto kern = gmm_kernel<MODE, EPI>;
   static int configured_dev = -1;
   int dev = 0;
@@ -421,7 +425,8 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
       return MOE_ERR_CUDA;
     configured_dev = dev;
   }
-  if (launch_pdl(kern, dim3(num_sms()), dim3(NUM_THREADS), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
+  const int grid = (max_ctas > 0 && max_ctas < num_sms()) ? max_ctas : num_sms();
+  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -430,14 +435,16 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
 
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s) {
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
+                        const GmmLaunch& how) {
   // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
   // CTA pairs (256 x 256 tiles) for every weight gradient, and for forward and
   // dX when groups average at least 512 rows; below that the extra padding of
   // a 256-row tile costs more than the pair saves, and the 128-row kernel here
   // runs instead.
   if (mode == GMM_DW || M >= kPairMinRowsPerGroup * E)
-    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, gmm_scratch, s);
+    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, gmm_scratch, s,
+                           how);
   GmmParams p{};
   p.group_list = group_list;
   p.E = static_cast<int>(E);
@@ -446,6 +453,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.out = out;
   p.h_save = h_save;
   p.clip = clip > 0.0f ? clip : INFINITY;
+  p.concurrent = how.concurrent ? 1 : 0;
   CUtensorMap ta, tb;
   if (mode == GMM_FWD) {
     const bool sw = (epilogue == EPI_SWIGLU);
@@ -455,7 +463,8 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
-    return sw ? launch_mode<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s) : launch_mode<GMM_FWD, EPI_PLAIN>(ta, tb, p, s);
+    return sw ? launch_mode<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s, how.max_ctas)
+              : launch_mode<GMM_FWD, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
   }
   const bool dsw = (epilogue == EPI_DSWIGLU);
   p.out_cols = static_cast<int>(K);
@@ -465,7 +474,39 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.tile_cols = static_cast<int>((K + BN - 1) / BN);
   p.kblocks = static_cast<int>(N / BK);
   if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
-  return dsw ? launch_mode<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s) : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s);
+  return dsw ? launch_mode<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s, how.max_ctas)
+             : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// dX then dW.  When dX is small (at most about four waves of 256 x 256 tiles
+// on the whole GPU, counting one partial row tile per group), the two run side
+// by side: dX on half the SMs, and dW, launched right behind it with
+// programmatic serialisation, starts at once on the other half (it reads only
+// inputs that exist before dX starts) and finishes no earlier than dX.  That
+// hides the last partial wave and the prologue and epilogue of one launch.
+moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, float clip,
+                                 const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
+                                 cudaStream_t s) {
+  GmmLaunch first, second;
+  const int half = (num_sms() / 2) & ~1;
+  if (dx && dw && half >= 2 && (M / 256 + E) * ((K + 255) / 256) <= 4 * static_cast<int64_t>(half)) {
+    first.max_ctas = half;
+    second.max_ctas = num_sms() - half;
+    second.concurrent = true;
+  }
+  moe_status_t st = MOE_OK;
+  if (dx && (st = launch_gmm(GMM_DX, dx_epilogue, dy, w, group_list, M, K, N, E, clip, dx,
+                             const_cast<uint16_t*>(h), status, gmm_scratch, s, first)) != MOE_OK)
+    return st;
+  if (dw && (st = launch_gmm(GMM_DW, EPI_PLAIN, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status,
+                             gmm_scratch, s, second)) != MOE_OK)
+    return st;
+  return MOE_OK;
 }
 
 }  // namespace moe

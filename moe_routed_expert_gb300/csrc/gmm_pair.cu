@@ -70,6 +70,8 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;
 // take at most this many bytes and at most this many groups have rows.
 constexpr int64_t kByGroupMaxBytes = 64ll << 20;
 constexpr int kByGroupMaxGroups = 32;
+// A dW tile's epilogue takes about as long as this many 64-deep MMA blocks.
+constexpr uint32_t kEpilogueBlocks = 8;
 
 struct PairParams {
   const int64_t* group_list;
@@ -92,6 +94,7 @@ struct PairParams {
   int64_t a_pitch;
   int64_t b_pitch;
   uint8_t* map_slots;
+  int concurrent;   // see GmmLaunch
 };
 
 struct __align__(128) PairSmem {
@@ -106,9 +109,7 @@ struct __align__(128) PairSmem {
   int32_t bad;
   int32_t n_empty;                     // groups without rows
   int32_t n_live;                      // groups with rows
-  int32_t kb_max;                      // dW: deepest contraction of a tile, in blocks of 64
   int32_t by_group;                    // dW: tiles scheduled by group
-  uint32_t best_load;                  // dW: smallest feasible per-cluster load of the search
   int64_t units;                       // dW: contraction blocks of all tiles
   int64_t grp_off[kMaxExperts + 1];
   int32_t grp_cnt[kMaxExperts];
@@ -116,8 +117,6 @@ struct __align__(128) PairSmem {
   int32_t tile_start[kMaxExperts + 1]; // tile prefix over visiting positions (dW: groups with rows only)
   int32_t run_start[kMaxExperts + 1];  // dW by group: prefix over visiting positions of the cluster runs
   int32_t empty_ids[kMaxExperts];      // dW: the groups without rows
-  int32_t live_ids[kByGroupMaxGroups]; // dW: the groups with rows, when few
-  int32_t strided_load[kMaxGmmCtas / 2];  // dW: blocks per cluster of the strided schedule
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + sizeof(PairSmem);
@@ -132,6 +131,12 @@ struct PairTile {
   int64_t m0;       // DW: first contraction row (the group's first row)
   int depth;        // DW: contraction rows of the group
 };
+
+// Cost of a dW tile of a group with `cnt` rows, in 64-deep blocks.
+__device__ __forceinline__ uint32_t tile_cost(int cnt) {
+  const uint32_t kb = (cnt + BK - 1) / BK;
+  return kb > kEpilogueBlocks ? kb : kEpilogueBlocks;
+}
 
 // Tile `local` of group g (row tile major, column tile fastest).
 template <int MODE, int EPI>
@@ -272,7 +277,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (tid == 0) {
     sm->bad = 0;
     sm->abort = 0;
-    sm->best_load = ~0u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&sm->full[s]), 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
@@ -291,14 +295,13 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
     tmem_relinquish_pair();
   }
-  for (int c = tid; c < kMaxGmmCtas / 2; c += NUM_THREADS) sm->strided_load[c] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy completion
   // Everything above touches only shared memory, TMEM and the kernel
   // parameters, so it overlaps the tail of the previous kernel on the stream.
-  pdl_wait();
+  if (!p.concurrent) pdl_wait();
   pdl_trigger();
   for (int e = tid; e < E; e += NUM_THREADS) {
     const int64_t c = p.group_list[e];
@@ -322,7 +325,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
   __syncthreads();
   // Prefix over the groups of rows, over visiting positions of tiles (dW:
-  // groups with rows only), and the lists of the groups with and without rows.
+  // groups with rows only), and the list of the groups without rows.
   const int dw_tiles = ((p.out_rows + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
   auto tiles_of = [&](int c) -> int {
     return (MODE == GMM_DW) ? (c > 0 ? dw_tiles : 0) : ((c + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
@@ -331,7 +334,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int64_t rows = 0, units = 0;
-    int32_t tiles = 0, empties = 0, kbm = 0;
+    int32_t tiles = 0, empties = 0;
     for (int e = lo; e < hi; ++e) {
       const int c = sm->grp_cnt[e];
       const int kb = (c + BK - 1) / BK;
@@ -339,7 +342,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tiles += tiles_of(sm->grp_cnt[sm->order[e]]);
       units += static_cast<int64_t>(tiles_of(c)) * kb;
       empties += (c == 0);
-      kbm = max(kbm, kb);
     }
     int64_t rows_incl = rows, units_incl = units;
     int32_t tiles_incl = tiles, empties_incl = empties;
@@ -351,8 +353,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int32_t e2 = __shfl_up_sync(0xffffffffu, empties_incl, d);
       if (lane >= d) { rows_incl += r2; units_incl += u2; tiles_incl += t2; empties_incl += e2; }
     }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) kbm = max(kbm, __shfl_xor_sync(0xffffffffu, kbm, d));
     int64_t rb = rows_incl - rows;
     int32_t tb = tiles_incl - tiles, eb = empties_incl - empties;
     for (int e = lo; e < hi; ++e) {
@@ -362,14 +362,12 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       rb += c;
       tb += tiles_of(sm->grp_cnt[sm->order[e]]);
       if (c == 0) sm->empty_ids[eb++] = e;
-      else if (e - eb < kByGroupMaxGroups) sm->live_ids[e - eb] = e;
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
       sm->tile_start[E] = tiles_incl;
       sm->n_empty = empties_incl;
       sm->n_live = E - empties_incl;
-      sm->kb_max = kbm;
       sm->units = units_incl;
       sm->by_group = 0;
       if (rows_incl > p.rows_cap) sm->bad = 1;
@@ -377,61 +375,59 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
   __syncthreads();
   if (MODE == GMM_DW) {
-    // Few groups whose operands fit in L2: the smallest per-cluster load L
-    // (in blocks of 64) among NUM_THREADS candidates in [lb, 2 lb), lb the
-    // larger of the deepest tile and the average; group j then gets
-    // ceil(tiles / floor(L / kb_j)) clusters.  Taken only if L is below the
-    // largest load of the strided schedule.  32-bit arithmetic: the blocks of
-    // all tiles are below 2^30 here.
+    // Few groups whose operands fit in L2: warp 0 searches the smallest
+    // per-cluster load L for which every group j gets a run of
+    // ceil(tiles / floor(L / cost_j)) clusters within the grid, cost_j the
+    // tile's blocks of 64 but at least kEpilogueBlocks (a tile's epilogue
+    // takes about that long, and it bounds short tiles).  Two rounds of 32
+    // candidates (one per lane), the first over [lb, 2 lb), lb the larger of
+    // the costliest tile and the average load.  Taken when L is within 15% of
+    // the average.
     const int nl = sm->n_live;
     const int64_t bytes = sm->grp_off[E] * (static_cast<int64_t>(p.out_rows) + p.out_cols) * 2;
-    if (!sm->bad && nl >= 1 && nl <= kByGroupMaxGroups && nl <= ncl && bytes <= kByGroupMaxBytes &&
-        sm->units < (1ll << 30)) {
-      const uint32_t lb = max(static_cast<uint32_t>(sm->kb_max),
-                              static_cast<uint32_t>((sm->units + ncl - 1) / ncl));
-      const uint32_t L = lb + static_cast<uint32_t>((static_cast<uint64_t>(lb) * tid) / NUM_THREADS);
-      uint32_t need = 0;
-      for (int i = 0; i < nl; ++i) need += group_clusters(dw_tiles, (sm->grp_cnt[sm->live_ids[i]] + BK - 1) / BK, L, ncl);
-      const uint32_t cand = __reduce_min_sync(0xffffffffu, need <= static_cast<uint32_t>(ncl) ? L : ~0u);
-      if (lane == 0) atomicMin(&sm->best_load, cand);
-      for (int t = tid; t < sm->tile_start[E]; t += NUM_THREADS) {
-        const int g = sm->order[prefix_find(sm->tile_start, E, t)];
-        atomicAdd(&sm->strided_load[t % ncl], (sm->grp_cnt[g] + BK - 1) / BK);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        uint32_t smax = 0;
-        for (int c = lane; c < ncl; c += 32) smax = max(smax, static_cast<uint32_t>(sm->strided_load[c]));
-        smax = __reduce_max_sync(0xffffffffu, smax);
-        const uint32_t best = sm->best_load;
-        if (best < smax) {
-          const int per = (E + 31) / 32;
-          const int lo = min(E, lane * per), hi = min(E, lo + per);
-          auto runs_of = [&](int j) -> int32_t {  // visiting position j
-            return static_cast<int32_t>(
-                group_clusters(dw_tiles, (sm->grp_cnt[sm->order[j]] + BK - 1) / BK, best, ncl));
-          };
-          int32_t runs = 0;
-          for (int e = lo; e < hi; ++e) runs += runs_of(e);
-          int32_t incl = runs;
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const int32_t r2 = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += r2;
-          }
-          int32_t rb = incl - runs;
-          for (int e = lo; e < hi; ++e) {
-            sm->run_start[e] = rb;
-            rb += runs_of(e);
-          }
-          if (lane == 31) {
-            sm->run_start[E] = incl;
-            sm->by_group = 1;
-          }
+    if (warp == 0 && !sm->bad && nl >= 1 && nl <= kByGroupMaxGroups && nl <= ncl && bytes <= kByGroupMaxBytes &&
+        sm->units < (1ll << 18) && dw_tiles < (1 << 12)) {
+      // Lane j holds the tile cost of visiting position j; with dW visiting
+      // the groups largest first, positions [0, nl) are the groups with rows.
+      const uint32_t my_cost = lane < nl ? tile_cost(sm->grp_cnt[sm->order[lane]]) : 0;
+      const uint32_t cost_max = __reduce_max_sync(0xffffffffu, my_cost);
+      const uint32_t cost_sum = __reduce_add_sync(0xffffffffu, my_cost) * static_cast<uint32_t>(dw_tiles);
+      auto need = [&](uint32_t L) -> uint32_t {  // clusters for load L (every lane takes part)
+        uint32_t n = 0;
+#pragma unroll 1
+        for (int i = 0; i < nl; ++i) n += group_clusters(dw_tiles, __shfl_sync(0xffffffffu, my_cost, i), L, ncl);
+        return n;
+      };
+      uint32_t best = 0;
+      if (cost_sum < (1u << 20)) {  // every candidate L stays below 2^21
+        const uint32_t lb = max(cost_max, udiv_small(cost_sum + ncl - 1, ncl));
+        uint32_t lo = lb, step = (lb + 31) / 32;
+#pragma unroll 1
+        for (int round = 0; round < 2; ++round) {
+          const unsigned ok = __ballot_sync(0xffffffffu, need(lo + step * lane) <= static_cast<uint32_t>(ncl));
+          if (ok == 0) break;
+          const int f = __ffs(ok) - 1;
+          best = lo + step * f;
+          if (f == 0) break;
+          lo = lo + step * (f - 1) + 1;
+          step = (step + 30) / 31;
         }
       }
-      __syncthreads();
+      if (best != 0 && static_cast<uint64_t>(best) * ncl * 100 <= static_cast<uint64_t>(cost_sum) * 115) {
+        const int32_t runs = lane < nl ? static_cast<int32_t>(group_clusters(dw_tiles, my_cost, best, ncl)) : 0;
+        int32_t incl = runs;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int32_t r2 = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += r2;
+        }
+        const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane < nl) sm->run_start[lane] = incl - runs;
+        for (int j = nl + lane; j <= E; j += 32) sm->run_start[j] = total;
+        if (lane == 0) sm->by_group = 1;
+      }
     }
+    __syncthreads();
   }
   if (sm->bad && tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
   const bool no_work = sm->bad != 0;  // both CTAs of the pair read the same group_list: no tiles for either
@@ -736,20 +732,12 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
       } else {
         // dW rows come in whole warps (K is a multiple of 64); forward and dX
-        // rows past the group end can fall inside a warp's 32.
+        // rows past the group end can fall inside a warp's 32.  Half 0 is
+        // loaded from TMEM two 32-column chunks per wait; all of half 1 is
+        // loaded (and the accumulator released) before waiting for the
+        // staging buffer to be read by half 0's stores.
         const int64_t grow0 = (MODE == GMM_DW) ? static_cast<int64_t>(ti.g) * p.out_rows + wrow0 : wrow0;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          if (lane == 0) bulk_wait_read();  // the previous stores have read the staging buffer
-          __syncwarp();
-#pragma unroll 1
-          for (int cc = 0; cc < BN / 2; cc += 32) {
-            uint32_t r[32];
-            tmem_ld32(taddr + half * (BN / 2) + cc, r);
-            tmem_ld_wait();
-            stage_box(ebuf, lane, cc, r);
-          }
-          if (half == 1) release_tmem();
+        auto store_half = [&](int half) {
           const int col = ti.col0 + half * (BN / 2);
           if (rows_valid >= 32) {
             fence_proxy_async_smem();
@@ -765,6 +753,30 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             flush_rows_box(ebuf, lane, obase + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
           }
           __syncwarp();
+        };
+        if (lane == 0) bulk_wait_read();  // the previous tile's stores have read the staging buffer
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < BN / 2; cc += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr + cc, r0);
+          tmem_ld32(taddr + cc + 32, r1);
+          tmem_ld_wait();
+          stage_box(ebuf, lane, cc, r0);
+          stage_box(ebuf, lane, cc + 32, r1);
+        }
+        store_half(0);
+        {
+          uint32_t h[4][32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tmem_ld32(taddr + BN / 2 + 32 * i, h[i]);
+          tmem_ld_wait();
+          release_tmem();
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) stage_box(ebuf, lane, 32 * i, h[i]);
+          store_half(1);
         }
       }
       ++local;
@@ -788,11 +800,12 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+  if (p.concurrent && tid == 0) pdl_wait();  // finish no earlier than the launch before this one
 }
 
 template <int MODE, int EPI>
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const PairParams& p,
-                         cudaStream_t s) {
+                         cudaStream_t s, int max_ctas) {
   auto kern = gmm_pair_kernel<MODE, EPI>;
   static int configured_dev = -1;
   static int grid = 0;
@@ -820,7 +833,8 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
     if (grid > kMaxGmmCtas) grid = kMaxGmmCtas;  // the descriptor slots cover this many CTAs
     configured_dev = dev;
   }
-  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, tc, p) != cudaSuccess)
+  const int g = (max_ctas >= 2 && max_ctas < grid) ? (max_ctas & ~1) : grid;
+  if (launch_pdl(kern, dim3(g), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, tc, p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -830,8 +844,9 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
 // FWD (optionally with the SwiGLU epilogue), DX and DW on CTA pairs.
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip, uint16_t* out, uint16_t* h_save,
-                             uint32_t* status, void* gmm_scratch, cudaStream_t s) {
+                             uint32_t* status, void* gmm_scratch, cudaStream_t s, const GmmLaunch& how) {
   PairParams p{};
+  p.concurrent = how.concurrent ? 1 : 0;
   p.group_list = group_list;
   p.E = static_cast<int>(E);
   p.rows_cap = M;
@@ -848,9 +863,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
     if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
-    if (sw) return launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, tb, p, s);
+    if (sw) return launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, tb, p, s, how.max_ctas);
     if (!make_map_2d(&tc, out, M, N, 32)) return MOE_ERR_CUDA;
-    return launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, tc, p, s);
+    return launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);
   }
   if (mode == GMM_DX) {
     const bool dsw = (epilogue == EPI_DSWIGLU);
@@ -861,9 +876,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.tile_cols = static_cast<int>((K + BN - 1) / BN);
     p.kblocks = static_cast<int>(N / BK);
     if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
-    if (dsw) return launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, tb, p, s);
+    if (dsw) return launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, tb, p, s, how.max_ctas);
     if (!make_map_2d(&tc, out, M, K, 32)) return MOE_ERR_CUDA;
-    return launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, tc, p, s);
+    return launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);
   }
   // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
   if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
@@ -878,7 +893,7 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.tile_cols = static_cast<int>((N + BN - 1) / BN);
   if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64) || !make_map_2d(&tc, out, E * K, N, 32))
     return MOE_ERR_CUDA;
-  return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, tc, p, s);
+  return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);
 }
 
 }  // namespace moe

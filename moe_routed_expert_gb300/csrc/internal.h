@@ -50,13 +50,29 @@ constexpr int64_t kPairMinRowsPerGroup = 512;
 constexpr int kMapSlots = 6;
 constexpr int kMaxGmmCtas = 256;
 constexpr size_t kGmmScratchBytes = static_cast<size_t>(kMaxGmmCtas) * kMapSlots * 256;
+// How a grouped matmul shares the GPU with the launch before it on the stream.
+struct GmmLaunch {
+  int max_ctas = 0;         // cap on the persistent grid (0: one CTA per SM)
+  bool concurrent = false;  // start without waiting for the previous kernel (whose
+                            // inputs must not be read) and wait for it before finishing
+};
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                             uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);
+                             uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
+                             const GmmLaunch& how = GmmLaunch());
 // gmm_scratch: kGmmScratchBytes of workspace (used by dW).  h: SwiGLU forward
 // output of H, or the saved H read by the SwiGLU-gradient epilogue.
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                         int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s);
+                        uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
+                        const GmmLaunch& how = GmmLaunch());
+// dX and dW of one grouped matmul (both read only inputs that exist before
+// either starts): small problems run them side by side on halves of the GPU,
+// large ones one after the other on all of it.  `dx_epilogue` / `h` as for
+// launch_gmm's dX (plain, or the SwiGLU gradient with the saved H).
+moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, float clip,
+                                 const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
+                                 cudaStream_t s);
 
 }  // namespace moe

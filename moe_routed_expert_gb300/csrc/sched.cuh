@@ -40,15 +40,28 @@ MOE_HD int prefix_find(const Int* P, int E, int64_t v) {
   return lo;
 }
 
+// a / b for a < 2^22, b >= 1.  On the device a float quotient, exact after
+// one correction step (its error is below one there), since integer division
+// is a long dependent sequence and the schedule search does many.
+MOE_HD uint32_t udiv_small(uint32_t a, uint32_t b) {
+#if defined(__CUDA_ARCH__)
+  uint32_t q = static_cast<uint32_t>(__fdividef(static_cast<float>(a), static_cast<float>(b)));
+  if (q * b > a) --q;
+  else if ((q + 1) * b <= a) ++q;
+  return q;
+#else
+  return a / b;
+#endif
+}
+
 // Clusters that a group of `tiles` tiles of kb blocks each needs when no
 // cluster may take more than L blocks: 0 without tiles; ncl + 1 (infeasible)
-// when one tile is deeper than L.  32-bit: the callers keep every block count
-// below 2^30.
+// when one tile is deeper than L.  The callers keep tiles + L below 2^22.
 MOE_HD uint32_t group_clusters(uint32_t tiles, uint32_t kb, uint32_t L, uint32_t ncl) {
   if (tiles == 0 || kb == 0) return 0;
-  const uint32_t per = L / kb;
+  const uint32_t per = udiv_small(L, kb);
   if (per == 0) return ncl + 1;
-  return (tiles + per - 1) / per;
+  return udiv_small(tiles + per - 1, per);
 }
 
 struct TileRef {

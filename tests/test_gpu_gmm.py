@@ -114,6 +114,35 @@ def test_weight_gradient_schedules(counts, K, N):
     assert_close("dw", dw, dw_o)
 
 
+def test_backward_results_feed_the_next_launch():
+    """dX and dW of a small gmm_backward run side by side; the launch right
+    behind it on the stream (a forward over dX, then over dW's first expert)
+    must see both finished."""
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(41)
+    gl = np.array([700, 0, 1300, 520, 1550], np.int64)
+    K, N = 512, 1024
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    w2 = normal_bf16(rng, (len(gl), K, 256), 1 / np.sqrt(K))
+    w3 = normal_bf16(rng, (1, K, 64), 1 / np.sqrt(K))
+    one = np.array([N], np.int64)
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    ws = M.Workspace(256)
+    for _ in range(3):
+        dx, dw = M.gmm_backward(dev_bf16(x), dev_bf16(w), dev(gl), dev_bf16(dy), ws=ws)
+        y2 = M.gmm_forward(dx, dev_bf16(w2), dev(gl), ws=ws)                        # reads dX at once
+        y3 = M.gmm_forward(dw[0].t().contiguous(), dev_bf16(w3), dev(one), ws=ws)   # reads dW
+        assert M.read_status(ws) == 0
+        assert_close("dx", dx, dx_o)
+        assert_close("dw", dw, dw_o)
+        assert_close("forward over dx", y2, O.gmm_forward(host_f64(dx), f64(w2), gl))
+        assert_close("forward over dw[0]^T", y3, O.gmm_forward(host_f64(dw)[0].T.copy(), f64(w3), one))
+
+
 @pytest.mark.parametrize("clip", [0.0, 2.0])
 def test_swiglu_epilogue_pair_path(clip):
     rng = np.random.default_rng(17)

@@ -43,11 +43,12 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # (profiles/gmm_traffic_layer_train_t16384.md); reported only while they match.
 GMM_TRAFFIC = {
     "workload": "layer_train_t16384",
-    "bytes_per_launch": 2.714e9,
+    "bytes_per_launch": 2.701e9,
     "sources": {
-        "gmm.cu": "6b20128de24b671f426a8e30e793213d5e70900cf071cb434dea9bf710756605",
-        "gmm_pair.cu": "85e7139c308b823f2e8c23dda6d38d5b4e5b96101dad05d60a521930ba309b76",
-        "common.cuh": "16fca4e890f126fb8eb439df36d919c3fac0b23cf79361f65c0cd30b0f4bc4fd",
+        "gmm.cu": "8f092e0c820c31ae2a56b27adbf7b485b2e1a0a8e4d6144f6f6405ab023d9d3d",
+        "gmm_pair.cu": "e61019121dca19823bf8cf149c8d79f2c6104c43e39d2e48d9600a0f1744fc46",
+        "common.cuh": "5875786d34cd16a168ad7ac538a7c0270e46c1f3c2714e657ae6e42705aeeada",
+        "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365",
     },
 }
 

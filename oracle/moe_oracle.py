@@ -24,7 +24,13 @@ Sources (page title, then section):
   - section "验证项": bf16 tolerance rtol=1e-2, atol=1e-2.
 * [MegaMoE] "MegaMoE" (ops-transformer operator doc):
   - "计算公式 / 激活函数公式": sigma, SiLU, the clip value c (unset or 0 means
-    +inf), G_c = min(G, c), U_c = clip(U, -c, c), swiglu = SiLU(G_c) * U_c;
+    +inf), G_c = min(G, c), U_c = clip(U, -c, c), swiglu = SiLU(G_c) * U_c,
+    swiglustep = min(SiLU(G), c) * U_c, swigluoai = G_c * sigma(alpha G_c) *
+    (U_c + beta), situglu = beta tanh(G / beta) * sigma(G) * L(U) with
+    L(U) = U, or linear_beta tanh(U / linear_beta) when linear_beta is given;
+  - "参数说明" (activation, activation_params): the parameter lists and their
+    defaults (clamp: no clip; alpha 1.702; swigluoai beta 1.0; situglu beta
+    1.0 and no linear_beta);
   - "A16W16 非量化场景": EP Dispatch (row(i,k), rows of X_e stacked in any fixed
     order), Expert Compute (H_e = X_e W1[e], split into gate G and up U,
     Y_e = A_e W2[e]), Token Combine (y_i = sum_k w_k Y_{e_ik}[row(i,k)],
@@ -59,6 +65,10 @@ design notes of the repository):
    pipeline stores the gate_up GMM output, then applies swiglu).
 10. Rounding is round-to-nearest-even everywhere.
 11. dW is stored in bf16, like W; an empty group's dW is zero.
+12. The activation variants' gradients (the pages give none: MegaMoE is an
+    inference operator) are the derivatives of their formulas, taking every
+    min / clip kink as passing the gradient (as in reading 4): swiglustep's
+    min(SiLU(G), c) passes d/dG where SiLU(G) <= c.
 """
 from __future__ import annotations
 
@@ -69,6 +79,7 @@ __all__ = [
     "histogram", "exclusive_scan", "stable_counting_sort", "moe_permute",
     "expert_matmul", "gmm_forward", "gmm_backward",
     "sigmoid", "silu", "clip_bound", "swiglu", "swiglu_backward",
+    "ACTIVATIONS", "activation", "gated_activation", "gated_activation_backward",
     "moe_unpermute", "moe_unpermute_backward", "moe_permute_backward",
     "moe_layer_forward", "moe_layer_backward",
 ]
@@ -300,6 +311,103 @@ def swiglu_backward(h, da, clip=None, store=round_to_bf16):
 # Combine (unpermute) and its gradients -- [MegaMoE] Token Combine;
 # [PermuteGrad] sections 2.2, 2.3, 6.2
 # --------------------------------------------------------------------------
+# Gated activation variants ([MegaMoE] 激活函数公式, 参数说明)
+# --------------------------------------------------------------------------
+ACTIVATIONS = ("swiglu", "swiglustep", "swigluoai", "situglu")
+
+
+def activation(kind="swiglu", params=()):
+    """The activation and its parameters from the pages' (activation,
+    activation_params) pair, with the defaults of an empty list:
+    swiglu / swiglustep take [] or [clamp]; swigluoai [] or [clamp, alpha,
+    beta] (alpha 1.702, beta 1.0); situglu [], [beta] or [beta, linear_beta]
+    (beta 1.0, no linear_beta).  clamp 0 or absent means no clip."""
+    if kind not in ACTIVATIONS:
+        raise ValueError("unknown activation %r" % (kind,))
+    params = [float(v) for v in params]
+    a = dict(kind=kind, c=np.inf, alpha=1.702, beta=1.0, linear_beta=None)
+    if kind in ("swiglu", "swiglustep", "swigluoai"):
+        if len(params) not in ((0, 1) if kind != "swigluoai" else (0, 3)):
+            raise ValueError("bad activation_params for %s" % kind)
+        if params:
+            a["c"] = clip_bound(params[0])
+        if kind == "swigluoai" and params:
+            a["alpha"], a["beta"] = params[1], params[2]
+    else:
+        if len(params) > 2:
+            raise ValueError("bad activation_params for situglu")
+        if params:
+            a["beta"] = params[0]
+        if len(params) == 2:
+            a["linear_beta"] = params[1]
+        if not (a["beta"] > 0 and np.isfinite(a["beta"])):
+            raise ValueError("situglu beta must be finite and > 0")
+        if a["linear_beta"] is not None and not (a["linear_beta"] > 0 and np.isfinite(a["linear_beta"])):
+            raise ValueError("situglu linear_beta must be finite and > 0")
+    return a
+
+
+def gated_activation(h, act, store=round_to_bf16):
+    """A from h = [G | U] for one of the four activations (formulas above)."""
+    h = np.asarray(h, np.float64)
+    I = h.shape[1] // 2
+    g, u = h[:, :I], h[:, I:]
+    c, kind = act["c"], act["kind"]
+    if kind == "swiglu":
+        v = silu(np.minimum(g, c)) * np.clip(u, -c, c)
+    elif kind == "swiglustep":
+        v = np.minimum(silu(g), c) * np.clip(u, -c, c)
+    elif kind == "swigluoai":
+        gc = np.minimum(g, c)
+        v = gc * sigmoid(act["alpha"] * gc) * (np.clip(u, -c, c) + act["beta"])
+    else:
+        b, lb = act["beta"], act["linear_beta"]
+        lu = u if lb is None else lb * np.tanh(u / lb)
+        v = b * np.tanh(g / b) * sigmoid(g) * lu
+    return _store(store, v)
+
+
+def gated_activation_backward(h, da, act, store=round_to_bf16):
+    """dH = [dG | dU] for gated_activation, the derivative of each formula
+    (reading 12 for the kinks)."""
+    h = np.asarray(h, np.float64)
+    da = np.asarray(da, np.float64)
+    I = h.shape[1] // 2
+    g, u = h[:, :I], h[:, I:]
+    c, kind = act["c"], act["kind"]
+    in_u = (u >= -c) & (u <= c)
+    uc = np.clip(u, -c, c)
+    if kind == "swiglu":
+        gc = np.minimum(g, c)
+        s = sigmoid(gc)
+        dg = da * uc * s * (1.0 + gc * (1.0 - s)) * (g <= c)
+        du = da * silu(gc) * in_u
+    elif kind == "swiglustep":
+        s = sigmoid(g)
+        sg = silu(g)
+        dg = da * uc * s * (1.0 + g * (1.0 - s)) * (sg <= c)
+        du = da * np.minimum(sg, c) * in_u
+    elif kind == "swigluoai":
+        al, be = act["alpha"], act["beta"]
+        gc = np.minimum(g, c)
+        s = sigmoid(al * gc)
+        dg = da * (uc + be) * (s + al * gc * s * (1.0 - s)) * (g <= c)
+        du = da * gc * s * in_u
+    else:
+        b, lb = act["beta"], act["linear_beta"]
+        t = np.tanh(g / b)
+        s = sigmoid(g)
+        if lb is None:
+            lu, dlu = u, np.ones_like(u)
+        else:
+            tl = np.tanh(u / lb)
+            lu, dlu = lb * tl, 1.0 - tl * tl
+        dg = da * lu * ((1.0 - t * t) * s + b * t * s * (1.0 - s))
+        du = da * b * t * s * dlu
+    return _store(store, np.concatenate([dg, du], axis=1))
+
+
+# --------------------------------------------------------------------------
 def _slots(row_id_map, T, k):
     r = np.asarray(row_id_map, dtype=np.int64).reshape(T, k)
     return r
@@ -351,9 +459,11 @@ def moe_permute_backward(dx_perm, row_id_map, T: int, k: int, store=round_to_bf1
 # --------------------------------------------------------------------------
 # The routed-expert layer -- [GMM] "Qwen3.5 MoE 路径"; [MegaMoE] A16W16
 # --------------------------------------------------------------------------
-def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip=None, store=round_to_bf16):
+def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip=None, store=round_to_bf16, act=None):
     """permute -> GMM(gate_up) -> SwiGLU -> GMM(down) -> weighted combine.
 
+    `act` (from activation()) selects another gated activation; by default
+    SwiGLU with the clip `clip`.
     Returns (y[T, H], saved) where saved holds the tensors the backward needs:
     x_perm, group_list, row_id_map, sorted_flat, h (pre-activation), a, y2."""
     ids = np.asarray(topk_ids)
@@ -361,7 +471,7 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip=None, store=round_to_bf1
     E = np.asarray(w1).shape[0]
     x_perm, counts, row_id_map, sorted_flat = moe_permute(np.asarray(x, np.float64), ids, E)
     h = gmm_forward(x_perm, w1, counts, store)
-    a = swiglu(h, clip, store)
+    a = swiglu(h, clip, store) if act is None else gated_activation(h, act, store)
     y2 = gmm_forward(a, w2, counts, store)
     y = moe_unpermute(y2, row_id_map, topk_w, T, k, store)
     saved = dict(x_perm=x_perm, group_list=counts, row_id_map=row_id_map, sorted_flat=sorted_flat,
@@ -369,7 +479,7 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip=None, store=round_to_bf1
     return y, saved
 
 
-def moe_layer_backward(dy, saved, topk_w, w1, w2, clip=None, store=round_to_bf16):
+def moe_layer_backward(dy, saved, topk_w, w1, w2, clip=None, store=round_to_bf16, act=None):
     """Backward of moe_layer_forward.  Returns (dx[T, H], dw1, dw2, dprobs[T, k])."""
     dy = np.asarray(dy, np.float64)
     T = dy.shape[0]
@@ -378,7 +488,8 @@ def moe_layer_backward(dy, saved, topk_w, w1, w2, clip=None, store=round_to_bf16
     counts = saved["group_list"]
     dy2, dprobs = moe_unpermute_backward(dy, saved["y2"], rows, topk_w, T, k, store)
     da, dw2 = gmm_backward(saved["a"], w2, counts, dy2, store)
-    dh = swiglu_backward(saved["h"], da, clip, store)
+    dh = swiglu_backward(saved["h"], da, clip, store) if act is None else \
+        gated_activation_backward(saved["h"], da, act, store)
     dx_perm, dw1 = gmm_backward(saved["x_perm"], w1, counts, dh, store)
     dx = moe_permute_backward(dx_perm, rows, T, k, store)
     return dx, dw1, dw2, dprobs

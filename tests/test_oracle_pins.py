@@ -259,6 +259,94 @@ def test_swiglu_backward_finite_differences():
                 assert abs(fd - dh[i, j]) < 1e-7 * max(1.0, abs(fd))
 
 
+# ---------------------------------------------------------------- activation variants ([MegaMoE])
+def test_activation_parameters_and_defaults():
+    # the empty-list defaults the pages state: no clip, alpha 1.702, beta 1.0, no linear_beta
+    a = O.activation("swigluoai")
+    assert (a["c"], a["alpha"], a["beta"]) == (np.inf, 1.702, 1.0)
+    a = O.activation("situglu")
+    assert (a["beta"], a["linear_beta"]) == (1.0, None)
+    assert O.activation("swiglustep", [0.0])["c"] == np.inf          # clamp 0: no clip
+    assert O.activation("swigluoai", [5.0, 2.0, -0.5])["alpha"] == 2.0
+    assert O.activation("situglu", [2.0, 3.0])["linear_beta"] == 3.0
+    for kind, params in (("swiglu", [1.0, 2.0]), ("swigluoai", [1.0]), ("situglu", [1.0, 2.0, 3.0]),
+                         ("situglu", [0.0]), ("situglu", [1.0, -1.0]), ("gelu", [])):
+        with pytest.raises(ValueError):
+            O.activation(kind, params)
+
+
+def test_activation_variants_reduce_to_swiglu():
+    h = np.random.default_rng(21).standard_normal((6, 16)) * 3
+    for clip in (None, 1.5):
+        sw = O.swiglu(h, clip, store=None)
+        np.testing.assert_array_equal(O.gated_activation(h, O.activation("swiglu", [clip or 0.0]), store=None), sw)
+        # swigluoai with alpha = 1 and beta = 0 is G_c sigma(G_c) U_c
+        oai = O.gated_activation(h, O.activation("swigluoai", [clip or 0.0, 1.0, 0.0]), store=None)
+        np.testing.assert_allclose(oai, sw, rtol=1e-14, atol=1e-15)
+    # swiglustep without a clip is SiLU(G) U
+    np.testing.assert_allclose(O.gated_activation(h, O.activation("swiglustep"), store=None),
+                               O.swiglu(h, None, store=None), rtol=1e-14, atol=1e-15)
+    # situglu: beta tanh(G / beta) -> G as beta grows, and so does linear_beta tanh(U / linear_beta) -> U
+    big = O.gated_activation(h, O.activation("situglu", [1e6, 1e6]), store=None)
+    np.testing.assert_allclose(big, O.swiglu(h, None, store=None), rtol=1e-9, atol=1e-12)
+    big = O.gated_activation(h, O.activation("situglu", [1e6]), store=None)
+    np.testing.assert_allclose(big, O.swiglu(h, None, store=None), rtol=1e-9, atol=1e-12)
+
+
+def test_activation_variants_by_hand():
+    s = lambda z: 1.0 / (1.0 + math.exp(-z))
+    # swiglustep: SiLU(20) > c = 5 is cut to 5; U = 3 is inside the clip
+    a = O.gated_activation(np.array([[20.0, 3.0]]), O.activation("swiglustep", [5.0]), store=None)
+    assert abs(a[0, 0] - 15.0) < 1e-12
+    # ... while the gate itself is not clipped: G = -3 keeps SiLU(-3); U = 9 -> 5
+    a = O.gated_activation(np.array([[-3.0, 9.0]]), O.activation("swiglustep", [5.0]), store=None)
+    assert abs(a[0, 0] - (-3.0 * s(-3.0) * 5.0)) < 1e-12
+    # swigluoai at G = 0 is 0 whatever U; with G = c = 2, alpha = 1.702, U = 10 -> 2, beta = 1
+    oai = O.activation("swigluoai", [2.0, 1.702, 1.0])
+    assert O.gated_activation(np.array([[0.0, 5.0]]), oai, store=None)[0, 0] == 0.0
+    a = O.gated_activation(np.array([[4.0, 10.0]]), oai, store=None)
+    assert abs(a[0, 0] - 2.0 * s(1.702 * 2.0) * 3.0) < 1e-12
+    # situglu with beta = 1 at G = 1: tanh(1) sigma(1) U
+    a = O.gated_activation(np.array([[1.0, 2.0]]), O.activation("situglu", [1.0]), store=None)
+    assert abs(a[0, 0] - math.tanh(1.0) * s(1.0) * 2.0) < 1e-12
+    # situglu's L: U = linear_beta * artanh(1/2) gives L = linear_beta / 2
+    lb = 3.0
+    a = O.gated_activation(np.array([[1.0, lb * math.atanh(0.5)]]), O.activation("situglu", [1.0, lb]), store=None)
+    assert abs(a[0, 0] - math.tanh(1.0) * s(1.0) * lb / 2) < 1e-12
+    # gradients at G = 0 by hand: swigluoai d/dG = sigma(0) (U + beta); situglu d/dG = sigma(0) L(U)
+    d = O.gated_activation_backward(np.array([[0.0, 1.0]]), np.array([[1.0]]), O.activation("swigluoai"), store=None)
+    assert abs(d[0, 0] - 0.5 * 2.0) < 1e-12 and d[0, 1] == 0.0
+    d = O.gated_activation_backward(np.array([[0.0, 2.0]]), np.array([[1.0]]), O.activation("situglu"), store=None)
+    assert abs(d[0, 0] - 0.5 * 2.0) < 1e-12 and d[0, 1] == 0.0
+
+
+@pytest.mark.parametrize("kind,params", [("swiglu", [1.5]), ("swiglustep", [0.6]), ("swigluoai", [1.5, 1.702, 1.0]),
+                                         ("swigluoai", []), ("situglu", [0.7]), ("situglu", [1.3, 0.8])])
+def test_activation_variants_backward_finite_differences(kind, params):
+    act = O.activation(kind, params)
+    rng = np.random.default_rng(22)
+    h = rng.standard_normal((5, 12)) * 2
+    I = 6
+    c = act["c"]
+    if np.isfinite(c):  # stay off the kinks
+        h[np.abs(np.abs(h) - c) < 2e-2] += 0.1
+        if kind == "swiglustep":
+            g = h[:, :I]
+            near = np.abs(O.silu(g) - c) < 2e-2
+            g[near] += 0.2
+    da = rng.standard_normal((5, I))
+    dh = O.gated_activation_backward(h, da, act, store=None)
+    eps = 1e-6
+    for i in range(5):
+        for j in range(12):
+            hp, hm = h.copy(), h.copy()
+            hp[i, j] += eps
+            hm[i, j] -= eps
+            fd = (np.sum(da * O.gated_activation(hp, act, store=None)) -
+                  np.sum(da * O.gated_activation(hm, act, store=None))) / (2 * eps)
+            assert abs(fd - dh[i, j]) < 1e-7 * max(1.0, abs(fd)), (kind, i, j, fd, dh[i, j])
+
+
 # ---------------------------------------------------------------- combine and its gradients
 def test_combine_identity_route_returns_input():
     rng = np.random.default_rng(10)

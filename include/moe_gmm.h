@@ -76,6 +76,35 @@ typedef enum {
 
 enum { MOE_EPILOGUE_NONE = 0, MOE_EPILOGUE_SWIGLU = 1 };
 
+/* Gated activations of the gate_up product ([MegaMoE] 激活函数公式), with
+ * G = first I columns, U = last I columns, G_c = min(G, c), U_c = clip(U, -c, c):
+ *   swiglu      A = SiLU(G_c) * U_c
+ *   swiglustep  A = min(SiLU(G), c) * U_c
+ *   swigluoai   A = G_c * sigmoid(alpha * G_c) * (U_c + beta)
+ *   situglu     A = beta * tanh(G / beta) * sigmoid(G) * L(U),
+ *               L(U) = U, or linear_beta * tanh(U / linear_beta) when given.
+ * `params` holds the first n_params entries of the pages' activation_params
+ * list ([MegaMoE] 参数说明): swiglu and swiglustep [] or [clamp]; swigluoai
+ * [] or [clamp, alpha, beta]; situglu [], [beta] or [beta, linear_beta].
+ * Missing values take the pages' defaults: clamp none (+inf; 0 also means
+ * none), alpha 1.702, swigluoai beta 1.0, situglu beta 1.0 and L(U) = U.
+ * clamp must be >= 0 and not NaN, alpha and beta finite, situglu's beta and
+ * linear_beta finite and > 0; otherwise MOE_ERR_INVALID.  Gradients (the
+ * pages give none) are the formulas' derivatives, with every min / clip kink
+ * passing the gradient. */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,
+  MOE_ACT_SWIGLUSTEP = 1,
+  MOE_ACT_SWIGLUOAI = 2,
+  MOE_ACT_SITUGLU = 3
+} moe_act_kind_t;
+
+typedef struct {
+  int32_t kind;      /* moe_act_kind_t */
+  int32_t n_params;  /* 0 .. 3 */
+  float params[3];
+} moe_activation_t;
+
 /* Bytes at the start of every workspace that hold the device status word. */
 #define MOE_STATUS_BYTES 256
 
@@ -165,6 +194,16 @@ MOE_API moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int
                          int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* gmm_forward with a gated-activation epilogue of any kind (see
+ * moe_activation_t): N = 2I (a multiple of 256), y [M, I] = Activation(G, U)
+ * of the bf16-rounded product; h_save as for MOE_EPILOGUE_SWIGLU.
+ * activation NULL -> MOE_ERR_NULLPTR; bad parameters -> MOE_ERR_INVALID;
+ * an unknown kind -> MOE_ERR_UNSUPPORTED. */
+MOE_API moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
+                             int64_t M, int64_t K, int64_t N, int64_t E,
+                             const moe_activation_t* activation, moe_bf16* y, moe_bf16* h_save,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Grouped matmul backward: [GMM] "算子语义" backward formulas
  *   dx[s:e] = dy[s:e] @ w[g]^T            (dx [M, K], NULL to skip)
  *   dw[g]   = x[s:e]^T @ dy[s:e]          (dw [E, K, N], NULL to skip;
@@ -187,6 +226,13 @@ MOE_API moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const in
 MOE_API moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
                           const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                           moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* gmm_backward_dx_swiglu for any gated activation: dh = Activation'(h, dA).
+ * Equal, bit for bit, to gmm_backward's dx followed by moe_activation_backward. */
+MOE_API moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
+                          const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E,
+                          const moe_activation_t* activation, moe_bf16* dh,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- combine and gradients */
 
@@ -226,6 +272,12 @@ MOE_API moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, 
                                  float clip, moe_bf16* dh,
                                  void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_swiglu_backward for any gated activation (moe_activation_t): the
+ * derivative of its formula, [dG | dU] = Activation'(h) applied to da. */
+MOE_API moe_status_t moe_activation_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I,
+                                     const moe_activation_t* activation, moe_bf16* dh,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- whole layer */
 
 /* Tensors the forward keeps for the backward (all device pointers, caller-owned). */
@@ -254,6 +306,13 @@ MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_id
                                moe_bf16* y, const moe_layer_saved_t* saved,
                                void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_layer_forward with any gated activation between the two GMMs. */
+MOE_API moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
+                               const moe_bf16* w1, const moe_bf16* w2,
+                               int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                               const moe_activation_t* activation, moe_bf16* y, const moe_layer_saved_t* saved,
+                               void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Backward of moe_layer_forward (saved must be what the forward filled):
  *   dy [T, H] bf16 in; dx [T, H], dw1 [E, H, 2I], dw2 [E, I, H] bf16 and
  *   dprobs [T, k] fp32 out (any of them may be NULL except dx). */
@@ -261,6 +320,15 @@ MOE_API moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w,
                                 const moe_bf16* w1, const moe_bf16* w2,
                                 const moe_layer_saved_t* saved,
                                 int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
+                                moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Backward of moe_layer_forward_act (the same activation). */
+MOE_API moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w,
+                                const moe_bf16* w1, const moe_bf16* w2,
+                                const moe_layer_saved_t* saved,
+                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                                const moe_activation_t* activation,
                                 moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs,
                                 void* ws, size_t ws_bytes, moe_stream_t stream);
 

@@ -23,6 +23,13 @@ STATUS_NAMES = {
 }
 
 
+ACTIVATIONS = {"swiglu": 0, "swiglustep": 1, "swigluoai": 2, "situglu": 3}  # moe_act_kind_t
+
+
+class MoeActivation(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("n_params", C.c_int32), ("params", C.c_float * 3)]
+
+
 class MoeLayerSaved(C.Structure):
     _fields_ = [("x_perm", P), ("h", P), ("a", P), ("y2", P),
                 ("row_id_map", P), ("sorted_flat", P), ("group_list", P)]
@@ -38,17 +45,24 @@ SIGNATURES = {
     "gmm_workspace_size": (SZ, [I64, I64, I64, I64]),
     "gmm_forward": (ST, [P, P, P, I64, I64, I64, I64, INT, F32, P, P, P, SZ, P]),
     "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
+    "gmm_forward_act": (ST, [P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), P, P, P, SZ, P]),
     "gmm_backward_dx_swiglu": (ST, [P, P, P, P, I64, I64, I64, I64, F32, P, P, SZ, P]),
+    "gmm_backward_dx_act": (ST, [P, P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), P, P, SZ, P]),
     "moe_unpermute_workspace_size": (SZ, []),
     "moe_unpermute": (ST, [P, P, P, I64, I64, I64, P, P, SZ, P]),
     "moe_unpermute_backward": (ST, [P, P, P, P, I64, I64, I64, P, P, P, SZ, P]),
     "moe_permute_backward": (ST, [P, P, I64, I64, I64, P, P, SZ, P]),
     "moe_swiglu_backward": (ST, [P, P, I64, I64, F32, P, P, SZ, P]),
+    "moe_activation_backward": (ST, [P, P, I64, I64, C.POINTER(MoeActivation), P, P, SZ, P]),
     "moe_layer_workspace_size": (SZ, [I64, I64, I64, I64, I64]),
     "moe_layer_forward": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, F32, P, C.POINTER(MoeLayerSaved),
                                P, SZ, P]),
     "moe_layer_backward": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64, F32,
                                 P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_act": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, C.POINTER(MoeActivation), P,
+                                   C.POINTER(MoeLayerSaved), P, SZ, P]),
+    "moe_layer_backward_act": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64,
+                                    C.POINTER(MoeActivation), P, P, P, P, P, SZ, P]),
 }
 
 _lib = None

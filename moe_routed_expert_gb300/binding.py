@@ -155,11 +155,31 @@ def moe_permute_no_alloc(x: Optional[torch.Tensor], topk_ids: torch.Tensor, E: i
     return x_perm, group_list, row_id_map, sorted_flat
 
 
+# ------------------------------------------------------------------ gated activations
+def _act(activation):
+    """(kind, params) -> the C moe_activation_t: kind one of "swiglu",
+    "swiglustep", "swigluoai", "situglu"; params the activation_params list
+    (its defaults and checks are the library's)."""
+    kind, params = activation if isinstance(activation, tuple) else (activation, ())
+    if kind not in _abi.ACTIVATIONS:
+        raise ValueError("unknown activation %r" % (kind,))
+    params = [float(v) for v in params]
+    if len(params) > 3:
+        raise ValueError("at most 3 activation parameters")
+    a = _abi.MoeActivation()
+    a.kind = _abi.ACTIVATIONS[kind]
+    a.n_params = len(params)
+    for i, v in enumerate(params):
+        a.params[i] = v
+    return a
+
+
 # ------------------------------------------------------------------ grouped matmul
 def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, epilogue: int = 0,
                 clip: float = 0.0, y: Optional[torch.Tensor] = None, h_save: Optional[torch.Tensor] = None,
-                ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
-    """y = grouped x @ w (epilogue 1: SwiGLU over the [gate | up] halves)."""
+                activation=None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """y = grouped x @ w (epilogue 1: SwiGLU over the [gate | up] halves; or,
+    with `activation` = (kind, params), that gated activation)."""
     _dtype(x, BF16, "x")
     _dtype(w, BF16, "w")
     _dtype(group_list, torch.int64, "group_list")
@@ -167,10 +187,14 @@ def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, e
     E, K2, N = w.shape
     if K2 != K:
         raise ValueError("x and w disagree on K")
-    out_cols = N // 2 if epilogue == _abi.MOE_EPILOGUE_SWIGLU else N
+    out_cols = N // 2 if (epilogue == _abi.MOE_EPILOGUE_SWIGLU or activation is not None) else N
     if y is None:
         y = torch.empty(M, out_cols, dtype=BF16, device=x.device)
     wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
+    if activation is not None:
+        _check(_lib().gmm_forward_act(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, C.byref(_act(activation)),
+                                      _ptr(y), _ptr(h_save), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_forward_act")
+        return y
     _check(_lib().gmm_forward(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, int(epilogue), float(clip),
                               _ptr(y), _ptr(h_save), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_forward")
     return y
@@ -197,8 +221,10 @@ def gmm_backward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, dy:
 
 
 def gmm_backward_dx_swiglu(dy: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, h: torch.Tensor,
-                           clip: float = 0.0, *, dh=None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
-    """dh = SwiGLU gradient of h given dA = grouped dy @ w^T, in one pass (dA is not stored)."""
+                           clip: float = 0.0, *, dh=None, activation=None, ws: Optional[Workspace] = None,
+                           stream=None) -> torch.Tensor:
+    """dh = SwiGLU (or `activation`) gradient of h given dA = grouped dy @ w^T,
+    in one pass (dA is not stored)."""
     for t, n in ((dy, "dy"), (w, "w"), (h, "h")):
         _dtype(t, BF16, n)
     M, N = dy.shape
@@ -206,6 +232,11 @@ def gmm_backward_dx_swiglu(dy: torch.Tensor, w: torch.Tensor, group_list: torch.
     if dh is None:
         dh = torch.empty(M, 2 * K, dtype=BF16, device=dy.device)
     wsp = _ws(ws, gmm_workspace_size(M, K, N, E), dy.device)
+    if activation is not None:
+        _check(_lib().gmm_backward_dx_act(_ptr(dy), _ptr(w), _ptr(group_list), _ptr(h), M, K, N, E,
+                                          C.byref(_act(activation)), _ptr(dh), wsp.ptr, wsp.nbytes, _stream(stream)),
+               "gmm_backward_dx_act")
+        return dh
     _check(_lib().gmm_backward_dx_swiglu(_ptr(dy), _ptr(w), _ptr(group_list), _ptr(h), M, K, N, E, float(clip),
                                          _ptr(dh), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward_dx_swiglu")
     return dh
@@ -251,13 +282,17 @@ def moe_permute_backward(dx_perm, row_id_map, T: int, k: int, *, dx=None, ws=Non
     return dx
 
 
-def moe_swiglu_backward(h, da, clip: float = 0.0, *, dh=None, ws=None, stream=None):
+def moe_swiglu_backward(h, da, clip: float = 0.0, *, dh=None, activation=None, ws=None, stream=None):
     rows, I2 = h.shape
     _dtype(h, BF16, "h")
     _dtype(da, BF16, "da")
     if dh is None:
         dh = torch.empty_like(h)
     wsp = _ws(ws, moe_unpermute_workspace_size(), h.device)
+    if activation is not None:
+        _check(_lib().moe_activation_backward(_ptr(h), _ptr(da), rows, I2 // 2, C.byref(_act(activation)), _ptr(dh),
+                                              wsp.ptr, wsp.nbytes, _stream(stream)), "moe_activation_backward")
+        return dh
     _check(_lib().moe_swiglu_backward(_ptr(h), _ptr(da), rows, I2 // 2, float(clip), _ptr(dh),
                                       wsp.ptr, wsp.nbytes, _stream(stream)), "moe_swiglu_backward")
     return dh
@@ -283,7 +318,7 @@ class LayerSaved:
 
 
 def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: Optional[LayerSaved] = None,
-                      y=None, ws: Optional[Workspace] = None, stream=None):
+                      y=None, activation=None, ws: Optional[Workspace] = None, stream=None):
     T, H = x.shape
     E, _, I2 = w1.shape
     I = I2 // 2
@@ -296,6 +331,11 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: 
         y = torch.empty(T, H, dtype=BF16, device=x.device)
     wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), x.device)
     sv = C.byref(saved.struct()) if saved is not None else None
+    if activation is not None:
+        _check(_lib().moe_layer_forward_act(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2), T, H, I, E,
+                                            k, C.byref(_act(activation)), _ptr(y), sv, wsp.ptr, wsp.nbytes,
+                                            _stream(stream)), "moe_layer_forward_act")
+        return y
     _check(_lib().moe_layer_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2), T, H, I, E, k,
                                     float(clip), _ptr(y), sv, wsp.ptr, wsp.nbytes, _stream(stream)),
            "moe_layer_forward")
@@ -303,7 +343,7 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: 
 
 
 def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0, *, dx=None, dw1=None, dw2=None,
-                       dprobs=None, ws: Optional[Workspace] = None, stream=None):
+                       dprobs=None, activation=None, ws: Optional[Workspace] = None, stream=None):
     T, H = dy.shape
     E, _, I2 = w1.shape
     I = I2 // 2
@@ -314,6 +354,12 @@ def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0,
     dw2 = torch.empty_like(w2) if dw2 is None else dw2
     dprobs = torch.empty(T, k, dtype=torch.float32, device=dev) if dprobs is None else dprobs
     wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), dev)
+    if activation is not None:
+        _check(_lib().moe_layer_backward_act(_ptr(dy), _ptr(topk_w), _ptr(w1), _ptr(w2), C.byref(saved.struct()),
+                                             T, H, I, E, k, C.byref(_act(activation)), _ptr(dx), _ptr(dw1), _ptr(dw2),
+                                             _ptr(dprobs), wsp.ptr, wsp.nbytes, _stream(stream)),
+               "moe_layer_backward_act")
+        return dx, dw1, dw2, dprobs
     _check(_lib().moe_layer_backward(_ptr(dy), _ptr(topk_w), _ptr(w1), _ptr(w2), C.byref(saved.struct()),
                                      T, H, I, E, k, float(clip), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprobs),
                                      wsp.ptr, wsp.nbytes, _stream(stream)), "moe_layer_backward")

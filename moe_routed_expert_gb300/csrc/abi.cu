@@ -44,6 +44,55 @@ moe_status_t check_ws(const void* ws, size_t have, size_t need) {
 
 bool bad_clip(float clip) { return !(clip >= 0.0f) || isinf(clip); }  // NaN fails the first test
 
+// The ABI's (activation, activation_params) pair -> Act, with the pages'
+// defaults and value checks ([MegaMoE] 参数说明).
+moe_status_t resolve_act(const moe_activation_t* a, Act* out) {
+  if (!a) return MOE_ERR_NULLPTR;
+  const int n = a->n_params;
+  const float* v = a->params;
+  if (n < 0 || n > 3) return MOE_ERR_INVALID;
+  Act r;
+  r.kind = a->kind;
+  auto clamp_to = [&](float c) {  // >= 0, not NaN; 0 and +inf mean no clip
+    if (c > 0.0f && !isinf(c)) r.c = c;
+  };
+  switch (a->kind) {
+    case MOE_ACT_SWIGLU:
+    case MOE_ACT_SWIGLUSTEP:
+      if (n > 1 || (n == 1 && !(v[0] >= 0.0f))) return MOE_ERR_INVALID;
+      if (n == 1) clamp_to(v[0]);
+      break;
+    case MOE_ACT_SWIGLUOAI:
+      if (n != 0 && n != 3) return MOE_ERR_INVALID;
+      if (n == 3) {
+        if (!(v[0] >= 0.0f) || !isfinite(v[1]) || !isfinite(v[2])) return MOE_ERR_INVALID;
+        clamp_to(v[0]);
+        r.alpha = v[1];
+        r.beta = v[2];
+      }
+      break;
+    case MOE_ACT_SITUGLU:
+      if (n > 2) return MOE_ERR_INVALID;
+      if (n >= 1 && !(v[0] > 0.0f && isfinite(v[0]))) return MOE_ERR_INVALID;
+      if (n == 2 && !(v[1] > 0.0f && isfinite(v[1]))) return MOE_ERR_INVALID;
+      if (n >= 1) r.beta = v[0];
+      if (n == 2) r.lbeta = v[1];
+      break;
+    default:
+      return MOE_ERR_UNSUPPORTED;
+  }
+  *out = r;
+  return MOE_OK;
+}
+
+moe_activation_t swiglu_desc(float clip) {
+  moe_activation_t a = {};
+  a.kind = MOE_ACT_SWIGLU;
+  a.n_params = 1;
+  a.params[0] = clip;
+  return a;
+}
+
 size_t layer_acts_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const size_t R = static_cast<size_t>(T * k);
   const size_t fwd = align256(R * H * 2) + align256(R * I * 2) + align256(R * H * 2) + 2 * align256(R * 4) +
@@ -131,22 +180,42 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, 
 // ------------------------------------------------------------------ grouped matmul
 size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES + kGmmScratchBytes; }
 
-moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
-                         int64_t N, int64_t E, int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
-                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
+                             int64_t N, int64_t E, const moe_activation_t* activation, moe_bf16* y,
+                             moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
-  moe_status_t st = check_gmm_dims(M, K, N, E);
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
-  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_UNSUPPORTED;
-  if (epilogue == MOE_EPILOGUE_SWIGLU && N % 256) return MOE_ERR_UNSUPPORTED;
-  if (epilogue == MOE_EPILOGUE_NONE && h_save) return MOE_ERR_INVALID;
-  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  if ((st = check_gmm_dims(M, K, N, E)) != MOE_OK) return st;
+  if (N % 256) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (h_save && !aligned16(h_save)) ||
       (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
   if (M == 0) return MOE_OK;
-  return launch_gmm(GMM_FWD, epilogue, x, w, group_list, M, K, N, E, clip, y, h_save, status_of(ws),
+  return launch_gmm(GMM_FWD, EPI_SWIGLU, x, w, group_list, M, K, N, E, act, y, h_save, status_of(ws),
+                    after_status(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
+                         int64_t N, int64_t E, int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_UNSUPPORTED;
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  if (epilogue == MOE_EPILOGUE_SWIGLU) {
+    const moe_activation_t a = swiglu_desc(clip);
+    return gmm_forward_act(x, w, group_list, M, K, N, E, &a, y, h_save, ws, ws_bytes, stream);
+  }
+  if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_gmm_dims(M, K, N, E);
+  if (st != MOE_OK) return st;
+  if (h_save) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(group_list) & 7u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  return launch_gmm(GMM_FWD, EPI_PLAIN, x, w, group_list, M, K, N, E, Act(), y, nullptr, status_of(ws),
                     after_status(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -166,24 +235,34 @@ moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* g
     if (dw && cudaMemsetAsync(dw, 0, static_cast<size_t>(E * K * N) * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  return launch_gmm_backward(x, w, group_list, dy, M, K, N, E, EPI_PLAIN, 0.f, nullptr, dx, dw, status_of(ws),
+  return launch_gmm_backward(x, w, group_list, dy, M, K, N, E, EPI_PLAIN, Act(), nullptr, dx, dw, status_of(ws),
                              after_status(ws), s);
 }
 
-moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
-                                    const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
-                                    moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
+                                 const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E,
+                                 const moe_activation_t* activation, moe_bf16* dh, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
   if (!dy || !w || !group_list || !h || !dh) return MOE_ERR_NULLPTR;
-  moe_status_t st = check_gmm_dims(M, K, N, E);
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
-  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  if ((st = check_gmm_dims(M, K, N, E)) != MOE_OK) return st;
   if (!aligned16(dy) || !aligned16(w) || !aligned16(h) || !aligned16(dh) ||
       (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
   if (M == 0) return MOE_OK;
-  return launch_gmm(GMM_DX, EPI_DSWIGLU, dy, w, group_list, M, K, N, E, clip, dh, const_cast<moe_bf16*>(h),
+  return launch_gmm(GMM_DX, EPI_DSWIGLU, dy, w, group_list, M, K, N, E, act, dh, const_cast<moe_bf16*>(h),
                     status_of(ws), after_status(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
+                                    const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                                    moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  const moe_activation_t a = swiglu_desc(clip);
+  return gmm_backward_dx_act(dy, w, group_list, h, M, K, N, E, &a, dh, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ combine side
@@ -226,16 +305,26 @@ moe_status_t moe_permute_backward(const moe_bf16* dx_perm, const int32_t* row_id
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I, float clip,
-                                 moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status_t moe_activation_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I,
+                                     const moe_activation_t* activation, moe_bf16* dh, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
   if (!h || !da || !dh) return MOE_ERR_NULLPTR;
-  if (rows < 0 || I <= 0 || bad_clip(clip)) return MOE_ERR_INVALID;
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
+  if (st != MOE_OK) return st;
+  if (rows < 0 || I <= 0) return MOE_ERR_INVALID;
   if (I % 8) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(h) || !aligned16(da) || !aligned16(dh)) return MOE_ERR_INVALID;
-  moe_status_t st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES);
-  if (st != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES)) != MOE_OK) return st;
   if (rows == 0) return MOE_OK;
-  return launch_swiglu_backward(h, da, rows, I, clip, dh, reinterpret_cast<cudaStream_t>(stream));
+  return launch_act_backward(h, da, rows, I, act, dh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I, float clip,
+                                 moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  const moe_activation_t a = swiglu_desc(clip);
+  return moe_activation_backward(h, da, rows, I, &a, dh, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ whole layer
@@ -245,8 +334,8 @@ size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int6
 }
 
 namespace {
-moe_status_t check_layer(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip) {
-  if (E <= 0 || I <= 0 || k > E || bad_clip(clip)) return MOE_ERR_INVALID;
+moe_status_t check_layer(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  if (E <= 0 || I <= 0 || k > E) return MOE_ERR_INVALID;
   moe_status_t st = check_tokens(T, H, k);
   if (st != MOE_OK) return st;
   if (E > kMaxExperts || H % 64 || I % 128) return MOE_ERR_UNSUPPORTED;
@@ -261,14 +350,16 @@ bool saved_aligned(const moe_layer_saved_t* sv) {
 }
 }  // namespace
 
-moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w, const moe_bf16* w1,
-                               const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
-                               moe_bf16* y, const moe_layer_saved_t* saved, void* ws, size_t ws_bytes,
-                               moe_stream_t stream) {
+moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
+                                   const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E,
+                                   int64_t k, const moe_activation_t* activation, moe_bf16* y,
+                                   const moe_layer_saved_t* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !topk_ids || !topk_w || !w1 || !w2 || !y) return MOE_ERR_NULLPTR;
   if (saved && !saved_ok(saved)) return MOE_ERR_NULLPTR;
-  moe_status_t st = check_layer(T, H, I, E, k, clip);
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
+  if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) || (saved && !saved_aligned(saved)))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, moe_layer_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
@@ -296,23 +387,35 @@ moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const
     h = nullptr;
   }
   if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
-  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, clip, a, h, status, gmm_scratch,
-                       s)) != MOE_OK)
+  if ((st = launch_gmm(GMM_FWD, EPI_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, act, a, h, status, gmm_scratch, s)) !=
+      MOE_OK)
     return st;
-  if ((st = launch_gmm(GMM_FWD, MOE_EPILOGUE_NONE, a, w2, gl, R, I, H, E, 0.f, y2, nullptr, status, gmm_scratch, s)) !=
+  if ((st = launch_gmm(GMM_FWD, EPI_PLAIN, a, w2, gl, R, I, H, E, Act(), y2, nullptr, status, gmm_scratch, s)) !=
       MOE_OK)
     return st;
   return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
 }
 
-moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const moe_bf16* w1, const moe_bf16* w2,
-                                const moe_layer_saved_t* saved, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
-                                float clip, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
-                                size_t ws_bytes, moe_stream_t stream) {
+moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w, const moe_bf16* w1,
+                               const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
+                               moe_bf16* y, const moe_layer_saved_t* saved, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  const moe_activation_t a = swiglu_desc(clip);
+  return moe_layer_forward_act(x, topk_ids, topk_w, w1, w2, T, H, I, E, k, &a, y, saved, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w, const moe_bf16* w1,
+                                    const moe_bf16* w2, const moe_layer_saved_t* saved, int64_t T, int64_t H,
+                                    int64_t I, int64_t E, int64_t k, const moe_activation_t* activation, moe_bf16* dx,
+                                    moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
   if (!dy || !topk_w || !w1 || !w2 || !saved || !dx) return MOE_ERR_NULLPTR;
   if (!saved_ok(saved)) return MOE_ERR_NULLPTR;
-  moe_status_t st = check_layer(T, H, I, E, k, clip);
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
+  if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
   if (!aligned16(dy) || !aligned16(w1) || !aligned16(w2) || !aligned16(dx) || (dw1 && !aligned16(dw1)) ||
       (dw2 && !aligned16(dw2)) || !saved_aligned(saved))
     return MOE_ERR_INVALID;
@@ -334,13 +437,23 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
       MOE_OK)
     return st;
   // dH = SwiGLU'(H, dY2 @ W2^T) in one grouped matmul (dA is never stored)
-  if ((st = launch_gmm_backward(saved->a, w2, saved->group_list, dy2, R, I, H, E, EPI_DSWIGLU, clip, saved->h, dh,
+  if ((st = launch_gmm_backward(saved->a, w2, saved->group_list, dy2, R, I, H, E, EPI_DSWIGLU, act, saved->h, dh,
                                 dw2, status, gmm_scratch, s)) != MOE_OK)
     return st;
-  if ((st = launch_gmm_backward(saved->x_perm, w1, saved->group_list, dh, R, H, 2 * I, E, EPI_PLAIN, 0.f, nullptr,
+  if ((st = launch_gmm_backward(saved->x_perm, w1, saved->group_list, dh, R, H, 2 * I, E, EPI_PLAIN, Act(), nullptr,
                                 dx_perm, dw1, status, gmm_scratch, s)) != MOE_OK)
     return st;
   return launch_unpermute(dx_perm, saved->row_id_map, nullptr, T, H, k, dx, status, s);
+}
+
+moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const moe_bf16* w1, const moe_bf16* w2,
+                                const moe_layer_saved_t* saved, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                                float clip, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  if (bad_clip(clip)) return MOE_ERR_INVALID;
+  const moe_activation_t a = swiglu_desc(clip);
+  return moe_layer_backward_act(dy, topk_w, w1, w2, saved, T, H, I, E, k, &a, dx, dw1, dw2, dprobs, ws, ws_bytes,
+                                stream);
 }
 
 }  // extern "C"

@@ -10,7 +10,7 @@
 //                 weights.
 //   probs grad    the same article, 2.2, in the [T, topK] shape of its 6.3:
 //                 dprobs[t,j] = <dy[t], Y[row(t,j)]>, with dY[row(t,j)] = w dy[t].
-//   SwiGLU grad   "MegaMoE", 激活函数公式 (swiglu with clip c) differentiated.
+//   activation grad  "MegaMoE", 激活函数公式 (swiglu and its variants) differentiated.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(THREADS) unpermute_backward_kernel(
 }
 
 // Elementwise over rows x I: 8 columns per thread (gate at c, up at I + c).
-__global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t* __restrict__ h,
-                                                                  const uint16_t* __restrict__ da, int64_t rows,
-                                                                  int64_t I, float c, uint16_t* __restrict__ dh) {
+__global__ void __launch_bounds__(THREADS) act_backward_kernel(const uint16_t* __restrict__ h,
+                                                               const uint16_t* __restrict__ da, int64_t rows,
+                                                               int64_t I, const Act act, uint16_t* __restrict__ dh) {
   pdl_wait();
   pdl_trigger();
   const int64_t per_row = I / 8;
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(THREADS) swiglu_backward_kernel(const uint16_t
       const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
       const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
       const float d = (i & 1) ? bf16_hi(dw[i >> 1]) : bf16_lo(dw[i >> 1]);
-      swiglu_grad(g, u, d, c, dg[i], du[i]);
+      act_grad(g, u, d, act, dg[i], du[i]);
     }
     *reinterpret_cast<uint4*>(dh + r * 2 * I + col) = pack8(dg);
     *reinterpret_cast<uint4*>(dh + r * 2 * I + I + col) = pack8(du);
@@ -204,16 +204,15 @@ moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_per
              ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
-                                    uint16_t* dh, cudaStream_t s) {
-  const float c = clip > 0.0f ? clip : INFINITY;
+moe_status_t launch_act_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, const Act& act,
+                                 uint16_t* dh, cudaStream_t s) {
   const int64_t items = rows * (I / 8);
   int64_t blocks = (items + THREADS - 1) / THREADS;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_pdl(swiglu_backward_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, h, da, rows, I,
-                    c, dh) == cudaSuccess
+  return launch_pdl(act_backward_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, h, da, rows, I,
+                    act, dh) == cudaSuccess
              ? MOE_OK : MOE_ERR_CUDA;
 }
 

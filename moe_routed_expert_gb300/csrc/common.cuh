@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "internal.h"
 #include "moe_gmm.h"
 
 namespace moe {
@@ -35,18 +36,75 @@ __device__ __forceinline__ float round_bf16(float v) {
 // reciprocal (2 ulp): every use rounds its result to bf16 (8 significant bits).
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
-// SwiGLU gradient ("MegaMoE", 激活函数公式, differentiated) for one element:
-// g, u = bf16 gate / up pre-activation, d = dA (already bf16-valued), clip c
-// (+inf: none).  dG = d * U_c * SiLU'(G_c) * [G <= c], dU = d * SiLU(G_c) * [-c <= U <= c].
+// tanh from its exponential form, 1 - 2 / (1 + e^{2z}); exact at the limits
+// (e^{2z} overflows to +inf for large z, underflows to 0 for very negative z).
+__device__ __forceinline__ float tanh_fast(float z) { return 1.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * z)); }
+
+// The gated activations of "MegaMoE" (激活函数公式) for one element: g, u are
+// the bf16-valued gate / up pre-activations (see Act in internal.h).
+__device__ __forceinline__ float act_forward(float g, float u, const Act& a) {
+  const float uc = fminf(fmaxf(u, -a.c), a.c);
+  switch (a.kind) {
+    case MOE_ACT_SWIGLUSTEP: return fminf(g * sigmoid_fast(g), a.c) * uc;
+    case MOE_ACT_SWIGLUOAI: {
+      const float gc = fminf(g, a.c);
+      return gc * sigmoid_fast(a.alpha * gc) * (uc + a.beta);
+    }
+    case MOE_ACT_SITUGLU: {
+      const float lu = a.lbeta > 0.0f ? a.lbeta * tanh_fast(u / a.lbeta) : u;
+      return a.beta * tanh_fast(g / a.beta) * sigmoid_fast(g) * lu;
+    }
+    default: {
+      const float gc = fminf(g, a.c);
+      return gc * sigmoid_fast(gc) * uc;
+    }
+  }
+}
+
+// Its gradient: dG, dU from d = dA (already bf16-valued).  The pages give no
+// gradients; these are the formulas' derivatives, every min / clip kink
+// passing the gradient (d/dG = 1 where G <= c, d/dU = 1 where -c <= U <= c,
+// swiglustep's min(SiLU(G), c) where SiLU(G) <= c).  SiLU'(z) = s (1 + z (1 - s)).
 // One definition, shared by the standalone kernel and the dX epilogues.
-__device__ __forceinline__ void swiglu_grad(float g, float u, float d, float c, float& dg, float& du) {
-  const float gc = fminf(g, c);
-  const float uc = fminf(fmaxf(u, -c), c);
-  const float s = sigmoid_fast(gc);
-  const float silu = gc * s;
-  const float dsilu = s * (1.0f + gc * (1.0f - s));
-  dg = (g <= c) ? d * uc * dsilu : 0.0f;
-  du = (u >= -c && u <= c) ? d * silu : 0.0f;
+__device__ __forceinline__ void act_grad(float g, float u, float d, const Act& a, float& dg, float& du) {
+  const bool u_in = (u >= -a.c && u <= a.c);
+  const float uc = fminf(fmaxf(u, -a.c), a.c);
+  switch (a.kind) {
+    case MOE_ACT_SWIGLUSTEP: {
+      const float s = sigmoid_fast(g);
+      const float silu = g * s;
+      dg = (silu <= a.c) ? d * uc * s * (1.0f + g * (1.0f - s)) : 0.0f;
+      du = u_in ? d * fminf(silu, a.c) : 0.0f;
+      return;
+    }
+    case MOE_ACT_SWIGLUOAI: {
+      const float gc = fminf(g, a.c);
+      const float s = sigmoid_fast(a.alpha * gc);
+      dg = (g <= a.c) ? d * (uc + a.beta) * (s + a.alpha * gc * s * (1.0f - s)) : 0.0f;
+      du = u_in ? d * gc * s : 0.0f;
+      return;
+    }
+    case MOE_ACT_SITUGLU: {
+      const float t = tanh_fast(g / a.beta);
+      const float s = sigmoid_fast(g);
+      float lu = u, dlu = 1.0f;
+      if (a.lbeta > 0.0f) {
+        const float tl = tanh_fast(u / a.lbeta);
+        lu = a.lbeta * tl;
+        dlu = 1.0f - tl * tl;
+      }
+      dg = d * lu * ((1.0f - t * t) * s + a.beta * t * s * (1.0f - s));
+      du = d * a.beta * t * s * dlu;
+      return;
+    }
+    default: {
+      const float gc = fminf(g, a.c);
+      const float s = sigmoid_fast(gc);
+      dg = (g <= a.c) ? d * uc * s * (1.0f + gc * (1.0f - s)) : 0.0f;
+      du = u_in ? d * gc * s : 0.0f;
+      return;
+    }
+  }
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {

@@ -65,7 +65,7 @@ struct GmmParams {
   uint16_t* h_save;    // SwiGLU: bf16 pre-activation [M, 2I] out
   const uint16_t* h_in;  // SwiGLU gradient: saved pre-activation [M, 2I] in
   int act_cols;        // SwiGLU: I
-  float clip;          // SwiGLU: c (+inf: none)
+  Act act;             // gated activation (SwiGLU epilogues)
   uint32_t* status;
   int concurrent;      // see GmmLaunch
 };
@@ -316,7 +316,6 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (EPI == EPI_SWIGLU) {
-        const float c = p.clip;
 #pragma unroll 1
         for (int cc = 0; cc < BN / 2; cc += 32) {
           uint32_t g[32], u[32];
@@ -336,18 +335,13 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             }
             uint32_t a[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gc = fminf(__uint_as_float(g[i]), c);
-              const float uc = fminf(fmaxf(__uint_as_float(u[i]), -c), c);
-              const float sg = sigmoid_fast(gc);
-              a[i] = __float_as_uint(gc * sg * uc);
-            }
+            for (int i = 0; i < 32; ++i)
+              a[i] = __float_as_uint(act_forward(__uint_as_float(g[i]), __uint_as_float(u[i]), p.act));
             store_row32(p.out + row * p.ld_out + ti.col0 + cc, a);
           }
         }
       } else if (EPI == EPI_DSWIGLU) {
         // dH from dA (this accumulator, rounded to bf16) and the saved H, row by row
-        const float c = p.clip;
         const int I = p.act_cols;
         const int64_t ldh = 2 * static_cast<int64_t>(I);
 #pragma unroll 1
@@ -371,7 +365,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 const float g = (e & 1) ? bf16_hi(gw[e >> 1]) : bf16_lo(gw[e >> 1]);
                 const float u = (e & 1) ? bf16_hi(uw[e >> 1]) : bf16_lo(uw[e >> 1]);
                 const float da = round_bf16(__uint_as_float(d[8 * v + e]));
-                swiglu_grad(g, u, da, c, dg[e], du[e]);
+                act_grad(g, u, da, p.act, dg[e], du[e]);
               }
               uint4 og, ou;
               og.x = pack_bf16x2(dg[0], dg[1]); og.y = pack_bf16x2(dg[2], dg[3]);
@@ -434,7 +428,7 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
 }  // namespace
 
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
-                        int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                        int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                         const GmmLaunch& how) {
   // a: FWD x [M,K]; DX dy [M,N]; DW x [M,K].   b: FWD/DX w [E,K,N]; DW dy [M,N].
@@ -443,7 +437,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   // a 256-row tile costs more than the pair saves, and the 128-row kernel here
   // runs instead.
   if (mode == GMM_DW || M >= kPairMinRowsPerGroup * E)
-    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, clip, out, h_save, status, gmm_scratch, s,
+    return launch_gmm_pair(mode, epilogue, a, b, group_list, M, K, N, E, act, out, h_save, status, gmm_scratch, s,
                            how);
   GmmParams p{};
   p.group_list = group_list;
@@ -452,7 +446,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.status = status;
   p.out = out;
   p.h_save = h_save;
-  p.clip = clip > 0.0f ? clip : INFINITY;
+  p.act = act;
   p.concurrent = how.concurrent ? 1 : 0;
   CUtensorMap ta, tb;
   if (mode == GMM_FWD) {
@@ -489,7 +483,7 @@ namespace moe {
 // inputs that exist before dX starts) and finishes no earlier than dX.  That
 // hides the last partial wave and the prologue and epilogue of one launch.
 moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
-                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, float clip,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, const Act& act,
                                  const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
                                  cudaStream_t s) {
   GmmLaunch first, second;
@@ -500,10 +494,10 @@ moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int
     second.concurrent = true;
   }
   moe_status_t st = MOE_OK;
-  if (dx && (st = launch_gmm(GMM_DX, dx_epilogue, dy, w, group_list, M, K, N, E, clip, dx,
+  if (dx && (st = launch_gmm(GMM_DX, dx_epilogue, dy, w, group_list, M, K, N, E, act, dx,
                              const_cast<uint16_t*>(h), status, gmm_scratch, s, first)) != MOE_OK)
     return st;
-  if (dw && (st = launch_gmm(GMM_DW, EPI_PLAIN, x, dy, group_list, M, K, N, E, 0.f, dw, nullptr, status,
+  if (dw && (st = launch_gmm(GMM_DW, EPI_PLAIN, x, dy, group_list, M, K, N, E, Act(), dw, nullptr, status,
                              gmm_scratch, s, second)) != MOE_OK)
     return st;
   return MOE_OK;

@@ -86,7 +86,7 @@ struct PairParams {
   uint16_t* h_save;
   const uint16_t* h_in;   // SwiGLU gradient: saved pre-activation [rows, 2I]
   int act_cols;     // SwiGLU: I
-  float clip;
+  Act act;          // gated activation (SwiGLU epilogues)
   uint32_t* status;
   // dW: the operands' bases and row pitches, and kMapSlots descriptor pairs per CTA
   const uint8_t* a_base;
@@ -617,7 +617,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) mbar_arrive_cluster(release);
       };
       if (EPI == EPI_SWIGLU) {
-        const float c = p.clip;
         const int64_t ldh = 2 * static_cast<int64_t>(p.act_cols);
         // pass 1: the activation
 #pragma unroll 1
@@ -631,9 +630,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           for (int i = 0; i < 32; ++i) {
             const float gv = round_bf16(__uint_as_float(g[i]));  // H is stored in bf16
             const float uv = round_bf16(__uint_as_float(u[i]));
-            const float gc = fminf(gv, c);
-            const float uc = fminf(fmaxf(uv, -c), c);
-            a[i] = __float_as_uint(gc * sigmoid_fast(gc) * uc);
+            a[i] = __float_as_uint(act_forward(gv, uv, p.act));
           }
           stage_chunk(ebuf, lane, cc / 8, a);
         }
@@ -663,7 +660,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // and the saved H: per 64 columns, the warp loads its 32 rows of gate and
         // up into shared memory (coalesced), each thread turns its row into dG
         // and dU in place, and the warp writes them back (coalesced).
-        const float c = p.clip;
         const int I = p.act_cols;
         const int64_t ldh = 2 * static_cast<int64_t>(I);
         uint8_t* gbuf = ebuf;                 // 32 rows x 128 bytes
@@ -704,7 +700,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const float g = (e & 1) ? bf16_hi(gw[e >> 1]) : bf16_lo(gw[e >> 1]);
                 const float u = (e & 1) ? bf16_hi(uw[e >> 1]) : bf16_lo(uw[e >> 1]);
                 const float da = round_bf16(__uint_as_float(d[q4 * 8 + e]));
-                swiglu_grad(g, u, da, c, dg[e], du[e]);
+                act_grad(g, u, da, p.act, dg[e], du[e]);
               }
               gv.x = pack_bf16x2(dg[0], dg[1]); gv.y = pack_bf16x2(dg[2], dg[3]);
               gv.z = pack_bf16x2(dg[4], dg[5]); gv.w = pack_bf16x2(dg[6], dg[7]);
@@ -843,7 +839,7 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
 
 // FWD (optionally with the SwiGLU epilogue), DX and DW on CTA pairs.
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
-                             int64_t M, int64_t K, int64_t N, int64_t E, float clip, uint16_t* out, uint16_t* h_save,
+                             int64_t M, int64_t K, int64_t N, int64_t E, const Act& act, uint16_t* out, uint16_t* h_save,
                              uint32_t* status, void* gmm_scratch, cudaStream_t s, const GmmLaunch& how) {
   PairParams p{};
   p.concurrent = how.concurrent ? 1 : 0;
@@ -853,7 +849,7 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   p.status = status;
   p.out = out;
   p.h_save = h_save;
-  p.clip = clip > 0.0f ? clip : INFINITY;
+  p.act = act;
   CUtensorMap ta, tb, tc;
   if (mode == GMM_FWD) {
     const bool sw = (epilogue == EPI_SWIGLU);

@@ -14,6 +14,25 @@ namespace moe {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 64;
 
+// Gated activation of the gate_up product ("MegaMoE", 激活函数公式), resolved
+// from the ABI's (activation, activation_params) pair with the pages'
+// defaults: swiglu SiLU(G_c) U_c; swiglustep min(SiLU(G), c) U_c; swigluoai
+// G_c sigma(alpha G_c) (U_c + beta); situglu beta tanh(G / beta) sigma(G) L(U),
+// L(U) = U, or lbeta tanh(U / lbeta) when lbeta > 0.  G_c = min(G, c),
+// U_c = clip(U, -c, c); c = +inf when no clip is configured.
+struct Act {
+  int kind = MOE_ACT_SWIGLU;
+  float c = __builtin_huge_valf();
+  float alpha = 1.702f;
+  float beta = 1.0f;
+  float lbeta = 0.0f;
+};
+inline Act act_swiglu(float clip) {
+  Act a;
+  if (clip > 0.0f) a.c = clip;
+  return a;
+}
+
 // Workspace layout: [status block | op scratch ...], every piece 256-byte aligned.
 inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
@@ -31,8 +50,8 @@ moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map,
 moe_status_t launch_unpermute_backward(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_id_map,
                                        const float* topk_w, int64_t T, int64_t H, int64_t k,
                                        uint16_t* dy_perm, float* dprobs, uint32_t* status, cudaStream_t s);
-moe_status_t launch_swiglu_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, float clip,
-                                    uint16_t* dh, cudaStream_t s);
+moe_status_t launch_act_backward(const uint16_t* h, const uint16_t* da, int64_t rows, int64_t I, const Act& act,
+                                 uint16_t* dh, cudaStream_t s);
 
 // ---- TMA descriptors (tmap.cu): bf16, 128B swizzle, 64-element inner box
 bool make_map_2d(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t cols, int box_rows);
@@ -57,13 +76,13 @@ struct GmmLaunch {
                             // inputs must not be read) and wait for it before finishing
 };
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
-                             int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                             int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                              uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                              const GmmLaunch& how = GmmLaunch());
 // gmm_scratch: kGmmScratchBytes of workspace (used by dW).  h: SwiGLU forward
 // output of H, or the saved H read by the SwiGLU-gradient epilogue.
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
-                        int64_t M, int64_t K, int64_t N, int64_t E, float clip,
+                        int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                         const GmmLaunch& how = GmmLaunch());
 // dX and dW of one grouped matmul (both read only inputs that exist before
@@ -71,7 +90,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
 // large ones one after the other on all of it.  `dx_epilogue` / `h` as for
 // launch_gmm's dX (plain, or the SwiGLU gradient with the saved H).
 moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
-                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, float clip,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, const Act& act,
                                  const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
                                  cudaStream_t s);
 

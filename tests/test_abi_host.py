@@ -97,6 +97,42 @@ def test_null_and_invalid_arguments_fail_on_the_host(lib):
     assert lib.moe_workspace_init(FAKE, 16, None) == 2
 
 
+def test_activation_descriptor_checks(lib):
+    """The (activation, activation_params) pair is checked on the host with the
+    pages' rules: parameter counts per kind, clamp >= 0 and not NaN, finite
+    alpha / beta, situglu's beta and linear_beta finite and > 0."""
+    from moe_routed_expert_gb300 import _abi
+    ws, nws = FAKE, 1 << 20
+
+    def act(kind, *params):
+        a = _abi.MoeActivation()
+        a.kind, a.n_params = kind, len(params)
+        for i, v in enumerate(params):
+            a.params[i] = v
+        return C.byref(a)
+
+    def fwd(a):
+        return lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 256, 4, a, FAKE, None, ws, nws, None)
+
+    SW, STEP, OAI, SITU = 0, 1, 2, 3
+    nan, inf = float("nan"), float("inf")
+    assert fwd(None) == 1
+    for bad in (act(SW, 1.0, 2.0), act(SW, -1.0), act(STEP, nan), act(OAI, 1.0), act(OAI, 1.0, inf, 1.0),
+                act(OAI, 1.0, 1.0, nan), act(OAI, -2.0, 1.0, 1.0), act(SITU, 0.0), act(SITU, -1.0),
+                act(SITU, 1.0, 0.0), act(SITU, inf), act(SITU, 1.0, 2.0, 3.0)):
+        assert fwd(bad) == 2
+    assert fwd(act(7)) == 3                                                   # unknown kind
+    assert lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 192, 4, act(SW), FAKE, None, ws, nws, None) == 3  # N
+    # valid descriptors get past the checks: a misaligned x is then what fails
+    for good in (act(SW), act(SW, 0.0), act(STEP, 7.0), act(OAI), act(OAI, inf, 1.702, 1.0), act(SITU),
+                 act(SITU, 2.0), act(SITU, 2.0, 3.0)):
+        assert lib.gmm_forward_act(MIS, FAKE, FAKE, 64, 128, 256, 4, good, FAKE, None, ws, nws, None) == 2
+    assert lib.moe_activation_backward(FAKE, FAKE, 8, 64, act(SITU, -1.0), FAKE, ws, nws, None) == 2
+    assert lib.gmm_backward_dx_act(FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, None, FAKE, ws, nws, None) == 1
+    assert lib.moe_layer_forward_act(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 128, 4, 2, act(OAI, 1.0), FAKE, None,
+                                     ws, nws, None) == 2
+
+
 def test_python_binding_refuses_cpu_tensors(lib):
     import torch
     import moe_routed_expert_gb300 as M

@@ -287,3 +287,54 @@ def test_dx_swiglu_fused_equals_dx_then_swiglu_backward(counts, K, N, clip):
     assert_close("dh", dh, O.swiglu_backward(f64(h), host_f64(da), clip))
     da_o, _ = O.gmm_backward(np.zeros((M_, K)), f64(w), gl, f64(dy))
     assert_close("da", da, da_o)
+
+
+# ---------------------------------------------------------------- gated activation variants ([MegaMoE])
+ACT_CASES = [("swiglu", [1.5]), ("swiglustep", [1.5]), ("swigluoai", []), ("swigluoai", [2.0, 1.2, 0.5]),
+             ("situglu", [1.5]), ("situglu", [2.0, 0.8])]
+
+
+@pytest.mark.parametrize("kind,params", ACT_CASES)
+@pytest.mark.parametrize("counts", [[1500, 3, 0, 1100], [300, 90, 0, 150]])   # CTA pairs; 128-row kernel
+def test_activation_epilogue(kind, params, counts):
+    """The gate_up forward with each activation: H matches the oracle's product,
+    A the oracle's activation of the stored H."""
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(31 + sum(counts))
+    gl = np.array(counts, np.int64)
+    K, I = 256, 384
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, 2 * I), 2 / np.sqrt(K))
+    import torch
+    h = torch.empty(M_, 2 * I, dtype=torch.bfloat16, device="cuda")
+    ws = M.Workspace(256)
+    a = M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), h_save=h, activation=(kind, params), ws=ws)
+    assert M.read_status(ws) == 0
+    assert_close("h", h, O.gmm_forward(f64(x), f64(w), gl))
+    assert_close("a", a, O.gated_activation(host_f64(h), O.activation(kind, params)))
+    # without h_save the activation is the same, bit for bit
+    a2 = M.gmm_forward(dev_bf16(x), dev_bf16(w), dev(gl), activation=(kind, params), ws=ws)
+    assert np.array_equal(host_f64(a2), host_f64(a))
+
+
+@pytest.mark.parametrize("kind,params", ACT_CASES)
+@pytest.mark.parametrize("counts,K,N", [([300, 0, 211, 90], 256, 512), ([2048, 0, 900, 1200], 384, 256)])
+def test_activation_gradient_fused_in_dx(kind, params, counts, K, N):
+    """The dX epilogue's activation gradient == dx then moe_activation_backward,
+    bit for bit, and both match the oracle's gradient on the same dA."""
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(K + N + len(counts) + len(kind))
+    gl = np.array(counts, np.int64)
+    M_ = int(gl.sum())
+    dy = normal_bf16(rng, (M_, N))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(N))
+    h = normal_bf16(rng, (M_, 2 * K), 1.5)
+    ws = M.Workspace(256)
+    dyd, wd, hd, gld = dev_bf16(dy), dev_bf16(w), dev_bf16(h), dev(gl)
+    dh = M.gmm_backward_dx_swiglu(dyd, wd, gld, hd, activation=(kind, params), ws=ws)
+    da, _ = M.gmm_backward(dev_bf16(np.zeros((M_, K), np.uint16)), wd, gld, dyd, need_dw=False, ws=ws)
+    dh_ref = M.moe_swiglu_backward(hd, da, activation=(kind, params), ws=ws)
+    assert M.read_status(ws) == 0
+    assert np.array_equal(host_f64(dh), host_f64(dh_ref))
+    assert_close("dh", dh, O.gated_activation_backward(f64(h), host_f64(da), O.activation(kind, params)))

@@ -20,22 +20,23 @@ from workloads import WORKLOADS, LayerWorkload, layer_inputs
 pytestmark = pytest.mark.gpu
 
 
-def gpu_layer(inp, wl, backward, want_saved=False):
+def gpu_layer(inp, wl, backward, want_saved=False, act=None):
     import moe_routed_expert_gb300 as M
     x, w1, w2 = dev_bf16(inp["x"]), dev_bf16(inp["w1"]), dev_bf16(inp["w2"])
     ids, tw = dev(inp["topk_ids"]), dev(inp["topk_w"])
     ws = M.Workspace(M.moe_layer_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.k))
     saved = M.LayerSaved(wl.T, wl.H, wl.I, wl.E, wl.k) if (backward or want_saved) else None
-    y = M.moe_layer_forward(x, ids, tw, w1, w2, wl.clip, saved=saved, ws=ws)
+    y = M.moe_layer_forward(x, ids, tw, w1, w2, wl.clip, saved=saved, activation=act, ws=ws)
     out = {"y": y, "saved": saved}
     if backward:
-        dx, dw1, dw2, dpr = M.moe_layer_backward(dev_bf16(inp["dy"]), tw, w1, w2, saved, wl.clip, ws=ws)
+        dx, dw1, dw2, dpr = M.moe_layer_backward(dev_bf16(inp["dy"]), tw, w1, w2, saved, wl.clip, activation=act,
+                                                 ws=ws)
         out.update(dx=dx, dw1=dw1, dw2=dw2, dprobs=dpr)
     assert M.read_status(ws) == 0
     return out
 
 
-def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None, gpu_saved=None, steps=True):
+def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None, gpu_saved=None, steps=True, act=None):
     """Oracle on the whole problem, on a token subset, or on the sub-problem that
     keeps only expert ``keep_expert``'s slots.
 
@@ -51,7 +52,8 @@ def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None, gpu_
         ids[ids != keep_expert] = -1
     x, tw = f64(inp["x"][sel]), inp["topk_w"][sel]
     w1, w2 = wf if wf is not None else (f64(inp["w1"]), f64(inp["w2"]))
-    y, sv = O.moe_layer_forward(x, ids, tw, w1, w2, wl.clip)
+    oa = O.activation(*act) if act is not None else None
+    y, sv = O.moe_layer_forward(x, ids, tw, w1, w2, wl.clip, act=oa)
     out = {"y": y, "saved": sv}
     if gpu_saved is not None:
         # rows of this (sub-)problem -> rows of the GPU's full problem
@@ -66,12 +68,12 @@ def oracle_layer(inp, wl, backward, tokens=None, keep_expert=None, wf=None, gpu_
         out["gpu_rows"] = grow
         out["steps"] = {} if not steps else {
             "h": (sv["h"], O.gmm_forward(sv["x_perm"], w1, sv["group_list"])),
-            "a": (sv["a"], O.swiglu(sv["h"], wl.clip)),
+            "a": (sv["a"], O.swiglu(sv["h"], wl.clip) if oa is None else O.gated_activation(sv["h"], oa)),
             "y2": (sv["y2"], O.gmm_forward(sv["a"], w2, sv["group_list"])),
         }
         out["y_steps"] = O.moe_unpermute(sv["y2"], sv["row_id_map"], tw, T, k)
     if backward:
-        dx, dw1, dw2, dpr = O.moe_layer_backward(f64(inp["dy"][sel]), sv, tw, w1, w2, wl.clip)
+        dx, dw1, dw2, dpr = O.moe_layer_backward(f64(inp["dy"][sel]), sv, tw, w1, w2, wl.clip, act=oa)
         out.update(dx=dx, dw1=dw1, dw2=dw2, dprobs=dpr)
     return out
 
@@ -89,14 +91,14 @@ def check_steps(o):
         assert_close(key, got, want)
 
 
-def gpu_chain_backward(saved, dy, tw, w1, w2, clip, T, k):
+def gpu_chain_backward(saved, dy, tw, w1, w2, clip, T, k, act=None):
     """The backward as the chain of individual C-ABI calls on the saved tensors."""
     import moe_routed_expert_gb300 as M
     ws = M.Workspace(256)
     c = {}
     c["dy2"], c["dprobs"] = M.moe_unpermute_backward(dy, saved.y2, saved.row_id_map, tw, k, ws=ws)
     c["da"], c["dw2"] = M.gmm_backward(saved.a, w2, saved.group_list, c["dy2"], ws=ws)
-    c["dh"] = M.moe_swiglu_backward(saved.h, c["da"], clip, ws=ws)
+    c["dh"] = M.moe_swiglu_backward(saved.h, c["da"], clip, activation=act, ws=ws)
     c["dxp"], c["dw1"] = M.gmm_backward(saved.x_perm, w1, saved.group_list, c["dh"], ws=ws)
     c["dx"] = M.moe_permute_backward(c["dxp"], saved.row_id_map, T, k, ws=ws)
     assert M.read_status(ws) == 0
@@ -110,7 +112,7 @@ def check_layer_equals_chain(g, chain):
         assert torch.equal(g[key], chain[key]), key
 
 
-def check_chain_ops(inp, wl, gs, chain, experts=None, tokens=None):
+def check_chain_ops(inp, wl, gs, chain, experts=None, tokens=None, act=None):
     """Each op of the backward chain against the oracle on that op's own inputs
     (the GPU's previous-step output).  Whole problem by default; at full size,
     the given experts (every row and the whole dW) and tokens."""
@@ -133,7 +135,9 @@ def check_chain_ops(inp, wl, gs, chain, experts=None, tokens=None):
         da_o, dw2_o = O.gmm_backward(f64(hb["a"][s:t]), W2, n, f64(hb["dy2"][s:t]))
         assert_close("da[e=%d]" % e, f64(hb["da"][s:t]), da_o)
         assert_close("dw2[e=%d]" % e, dw2[e], dw2_o[0])
-        assert_close("dh[e=%d]" % e, f64(hb["dh"][s:t]), O.swiglu_backward(f64(hb["h"][s:t]), f64(hb["da"][s:t]), wl.clip))
+        dh_o = (O.swiglu_backward(f64(hb["h"][s:t]), f64(hb["da"][s:t]), wl.clip) if act is None else
+                O.gated_activation_backward(f64(hb["h"][s:t]), f64(hb["da"][s:t]), O.activation(*act)))
+        assert_close("dh[e=%d]" % e, f64(hb["dh"][s:t]), dh_o)
         dxp_o, dw1_o = O.gmm_backward(f64(hb["x_perm"][s:t]), W1, n, f64(hb["dh"][s:t]))
         assert_close("dx_perm[e=%d]" % e, f64(hb["dxp"][s:t]), dxp_o)
         assert_close("dw1[e=%d]" % e, dw1[e], dw1_o[0])
@@ -185,6 +189,32 @@ def test_layer_small_every_output(wl):
                                dev_bf16(inp["w2"]), wl.clip, wl.T, wl.k)
     check_layer_equals_chain(g, chain)
     check_chain_ops(inp, wl, gs, chain)
+
+
+@pytest.mark.parametrize("act", [("swiglustep", [0.8]), ("swigluoai", [7.0, 1.702, 1.0]), ("situglu", [1.0, 2.0])],
+                         ids=lambda a: a[0])
+def test_layer_small_activation_variants(act):
+    """The layer forward and backward with the other activations of the pages:
+    every output, each step on its own inputs, and the layer entry points equal
+    to the chain of individual calls."""
+    wl = SMALL[1]
+    inp = layer_inputs(wl)
+    g = gpu_layer(inp, wl, backward=True, act=act)
+    gs = saved_to_host(g["saved"])
+    o = oracle_layer(inp, wl, backward=True, gpu_saved=gs, act=act)
+    check_steps(o)
+    assert_close("y", g["y"], o["y_steps"])
+    o_pure = oracle_layer(inp, wl, backward=True, act=act)
+    # swiglustep's gradient jumps at SiLU(G) = c: where that kink lies inside one
+    # bf16 step of H, the GPU's and the oracle's separately rounded H can take
+    # different branches, so its dx is checked step by step (below), each op on
+    # the GPU's own inputs, and end to end only where the path is continuous.
+    for key in (("y", "dprobs") if act[0] == "swiglustep" else ("y", "dx", "dprobs")):
+        assert_close(key + " (end to end)", g[key], o_pure[key])
+    chain = gpu_chain_backward(g["saved"], dev_bf16(inp["dy"]), dev(inp["topk_w"]), dev_bf16(inp["w1"]),
+                               dev_bf16(inp["w2"]), wl.clip, wl.T, wl.k, act=act)
+    check_layer_equals_chain(g, chain)
+    check_chain_ops(inp, wl, gs, chain, act=act)
 
 
 @pytest.mark.parametrize("name", ["layer_decode_t64", "layer_prefill_t4096"])

@@ -105,6 +105,13 @@ typedef struct {
   float params[3];
 } moe_activation_t;
 
+/* Weight layouts ([MegaMoE] 参数说明: transposeWeight1, transposeWeight2).
+ * By default each expert's weight is [K, N] (w [E, K, N]); transposed it is
+ * stored [N, K] (w [E, N, K]), and its gradient is produced in the same
+ * layout.  The layer takes one bit per weight. */
+enum { MOE_W_TRANSPOSED = 1 };
+enum { MOE_W1_TRANSPOSED = 1, MOE_W2_TRANSPOSED = 2 };
+
 /* Bytes at the start of every workspace that hold the device status word. */
 #define MOE_STATUS_BYTES 256
 
@@ -197,11 +204,12 @@ MOE_API moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int
 /* gmm_forward with a gated-activation epilogue of any kind (see
  * moe_activation_t): N = 2I (a multiple of 256), y [M, I] = Activation(G, U)
  * of the bf16-rounded product; h_save as for MOE_EPILOGUE_SWIGLU.
- * activation NULL -> MOE_ERR_NULLPTR; bad parameters -> MOE_ERR_INVALID;
- * an unknown kind -> MOE_ERR_UNSUPPORTED. */
+ * activation NULL: no epilogue, y [M, N] = the product (h_save must be NULL).
+ * w_flags: 0, or MOE_W_TRANSPOSED for w stored [E, N, K].  Bad activation
+ * parameters or flags -> MOE_ERR_INVALID; an unknown kind -> MOE_ERR_UNSUPPORTED. */
 MOE_API moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E,
-                             const moe_activation_t* activation, moe_bf16* y, moe_bf16* h_save,
+                             const moe_activation_t* activation, int w_flags, moe_bf16* y, moe_bf16* h_save,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Grouped matmul backward: [GMM] "算子语义" backward formulas
@@ -211,6 +219,13 @@ MOE_API moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const
  *   dy [M, N] bf16 upstream gradient. */
 MOE_API moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
                           const moe_bf16* dy, int64_t M, int64_t K, int64_t N, int64_t E,
+                          moe_bf16* dx, moe_bf16* dw,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* gmm_backward with a weight layout: w_flags MOE_W_TRANSPOSED reads w as
+ * [E, N, K] and writes dw as [E, N, K] (dw[g] = dy[s:e]^T @ x[s:e]). */
+MOE_API moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list,
+                          const moe_bf16* dy, int64_t M, int64_t K, int64_t N, int64_t E, int w_flags,
                           moe_bf16* dx, moe_bf16* dw,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
 
@@ -231,7 +246,7 @@ MOE_API moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* 
  * Equal, bit for bit, to gmm_backward's dx followed by moe_activation_backward. */
 MOE_API moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
                           const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E,
-                          const moe_activation_t* activation, moe_bf16* dh,
+                          const moe_activation_t* activation, int w_flags, moe_bf16* dh,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- combine and gradients */
@@ -306,12 +321,14 @@ MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_id
                                moe_bf16* y, const moe_layer_saved_t* saved,
                                void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* moe_layer_forward with any gated activation between the two GMMs. */
+/* moe_layer_forward with any gated activation between the two GMMs, and the
+ * weights' layouts: w_flags MOE_W1_TRANSPOSED (w1 [E, 2I, H]) and / or
+ * MOE_W2_TRANSPOSED (w2 [E, H, I]). */
 MOE_API moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
                                const moe_bf16* w1, const moe_bf16* w2,
                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
-                               const moe_activation_t* activation, moe_bf16* y, const moe_layer_saved_t* saved,
-                               void* ws, size_t ws_bytes, moe_stream_t stream);
+                               const moe_activation_t* activation, int w_flags, moe_bf16* y,
+                               const moe_layer_saved_t* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Backward of moe_layer_forward (saved must be what the forward filled):
  *   dy [T, H] bf16 in; dx [T, H], dw1 [E, H, 2I], dw2 [E, I, H] bf16 and
@@ -323,12 +340,13 @@ MOE_API moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w,
                                 moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs,
                                 void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Backward of moe_layer_forward_act (the same activation). */
+/* Backward of moe_layer_forward_act (the same activation and w_flags; dw1 and
+ * dw2 are written in their weights' layouts). */
 MOE_API moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w,
                                 const moe_bf16* w1, const moe_bf16* w2,
                                 const moe_layer_saved_t* saved,
                                 int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
-                                const moe_activation_t* activation,
+                                const moe_activation_t* activation, int w_flags,
                                 moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs,
                                 void* ws, size_t ws_bytes, moe_stream_t stream);
 

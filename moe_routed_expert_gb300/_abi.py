@@ -45,9 +45,10 @@ SIGNATURES = {
     "gmm_workspace_size": (SZ, [I64, I64, I64, I64]),
     "gmm_forward": (ST, [P, P, P, I64, I64, I64, I64, INT, F32, P, P, P, SZ, P]),
     "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
-    "gmm_forward_act": (ST, [P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), P, P, P, SZ, P]),
+    "gmm_backward_ex": (ST, [P, P, P, P, I64, I64, I64, I64, INT, P, P, P, SZ, P]),
+    "gmm_forward_act": (ST, [P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P, P, P, SZ, P]),
     "gmm_backward_dx_swiglu": (ST, [P, P, P, P, I64, I64, I64, I64, F32, P, P, SZ, P]),
-    "gmm_backward_dx_act": (ST, [P, P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), P, P, SZ, P]),
+    "gmm_backward_dx_act": (ST, [P, P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P, P, SZ, P]),
     "moe_unpermute_workspace_size": (SZ, []),
     "moe_unpermute": (ST, [P, P, P, I64, I64, I64, P, P, SZ, P]),
     "moe_unpermute_backward": (ST, [P, P, P, P, I64, I64, I64, P, P, P, SZ, P]),
@@ -59,10 +60,10 @@ SIGNATURES = {
                                P, SZ, P]),
     "moe_layer_backward": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64, F32,
                                 P, P, P, P, P, SZ, P]),
-    "moe_layer_forward_act": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, C.POINTER(MoeActivation), P,
+    "moe_layer_forward_act": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P,
                                    C.POINTER(MoeLayerSaved), P, SZ, P]),
     "moe_layer_backward_act": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64,
-                                    C.POINTER(MoeActivation), P, P, P, P, P, SZ, P]),
+                                    C.POINTER(MoeActivation), INT, P, P, P, P, P, SZ, P]),
 }
 
 _lib = None

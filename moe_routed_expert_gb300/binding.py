@@ -177,22 +177,29 @@ def _act(activation):
 # ------------------------------------------------------------------ grouped matmul
 def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, epilogue: int = 0,
                 clip: float = 0.0, y: Optional[torch.Tensor] = None, h_save: Optional[torch.Tensor] = None,
-                activation=None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+                activation=None, w_transposed: bool = False, ws: Optional[Workspace] = None,
+                stream=None) -> torch.Tensor:
     """y = grouped x @ w (epilogue 1: SwiGLU over the [gate | up] halves; or,
-    with `activation` = (kind, params), that gated activation)."""
+    with `activation` = (kind, params), that gated activation).  With
+    w_transposed, w is [E, N, K] (each expert's weight transposed)."""
     _dtype(x, BF16, "x")
     _dtype(w, BF16, "w")
     _dtype(group_list, torch.int64, "group_list")
     M, K = x.shape
     E, K2, N = w.shape
+    if w_transposed:
+        K2, N = N, K2
     if K2 != K:
         raise ValueError("x and w disagree on K")
     out_cols = N // 2 if (epilogue == _abi.MOE_EPILOGUE_SWIGLU or activation is not None) else N
     if y is None:
         y = torch.empty(M, out_cols, dtype=BF16, device=x.device)
     wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
-    if activation is not None:
-        _check(_lib().gmm_forward_act(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, C.byref(_act(activation)),
+    if activation is not None or w_transposed:
+        if activation is None and epilogue == _abi.MOE_EPILOGUE_SWIGLU:
+            activation = ("swiglu", [clip])
+        a = C.byref(_act(activation)) if activation is not None else None
+        _check(_lib().gmm_forward_act(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, a, int(bool(w_transposed)),
                                       _ptr(y), _ptr(h_save), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_forward_act")
         return y
     _check(_lib().gmm_forward(_ptr(x), _ptr(w), _ptr(group_list), M, K, N, E, int(epilogue), float(clip),
@@ -201,41 +208,44 @@ def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, e
 
 
 def gmm_backward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, dy: torch.Tensor, *,
-                 need_dx: bool = True, need_dw: bool = True, dx=None, dw=None,
+                 need_dx: bool = True, need_dw: bool = True, dx=None, dw=None, w_transposed: bool = False,
                  ws: Optional[Workspace] = None, stream=None):
-    """Returns (dx [M, K] or None, dw [E, K, N] or None)."""
+    """Returns (dx [M, K] or None, dw [E, K, N] or None); with w_transposed, w
+    is [E, N, K] and so is dw."""
     _dtype(x, BF16, "x")
     _dtype(w, BF16, "w")
     _dtype(dy, BF16, "dy")
     M, K = x.shape
-    E, _, N = w.shape
+    E, N = w.shape[0], dy.shape[1]
     if need_dx and dx is None:
         dx = torch.empty(M, K, dtype=BF16, device=x.device)
     if need_dw and dw is None:
-        dw = torch.empty(E, K, N, dtype=BF16, device=x.device)
+        dw = torch.empty(E, *((N, K) if w_transposed else (K, N)), dtype=BF16, device=x.device)
     wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
-    _check(_lib().gmm_backward(_ptr(x), _ptr(w), _ptr(group_list), _ptr(dy), M, K, N, E,
-                               _ptr(dx if need_dx else None), _ptr(dw if need_dw else None),
-                               wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward")
+    _check(_lib().gmm_backward_ex(_ptr(x), _ptr(w), _ptr(group_list), _ptr(dy), M, K, N, E, int(bool(w_transposed)),
+                                  _ptr(dx if need_dx else None), _ptr(dw if need_dw else None),
+                                  wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward_ex")
     return (dx if need_dx else None), (dw if need_dw else None)
 
 
 def gmm_backward_dx_swiglu(dy: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, h: torch.Tensor,
-                           clip: float = 0.0, *, dh=None, activation=None, ws: Optional[Workspace] = None,
-                           stream=None) -> torch.Tensor:
+                           clip: float = 0.0, *, dh=None, activation=None, w_transposed: bool = False,
+                           ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
     """dh = SwiGLU (or `activation`) gradient of h given dA = grouped dy @ w^T,
     in one pass (dA is not stored)."""
     for t, n in ((dy, "dy"), (w, "w"), (h, "h")):
         _dtype(t, BF16, n)
     M, N = dy.shape
-    E, K, _ = w.shape
+    E = w.shape[0]
+    K = w.shape[2] if w_transposed else w.shape[1]
     if dh is None:
         dh = torch.empty(M, 2 * K, dtype=BF16, device=dy.device)
     wsp = _ws(ws, gmm_workspace_size(M, K, N, E), dy.device)
-    if activation is not None:
+    if activation is not None or w_transposed:
+        activation = activation if activation is not None else ("swiglu", [clip])
         _check(_lib().gmm_backward_dx_act(_ptr(dy), _ptr(w), _ptr(group_list), _ptr(h), M, K, N, E,
-                                          C.byref(_act(activation)), _ptr(dh), wsp.ptr, wsp.nbytes, _stream(stream)),
-               "gmm_backward_dx_act")
+                                          C.byref(_act(activation)), int(bool(w_transposed)), _ptr(dh), wsp.ptr,
+                                          wsp.nbytes, _stream(stream)), "gmm_backward_dx_act")
         return dh
     _check(_lib().gmm_backward_dx_swiglu(_ptr(dy), _ptr(w), _ptr(group_list), _ptr(h), M, K, N, E, float(clip),
                                          _ptr(dh), wsp.ptr, wsp.nbytes, _stream(stream)), "gmm_backward_dx_swiglu")
@@ -318,9 +328,11 @@ class LayerSaved:
 
 
 def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: Optional[LayerSaved] = None,
-                      y=None, activation=None, ws: Optional[Workspace] = None, stream=None):
+                      y=None, activation=None, w_flags: int = 0, ws: Optional[Workspace] = None, stream=None):
+    """w_flags: bit 0 = w1 stored [E, 2I, H], bit 1 = w2 stored [E, H, I]."""
     T, H = x.shape
-    E, _, I2 = w1.shape
+    E = w1.shape[0]
+    I2 = w1.shape[1] if w_flags & 1 else w1.shape[2]
     I = I2 // 2
     k = topk_ids.shape[1]
     for t, n in ((x, "x"), (w1, "w1"), (w2, "w2")):
@@ -331,10 +343,11 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: 
         y = torch.empty(T, H, dtype=BF16, device=x.device)
     wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), x.device)
     sv = C.byref(saved.struct()) if saved is not None else None
-    if activation is not None:
+    if activation is not None or w_flags:
+        activation = activation if activation is not None else ("swiglu", [clip])
         _check(_lib().moe_layer_forward_act(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2), T, H, I, E,
-                                            k, C.byref(_act(activation)), _ptr(y), sv, wsp.ptr, wsp.nbytes,
-                                            _stream(stream)), "moe_layer_forward_act")
+                                            k, C.byref(_act(activation)), int(w_flags), _ptr(y), sv, wsp.ptr,
+                                            wsp.nbytes, _stream(stream)), "moe_layer_forward_act")
         return y
     _check(_lib().moe_layer_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2), T, H, I, E, k,
                                     float(clip), _ptr(y), sv, wsp.ptr, wsp.nbytes, _stream(stream)),
@@ -343,9 +356,11 @@ def moe_layer_forward(x, topk_ids, topk_w, w1, w2, clip: float = 0.0, *, saved: 
 
 
 def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0, *, dx=None, dw1=None, dw2=None,
-                       dprobs=None, activation=None, ws: Optional[Workspace] = None, stream=None):
+                       dprobs=None, activation=None, w_flags: int = 0, ws: Optional[Workspace] = None, stream=None):
+    """dw1 and dw2 come in the weights' layouts (w_flags as for moe_layer_forward)."""
     T, H = dy.shape
-    E, _, I2 = w1.shape
+    E = w1.shape[0]
+    I2 = w1.shape[1] if w_flags & 1 else w1.shape[2]
     I = I2 // 2
     k = topk_w.shape[1]
     dev = dy.device
@@ -354,11 +369,12 @@ def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0,
     dw2 = torch.empty_like(w2) if dw2 is None else dw2
     dprobs = torch.empty(T, k, dtype=torch.float32, device=dev) if dprobs is None else dprobs
     wsp = _ws(ws, moe_layer_workspace_size(T, H, I, E, k), dev)
-    if activation is not None:
+    if activation is not None or w_flags:
+        activation = activation if activation is not None else ("swiglu", [clip])
         _check(_lib().moe_layer_backward_act(_ptr(dy), _ptr(topk_w), _ptr(w1), _ptr(w2), C.byref(saved.struct()),
-                                             T, H, I, E, k, C.byref(_act(activation)), _ptr(dx), _ptr(dw1), _ptr(dw2),
-                                             _ptr(dprobs), wsp.ptr, wsp.nbytes, _stream(stream)),
-               "moe_layer_backward_act")
+                                             T, H, I, E, k, C.byref(_act(activation)), int(w_flags), _ptr(dx),
+                                             _ptr(dw1), _ptr(dw2), _ptr(dprobs), wsp.ptr, wsp.nbytes,
+                                             _stream(stream)), "moe_layer_backward_act")
         return dx, dw1, dw2, dprobs
     _check(_lib().moe_layer_backward(_ptr(dy), _ptr(topk_w), _ptr(w1), _ptr(w2), C.byref(saved.struct()),
                                      T, H, I, E, k, float(clip), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprobs),

@@ -181,21 +181,25 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, 
 size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES + kGmmScratchBytes; }
 
 moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
-                             int64_t N, int64_t E, const moe_activation_t* activation, moe_bf16* y,
+                             int64_t N, int64_t E, const moe_activation_t* activation, int w_flags, moe_bf16* y,
                              moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
   Act act;
-  moe_status_t st = resolve_act(activation, &act);
+  moe_status_t st = activation ? resolve_act(activation, &act) : MOE_OK;
   if (st != MOE_OK) return st;
   if ((st = check_gmm_dims(M, K, N, E)) != MOE_OK) return st;
-  if (N % 256) return MOE_ERR_UNSUPPORTED;
+  if (w_flags & ~MOE_W_TRANSPOSED) return MOE_ERR_INVALID;
+  if (activation && N % 256) return MOE_ERR_UNSUPPORTED;
+  if (!activation && h_save) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (h_save && !aligned16(h_save)) ||
       (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
   if (M == 0) return MOE_OK;
-  return launch_gmm(GMM_FWD, EPI_SWIGLU, x, w, group_list, M, K, N, E, act, y, h_save, status_of(ws),
-                    after_status(ws), reinterpret_cast<cudaStream_t>(stream));
+  GmmLaunch how;
+  how.w_transposed = (w_flags & MOE_W_TRANSPOSED) != 0;
+  return launch_gmm(GMM_FWD, activation ? EPI_SWIGLU : EPI_PLAIN, x, w, group_list, M, K, N, E, act, y, h_save,
+                    status_of(ws), after_status(ws), reinterpret_cast<cudaStream_t>(stream), how);
 }
 
 moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
@@ -203,28 +207,18 @@ moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* gr
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_UNSUPPORTED;
   if (bad_clip(clip)) return MOE_ERR_INVALID;
-  if (epilogue == MOE_EPILOGUE_SWIGLU) {
-    const moe_activation_t a = swiglu_desc(clip);
-    return gmm_forward_act(x, w, group_list, M, K, N, E, &a, y, h_save, ws, ws_bytes, stream);
-  }
-  if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
-  moe_status_t st = check_gmm_dims(M, K, N, E);
-  if (st != MOE_OK) return st;
-  if (h_save) return MOE_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(group_list) & 7u))
-    return MOE_ERR_INVALID;
-  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
-  if (M == 0) return MOE_OK;
-  return launch_gmm(GMM_FWD, EPI_PLAIN, x, w, group_list, M, K, N, E, Act(), y, nullptr, status_of(ws),
-                    after_status(ws), reinterpret_cast<cudaStream_t>(stream));
+  const moe_activation_t a = swiglu_desc(clip);
+  return gmm_forward_act(x, w, group_list, M, K, N, E, epilogue == MOE_EPILOGUE_SWIGLU ? &a : nullptr, 0, y, h_save,
+                         ws, ws_bytes, stream);
 }
 
-moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
-                          int64_t M, int64_t K, int64_t N, int64_t E, moe_bf16* dx, moe_bf16* dw,
-                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
+                             int64_t M, int64_t K, int64_t N, int64_t E, int w_flags, moe_bf16* dx, moe_bf16* dw,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !w || !group_list || !dy) return MOE_ERR_NULLPTR;
   moe_status_t st = check_gmm_dims(M, K, N, E);
   if (st != MOE_OK) return st;
+  if (w_flags & ~MOE_W_TRANSPOSED) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || (dx && !aligned16(dx)) || (dw && !aligned16(dw)) ||
       (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
@@ -236,25 +230,34 @@ moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* g
     return MOE_OK;
   }
   return launch_gmm_backward(x, w, group_list, dy, M, K, N, E, EPI_PLAIN, Act(), nullptr, dx, dw, status_of(ws),
-                             after_status(ws), s);
+                             after_status(ws), s, (w_flags & MOE_W_TRANSPOSED) != 0);
+}
+
+moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
+                          int64_t M, int64_t K, int64_t N, int64_t E, moe_bf16* dx, moe_bf16* dw,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return gmm_backward_ex(x, w, group_list, dy, M, K, N, E, 0, dx, dw, ws, ws_bytes, stream);
 }
 
 moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
                                  const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E,
-                                 const moe_activation_t* activation, moe_bf16* dh, void* ws, size_t ws_bytes,
-                                 moe_stream_t stream) {
+                                 const moe_activation_t* activation, int w_flags, moe_bf16* dh, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
   if (!dy || !w || !group_list || !h || !dh) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
   if ((st = check_gmm_dims(M, K, N, E)) != MOE_OK) return st;
+  if (w_flags & ~MOE_W_TRANSPOSED) return MOE_ERR_INVALID;
   if (!aligned16(dy) || !aligned16(w) || !aligned16(h) || !aligned16(dh) ||
       (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
   if (M == 0) return MOE_OK;
+  GmmLaunch how;
+  how.w_transposed = (w_flags & MOE_W_TRANSPOSED) != 0;
   return launch_gmm(GMM_DX, EPI_DSWIGLU, dy, w, group_list, M, K, N, E, act, dh, const_cast<moe_bf16*>(h),
-                    status_of(ws), after_status(ws), reinterpret_cast<cudaStream_t>(stream));
+                    status_of(ws), after_status(ws), reinterpret_cast<cudaStream_t>(stream), how);
 }
 
 moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
@@ -262,7 +265,7 @@ moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const
                                     moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
-  return gmm_backward_dx_act(dy, w, group_list, h, M, K, N, E, &a, dh, ws, ws_bytes, stream);
+  return gmm_backward_dx_act(dy, w, group_list, h, M, K, N, E, &a, 0, dh, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ combine side
@@ -352,7 +355,7 @@ bool saved_aligned(const moe_layer_saved_t* sv) {
 
 moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
                                    const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E,
-                                   int64_t k, const moe_activation_t* activation, moe_bf16* y,
+                                   int64_t k, const moe_activation_t* activation, int w_flags, moe_bf16* y,
                                    const moe_layer_saved_t* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !topk_ids || !topk_w || !w1 || !w2 || !y) return MOE_ERR_NULLPTR;
   if (saved && !saved_ok(saved)) return MOE_ERR_NULLPTR;
@@ -360,6 +363,7 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
   moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
   if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
+  if (w_flags & ~(MOE_W1_TRANSPOSED | MOE_W2_TRANSPOSED)) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) || (saved && !saved_aligned(saved)))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, moe_layer_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
@@ -387,11 +391,14 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
     h = nullptr;
   }
   if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
-  if ((st = launch_gmm(GMM_FWD, EPI_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, act, a, h, status, gmm_scratch, s)) !=
-      MOE_OK)
+  GmmLaunch how1, how2;
+  how1.w_transposed = (w_flags & MOE_W1_TRANSPOSED) != 0;
+  how2.w_transposed = (w_flags & MOE_W2_TRANSPOSED) != 0;
+  if ((st = launch_gmm(GMM_FWD, EPI_SWIGLU, x_perm, w1, gl, R, H, 2 * I, E, act, a, h, status, gmm_scratch, s,
+                       how1)) != MOE_OK)
     return st;
-  if ((st = launch_gmm(GMM_FWD, EPI_PLAIN, a, w2, gl, R, I, H, E, Act(), y2, nullptr, status, gmm_scratch, s)) !=
-      MOE_OK)
+  if ((st = launch_gmm(GMM_FWD, EPI_PLAIN, a, w2, gl, R, I, H, E, Act(), y2, nullptr, status, gmm_scratch, s,
+                       how2)) != MOE_OK)
     return st;
   return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
 }
@@ -402,20 +409,21 @@ moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const
                                moe_stream_t stream) {
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
-  return moe_layer_forward_act(x, topk_ids, topk_w, w1, w2, T, H, I, E, k, &a, y, saved, ws, ws_bytes, stream);
+  return moe_layer_forward_act(x, topk_ids, topk_w, w1, w2, T, H, I, E, k, &a, 0, y, saved, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w, const moe_bf16* w1,
                                     const moe_bf16* w2, const moe_layer_saved_t* saved, int64_t T, int64_t H,
-                                    int64_t I, int64_t E, int64_t k, const moe_activation_t* activation, moe_bf16* dx,
-                                    moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws, size_t ws_bytes,
-                                    moe_stream_t stream) {
+                                    int64_t I, int64_t E, int64_t k, const moe_activation_t* activation,
+                                    int w_flags, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream) {
   if (!dy || !topk_w || !w1 || !w2 || !saved || !dx) return MOE_ERR_NULLPTR;
   if (!saved_ok(saved)) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
   if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
+  if (w_flags & ~(MOE_W1_TRANSPOSED | MOE_W2_TRANSPOSED)) return MOE_ERR_INVALID;
   if (!aligned16(dy) || !aligned16(w1) || !aligned16(w2) || !aligned16(dx) || (dw1 && !aligned16(dw1)) ||
       (dw2 && !aligned16(dw2)) || !saved_aligned(saved))
     return MOE_ERR_INVALID;
@@ -438,10 +446,10 @@ moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w, con
     return st;
   // dH = SwiGLU'(H, dY2 @ W2^T) in one grouped matmul (dA is never stored)
   if ((st = launch_gmm_backward(saved->a, w2, saved->group_list, dy2, R, I, H, E, EPI_DSWIGLU, act, saved->h, dh,
-                                dw2, status, gmm_scratch, s)) != MOE_OK)
+                                dw2, status, gmm_scratch, s, (w_flags & MOE_W2_TRANSPOSED) != 0)) != MOE_OK)
     return st;
   if ((st = launch_gmm_backward(saved->x_perm, w1, saved->group_list, dh, R, H, 2 * I, E, EPI_PLAIN, Act(), nullptr,
-                                dx_perm, dw1, status, gmm_scratch, s)) != MOE_OK)
+                                dx_perm, dw1, status, gmm_scratch, s, (w_flags & MOE_W1_TRANSPOSED) != 0)) != MOE_OK)
     return st;
   return launch_unpermute(dx_perm, saved->row_id_map, nullptr, T, H, k, dx, status, s);
 }
@@ -452,7 +460,7 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
                                 size_t ws_bytes, moe_stream_t stream) {
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
-  return moe_layer_backward_act(dy, topk_w, w1, w2, saved, T, H, I, E, k, &a, dx, dw1, dw2, dprobs, ws, ws_bytes,
+  return moe_layer_backward_act(dy, topk_w, w1, w2, saved, T, H, I, E, k, &a, 0, dx, dw1, dw2, dprobs, ws, ws_bytes,
                                 stream);
 }
 

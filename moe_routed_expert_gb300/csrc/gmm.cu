@@ -68,6 +68,7 @@ struct GmmParams {
   Act act;             // gated activation (SwiGLU epilogues)
   uint32_t* status;
   int concurrent;      // see GmmLaunch
+  int wt;              // each expert's weight stored transposed, [N, K]
 };
 
 struct __align__(16) GmmSmem {
@@ -144,8 +145,10 @@ template <int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
   static_assert(MODE == GMM_FWD || MODE == GMM_DX, "dW runs on CTA pairs");
-  constexpr bool B_MN = (MODE == GMM_FWD);
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, B_MN);
+  // B is MN-major (output columns contiguous) for the forward over [K, N]
+  // weights and for dX over transposed [N, K] weights.
+  const bool B_MN = (MODE == GMM_FWD) != (p.wt != 0);
+  const uint32_t IDESC = idesc_bf16_f32(BM, BN, false, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -248,16 +251,17 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           const uint32_t a_dst = stage_base + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           mbar_expect_tx(bar, STAGE_BYTES);
-          if (MODE == GMM_FWD) {
-            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          // output columns [0, 128) and [128, 256) of the tile: the gate and the up half with SwiGLU
+          const int c0 = ti.col0, c1 = EPI == EPI_SWIGLU ? p.act_cols + ti.col0 : ti.col0 + BN / 2;
+          if (B_MN) {  // weight rows hold output columns: four 64-column boxes
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) {
-              const int col = EPI == EPI_SWIGLU ? ((j < 2) ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * (j - 2))
-                                     : ti.col0 + 64 * j;
-              tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
-            }
-          } else {
-            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, (j < 2 ? c0 : c1) + 64 * (j & 1), kb * BK, ti.g);
+          } else if (MODE == GMM_FWD) {  // transposed weights: two boxes of 128 rows
+            tma_load_3d(b_dst, &tmB, bar, kb * BK, c0, ti.g);
+            tma_load_3d(b_dst + (BN / 2) * 128, &tmB, bar, kb * BK, c1, ti.g);
+          } else {     // dX over [K, N] weights: one box of 256 rows
             tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
           }
         }
@@ -448,6 +452,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.h_save = h_save;
   p.act = act;
   p.concurrent = how.concurrent ? 1 : 0;
+  p.wt = how.w_transposed ? 1 : 0;
   CUtensorMap ta, tb;
   if (mode == GMM_FWD) {
     const bool sw = (epilogue == EPI_SWIGLU);
@@ -456,7 +461,9 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
     p.act_cols = static_cast<int>(N / 2);
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
-    if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
+    if (!make_map_2d(&ta, a, M, K, BM) ||
+        !(how.w_transposed ? make_map_3d(&tb, b, E, N, K, BN / 2) : make_map_3d(&tb, b, E, K, N, 64)))
+      return MOE_ERR_CUDA;
     return sw ? launch_mode<GMM_FWD, EPI_SWIGLU>(ta, tb, p, s, how.max_ctas)
               : launch_mode<GMM_FWD, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
   }
@@ -467,7 +474,9 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
   p.h_in = h_save;
   p.tile_cols = static_cast<int>((K + BN - 1) / BN);
   p.kblocks = static_cast<int>(N / BK);
-  if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BN)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&ta, a, M, N, BM) ||
+      !(how.w_transposed ? make_map_3d(&tb, b, E, N, K, 64) : make_map_3d(&tb, b, E, K, N, BN)))
+    return MOE_ERR_CUDA;
   return dsw ? launch_mode<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s, how.max_ctas)
              : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
 }
@@ -485,8 +494,9 @@ namespace moe {
 moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
                                  int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, const Act& act,
                                  const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool w_transposed) {
   GmmLaunch first, second;
+  first.w_transposed = w_transposed;
   const int half = (num_sms() / 2) & ~1;
   if (dx && dw && half >= 2 && (M / 256 + E) * ((K + 255) / 256) <= 4 * static_cast<int64_t>(half)) {
     first.max_ctas = half;
@@ -497,8 +507,11 @@ moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int
   if (dx && (st = launch_gmm(GMM_DX, dx_epilogue, dy, w, group_list, M, K, N, E, act, dx,
                              const_cast<uint16_t*>(h), status, gmm_scratch, s, first)) != MOE_OK)
     return st;
-  if (dw && (st = launch_gmm(GMM_DW, EPI_PLAIN, x, dy, group_list, M, K, N, E, Act(), dw, nullptr, status,
-                             gmm_scratch, s, second)) != MOE_OK)
+  // dW in the weights' layout: [E, K, N] = x^T dy, or transposed [E, N, K] = dy^T x
+  if (dw && (st = w_transposed ? launch_gmm(GMM_DW, EPI_PLAIN, dy, x, group_list, M, N, K, E, Act(), dw, nullptr,
+                                            status, gmm_scratch, s, second)
+                               : launch_gmm(GMM_DW, EPI_PLAIN, x, dy, group_list, M, K, N, E, Act(), dw, nullptr,
+                                            status, gmm_scratch, s, second)) != MOE_OK)
     return st;
   return MOE_OK;
 }

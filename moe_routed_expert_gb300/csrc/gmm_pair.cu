@@ -95,6 +95,7 @@ struct PairParams {
   int64_t b_pitch;
   uint8_t* map_slots;
   int concurrent;   // see GmmLaunch
+  int wt;           // FWD/DX: each expert's weight stored transposed, [N, K]
 };
 
 struct __align__(128) PairSmem {
@@ -256,8 +257,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const PairParams p) {
   constexpr bool A_MN = (MODE == GMM_DW);
-  constexpr bool B_MN = (MODE != GMM_DX);
-  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+  // B is MN-major (output columns contiguous) for dW (dy rows), for the forward
+  // over [K, N] weights and for dX over transposed [N, K] weights.
+  const bool B_MN = (MODE == GMM_DW) || ((MODE == GMM_FWD) != (p.wt != 0));
+  const uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -520,15 +523,15 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const uint32_t bar = mapa_shared(bar_local, 0);  // the even CTA's stage barrier
           if (rank == 0) mbar_expect_tx(bar_local, 2 * STAGE_BYTES);
           tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
-          if (MODE == GMM_FWD) {
+          // this CTA's 128 output columns of B: the gate or the up half with SwiGLU
+          const int bcol = EPI == EPI_SWIGLU ? (rank == 0 ? ti.col0 : p.act_cols + ti.col0)
+                                             : ti.col0 + static_cast<int>(rank) * BNH;
+          if (B_MN) {  // weight rows hold output columns: two 64-column boxes
 #pragma unroll
-            for (int j = 0; j < BNH / 64; ++j) {
-              const int col = EPI == EPI_SWIGLU ? (rank == 0 ? ti.col0 + 64 * j : p.act_cols + ti.col0 + 64 * j)
-                                     : ti.col0 + static_cast<int>(rank) * BNH + 64 * j;
-              tma_load_3d_pair(b_dst + j * BOX_BYTES, &tmB, bar, col, kb * BK, ti.g);
-            }
-          } else {
-            tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, ti.col0 + static_cast<int>(rank) * BNH, ti.g);
+            for (int j = 0; j < BNH / 64; ++j)
+              tma_load_3d_pair(b_dst + j * BOX_BYTES, &tmB, bar, bcol + 64 * j, kb * BK, ti.g);
+          } else {     // weight rows hold the contraction: one box of 128 rows
+            tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, bcol, ti.g);
           }
         }
       }
@@ -843,6 +846,7 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
                              uint32_t* status, void* gmm_scratch, cudaStream_t s, const GmmLaunch& how) {
   PairParams p{};
   p.concurrent = how.concurrent ? 1 : 0;
+  p.wt = how.w_transposed ? 1 : 0;
   p.group_list = group_list;
   p.E = static_cast<int>(E);
   p.rows_cap = M;
@@ -858,7 +862,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.act_cols = static_cast<int>(N / 2);
     p.tile_cols = sw ? static_cast<int>((N / 2) / (BN / 2)) : static_cast<int>((N + BN - 1) / BN);
     p.kblocks = static_cast<int>(K / BK);
-    if (!make_map_2d(&ta, a, M, K, BM) || !make_map_3d(&tb, b, E, K, N, 64)) return MOE_ERR_CUDA;
+    if (!make_map_2d(&ta, a, M, K, BM) ||
+        !(how.w_transposed ? make_map_3d(&tb, b, E, N, K, BNH) : make_map_3d(&tb, b, E, K, N, 64)))
+      return MOE_ERR_CUDA;
     if (sw) return launch_pair<GMM_FWD, EPI_SWIGLU>(ta, tb, tb, p, s, how.max_ctas);
     if (!make_map_2d(&tc, out, M, N, 32)) return MOE_ERR_CUDA;
     return launch_pair<GMM_FWD, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);
@@ -871,7 +877,9 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
     p.h_in = h_save;
     p.tile_cols = static_cast<int>((K + BN - 1) / BN);
     p.kblocks = static_cast<int>(N / BK);
-    if (!make_map_2d(&ta, a, M, N, BM) || !make_map_3d(&tb, b, E, K, N, BNH)) return MOE_ERR_CUDA;
+    if (!make_map_2d(&ta, a, M, N, BM) ||
+        !(how.w_transposed ? make_map_3d(&tb, b, E, N, K, 64) : make_map_3d(&tb, b, E, K, N, BNH)))
+      return MOE_ERR_CUDA;
     if (dsw) return launch_pair<GMM_DX, EPI_DSWIGLU>(ta, tb, tb, p, s, how.max_ctas);
     if (!make_map_2d(&tc, out, M, K, 32)) return MOE_ERR_CUDA;
     return launch_pair<GMM_DX, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);

@@ -74,6 +74,7 @@ struct GmmLaunch {
   int max_ctas = 0;         // cap on the persistent grid (0: one CTA per SM)
   bool concurrent = false;  // start without waiting for the previous kernel (whose
                             // inputs must not be read) and wait for it before finishing
+  bool w_transposed = false;  // FWD/DX: weights stored [E, N, K]
 };
 moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,
                              int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
@@ -88,10 +89,11 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
 // dX and dW of one grouped matmul (both read only inputs that exist before
 // either starts): small problems run them side by side on halves of the GPU,
 // large ones one after the other on all of it.  `dx_epilogue` / `h` as for
-// launch_gmm's dX (plain, or the SwiGLU gradient with the saved H).
+// launch_gmm's dX (plain, or the SwiGLU gradient with the saved H).  With
+// w_transposed the weights are [E, N, K] and dw is written in that layout.
 moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
                                  int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, const Act& act,
                                  const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool w_transposed = false);
 
 }  // namespace moe

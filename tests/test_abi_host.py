@@ -112,25 +112,30 @@ def test_activation_descriptor_checks(lib):
         return C.byref(a)
 
     def fwd(a):
-        return lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 256, 4, a, FAKE, None, ws, nws, None)
+        return lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 256, 4, a, 0, FAKE, None, ws, nws, None)
 
     SW, STEP, OAI, SITU = 0, 1, 2, 3
     nan, inf = float("nan"), float("inf")
-    assert fwd(None) == 1
+    assert lib.gmm_forward_act(None, FAKE, FAKE, 64, 128, 256, 4, None, 0, FAKE, None, ws, nws, None) == 1
+    assert lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 256, 4, None, 2, FAKE, None, ws, nws, None) == 2  # flags
+    assert lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 256, 4, None, 0, FAKE, FAKE, ws, nws, None) == 2  # h_save
     for bad in (act(SW, 1.0, 2.0), act(SW, -1.0), act(STEP, nan), act(OAI, 1.0), act(OAI, 1.0, inf, 1.0),
                 act(OAI, 1.0, 1.0, nan), act(OAI, -2.0, 1.0, 1.0), act(SITU, 0.0), act(SITU, -1.0),
                 act(SITU, 1.0, 0.0), act(SITU, inf), act(SITU, 1.0, 2.0, 3.0)):
         assert fwd(bad) == 2
     assert fwd(act(7)) == 3                                                   # unknown kind
-    assert lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 192, 4, act(SW), FAKE, None, ws, nws, None) == 3  # N
+    assert lib.gmm_forward_act(FAKE, FAKE, FAKE, 64, 128, 192, 4, act(SW), 0, FAKE, None, ws, nws, None) == 3  # N
     # valid descriptors get past the checks: a misaligned x is then what fails
     for good in (act(SW), act(SW, 0.0), act(STEP, 7.0), act(OAI), act(OAI, inf, 1.702, 1.0), act(SITU),
                  act(SITU, 2.0), act(SITU, 2.0, 3.0)):
-        assert lib.gmm_forward_act(MIS, FAKE, FAKE, 64, 128, 256, 4, good, FAKE, None, ws, nws, None) == 2
+        assert lib.gmm_forward_act(MIS, FAKE, FAKE, 64, 128, 256, 4, good, 1, FAKE, None, ws, nws, None) == 2
     assert lib.moe_activation_backward(FAKE, FAKE, 8, 64, act(SITU, -1.0), FAKE, ws, nws, None) == 2
-    assert lib.gmm_backward_dx_act(FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, None, FAKE, ws, nws, None) == 1
-    assert lib.moe_layer_forward_act(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 128, 4, 2, act(OAI, 1.0), FAKE, None,
+    assert lib.gmm_backward_dx_act(FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, None, 0, FAKE, ws, nws, None) == 1
+    assert lib.moe_layer_forward_act(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 128, 4, 2, act(OAI, 1.0), 0, FAKE, None,
                                      ws, nws, None) == 2
+    assert lib.moe_layer_forward_act(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 128, 4, 2, act(SW), 4, FAKE, None,
+                                     ws, nws, None) == 2  # w_flags
+    assert lib.gmm_backward_ex(FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, 3, FAKE, FAKE, ws, nws, None) == 2
 
 
 def test_python_binding_refuses_cpu_tensors(lib):

@@ -338,3 +338,45 @@ def test_activation_gradient_fused_in_dx(kind, params, counts, K, N):
     assert M.read_status(ws) == 0
     assert np.array_equal(host_f64(dh), host_f64(dh_ref))
     assert_close("dh", dh, O.gated_activation_backward(f64(h), host_f64(da), O.activation(kind, params)))
+
+
+# ---------------------------------------------------------------- transposed weights ([MegaMoE] transposeWeight)
+@pytest.mark.parametrize("counts,K,N", [([300, 0, 211, 90], 256, 512),      # 128-row kernel
+                                        ([2048, 0, 900, 1200], 384, 512)])  # CTA pairs
+def test_transposed_weights(counts, K, N):
+    """w stored [E, N, K]: forward (plain and SwiGLU), dX (plain and with the
+    activation gradient) and dW (written [E, N, K]) against the oracle on W."""
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(K + N + 5)
+    gl = np.array(counts, np.int64)
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (len(gl), K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    wt = np.ascontiguousarray(np.transpose(w, (0, 2, 1)))      # [E, N, K]
+    xd, wtd, gld, dyd = dev_bf16(x), dev_bf16(wt), dev(gl), dev_bf16(dy)
+    ws = M.Workspace(256)
+    y = M.gmm_forward(xd, wtd, gld, w_transposed=True, ws=ws)
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+    h = torch.empty(M_, N, dtype=torch.bfloat16, device="cuda")
+    a = M.gmm_forward(xd, wtd, gld, activation=("swigluoai", []), h_save=h, w_transposed=True, ws=ws)
+    assert_close("h", h, O.gmm_forward(f64(x), f64(w), gl))
+    assert_close("a", a, O.gated_activation(host_f64(h), O.activation("swigluoai")))
+    dx, dwt = M.gmm_backward(xd, wtd, gld, dyd, w_transposed=True, ws=ws)
+    assert tuple(dwt.shape) == (len(gl), N, K)
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw^T", dwt, np.transpose(dw_o, (0, 2, 1)))
+    # dX over the transposed down weights with the activation gradient: w2^T [E, N, I]
+    I = K // 2
+    w2 = normal_bf16(rng, (len(gl), I, N), 1 / np.sqrt(N))
+    hh = normal_bf16(rng, (M_, 2 * I), 1.5)
+    w2t = dev_bf16(np.ascontiguousarray(np.transpose(w2, (0, 2, 1))))
+    dh = M.gmm_backward_dx_swiglu(dyd, w2t, gld, dev_bf16(hh), activation=("situglu", [1.5]), w_transposed=True,
+                                  ws=ws)
+    da, _ = M.gmm_backward(dev_bf16(np.zeros((M_, I), np.uint16)), w2t, gld, dyd, need_dw=False, w_transposed=True,
+                           ws=ws)
+    assert M.read_status(ws) == 0
+    assert_close("da", da, O.gmm_backward(np.zeros((M_, I)), f64(w2), gl, f64(dy))[0])
+    assert_close("dh", dh, O.gated_activation_backward(f64(hh), host_f64(da), O.activation("situglu", [1.5])))

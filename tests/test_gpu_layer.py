@@ -217,6 +217,33 @@ def test_layer_small_activation_variants(act):
     check_chain_ops(inp, wl, gs, chain, act=act)
 
 
+def test_layer_transposed_weights():
+    """w1 stored [E, 2I, H] and w2 [E, H, I]: the same layer, its weight
+    gradients in those layouts, against the oracle on the untransposed weights."""
+    import moe_routed_expert_gb300 as M
+    wl = SMALL[0]
+    inp = layer_inputs(wl)
+    x, ids, tw, dy = dev_bf16(inp["x"]), dev(inp["topk_ids"]), dev(inp["topk_w"]), dev_bf16(inp["dy"])
+    w1t = dev_bf16(np.ascontiguousarray(np.transpose(inp["w1"], (0, 2, 1))))
+    w2t = dev_bf16(np.ascontiguousarray(np.transpose(inp["w2"], (0, 2, 1))))
+    ws = M.Workspace(M.moe_layer_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.k))
+    saved = M.LayerSaved(wl.T, wl.H, wl.I, wl.E, wl.k)
+    y = M.moe_layer_forward(x, ids, tw, w1t, w2t, wl.clip, saved=saved, w_flags=3, ws=ws)
+    dx, dw1t, dw2t, dpr = M.moe_layer_backward(dy, tw, w1t, w2t, saved, wl.clip, w_flags=3, ws=ws)
+    assert M.read_status(ws) == 0
+    assert tuple(dw1t.shape) == (wl.E, 2 * wl.I, wl.H) and tuple(dw2t.shape) == (wl.E, wl.H, wl.I)
+    g = {"y": y, "dx": dx, "dprobs": dpr}
+    gs = saved_to_host(saved)
+    o = oracle_layer(inp, wl, backward=True, gpu_saved=gs)
+    check_steps(o)
+    o_pure = oracle_layer(inp, wl, backward=True)
+    for key in ("y", "dx", "dprobs"):
+        assert_close(key + " (end to end)", g[key], o_pure[key])
+    # weight gradients: the oracle's from the GPU's stored forward tensors, transposed
+    assert_close("dw1^T", host_f64(dw1t), np.transpose(o["dw1"], (0, 2, 1)))
+    assert_close("dw2^T", host_f64(dw2t), np.transpose(o["dw2"], (0, 2, 1)))
+
+
 @pytest.mark.parametrize("name", ["layer_decode_t64", "layer_prefill_t4096"])
 def test_layer_forward_workloads_every_output(name):
     wl = WORKLOADS[name]

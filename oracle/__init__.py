@@ -6,3 +6,4 @@ and the readings it takes.
 """
 from .moe_oracle import *  # noqa: F401,F403
 from .moe_oracle import __all__  # noqa: F401
+from . import mx_oracle  # noqa: F401,E402

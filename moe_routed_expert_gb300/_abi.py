@@ -1,4 +1,4 @@
-"""ctypes view of the C ABI declared in include/moe_gmm.h (signatures only)."""
+"""ctypes view of the C ABI declared in include/moe_gmm.h and include/moe_mx.h (signatures only)."""
 from __future__ import annotations
 
 import ctypes as C
@@ -22,6 +22,8 @@ STATUS_NAMES = {
     4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT",
 }
 
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}  # moe_fp8_format_t
 
 ACTIVATIONS = {"swiglu": 0, "swiglustep": 1, "swigluoai": 2, "situglu": 3}  # moe_act_kind_t
 
@@ -64,6 +66,16 @@ SIGNATURES = {
                                    C.POINTER(MoeLayerSaved), P, SZ, P]),
     "moe_layer_backward_act": (ST, [P, P, P, P, C.POINTER(MoeLayerSaved), I64, I64, I64, I64, I64,
                                     C.POINTER(MoeActivation), INT, P, P, P, P, P, SZ, P]),
+    # moe_mx.h
+    "moe_mx_quantize_workspace_size": (SZ, []),
+    "moe_mx_quantize": (ST, [P, I64, I64, C.c_int32, P, P, P, SZ, P]),
+    "moe_permute_mx": (ST, [P, P, I64, I64, I64, I64, C.c_int32, P, P, P, P, P, P, SZ, P]),
+    "gmm_mx_workspace_size": (SZ, [I64, I64, I64, I64]),
+    "gmm_forward_mx": (ST, [P, P, P, P, P, I64, I64, I64, I64, C.c_int32, C.c_int32, C.POINTER(MoeActivation),
+                            P, P, P, P, P, SZ, P]),
+    "moe_layer_mx_workspace_size": (SZ, [I64, I64, I64, I64, I64]),
+    "moe_layer_forward_mx": (ST, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, C.c_int32, C.c_int32,
+                                  C.POINTER(MoeActivation), P, P, SZ, P]),
 }
 
 _lib = None

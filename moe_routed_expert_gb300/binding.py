@@ -380,3 +380,100 @@ def moe_layer_backward(dy, topk_w, w1, w2, saved: LayerSaved, clip: float = 0.0,
                                      T, H, I, E, k, float(clip), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprobs),
                                      wsp.ptr, wsp.nbytes, _stream(stream)), "moe_layer_backward")
     return dx, dw1, dw2, dprobs
+
+
+# ------------------------------------------------------------------ MXFP8 forward (include/moe_mx.h)
+U8 = torch.uint8
+
+
+def _fmt(name):
+    if name not in _abi.FP8_FORMATS:
+        raise ValueError("unknown fp8 format %r (e4m3 or e5m2)" % (name,))
+    return _abi.FP8_FORMATS[name]
+
+
+def moe_mx_quantize(x, fmt: str = "e4m3", *, q=None, scales=None, ws: Optional[Workspace] = None, stream=None):
+    """Q_MX of each row of x [rows, K] bf16: (q [rows, K] uint8 codes,
+    scales [rows, K/32] uint8 E8M0 codes)."""
+    _dtype(x, BF16, "x")
+    rows, K = x.shape
+    q = torch.empty(rows, K, dtype=U8, device=x.device) if q is None else q
+    scales = torch.empty(rows, K // 32, dtype=U8, device=x.device) if scales is None else scales
+    _dtype(q, U8, "q")
+    _dtype(scales, U8, "scales")
+    w = _ws(ws, int(_lib().moe_mx_quantize_workspace_size()), x.device)
+    _check(_lib().moe_mx_quantize(_ptr(x), rows, K, _fmt(fmt), _ptr(q), _ptr(scales), w.ptr, w.nbytes,
+                                  _stream(stream)), "moe_mx_quantize")
+    return q, scales
+
+
+def moe_permute_mx(x, topk_ids, E: int, fmt: str = "e4m3", *, out=None, ws: Optional[Workspace] = None, stream=None):
+    """moe_permute whose gathered rows leave quantised: returns (x_q [T*k, H] uint8,
+    x_scales [T*k, H/32] uint8, group_list, row_id_map, sorted_flat)."""
+    _dtype(x, BF16, "x")
+    _dtype(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    H = x.shape[1]
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(T * k, H, dtype=U8, device=dev), torch.empty(T * k, H // 32, dtype=U8, device=dev),
+               torch.empty(E, dtype=torch.int64, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev))
+    x_q, x_s, group_list, row_id_map, sorted_flat = out
+    w = _ws(ws, moe_permute_workspace_size(T, k, E), dev)
+    _check(_lib().moe_permute_mx(_ptr(x), _ptr(topk_ids), T, H, k, E, _fmt(fmt), _ptr(x_q), _ptr(x_s),
+                                 _ptr(group_list), _ptr(row_id_map), _ptr(sorted_flat), w.ptr, w.nbytes,
+                                 _stream(stream)), "moe_permute_mx")
+    return x_q, x_s, group_list, row_id_map, sorted_flat
+
+
+def gmm_forward_mx(x_q, x_scales, w_q, w_scales, group_list, *, x_fmt: str = "e4m3", w_fmt: str = "e4m3",
+                   activation=None, y=None, a_q=None, a_scales=None, h_save=None, ws: Optional[Workspace] = None,
+                   stream=None):
+    """Block-scaled grouped matmul: x_q [M, K] / x_scales [M, K/32], w_q [E, N, K] /
+    w_scales [E, N, K/32] (uint8 codes).  Without an activation returns y [M, N]
+    bf16; with one returns (a_q [M, N/2], a_scales [M, N/64]) in x_fmt."""
+    M, K = x_q.shape
+    E, N, _ = w_q.shape
+    for t, n in ((x_q, "x_q"), (x_scales, "x_scales"), (w_q, "w_q"), (w_scales, "w_scales")):
+        _dtype(t, U8, n)
+    _dtype(group_list, torch.int64, "group_list")
+    dev = x_q.device
+    act = C.byref(_act(activation)) if activation is not None else None
+    if activation is None:
+        y = torch.empty(M, N, dtype=BF16, device=dev) if y is None else y
+    else:
+        a_q = torch.empty(M, N // 2, dtype=U8, device=dev) if a_q is None else a_q
+        a_scales = torch.empty(M, N // 64, dtype=U8, device=dev) if a_scales is None else a_scales
+    w = _ws(ws, int(_lib().gmm_mx_workspace_size(M, K, N, E)), dev)
+    _check(_lib().gmm_forward_mx(_ptr(x_q), _ptr(x_scales), _ptr(w_q), _ptr(w_scales), _ptr(group_list), M, K, N,
+                                 E, _fmt(x_fmt), _fmt(w_fmt), act, _ptr(y), _ptr(a_q), _ptr(a_scales),
+                                 _ptr(h_save), w.ptr, w.nbytes, _stream(stream)), "gmm_forward_mx")
+    return y if activation is None else (a_q, a_scales)
+
+
+def moe_layer_mx_workspace_size(T, H, I, E, k) -> int:
+    return int(_lib().moe_layer_mx_workspace_size(T, H, I, E, k))
+
+
+def moe_layer_forward_mx(x, topk_ids, topk_w, w1_q, w1_scales, w2_q, w2_scales, *, x_fmt: str = "e4m3",
+                         w_fmt: str = "e4m3", activation="swiglu", y=None, ws: Optional[Workspace] = None,
+                         stream=None):
+    """A8W8-FP layer forward: w1_q [E, 2I, H], w2_q [E, H, I] fp8 codes with their
+    [.., K/32] E8M0 scales; returns y [T, H] bf16."""
+    T, H = x.shape
+    E, I2, _ = w1_q.shape
+    I = I2 // 2
+    k = topk_ids.shape[1]
+    _dtype(x, BF16, "x")
+    _dtype(topk_ids, torch.int32, "topk_ids")
+    _dtype(topk_w, torch.float32, "topk_w")
+    for t, n in ((w1_q, "w1_q"), (w1_scales, "w1_scales"), (w2_q, "w2_q"), (w2_scales, "w2_scales")):
+        _dtype(t, U8, n)
+    y = torch.empty(T, H, dtype=BF16, device=x.device) if y is None else y
+    wsp = _ws(ws, moe_layer_mx_workspace_size(T, H, I, E, k), x.device)
+    _check(_lib().moe_layer_forward_mx(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1_q), _ptr(w1_scales),
+                                       _ptr(w2_q), _ptr(w2_scales), T, H, I, E, k, _fmt(x_fmt), _fmt(w_fmt),
+                                       C.byref(_act(activation)), _ptr(y), wsp.ptr, wsp.nbytes, _stream(stream)),
+           "moe_layer_forward_mx")
+    return y

@@ -14,6 +14,7 @@
 
 #include "internal.h"
 #include "moe_gmm.h"
+#include "moe_mx.h"
 
 namespace moe {
 
@@ -462,6 +463,145 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
   const moe_activation_t a = swiglu_desc(clip);
   return moe_layer_backward_act(dy, topk_w, w1, w2, saved, T, H, I, E, k, &a, 0, dx, dw1, dw2, dprobs, ws, ws_bytes,
                                 stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ MXFP8 forward (moe_mx.h)
+namespace moe {
+namespace {
+bool bad_fmt(int32_t f) { return f != MOE_FP8_E4M3 && f != MOE_FP8_E5M2; }
+
+size_t layer_mx_acts_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  const size_t R = static_cast<size_t>(T * k);
+  return align256(R * H) + align256(R * H / 32) + align256(R * I) + align256(R * I / 32) + align256(R * H * 2) +
+         2 * align256(R * 4) + align256(static_cast<size_t>(E) * 8);
+}
+
+moe_status_t check_mx_gmm(int64_t M, int64_t K, int64_t N, int64_t E) {
+  if (M < 0 || K <= 0 || N <= 0 || E <= 0) return MOE_ERR_INVALID;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (K % 128 || N % 128) return MOE_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || K > INT32_MAX / 2 || N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_mx_quantize_workspace_size(void) { return MOE_STATUS_BYTES; }
+
+moe_status_t moe_mx_quantize(const moe_bf16* x, int64_t rows, int64_t K, int32_t format, uint8_t* q,
+                             uint8_t* scales, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (rows != 0 && (!x || !q || !scales)) return MOE_ERR_NULLPTR;
+  if (rows < 0 || K <= 0 || bad_fmt(format)) return MOE_ERR_INVALID;
+  if (K % 32) return MOE_ERR_UNSUPPORTED;
+  if (rows != 0 && (!aligned16(x) || !aligned16(q))) return MOE_ERR_INVALID;
+  moe_status_t st = check_ws(ws, ws_bytes, moe_mx_quantize_workspace_size());
+  if (st != MOE_OK || rows == 0) return st;
+  return launch_mx_quantize(x, rows, K, format, q, scales, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute_mx(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k, int64_t E,
+                            int32_t format, uint8_t* x_q, uint8_t* x_scales, int64_t* group_list,
+                            int32_t* row_id_map, int32_t* sorted_flat, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  if (!group_list) return MOE_ERR_NULLPTR;
+  if (T != 0 && (!x || !topk_ids || !x_q || !x_scales || !row_id_map || !sorted_flat)) return MOE_ERR_NULLPTR;
+  if (E <= 0 || k > E || bad_fmt(format)) return MOE_ERR_INVALID;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = check_tokens(T, H, k);
+  if (st != MOE_OK) return st;
+  if (H % 32) return MOE_ERR_UNSUPPORTED;
+  if (T != 0 && (!aligned16(x) || !aligned16(x_q))) return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_permute_workspace_size(T, k, E))) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0)
+    return cudaMemsetAsync(group_list, 0, E * sizeof(int64_t), s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const MxOut mx{format, x_q, x_scales};
+  return launch_permute(x, topk_ids, T, H, k, E, nullptr, group_list, row_id_map, sorted_flat, status_of(ws),
+                        after_status(ws), s, &mx);
+}
+
+size_t gmm_mx_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATUS_BYTES; }
+
+moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales, const uint8_t* w_q, const uint8_t* w_scales,
+                            const int64_t* group_list, int64_t M, int64_t K, int64_t N, int64_t E, int32_t x_format,
+                            int32_t w_format, const moe_activation_t* activation, moe_bf16* y, uint8_t* a_q,
+                            uint8_t* a_scales, moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x_q || !x_scales || !w_q || !w_scales || !group_list) return MOE_ERR_NULLPTR;
+  if (activation ? (!a_q || !a_scales) : !y) return MOE_ERR_NULLPTR;
+  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
+  Act act;
+  moe_status_t st = activation ? resolve_act(activation, &act) : MOE_OK;
+  if (st != MOE_OK) return st;
+  if ((st = check_mx_gmm(M, K, N, E)) != MOE_OK) return st;
+  if (activation && N % 256) return MOE_ERR_UNSUPPORTED;
+  if (!activation && h_save) return MOE_ERR_INVALID;
+  if (!aligned16(x_q) || !aligned16(x_scales) || !aligned16(w_q) || !aligned16(w_scales) ||
+      (y && !aligned16(y)) || (a_q && !aligned16(a_q)) || (a_scales && !aligned16(a_scales)) ||
+      (h_save && !aligned16(h_save)) || (reinterpret_cast<uintptr_t>(group_list) & 7u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_mx_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  MxGmmArgs a{};
+  a.a = x_q; a.a_sf = x_scales; a.b = w_q; a.b_sf = w_scales; a.group_list = group_list;
+  a.M = M; a.K = K; a.N = N; a.E = E; a.a_fmt = x_format; a.b_fmt = w_format;
+  a.act = activation ? &act : nullptr;
+  a.out = y; a.aq = a_q; a.as = a_scales; a.out_fmt = x_format; a.h_save = h_save;
+  return launch_gmm_mx(a, status_of(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_layer_mx_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  if (T <= 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_STATUS_BYTES;
+  return MOE_STATUS_BYTES + permute_scratch_bytes(T, k, E) + layer_mx_acts_bytes(T, H, I, E, k);
+}
+
+moe_status_t moe_layer_forward_mx(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
+                                  const uint8_t* w1_q, const uint8_t* w1_scales, const uint8_t* w2_q,
+                                  const uint8_t* w2_scales, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                                  int32_t x_format, int32_t w_format, const moe_activation_t* activation,
+                                  moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !topk_ids || !topk_w || !w1_q || !w1_scales || !w2_q || !w2_scales || !y) return MOE_ERR_NULLPTR;
+  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
+  if (H % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w1_q) || !aligned16(w1_scales) || !aligned16(w2_q) || !aligned16(w2_scales) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_layer_mx_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = status_of(ws);
+  uint8_t* scratch = after_status(ws);
+  uint8_t* p = scratch + permute_scratch_bytes(T, k, E);
+  const int64_t R = T * k;
+  uint8_t* xq = p;                                      p += align256(R * H);
+  uint8_t* xs = p;                                      p += align256(R * H / 32);
+  uint8_t* aq = p;                                      p += align256(R * I);
+  uint8_t* as = p;                                      p += align256(R * I / 32);
+  moe_bf16* o = reinterpret_cast<moe_bf16*>(p);         p += align256(R * H * 2);
+  int32_t* rmap = reinterpret_cast<int32_t*>(p);        p += align256(R * 4);
+  int32_t* sflat = reinterpret_cast<int32_t*>(p);       p += align256(R * 4);
+  int64_t* gl = reinterpret_cast<int64_t*>(p);
+  const MxOut mx{x_format, xq, xs};
+  if ((st = launch_permute(x, topk_ids, T, H, k, E, nullptr, gl, rmap, sflat, status, scratch, s, &mx)) != MOE_OK)
+    return st;
+  MxGmmArgs g1{};
+  g1.a = xq; g1.a_sf = xs; g1.b = w1_q; g1.b_sf = w1_scales; g1.group_list = gl;
+  g1.M = R; g1.K = H; g1.N = 2 * I; g1.E = E; g1.a_fmt = x_format; g1.b_fmt = w_format;
+  g1.act = &act; g1.aq = aq; g1.as = as; g1.out_fmt = x_format;
+  if ((st = launch_gmm_mx(g1, status, s)) != MOE_OK) return st;
+  MxGmmArgs g2{};
+  g2.a = aq; g2.a_sf = as; g2.b = w2_q; g2.b_sf = w2_scales; g2.group_list = gl;
+  g2.M = R; g2.K = I; g2.N = H; g2.E = E; g2.a_fmt = x_format; g2.b_fmt = w_format;
+  g2.out = o;
+  if ((st = launch_gmm_mx(g2, status, s)) != MOE_OK) return st;
+  return launch_unpermute(o, rmap, topk_w, T, H, k, y, status, s);
 }
 
 }  // extern "C"

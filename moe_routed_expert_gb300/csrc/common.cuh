@@ -377,6 +377,59 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Shared-memory matrix descriptor without swizzle (tcgen05 format, version 1):
+// 8-row x 16-byte core matrices, `sbo` bytes between 8-row groups and `lbo`
+// between 16-byte column groups.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05; layout bits 61-63 = 0: no swizzle
+  return d;
+}
+
+// Shared memory (32 rows x 16 bytes, described by `sdesc`) -> TMEM lanes 0-31,
+// four 32-bit columns from `taddr`, replicated into all four lane quarters.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * scale_A) (B * scale_B), fp8 / fp6 / fp4 operands with one
+// E8M0 scale per 32 elements of K (kind::mxf8f6f4, scale_vec::1X); the scales
+// are read from TMEM at sfa / sfb, the byte chosen by the descriptor's ids.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A / B element
+// formats (0 E4M3, 1 E5M2), K-major A and B, fp32 D, E8M0 scales; the scale
+// byte ids (bits 4-5 for B, 29-30 for A) are or-ed in per K step.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_fmt, int b_fmt) {
+  return (static_cast<uint32_t>(a_fmt) << 7)        // A format
+         | (static_cast<uint32_t>(b_fmt) << 10)     // B format
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                               // scale format: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (b_id << 4) | (a_id << 29); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                   // D format: f32

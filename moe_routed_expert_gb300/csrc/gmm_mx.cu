@@ -1,0 +1,489 @@
+// Block-scaled (MXFP8) grouped matmul on the 5th-generation tensor cores.
+//
+// What it computes follows "MegaMoE", "A8W8-FP 量化场景": for each expert e
+// with rows [off_e, off_e + m_e) of the fp8 operand X,
+//   P_e = DQ_MX(X_e) DQ_MX(W_e)^T
+// with W_e = weight[e] stored [N, K] (one output channel per row) and one E8M0
+// scale per 32 elements of K on both sides, as the page's MXFP constraints lay
+// out weight1 / weight2 and weightScales1 / weightScales2.  Epilogues:
+//   plain  (stage 3)  O_e = bf16(P_e);
+//   ACT    (stage 2)  H = bf16(P_e) split into gate (first N/2 channels) and
+//                     up (last N/2), A = Activation(G, U), then Q_MX(A): fp8
+//                     codes and scales of the next matmul's operand.
+//
+// Design (one CTA per SM, 192 threads; 128 x 256 output tiles, K in blocks
+// of 128 fp8 elements = one 128-byte swizzle row):
+//   warp 0      producer.  Lane 0 issues the TMA copies of the A tile
+//               (128 rows x 128) and the B tile (256 channels x 128) into a
+//               4-stage ring.  All 32 lanes load the tile's scales, one stage
+//               ahead, as 32-bit words (4 consecutive scales of a row) and
+//               write them to shared memory in the order the tensor core
+//               reads them: per 128 rows a 512-byte block in which row r's
+//               word sits at word 4 (r % 32) + r / 32.
+//   warp 1      TMEM allocator; one thread copies the stage's scales into TMEM
+//               (tcgen05.cp 32x128b, replicated to all four lane quarters:
+//               4 columns for A, 8 for B) and issues four
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32)
+//               whose scale-factor ids pick byte kk of each scale word.
+//   warps 2..5  epilogue: tcgen05.ld -> registers -> release the accumulator
+//               -> global stores.
+// TMEM: one 256-column fp32 accumulator (the scales of the 4 stages take 48
+// more columns, so a second accumulator does not fit in 512); the epilogue
+// releases it as soon as the tile is in registers.
+// Group structure, tile order, bounded waits and the abort path are those of
+// the bf16 kernel (gmm.cu).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "launch.cuh"
+#include "mx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;                     // fp8 elements (bytes) per stage row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;            // 16 KB
+constexpr int B_BYTES = BN * BK;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SFA_BYTES = BM * 4;           // 4 scales per row per stage
+constexpr int SFB_BYTES = BN * 4;
+constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
+constexpr int ACC_COLS = BN;
+constexpr int SF_COLS = 12;                 // TMEM columns per stage: 4 (A) + 8 (B)
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+
+enum { MX_PLAIN = 0, MX_ACT = 1 };
+
+struct MxParams {
+  const int64_t* group_list;
+  const uint8_t* a_sf;   // [M, K/32]
+  const uint8_t* b_sf;   // [E, N, K/32]
+  int E;
+  int64_t rows_cap;      // M
+  int N;                 // channels of each expert's weight
+  int sf_ld;             // K / 32
+  int tile_cols;
+  int kblocks;           // K / 128
+  int out_cols;          // plain: N; ACT: N / 2
+  uint16_t* out;         // plain: bf16 [M, N]
+  uint8_t* aq;           // ACT: fp8 [M, N/2]
+  uint8_t* as;           // ACT: [M, N/64]
+  uint16_t* h_save;      // ACT: optional bf16 [M, N]
+  Act act;
+  uint32_t idesc;
+  uint32_t* status;
+};
+
+struct __align__(16) MxSmem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full;
+  uint64_t tmem_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+  int32_t bad;
+  int32_t ntiles;
+  int64_t grp_off[kMaxExperts + 1];
+  int32_t grp_cnt[kMaxExperts];
+  int32_t tile_start[kMaxExperts + 1];
+};
+
+// [A|B stages, 1024-aligned][scales per stage][MxSmem]
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_BYTES + sizeof(MxSmem);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct TileInfo {
+  int g;
+  int64_t row0;
+  int rows_valid;
+  int col0;   // first output column (ACT: first activation column)
+};
+
+template <int EPI>
+__device__ __forceinline__ TileInfo decode_tile(const MxSmem* sm, const MxParams& p, int t) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sm->tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  const int local = t - sm->tile_start[lo];
+  const int rt = local / p.tile_cols;
+  const int ct = local - rt * p.tile_cols;
+  ti.g = lo;
+  ti.col0 = ct * (EPI == MX_ACT ? BN / 2 : BN);
+  ti.row0 = sm->grp_off[lo] + static_cast<int64_t>(rt) * BM;
+  ti.rows_valid = min(BM, sm->grp_cnt[lo] - rt * BM);
+  return ti;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, kTimeoutNs) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  uint32_t dummy = 0;
+  mbar_wait_bounded(bar, parity, &dummy, 200000000ull);
+}
+
+// One lane's scale words of a stage: rows lane + 32 j of the A tile (j < 4),
+// channels lane + 32 j of the B tile (j < 8).  Rows past M and channels past
+// N read nothing (their data arrive as zeros from the TMA unit).
+struct SfWords {
+  uint32_t a[4];
+  uint32_t b[8];
+};
+
+template <int EPI>
+__device__ __forceinline__ void load_sf(const MxParams& p, const TileInfo& ti, int kb, int lane, SfWords& w) {
+  const int64_t ld = p.sf_ld;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t r = ti.row0 + lane + 32 * j;
+    w.a[j] = r < p.rows_cap ? ld_nc_u32(p.a_sf + r * ld + 4 * kb) : 0u;
+  }
+  const uint8_t* bsf = p.b_sf + static_cast<int64_t>(ti.g) * p.N * ld + 4 * kb;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    int n;
+    if (EPI == MX_ACT)  // channels [0, 128) of the tile: gate; [128, 256): the matching up channels
+      n = (j < 4 ? ti.col0 : p.out_cols + ti.col0) + lane + 32 * (j & 3);
+    else
+      n = ti.col0 + lane + 32 * j;
+    w.b[j] = n < p.N ? ld_nc_u32(bsf + static_cast<int64_t>(n) * ld) : 0u;
+  }
+}
+
+__device__ __forceinline__ void store_row32_bf16(uint16_t* dst, const uint32_t (&r)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 q;
+    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+    d[v] = q;
+  }
+}
+
+template <int EPI, int OUT_FMT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sf_smem = smem + STAGES * STAGE_BYTES;
+  MxSmem* sm = reinterpret_cast<MxSmem*>(sf_smem + STAGES * SF_STAGE_BYTES);
+  const uint32_t stage_base = smem_u32(smem);
+  const uint32_t sf_base = smem_u32(sf_smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    sm->bad = 0;
+    sm->abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm->tmem_full), 1);
+    mbar_init(smem_u32(&sm->tmem_empty), 4);
+    mbar_init(smem_u32(&sm->drain), 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  for (int e = tid; e < E; e += NUM_THREADS) {
+    const int64_t c = p.group_list[e];
+    if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
+    sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int64_t rows = 0;
+    int32_t tiles = 0;
+    for (int e = lo; e < hi; ++e) {
+      rows += sm->grp_cnt[e];
+      tiles += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
+    }
+    int64_t rows_incl = rows;
+    int32_t tiles_incl = tiles;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t r2 = __shfl_up_sync(0xffffffffu, rows_incl, d);
+      const int32_t t2 = __shfl_up_sync(0xffffffffu, tiles_incl, d);
+      if (lane >= d) { rows_incl += r2; tiles_incl += t2; }
+    }
+    int64_t rb = rows_incl - rows;
+    int32_t tb = tiles_incl - tiles;
+    for (int e = lo; e < hi; ++e) {
+      sm->grp_off[e] = rb;
+      sm->tile_start[e] = tb;
+      rb += sm->grp_cnt[e];
+      tb += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
+    }
+    if (lane == 31) {
+      sm->grp_off[E] = rows_incl;
+      sm->tile_start[E] = tiles_incl;
+      sm->ntiles = tiles_incl;
+      if (rows_incl > p.rows_cap) sm->bad = 1;
+    }
+  }
+  __syncthreads();
+  const uint32_t tmem_base = sm->tmem_base;
+  const int ntiles = sm->bad ? 0 : sm->ntiles;   // a bad group_list: no tile, straight to teardown
+  if (sm->bad && tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+  volatile uint32_t* abort_flag = &sm->abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer (whole warp)
+    uint32_t it = 0;
+    bool ok = true;
+    int t = blockIdx.x;
+    if (t < ntiles) {
+      TileInfo ti = decode_tile<EPI>(sm, p, t);
+      int kb = 0;
+      SfWords cur;
+      load_sf<EPI>(p, ti, 0, lane, cur);
+      while (true) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
+        const uint32_t sfa = sf_base + s * SF_STAGE_BYTES;
+        st_shared_v4(sfa + 16 * lane, cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
+        st_shared_v4(sfa + SFA_BYTES + 16 * lane, cur.b[0], cur.b[1], cur.b[2], cur.b[3]);
+        st_shared_v4(sfa + SFA_BYTES + 512 + 16 * lane, cur.b[4], cur.b[5], cur.b[6], cur.b[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bar = smem_u32(&sm->full[s]);
+          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          mbar_expect_tx(bar, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          if (EPI == MX_ACT) {  // 128 gate channels, then the 128 matching up channels
+            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
+            tma_load_3d(b_dst + (BN / 2) * BK, &tmB, bar, kb * BK, p.out_cols + ti.col0, ti.g);
+          } else {
+            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
+          }
+        }
+        ++it;
+        // next stage's scales, loaded now so their latency overlaps the next wait
+        if (++kb == p.kblocks) {
+          kb = 0;
+          t += gridDim.x;
+          if (t >= ntiles) break;
+          ti = decode_tile<EPI>(sm, p, t);
+        }
+        load_sf<EPI>(p, ti, kb, lane, cur);
+      }
+    }
+    if (!ok && lane == 0) {
+      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (one thread)
+    if (lane == 0) {
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++local) {
+        if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty), (local & 1u) ^ 1u, abort_flag, kTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = stage_base + s * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+          const uint32_t sfa_smem = sf_base + s * SF_STAGE_BYTES;
+          const uint32_t sf_col = tmem_base + ACC_COLS + s * SF_COLS;
+          tc_cp_32x128b_x4(sf_col, smem_desc_plain(sfa_smem, 128, 128));
+          tc_cp_32x128b_x4(sf_col + 4, smem_desc_plain(sfa_smem + SFA_BYTES, 128, 128));
+          tc_cp_32x128b_x4(sf_col + 8, smem_desc_plain(sfa_smem + SFA_BYTES + 512, 128, 128));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            tc_mma_mxf8(tmem_base, ad, bd, p.idesc | idesc_sf_ids(kk, kk), sf_col, sf_col + 4, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm->empty[s]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm->tmem_full));
+      }
+      if (!ok) {
+        tc_commit(smem_u32(&sm->drain));
+        drain_wait(smem_u32(&sm->drain), 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t local = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+      const TileInfo ti = decode_tile<EPI>(sm, p, t);
+      const bool row_ok = row_in_tile < ti.rows_valid;
+      const int64_t row = ti.row0 + row_in_tile;
+      if (!warp_wait(smem_u32(&sm->tmem_full), local & 1u, abort_flag, lane)) break;
+      tc_fence_after();
+      if (EPI == MX_ACT) {
+        const int I = p.out_cols;
+        uint32_t codes[32];
+        uint32_t scales = 0;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + 32 * cc, g);
+          tmem_ld32(taddr + BN / 2 + 32 * cc, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {   // H is bf16; the activation is taken on those values
+            g[i] = __float_as_uint(round_bf16(__uint_as_float(g[i])));
+            u[i] = __float_as_uint(round_bf16(__uint_as_float(u[i])));
+          }
+          if (p.h_save && row_ok) {
+            store_row32_bf16(p.h_save + row * (2 * static_cast<int64_t>(I)) + ti.col0 + 32 * cc, g);
+            store_row32_bf16(p.h_save + row * (2 * static_cast<int64_t>(I)) + I + ti.col0 + 32 * cc, u);
+          }
+          float a[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = act_forward(__uint_as_float(g[i]), __uint_as_float(u[i]), p.act);
+          uint32_t c8[8];
+          scales |= mx_quant32<OUT_FMT>(a, c8) << (8 * cc);
+#pragma unroll
+          for (int w = 0; w < 8; ++w) codes[8 * cc + w] = c8[w];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty));
+        if (row_ok) {
+          uint4* dq = reinterpret_cast<uint4*>(p.aq + row * I + ti.col0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) dq[v] = make_uint4(codes[4 * v], codes[4 * v + 1], codes[4 * v + 2], codes[4 * v + 3]);
+          *reinterpret_cast<uint32_t*>(p.as + row * (I / 32) + ti.col0 / 32) = scales;
+        }
+      } else {
+        uint32_t packed[BN / 2];   // the tile row in bf16 pairs
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; cc += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr + 32 * cc, r0);
+          tmem_ld32(taddr + 32 * (cc + 1), r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            packed[16 * cc + i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            packed[16 * (cc + 1) + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty));
+        if (row_ok) {
+          uint16_t* dst = p.out + row * p.out_cols + ti.col0;
+#pragma unroll
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            if (ti.col0 + 32 * cc < p.out_cols) {
+              uint4* d = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                d[v] = make_uint4(packed[16 * cc + 4 * v], packed[16 * cc + 4 * v + 1], packed[16 * cc + 4 * v + 2],
+                                  packed[16 * cc + 4 * v + 3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (sm->abort && tid == 0) set_status(p.status, MOE_ERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI, int OUT_FMT>
+moe_status_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& p, cudaStream_t s) {
+  auto kern = gmm_mx_kernel<EPI, OUT_FMT>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured_dev = dev;
+  }
+  if (launch_pdl(kern, dim3(num_sms()), dim3(NUM_THREADS), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s) {
+  MxParams p{};
+  p.group_list = x.group_list;
+  p.a_sf = x.a_sf;
+  p.b_sf = x.b_sf;
+  p.E = static_cast<int>(x.E);
+  p.rows_cap = x.M;
+  p.N = static_cast<int>(x.N);
+  p.sf_ld = static_cast<int>(x.K / 32);
+  p.kblocks = static_cast<int>(x.K / BK);
+  p.status = status;
+  p.idesc = idesc_mxf8(BM, BN, x.a_fmt, x.b_fmt);
+  const bool act = x.act != nullptr;
+  p.out_cols = static_cast<int>(act ? x.N / 2 : x.N);
+  p.tile_cols = act ? static_cast<int>((x.N / 2) / (BN / 2)) : static_cast<int>((x.N + BN - 1) / BN);
+  p.out = x.out;
+  p.aq = x.aq;
+  p.as = x.as;
+  p.h_save = x.h_save;
+  if (act) p.act = *x.act;
+  CUtensorMap ta, tb;
+  if (!make_map_2d_u8(&ta, x.a, x.M, x.K, BM) || !make_map_3d_u8(&tb, x.b, x.E, x.N, x.K, act ? BN / 2 : BN))
+    return MOE_ERR_CUDA;
+  if (!act) return launch_kernel<MX_PLAIN, MOE_FP8_E4M3>(ta, tb, p, s);
+  return x.out_fmt == MOE_FP8_E5M2 ? launch_kernel<MX_ACT, MOE_FP8_E5M2>(ta, tb, p, s)
+                                   : launch_kernel<MX_ACT, MOE_FP8_E4M3>(ta, tb, p, s);
+}
+
+}  // namespace moe

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "moe_gmm.h"
+#include "moe_mx.h"
 
 struct CUtensorMap_st;  // cuda.h
 
@@ -38,11 +39,24 @@ inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255);
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// ---- MX quantisation (mx.cu): fp8 codes + E8M0 scales, 32-element groups
+struct MxOut {
+  int fmt;           // MOE_FP8_E4M3 / MOE_FP8_E5M2
+  uint8_t* q;        // [rows, K] codes
+  uint8_t* scales;   // [rows, K/32]
+};
+moe_status_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, int fmt, uint8_t* q, uint8_t* scales,
+                                cudaStream_t s);
+// The permute's gather, quantising: slot f's token row of x -> row row_id_map[f].
+moe_status_t launch_mx_gather(const uint16_t* x, int64_t nslots, int64_t H, int k, const int32_t* row_id_map,
+                              const MxOut& out, cudaStream_t s);
+
 // ---- dispatch (permute.cu)
 size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E);
+// With `mx`, the gathered rows leave quantised into mx->q / mx->scales (x_perm unused).
 moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
                             uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
-                            uint32_t* status, void* scratch, cudaStream_t s);
+                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx = nullptr);
 
 // ---- combine side (combine.cu)
 moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
@@ -56,6 +70,9 @@ moe_status_t launch_act_backward(const uint16_t* h, const uint16_t* da, int64_t 
 // ---- TMA descriptors (tmap.cu): bf16, 128B swizzle, 64-element inner box
 bool make_map_2d(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 bool make_map_3d(::CUtensorMap_st* m, const void* base, int64_t E, int64_t K, int64_t N, int box_k);
+// fp8 codes: 128-byte inner box
+bool make_map_2d_u8(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+bool make_map_3d_u8(::CUtensorMap_st* m, const void* base, int64_t E, int64_t R, int64_t C, int box_rows);
 
 // ---- grouped matmul (gmm.cu, gmm_pair.cu)
 enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
@@ -86,6 +103,27 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
                         int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                         const GmmLaunch& how = GmmLaunch());
+// Block-scaled grouped matmul (gmm_mx.cu): a [M, K] fp8 with scales [M, K/32];
+// b [E, N, K] fp8 with scales [E, N, K/32].  act == nullptr: bf16 out [M, N];
+// else the activation of the [gate | up] halves, quantised into aq [M, N/2] /
+// as [M, N/64] (element format out_fmt), h_save optional bf16 [M, N].
+struct MxGmmArgs {
+  const uint8_t* a;
+  const uint8_t* a_sf;
+  const uint8_t* b;
+  const uint8_t* b_sf;
+  const int64_t* group_list;
+  int64_t M, K, N, E;
+  int a_fmt, b_fmt;
+  const Act* act;
+  uint16_t* out;
+  uint8_t* aq;
+  uint8_t* as;
+  int out_fmt;
+  uint16_t* h_save;
+};
+moe_status_t launch_gmm_mx(const MxGmmArgs& args, uint32_t* status, cudaStream_t s);
+
 // dX and dW of one grouped matmul (both read only inputs that exist before
 // either starts): small problems run them side by side on halves of the GPU,
 // large ones one after the other on all of it.  `dx_epilogue` / `h` as for

@@ -225,7 +225,7 @@ size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E) {
 
 moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
                             uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
-                            uint32_t* status, void* scratch, cudaStream_t s) {
+                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx) {
   const int64_t nslots = T * k;
   const int nchunks = static_cast<int>((nslots + CHUNK - 1) / CHUNK);
   int32_t* chunk_counts = static_cast<int32_t*>(scratch);
@@ -240,7 +240,9 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
   if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
                  static_cast<const int32_t*>(chunk_counts), row_id_map, sorted_flat) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (x != nullptr && x_perm != nullptr && H > 0) {
+  if (mx != nullptr && x != nullptr && H > 0) {
+    if (launch_mx_gather(x, nslots, H, static_cast<int>(k), row_id_map, *mx, s) != MOE_OK) return MOE_ERR_CUDA;
+  } else if (x != nullptr && x_perm != nullptr && H > 0) {
     const int64_t items = nslots * ((H + SEG - 1) / SEG);
     const int64_t warps_needed = items;
     int64_t blocks = (warps_needed + WARPS - 1) / WARPS;

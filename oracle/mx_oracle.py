@@ -151,8 +151,9 @@ def mx_quantize(x, fmt):
 
 
 def mx_dequantize(codes, scale_codes, fmt) -> np.ndarray:
-    """DQ_MX: element value times its group's scale."""
-    v = fp8_decode(codes, fmt)
+    """DQ_MX: element value times its group's scale (the element values looked
+    up in the table of all 256 decoded codes)."""
+    v = fp8_decode(np.arange(256), fmt)[np.asarray(codes, dtype=np.int64)]
     K = v.shape[-1]
     vb = v.reshape(v.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     s = e8m0_decode(scale_codes)[..., None]

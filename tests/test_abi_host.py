@@ -1,5 +1,5 @@
 """Host-only checks of the C ABI: the library builds and loads, exports every
-entry point include/moe_gmm.h declares, and rejects bad arguments on the host
+entry point include/*.h declares, and rejects bad arguments on the host
 before anything reaches a GPU (no call here launches a kernel)."""
 import ctypes as C
 import os
@@ -8,7 +8,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe_gmm.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -20,14 +21,17 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return re.findall(r"^MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    names = []
+    for h in HEADERS:
+        names += re.findall(r"^MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", open(h).read(), flags=re.M)
+    return names
 
 
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for n in ("gmm_forward", "gmm_backward", "moe_permute", "moe_unpermute", "moe_layer_forward",
-              "moe_layer_backward", "moe_unpermute_backward", "moe_permute_backward", "moe_swiglu_backward"):
+              "moe_layer_backward", "moe_unpermute_backward", "moe_permute_backward", "moe_swiglu_backward",
+              "moe_mx_quantize", "moe_permute_mx", "gmm_forward_mx", "moe_layer_forward_mx"):
         assert n in names
 
 
@@ -146,3 +150,54 @@ def test_python_binding_refuses_cpu_tensors(lib):
     gl = torch.tensor([16, 16, 0, 32])
     with pytest.raises((ValueError, RuntimeError)):
         M.gmm_forward(x, w, gl)
+
+
+def test_mx_entry_points_check_their_arguments(lib):
+    ws, nws = FAKE, 1 << 20
+    a = _abi_act(0)
+    assert lib.moe_mx_quantize_workspace_size() == 256
+    assert lib.gmm_mx_workspace_size(64, 128, 256, 4) == 256
+    T, H, I, E, k = 4096, 2048, 512, 256, 8
+    R = T * k
+    n = lib.moe_layer_mx_workspace_size(T, H, I, E, k)
+    assert n >= 256 + R * H + R * H // 32 + R * I + R * I // 32 + R * H * 2 + 2 * R * 4 + E * 8
+    # quantize: nulls, format, K % 32, alignment, zero rows is a no-op
+    assert lib.moe_mx_quantize(None, 4, 64, 0, FAKE, FAKE, ws, nws, None) == 1
+    assert lib.moe_mx_quantize(FAKE, 4, 64, 2, FAKE, FAKE, ws, nws, None) == 2
+    assert lib.moe_mx_quantize(FAKE, 4, 48, 0, FAKE, FAKE, ws, nws, None) == 3
+    assert lib.moe_mx_quantize(MIS, 4, 64, 0, FAKE, FAKE, ws, nws, None) == 2
+    assert lib.moe_mx_quantize(None, 0, 64, 1, None, None, ws, nws, None) == 0
+    # permute_mx
+    assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 2, 4, 0, None, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 1
+    assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 2, 4, 5, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2
+    assert lib.moe_permute_mx(FAKE, FAKE, 4, 48, 2, 4, 0, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 3
+    assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 5, 4, 0, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2
+    # gmm_forward_mx: plain needs y, activation needs a_q / a_scales; K and N multiples of 128
+    gm = lambda M, K, N, act, y, aq, as_, h, x=FAKE: lib.gmm_forward_mx(x, FAKE, FAKE, FAKE, FAKE, M, K, N, 4, 0, 1,
+                                                                         act, y, aq, as_, h, ws, nws, None)
+    assert gm(64, 128, 256, None, None, None, None, None) == 1
+    assert gm(64, 128, 256, a, FAKE, None, FAKE, None) == 1
+    assert gm(64, 192, 256, None, FAKE, None, None, None) == 3
+    assert gm(64, 128, 192, None, FAKE, None, None, None) == 3
+    assert gm(64, 128, 384, a, None, FAKE, FAKE, None) == 3          # 2I must be a multiple of 256
+    assert gm(64, 128, 256, None, FAKE, None, None, FAKE) == 2       # h_save without an activation
+    assert gm(64, 128, 256, None, FAKE, None, None, None, x=MIS) == 2
+    assert lib.gmm_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, 3, 0, None, FAKE, None, None, None,
+                              ws, nws, None) == 2                    # format
+    assert gm(0, 128, 256, None, FAKE, None, None, None) == 0        # no rows: nothing to do
+    # layer
+    lay = lambda H, I, xf, act: lib.moe_layer_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, H, I, 4, 2,
+                                                         xf, 0, act, FAKE, ws, nws, None)
+    assert lay(128, 128, 0, None) == 1
+    assert lay(128, 128, 9, a) == 2
+    assert lay(192, 128, 0, a) == 3                                   # H % 128
+    assert lay(128, 64, 0, a) == 3                                    # I % 128
+
+
+def _abi_act(kind, *params):
+    from moe_routed_expert_gb300 import _abi
+    x = _abi.MoeActivation()
+    x.kind, x.n_params = kind, len(params)
+    for i, v in enumerate(params):
+        x.params[i] = v
+    return C.byref(x)

@@ -30,7 +30,14 @@ layer_prefill_t4096      MoE layer fwd, T=4096, H=2048, E=256, k=8, I=512
 layer_decode_t64         MoE layer fwd, T=64, H=2048, E=256, k=8, I=512
 layer_train_t16384       MoE layer fwd+bwd, T=16384, H=4096, E=64, k=8,
                          I=1024, SwiGLU clip 7, one hot expert (+2 logit)
+layer_prefill_mx_t4096   the prefill layer in MXFP8 (E4M3 tokens and weights)
+layer_decode_mx_t64      the decode layer in MXFP8 (E4M3 tokens and weights)
 =======================  ====================================================
+
+MXFP8 weights are drawn directly as codes: N(0, 16^2) draws cast to the fp8
+type by torch's CPU conversion (a library cast, not the method's Q_MX), with
+E8M0 scale codes drawn uniformly from three values centred so that the
+dequantised weights have a standard deviation near 1/sqrt(K).
 """
 from __future__ import annotations
 
@@ -42,6 +49,7 @@ import numpy as np
 __all__ = [
     "GmmWorkload", "LayerWorkload", "WORKLOADS", "f32_to_bf16_bits",
     "gmm_inputs", "layer_inputs", "routing", "zipf_counts", "normal_bf16",
+    "fp8_codes", "e8m0_codes", "mx_weight", "mx_layer_weights",
 ]
 
 
@@ -74,6 +82,7 @@ class LayerWorkload:
     clip: float
     hot_bias: float
     backward: bool
+    mx: str = ""   # "" (bf16 path) or the fp8 element type of the MXFP8 forward
 
     @property
     def R(self) -> int:
@@ -92,6 +101,10 @@ WORKLOADS = {
                                       clip=0.0, hot_bias=0.0, backward=False),
     "layer_train_t16384": LayerWorkload("layer_train_t16384", 5, T=16384, H=4096, E=64, k=8, I=1024,
                                         clip=7.0, hot_bias=2.0, backward=True),
+    "layer_prefill_mx_t4096": LayerWorkload("layer_prefill_mx_t4096", 3, T=4096, H=2048, E=256, k=8, I=512,
+                                            clip=0.0, hot_bias=0.0, backward=False, mx="e4m3"),
+    "layer_decode_mx_t64": LayerWorkload("layer_decode_mx_t64", 4, T=64, H=2048, E=256, k=8, I=512,
+                                         clip=0.0, hot_bias=0.0, backward=False, mx="e4m3"),
 }
 
 
@@ -194,3 +207,33 @@ def layer_inputs(wl: LayerWorkload, seed: Optional[int] = None, tokens: Optional
             if key in out:
                 out[key] = np.ascontiguousarray(out[key][:tokens])
     return out
+
+
+def fp8_codes(rng: np.random.Generator, shape, fmt: str = "e4m3", std: float = 16.0) -> np.ndarray:
+    """N(0, std^2) draws cast to an fp8 type by torch's CPU conversion, as raw
+    uint8 codes (fmt "e4m3" = float8_e4m3fn or "e5m2")."""
+    import torch
+    dt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[fmt]
+    a = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std)
+    return torch.from_numpy(a).to(dt).view(torch.uint8).numpy().copy()
+
+
+def e8m0_codes(rng: np.random.Generator, shape, centre: int) -> np.ndarray:
+    """Scale codes drawn uniformly from centre-1, centre, centre+1."""
+    return rng.integers(centre - 1, centre + 2, size=shape).astype(np.uint8)
+
+
+def mx_weight(rng: np.random.Generator, E: int, N: int, K: int, fmt: str = "e4m3"):
+    """(codes [E, N, K], scales [E, N, K/32]) of an MX weight whose dequantised
+    values have a standard deviation near 1/sqrt(K) (codes ~ N(0, 16^2))."""
+    centre = 127 - 4 - int(round(0.5 * np.log2(K)))
+    return fp8_codes(rng, (E, N, K), fmt), e8m0_codes(rng, (E, N, K // 32), centre)
+
+
+def mx_layer_weights(wl: LayerWorkload, seed: Optional[int] = None, fmt: Optional[str] = None) -> dict:
+    """w1_q [E, 2I, H], w1_s [E, 2I, H/32], w2_q [E, H, I], w2_s [E, H, I/32] (uint8)."""
+    fmt = fmt or wl.mx or "e4m3"
+    wrng = np.random.default_rng((wl.seed if seed is None else seed) + 2000)
+    w1q, w1s = mx_weight(wrng, wl.E, 2 * wl.I, wl.H, fmt)
+    w2q, w2s = mx_weight(wrng, wl.E, wl.H, wl.I, fmt)
+    return {"w1_q": w1q, "w1_s": w1s, "w2_q": w2q, "w2_s": w2s}

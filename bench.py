@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from workloads import WORKLOADS, gmm_inputs, layer_inputs  # noqa: E402
+from workloads import WORKLOADS, gmm_inputs, layer_inputs, mx_layer_weights  # noqa: E402
 
 METRIC = "GMM fwd+bwd TFLOP/s and MoE-layer tokens/s on 1 GB300; % of bf16 peak / HBM BW"
 DEFAULT_WORKLOAD = "layer_train_t16384"
@@ -281,6 +281,85 @@ class LayerFwdStep(LayerTrainStep):
     e2e_api = "moe_layer_forward"
 
 
+class LayerMxStep:
+    """The MXFP8 (A8W8-FP) layer forward as the calls moe_layer_forward_mx makes:
+    quantising permute, block-scaled gate_up GMM with the activation and Q_MX in
+    its epilogue, block-scaled down GMM, combine."""
+
+    def __init__(self, wl, dev, inp):
+        import torch
+        import moe_routed_expert_gb300 as M
+        self.M, self.wl, self.dev = M, wl, dev
+        T, H, E, k, I = wl.T, wl.H, wl.E, wl.k, wl.I
+        R = T * k
+        u8 = torch.uint8
+        self.x = bf16_dev(inp["x"], dev)
+        self.ids = torch.from_numpy(inp["topk_ids"]).to(dev)
+        self.tw = torch.from_numpy(inp["topk_w"]).to(dev)
+        self.w1q, self.w1s = (torch.from_numpy(inp[n]).to(dev) for n in ("w1_q", "w1_s"))
+        self.w2q, self.w2s = (torch.from_numpy(inp[n]).to(dev) for n in ("w2_q", "w2_s"))
+        self.xq = torch.empty(R, H, dtype=u8, device=dev)
+        self.xs = torch.empty(R, H // 32, dtype=u8, device=dev)
+        self.gl = torch.empty(E, dtype=torch.int64, device=dev)
+        self.rmap = torch.empty(R, dtype=torch.int32, device=dev)
+        self.sflat = torch.empty(R, dtype=torch.int32, device=dev)
+        self.aq = torch.empty(R, I, dtype=u8, device=dev)
+        self.as_ = torch.empty(R, I // 32, dtype=u8, device=dev)
+        self.o = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.ws = M.Workspace(max(M.moe_permute_workspace_size(T, k, E), M.moe_layer_mx_workspace_size(T, H, I, E, k)),
+                              dev)
+        self.act = ("swiglu", [wl.clip])
+        ids = inp["topk_ids"]
+        counts = np.bincount(ids[ids >= 0].ravel(), minlength=E)
+        live = int((counts > 0).sum())
+        Rr = int(counts.sum())
+        f_up, f_dn = 2.0 * Rr * H * 2 * I, 2.0 * Rr * I * H
+        self.stages = [
+            ("permute_mx", self.permute, 0.0, 4),
+            ("gmm_mx_gate_up_act_quant", self.gmm1, f_up, 1),
+            ("gmm_mx_down", self.gmm2, f_dn, 1),
+            ("combine", self.combine, 0.0, 1),
+        ]
+        # algorithmic bytes: fp8 weights and their scales of the non-empty experts, operands in and results out once
+        self.gmm_bytes = {"gmm_mx_gate_up_act_quant": live * 2 * I * (H + H // 32) + Rr * (H + H // 32)
+                          + Rr * (I + I // 32),
+                          "gmm_mx_down": live * H * (I + I // 32) + Rr * (I + I // 32) + Rr * H * 2}
+        self.units = T
+        self.unit = "tokens/s"
+        self.dtype = "mxfp8_" + wl.mx
+        self.kernel = "gmm_mx_kernel (both block-scaled GMM launches of a step)"
+
+    def permute(self):
+        self.M.moe_permute_mx(self.x, self.ids, self.wl.E, self.wl.mx,
+                              out=(self.xq, self.xs, self.gl, self.rmap, self.sflat), ws=self.ws)
+
+    def gmm1(self):
+        self.M.gmm_forward_mx(self.xq, self.xs, self.w1q, self.w1s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wl.mx,
+                              activation=self.act, a_q=self.aq, a_scales=self.as_, ws=self.ws)
+
+    def gmm2(self):
+        self.M.gmm_forward_mx(self.aq, self.as_, self.w2q, self.w2s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wl.mx,
+                              y=self.o, ws=self.ws)
+
+    def combine(self):
+        self.M.moe_unpermute(self.o, self.rmap, self.tw, self.wl.T, self.wl.k, y=self.y, ws=self.ws)
+
+    def e2e_host_inputs(self, inp):
+        return {"x": pinned_bf16(inp["x"]), "topk_ids": pinned(inp["topk_ids"]), "topk_w": pinned(inp["topk_w"])}
+
+    def e2e_outputs(self):
+        import torch
+        return {"y": torch.empty(self.wl.T, self.wl.H, dtype=torch.bfloat16, device=self.dev)}
+
+    def e2e_compute(self, i, o):
+        self.M.moe_layer_forward_mx(i["x"], i["topk_ids"], i["topk_w"], self.w1q, self.w1s, self.w2q, self.w2s,
+                                    x_fmt=self.wl.mx, w_fmt=self.wl.mx, activation=self.act, y=o["y"], ws=self.ws)
+
+    e2e_launches = 4 + 2 + 1
+    e2e_api = "moe_layer_forward_mx"
+
+
 class GmmStep:
     """Standalone grouped matmul forward + dX + dW (the Zipf GMM workload)."""
 
@@ -385,6 +464,12 @@ def make_step(name, dev, tokens=None):
     if name.startswith("gmm"):
         inp = gmm_inputs(wl)
         return GmmStep(wl, dev, inp), inp
+    if wl.mx:
+        inp = layer_inputs(wl, tokens=tokens, with_weights=False)
+        inp.update(mx_layer_weights(wl))
+        if tokens is not None:
+            wl = wl.with_tokens(tokens)
+        return LayerMxStep(wl, dev, inp), inp
     inp = layer_inputs(wl, tokens=tokens)
     if tokens is not None:   # a smaller batch of the same workload (profiling captures)
         wl = wl.with_tokens(tokens)
@@ -401,6 +486,14 @@ def oracle_layer_step(wl, inp_sub):
         O.moe_layer_backward(f(inp_sub["dy"]), sv, inp_sub["topk_w"], w1, w2, wl.clip)
 
 
+def oracle_mx_layer_step(wl, inp_sub):
+    import oracle as O
+    from oracle import mx_oracle as X
+    X.mx_layer_forward(O.bf16_bits_to_f64(inp_sub["x"]), inp_sub["topk_ids"], inp_sub["topk_w"], inp_sub["w1_q"],
+                       inp_sub["w1_s"], inp_sub["w2_q"], inp_sub["w2_s"], wl.mx, wl.mx,
+                       O.activation("swiglu", [wl.clip]))
+
+
 def layer_sample(inp, T, E):
     """The first T tokens, with only the slots routed to experts 0..E-1 kept (the
     rest marked unused) and only those experts' weights: every kept expert does
@@ -412,7 +505,9 @@ def layer_sample(inp, T, E):
     for key in ("x", "topk_w", "dy"):
         if key in inp:
             d[key] = np.ascontiguousarray(inp[key][:T])
-    d["w1"], d["w2"] = inp["w1"][:E], inp["w2"][:E]
+    for key in ("w1", "w2", "w1_q", "w1_s", "w2_q", "w2_s"):
+        if key in inp:
+            d[key] = inp[key][:E]
     return d, int((ids >= 0).sum())
 
 
@@ -449,17 +544,19 @@ def cpu_sample(name, inp, target_s=15.0):
     # token-equivalents: a token owns k routed rows
     E_s = max(1, wl.E // 8)
     T_s = max(1, wl.T // 8)
+    run = oracle_mx_layer_step if wl.mx else oracle_layer_step
     sub, rows = layer_sample(inp, T_s, E_s)
-    t0 = time.perf_counter(); oracle_layer_step(wl, sub); dt = time.perf_counter() - t0
+    t0 = time.perf_counter(); run(wl, sub); dt = time.perf_counter() - t0
     if dt < target_s / 3 and T_s < wl.T:
         T_s = int(min(wl.T, T_s * max(1.0, target_s / max(dt, 1e-3))))
         sub, rows = layer_sample(inp, T_s, E_s)
-        t0 = time.perf_counter(); oracle_layer_step(wl, sub); dt = time.perf_counter() - t0
+        t0 = time.perf_counter(); run(wl, sub); dt = time.perf_counter() - t0
     tok_eq = rows / wl.k
     desc = ("first %d of %d tokens, slots of experts 0..%d of %d kept (%d routed rows = %.0f token-equivalents "
-            "at k=%d), layer fwd%s in float64" % (T_s, wl.T, E_s - 1, wl.E, rows, tok_eq, wl.k,
-                                                  "+bwd" if wl.backward else ""))
-    return tok_eq / dt, "tokens/s", desc, dt, (lambda: oracle_layer_step(wl, sub)), tok_eq
+            "at k=%d), layer fwd%s%s in float64" % (T_s, wl.T, E_s - 1, wl.E, rows, tok_eq, wl.k,
+                                                    "+bwd" if wl.backward else "",
+                                                    " (MXFP8 %s, quantisation included)" % wl.mx if wl.mx else ""))
+    return tok_eq / dt, "tokens/s", desc, dt, (lambda: run(wl, sub)), tok_eq
 
 
 def run_reference(args):
@@ -468,7 +565,13 @@ def run_reference(args):
         return 0
     name = args.workload
     wl = WORKLOADS[name]
-    inp = gmm_inputs(wl) if name.startswith("gmm") else layer_inputs(wl)
+    if name.startswith("gmm"):
+        inp = gmm_inputs(wl)
+    elif wl.mx:
+        inp = layer_inputs(wl, with_weights=False)
+        inp.update(mx_layer_weights(wl))
+    else:
+        inp = layer_inputs(wl)
     # one bounded sample per step, sized so the whole run stays within a few minutes
     per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     _, unit, sample, _, fn, units = cpu_sample(name, inp, target_s=per_step)
@@ -603,7 +706,8 @@ def main():
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": "gmm_kernel (all GMM launches of a step)", "peak_kind": "hbm copy, %s" % peaks["source"]}
+                "kernel": getattr(step, "kernel", "gmm_kernel (all GMM launches of a step)"),
+                "peak_kind": "hbm copy, %s" % peaks["source"]}
     else:
         achieved = gmm_flops / (gmm_ms / 1e3) / 1e12
         long_step = ms_per_step * args.steps > 500.0
@@ -616,10 +720,10 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": step.unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": getattr(step, "dtype", "bf16"), "data": "synthetic",
             "config": {"workload": args.workload, **{k_: v_ for k_, v_ in vars(step.wl).items() if k_ != "name"},
-                       "l2": "inputs larger than L2" if args.workload != "layer_decode_t64"
-                       else "weights (1.4 GB touched) larger than L2", "parallelism": "replicas" if world > 1 else "1 GPU"},
+                       "l2": "inputs larger than L2" if not args.workload.startswith("layer_decode")
+                       else "weights (%s touched) larger than L2" % ("0.7 GB" if step.wl.mx else "1.4 GB"), "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": roof, "kernels": kernels,
             "kernels_timing": "CUDA events after every launch, in a second pass of the same steps",
             "gpu_launches": launches * args.steps,

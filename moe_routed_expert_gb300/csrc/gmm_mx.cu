@@ -15,21 +15,24 @@
 // of 128 fp8 elements = one 128-byte swizzle row):
 //   warp 0      producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
-//               4-stage ring.  All 32 lanes load the tile's scales, one stage
-//               ahead, as 32-bit words (4 consecutive scales of a row) and
-//               write them to shared memory in the order the tensor core
-//               reads them: per 128 rows a 512-byte block in which row r's
-//               word sits at word 4 (r % 32) + r / 32.
+//               4-stage ring.  All 32 lanes copy the stage's scales 4 stages
+//               ahead with cp.async (4 bytes each: the 4 scales of one row),
+//               into an 8-slot ring, in the order the tensor core reads them:
+//               per 128 rows a 512-byte block in which row r's word sits at
+//               word 4 (r % 32) + r / 32.  Before a stage's TMA copies are
+//               issued the warp waits for its own copies of that stage
+//               (cp.async.wait_group) and fences them for the async proxy.
 //   warp 1      TMEM allocator; one thread copies the stage's scales into TMEM
 //               (tcgen05.cp 32x128b, replicated to all four lane quarters:
 //               4 columns for A, 8 for B) and issues four
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32)
 //               whose scale-factor ids pick byte kk of each scale word.
-//   warps 2..5  epilogue: tcgen05.ld -> registers -> release the accumulator
-//               -> global stores.
-// TMEM: one 256-column fp32 accumulator (the scales of the 4 stages take 48
-// more columns, so a second accumulator does not fit in 512); the epilogue
-// releases it as soon as the tile is in registers.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half
+//               of the tile's columns: tcgen05.ld -> registers (bf16) ->
+//               release the accumulator -> activation / Q_MX -> global stores.
+// TMEM: one 256-column fp32 accumulator (the scales of the 8 scale slots
+// take 96 more columns, so a second accumulator does not fit in 512); the
+// epilogue releases it as soon as the tile is in registers.
 // Group structure, tile order, bounded waits and the abort path are those of
 // the bf16 kernel (gmm.cu).
 #include <cuda.h>
@@ -57,11 +60,17 @@ constexpr int SFA_BYTES = BM * 4;           // 4 scales per row per stage
 constexpr int SFB_BYTES = BN * 4;
 constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 constexpr int ACC_COLS = BN;
-constexpr int SF_COLS = 12;                 // TMEM columns per stage: 4 (A) + 8 (B)
+constexpr int SF_COLS = 12;                 // TMEM columns per scale slot: 4 (A) + 8 (B)
+constexpr int SF_SLOTS = 8;                 // scale ring (shared memory and TMEM)
+constexpr int SF_AHEAD = 4;                 // stages between a scale copy and its use
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
-static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+static_assert(ACC_COLS + SF_SLOTS * SF_COLS <= TMEM_COLS, "TMEM budget");
+// the scale slot written at stage i + SF_AHEAD was last read at stage i + SF_AHEAD - SF_SLOTS,
+// which the wait for the data slot of stage i has already seen finish
+static_assert(SF_AHEAD + STAGES <= SF_SLOTS, "scale ring reuse");
 
 enum { MX_PLAIN = 0, MX_ACT = 1 };
 
@@ -100,8 +109,8 @@ struct __align__(16) MxSmem {
   int32_t tile_start[kMaxExperts + 1];
 };
 
-// [A|B stages, 1024-aligned][scales per stage][MxSmem]
-constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_BYTES + sizeof(MxSmem);
+// [A|B stages, 1024-aligned][scale slots][MxSmem]
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + SF_SLOTS * SF_STAGE_BYTES + sizeof(MxSmem);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct TileInfo {
@@ -140,21 +149,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   mbar_wait_bounded(bar, parity, &dummy, 200000000ull);
 }
 
-// One lane's scale words of a stage: rows lane + 32 j of the A tile (j < 4),
-// channels lane + 32 j of the B tile (j < 8).  Rows past M and channels past
-// N read nothing (their data arrive as zeros from the TMA unit).
-struct SfWords {
-  uint32_t a[4];
-  uint32_t b[8];
-};
-
+// Copy one stage's scales into a scale slot: lane l copies the words of rows
+// l + 32 j of the A tile (j < 4) and of channels l + 32 j of the B tile
+// (j < 8) to the tensor core's order.  Rows past M and channels past N copy
+// zeros (their data arrive as zeros from the TMA unit).
 template <int EPI>
-__device__ __forceinline__ void load_sf(const MxParams& p, const TileInfo& ti, int kb, int lane, SfWords& w) {
+__device__ __forceinline__ void copy_sf(const MxParams& p, const TileInfo& ti, int kb, int lane, uint32_t slot) {
   const int64_t ld = p.sf_ld;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int64_t r = ti.row0 + lane + 32 * j;
-    w.a[j] = r < p.rows_cap ? ld_nc_u32(p.a_sf + r * ld + 4 * kb) : 0u;
+    const bool in = r < p.rows_cap;
+    cp_async4(slot + 16 * lane + 4 * j, p.a_sf + (in ? r * ld + 4 * kb : 0), in ? 4u : 0u);
   }
   const uint8_t* bsf = p.b_sf + static_cast<int64_t>(ti.g) * p.N * ld + 4 * kb;
 #pragma unroll
@@ -164,20 +170,36 @@ __device__ __forceinline__ void load_sf(const MxParams& p, const TileInfo& ti, i
       n = (j < 4 ? ti.col0 : p.out_cols + ti.col0) + lane + 32 * (j & 3);
     else
       n = ti.col0 + lane + 32 * j;
-    w.b[j] = n < p.N ? ld_nc_u32(bsf + static_cast<int64_t>(n) * ld) : 0u;
+    const bool in = n < p.N;
+    cp_async4(slot + SFA_BYTES + 512 * (j >> 2) + 16 * lane + 4 * (j & 3),
+              in ? bsf + static_cast<int64_t>(n) * ld : p.b_sf, in ? 4u : 0u);
   }
 }
 
-__device__ __forceinline__ void store_row32_bf16(uint16_t* dst, const uint32_t (&r)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    uint4 q;
-    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-    d[v] = q;
+// Position of the producer in its walk over (tile, K block) stages.
+struct StageIter {
+  int t;
+  int kb;
+  bool valid;
+  TileInfo ti;
+};
+
+template <int EPI>
+__device__ __forceinline__ void stage_iter_start(StageIter& w, const MxSmem* sm, const MxParams& p, int ntiles) {
+  w.t = blockIdx.x;
+  w.kb = 0;
+  w.valid = w.t < ntiles;
+  if (w.valid) w.ti = decode_tile<EPI>(sm, p, w.t);
+}
+
+template <int EPI>
+__device__ __forceinline__ void stage_iter_next(StageIter& w, const MxSmem* sm, const MxParams& p, int ntiles) {
+  if (!w.valid) return;
+  if (++w.kb == p.kblocks) {
+    w.kb = 0;
+    w.t += gridDim.x;
+    w.valid = w.t < ntiles;
+    if (w.valid) w.ti = decode_tile<EPI>(sm, p, w.t);
   }
 }
 
@@ -187,7 +209,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_smem = smem + STAGES * STAGE_BYTES;
-  MxSmem* sm = reinterpret_cast<MxSmem*>(sf_smem + STAGES * SF_STAGE_BYTES);
+  MxSmem* sm = reinterpret_cast<MxSmem*>(sf_smem + SF_SLOTS * SF_STAGE_BYTES);
   const uint32_t stage_base = smem_u32(smem);
   const uint32_t sf_base = smem_u32(sf_smem);
 
@@ -205,7 +227,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       mbar_init(smem_u32(&sm->empty[s]), 1);
     }
     mbar_init(smem_u32(&sm->tmem_full), 1);
-    mbar_init(smem_u32(&sm->tmem_empty), 4);
+    mbar_init(smem_u32(&sm->tmem_empty), EPI_WARPS);
     mbar_init(smem_u32(&sm->drain), 1);
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -268,45 +290,44 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // ---------------------------------------------------------------- producer (whole warp)
     uint32_t it = 0;
     bool ok = true;
-    int t = blockIdx.x;
-    if (t < ntiles) {
-      TileInfo ti = decode_tile<EPI>(sm, p, t);
-      int kb = 0;
-      SfWords cur;
-      load_sf<EPI>(p, ti, 0, lane, cur);
-      while (true) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
-        const uint32_t sfa = sf_base + s * SF_STAGE_BYTES;
-        st_shared_v4(sfa + 16 * lane, cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
-        st_shared_v4(sfa + SFA_BYTES + 16 * lane, cur.b[0], cur.b[1], cur.b[2], cur.b[3]);
-        st_shared_v4(sfa + SFA_BYTES + 512 + 16 * lane, cur.b[4], cur.b[5], cur.b[6], cur.b[7]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t bar = smem_u32(&sm->full[s]);
-          const uint32_t a_dst = stage_base + s * STAGE_BYTES;
-          const uint32_t b_dst = a_dst + A_BYTES;
-          mbar_expect_tx(bar, STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
-          if (EPI == MX_ACT) {  // 128 gate channels, then the 128 matching up channels
-            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
-            tma_load_3d(b_dst + (BN / 2) * BK, &tmB, bar, kb * BK, p.out_cols + ti.col0, ti.g);
-          } else {
-            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
-          }
-        }
-        ++it;
-        // next stage's scales, loaded now so their latency overlaps the next wait
-        if (++kb == p.kblocks) {
-          kb = 0;
-          t += gridDim.x;
-          if (t >= ntiles) break;
-          ti = decode_tile<EPI>(sm, p, t);
-        }
-        load_sf<EPI>(p, ti, kb, lane, cur);
-      }
+    StageIter cur, pre;
+    stage_iter_start<EPI>(cur, sm, p, ntiles);
+    pre = cur;
+#pragma unroll 1
+    for (int d = 0; d < SF_AHEAD; ++d) {   // scales of the first SF_AHEAD stages (one group each)
+      if (pre.valid) copy_sf<EPI>(p, pre.ti, pre.kb, lane, sf_base + d * SF_STAGE_BYTES);
+      cp_async_commit();
+      stage_iter_next<EPI>(pre, sm, p, ntiles);
     }
+    while (cur.valid) {
+      const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+      if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
+      // scales of stage it + SF_AHEAD (their slot's last reader, stage it + SF_AHEAD - SF_SLOTS,
+      // finished before the data slot of stage it was released)
+      if (pre.valid) copy_sf<EPI>(p, pre.ti, pre.kb, lane, sf_base + ((it + SF_AHEAD) % SF_SLOTS) * SF_STAGE_BYTES);
+      cp_async_commit();
+      stage_iter_next<EPI>(pre, sm, p, ntiles);
+      cp_async_wait<SF_AHEAD>();           // this lane's copies of stage it have landed
+      fence_proxy_async_smem();            // ... and are visible to tcgen05.cp
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&sm->full[s]);
+        const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+        const uint32_t b_dst = a_dst + A_BYTES;
+        const TileInfo& ti = cur.ti;
+        mbar_expect_tx(bar, STAGE_BYTES);
+        tma_load_2d(a_dst, &tmA, bar, cur.kb * BK, static_cast<int32_t>(ti.row0));
+        if (EPI == MX_ACT) {  // 128 gate channels, then the 128 matching up channels
+          tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
+          tma_load_3d(b_dst + (BN / 2) * BK, &tmB, bar, cur.kb * BK, p.out_cols + ti.col0, ti.g);
+        } else {
+          tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
+        }
+      }
+      ++it;
+      stage_iter_next<EPI>(cur, sm, p, ntiles);
+    }
+    cp_async_wait_all();                   // no copy of this CTA outlives it
     if (!ok && lane == 0) {
       const uint32_t first = it > STAGES ? it - STAGES : 0;
       for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
@@ -328,8 +349,9 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           tc_fence_after();
           const uint32_t a_addr = stage_base + s * STAGE_BYTES;
           const uint32_t b_addr = a_addr + A_BYTES;
-          const uint32_t sfa_smem = sf_base + s * SF_STAGE_BYTES;
-          const uint32_t sf_col = tmem_base + ACC_COLS + s * SF_COLS;
+          const uint32_t sf_slot = it % SF_SLOTS;
+          const uint32_t sfa_smem = sf_base + sf_slot * SF_STAGE_BYTES;
+          const uint32_t sf_col = tmem_base + ACC_COLS + sf_slot * SF_COLS;
           tc_cp_32x128b_x4(sf_col, smem_desc_plain(sfa_smem, 128, 128));
           tc_cp_32x128b_x4(sf_col + 4, smem_desc_plain(sfa_smem + SFA_BYTES, 128, 128));
           tc_cp_32x128b_x4(sf_col + 8, smem_desc_plain(sfa_smem + SFA_BYTES + 512, 128, 128));
@@ -351,7 +373,8 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;         // which half of the tile's columns
     const int row_in_tile = q * 32 + lane;
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t local = 0;
@@ -362,48 +385,63 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (!warp_wait(smem_u32(&sm->tmem_full), local & 1u, abort_flag, lane)) break;
       tc_fence_after();
       if (EPI == MX_ACT) {
+        // activation columns [64 half, 64 half + 64): gate at TMEM columns 64 half + c,
+        // up at 128 + 64 half + c; held as bf16 pairs (gate low, up high)
         const int I = p.out_cols;
-        uint32_t codes[32];
-        uint32_t scales = 0;
+        uint32_t gu[64];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t g[32], u[32];
-          tmem_ld32(taddr + 32 * cc, g);
-          tmem_ld32(taddr + BN / 2 + 32 * cc, u);
+          tmem_ld32(taddr + 64 * half + 32 * cc, g);
+          tmem_ld32(taddr + BN / 2 + 64 * half + 32 * cc, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {   // H is bf16; the activation is taken on those values
-            g[i] = __float_as_uint(round_bf16(__uint_as_float(g[i])));
-            u[i] = __float_as_uint(round_bf16(__uint_as_float(u[i])));
-          }
-          if (p.h_save && row_ok) {
-            store_row32_bf16(p.h_save + row * (2 * static_cast<int64_t>(I)) + ti.col0 + 32 * cc, g);
-            store_row32_bf16(p.h_save + row * (2 * static_cast<int64_t>(I)) + I + ti.col0 + 32 * cc, u);
-          }
-          float a[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = act_forward(__uint_as_float(g[i]), __uint_as_float(u[i]), p.act);
-          uint32_t c8[8];
-          scales |= mx_quant32<OUT_FMT>(a, c8) << (8 * cc);
-#pragma unroll
-          for (int w = 0; w < 8; ++w) codes[8 * cc + w] = c8[w];
+          for (int i = 0; i < 32; ++i) gu[32 * cc + i] = pack_bf16x2(__uint_as_float(g[i]), __uint_as_float(u[i]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty));
         if (row_ok) {
-          uint4* dq = reinterpret_cast<uint4*>(p.aq + row * I + ti.col0);
+          const int c0 = ti.col0 + 64 * half;
+          uint32_t scales = 0;
 #pragma unroll
-          for (int v = 0; v < 8; ++v) dq[v] = make_uint4(codes[4 * v], codes[4 * v + 1], codes[4 * v + 2], codes[4 * v + 3]);
-          *reinterpret_cast<uint32_t*>(p.as + row * (I / 32) + ti.col0 / 32) = scales;
+          for (int cc = 0; cc < 2; ++cc) {
+            float a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)   // H is bf16; the activation is taken on those values
+              a[i] = act_forward(bf16_lo(gu[32 * cc + i]), bf16_hi(gu[32 * cc + i]), p.act);
+            uint32_t c8[8];
+            scales |= mx_quant32<OUT_FMT>(a, c8) << (8 * cc);
+            uint4* dq = reinterpret_cast<uint4*>(p.aq + row * I + c0 + 32 * cc);
+            dq[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
+            dq[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
+          }
+          *reinterpret_cast<uint16_t*>(p.as + row * (I / 32) + c0 / 32) = static_cast<uint16_t>(scales);
+          if (p.h_save) {
+            uint16_t* hg = p.h_save + row * (2 * static_cast<int64_t>(I)) + c0;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              uint4 gq, uq;
+              uint32_t* gw = &gq.x;
+              uint32_t* uw = &uq.x;
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint32_t p0 = gu[8 * v + 2 * w], p1 = gu[8 * v + 2 * w + 1];
+                gw[w] = (p0 & 0xFFFFu) | (p1 << 16);
+                uw[w] = (p0 >> 16) | (p1 & 0xFFFF0000u);
+              }
+              reinterpret_cast<uint4*>(hg)[v] = gq;
+              reinterpret_cast<uint4*>(hg + I)[v] = uq;
+            }
+          }
         }
       } else {
-        uint32_t packed[BN / 2];   // the tile row in bf16 pairs
+        uint32_t packed[64];   // this warp's 128 columns of the tile row, as bf16 pairs
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; cc += 2) {
+        for (int cc = 0; cc < 4; cc += 2) {
           uint32_t r0[32], r1[32];
-          tmem_ld32(taddr + 32 * cc, r0);
-          tmem_ld32(taddr + 32 * (cc + 1), r1);
+          tmem_ld32(taddr + 128 * half + 32 * cc, r0);
+          tmem_ld32(taddr + 128 * half + 32 * (cc + 1), r1);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -415,10 +453,11 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty));
         if (row_ok) {
-          uint16_t* dst = p.out + row * p.out_cols + ti.col0;
+          const int c0 = ti.col0 + 128 * half;
+          uint16_t* dst = p.out + row * p.out_cols + c0;
 #pragma unroll
-          for (int cc = 0; cc < BN / 32; ++cc) {
-            if (ti.col0 + 32 * cc < p.out_cols) {
+          for (int cc = 0; cc < 4; ++cc) {
+            if (c0 + 32 * cc < p.out_cols) {
               uint4* d = reinterpret_cast<uint4*>(dst + 32 * cc);
 #pragma unroll
               for (int v = 0; v < 4; ++v)

@@ -486,11 +486,13 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
 namespace moe {
 
 // dX then dW.  When dX is small (at most about four waves of 256 x 256 tiles
-// on the whole GPU, counting one partial row tile per group), the two run side
-// by side: dX on half the SMs, and dW, launched right behind it with
-// programmatic serialisation, starts at once on the other half (it reads only
-// inputs that exist before dX starts) and finishes no earlier than dX.  That
-// hides the last partial wave and the prologue and epilogue of one launch.
+// on the whole GPU, counting one partial row tile per group) and its groups
+// are large enough for CTA pairs, one launch does both (launch_gmm_pair_bwd).
+// Other small problems run them side by side: dX on half the SMs, and dW,
+// launched right behind it with programmatic serialisation, starts at once on
+// the other half (it reads only inputs that exist before dX starts) and
+// finishes no earlier than dX.  That hides the last partial wave and the
+// prologue and epilogue of one launch.
 moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
                                  int64_t M, int64_t K, int64_t N, int64_t E, int dx_epilogue, const Act& act,
                                  const uint16_t* h, uint16_t* dx, uint16_t* dw, uint32_t* status, void* gmm_scratch,
@@ -498,7 +500,12 @@ moe_status_t launch_gmm_backward(const uint16_t* x, const uint16_t* w, const int
   GmmLaunch first, second;
   first.w_transposed = w_transposed;
   const int half = (num_sms() / 2) & ~1;
-  if (dx && dw && half >= 2 && (M / 256 + E) * ((K + 255) / 256) <= 4 * static_cast<int64_t>(half)) {
+  const bool small = dx && dw && half >= 2 && (M / 256 + E) * ((K + 255) / 256) <= 4 * static_cast<int64_t>(half);
+  // Small problems on CTA pairs: one launch whose clusters each take dX or dW
+  // tiles, balanced on the device from the group sizes.
+  if (small && dx_epilogue == EPI_PLAIN && M >= kPairMinRowsPerGroup * E)
+    return launch_gmm_pair_bwd(x, w, group_list, dy, M, K, N, E, dx, dw, status, gmm_scratch, s, w_transposed);
+  if (small) {
     first.max_ctas = half;
     second.max_ctas = num_sms() - half;
     second.concurrent = true;

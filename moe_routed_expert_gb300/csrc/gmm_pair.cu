@@ -72,6 +72,10 @@ constexpr int64_t kByGroupMaxBytes = 64ll << 20;
 constexpr int kByGroupMaxGroups = 32;
 // A dW tile's epilogue takes about as long as this many 64-deep MMA blocks.
 constexpr uint32_t kEpilogueBlocks = 8;
+// dX and dW in one launch: relative cost of a 64-deep block of each (measured
+// on GB300: about 0.31 us for dX's K-major operands, 0.36 us for dW's MN-major ones).
+constexpr uint32_t kBlockCostDx = 7;
+constexpr uint32_t kBlockCostDw = 8;
 
 struct PairParams {
   const int64_t* group_list;
@@ -118,6 +122,8 @@ struct __align__(128) PairSmem {
   int32_t tile_start[kMaxExperts + 1]; // tile prefix over visiting positions (dW: groups with rows only)
   int32_t run_start[kMaxExperts + 1];  // dW by group: prefix over visiting positions of the cluster runs
   int32_t empty_ids[kMaxExperts];      // dW: the groups without rows
+  int32_t xtile_start[kMaxExperts + 1];  // dX and dW together: dX tile prefix over the groups
+  int32_t ncl_x;                       // dX and dW together, split schedule: clusters given to dX
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + sizeof(PairSmem);
@@ -139,17 +145,18 @@ __device__ __forceinline__ uint32_t tile_cost(int cnt) {
   return kb > kEpilogueBlocks ? kb : kEpilogueBlocks;
 }
 
-// Tile `local` of group g (row tile major, column tile fastest).
-template <int MODE, int EPI>
-__device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int g, int local,
-                                                     uint32_t rank) {
+// Tile `local` of group g (row tile major, column tile fastest) of a tile of
+// mode `mode` (FWD, DX or DW), p holding that mode's sizes.
+template <int EPI>
+__device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const PairParams& p, int mode, int g,
+                                                     int local, uint32_t rank) {
   const int rt = local / p.tile_cols;
   const int ct = local - rt * p.tile_cols;
   PairTile ti;
   ti.g = g;
   const int first = rt * (2 * BM) + static_cast<int>(rank) * BM;
   ti.col0 = ct * (EPI == EPI_SWIGLU ? BN / 2 : BN);
-  if (MODE == GMM_DW) {
+  if (mode == GMM_DW) {
     ti.row0 = first;
     ti.rows_valid = min(BM, p.out_rows - first);
     ti.m0 = sm->grp_off[g];
@@ -165,19 +172,28 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairSmem* sm, const P
   return ti;
 }
 
-// The tiles of one cluster, in the order every role of the kernel visits them.
+// Which tiles a cluster takes (the same for every role of both CTAs): a
+// strided walk over the tile prefix T of nT groups (start, start + stride,
+// ...), or its run of the by-group schedule (prefix T over nT groups, cluster
+// runs C).  TileRef.g is the index into T.
+struct Walk {
+  const int32_t* T;
+  const int32_t* C;
+  int nT, start, stride;
+  bool by_group, none;
+};
+
 struct ClusterTiles {
-  const PairSmem* sm;
-  int E, ncl;
+  Walk k;
   TileWalk w;
-  __device__ __forceinline__ ClusterTiles(const PairSmem* sm_, int E_, int ncl_, int cid, bool none)
-      : sm(sm_), E(E_), ncl(ncl_) {
-    if (sm->by_group) walk_group_init(w, cid, sm->run_start, E);
-    else walk_strided_init(w, cid);
-    if (none) w.t = INT64_MAX, w.g = -1;
+  __device__ __forceinline__ explicit ClusterTiles(const Walk& k_) : k(k_) {
+    if (k.by_group) walk_group_init(w, k.start, k.C, k.nT);
+    else walk_strided_init(w, k.start);
+    if (k.none) w.t = INT64_MAX, w.g = -1;
   }
   __device__ __forceinline__ bool next(TileRef& r) {
-    return sm->by_group ? walk_group_next(w, sm->tile_start, r) : walk_strided_next(w, sm->tile_start, E, ncl, r);
+    if (k.none) return false;
+    return k.by_group ? walk_group_next(w, k.T, r) : walk_strided_next(w, k.T, k.nT, k.stride, r);
   }
 };
 
@@ -252,15 +268,22 @@ __device__ __forceinline__ void flush_rows(const uint8_t* ebuf, int lane, uint16
   }
 }
 
+// MODE GMM_BWD runs the dX (tmA, tmB, tmC, p) and dW (tmA2, tmB2, tmC2, pw)
+// contractions of one grouped matmul in one launch: each cluster takes tiles
+// of one of the two (see the schedule below).  The other modes use the first
+// set only.
 template <int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const PairParams p) {
-  constexpr bool A_MN = (MODE == GMM_DW);
-  // B is MN-major (output columns contiguous) for dW (dy rows), for the forward
-  // over [K, N] weights and for dX over transposed [N, K] weights.
-  const bool B_MN = (MODE == GMM_DW) || ((MODE == GMM_FWD) != (p.wt != 0));
-  const uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC2,
+                const PairParams p, const PairParams pw) {
+  static_assert(MODE != GMM_BWD || EPI == EPI_PLAIN, "dX and dW together: plain epilogues only");
+  constexpr bool DW_SCHED = (MODE == GMM_DW) || (MODE == GMM_BWD);   // groups visited largest first
+  // the dW operands and parameters
+  const PairParams& pd = (MODE == GMM_BWD) ? pw : p;
+  const CUtensorMap* dwA = (MODE == GMM_BWD) ? &tmA2 : &tmA;
+  const CUtensorMap* dwB = (MODE == GMM_BWD) ? &tmB2 : &tmB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -293,6 +316,11 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (EPI == EPI_PLAIN) tma_prefetch_desc(&tmC);
+    if (MODE == GMM_BWD) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+      tma_prefetch_desc(&tmC2);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
@@ -312,7 +340,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
   }
   __syncthreads();
-  if (MODE == GMM_DW) {
+  if (DW_SCHED) {
     // largest group first (ties: lower id first)
     for (int e = tid; e < E; e += NUM_THREADS) {
       const int ce = sm->grp_cnt[e];
@@ -329,15 +357,16 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   __syncthreads();
   // Prefix over the groups of rows, over visiting positions of tiles (dW:
   // groups with rows only), and the list of the groups without rows.
-  const int dw_tiles = ((p.out_rows + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+  const int dw_tiles = ((pd.out_rows + 2 * BM - 1) / (2 * BM)) * pd.tile_cols;
   auto tiles_of = [&](int c) -> int {
-    return (MODE == GMM_DW) ? (c > 0 ? dw_tiles : 0) : ((c + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
+    return DW_SCHED ? (c > 0 ? dw_tiles : 0) : ((c + 2 * BM - 1) / (2 * BM)) * p.tile_cols;
   };
+  auto xtiles_of = [&](int c) -> int { return ((c + 2 * BM - 1) / (2 * BM)) * p.tile_cols; };
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int64_t rows = 0, units = 0;
-    int32_t tiles = 0, empties = 0;
+    int32_t tiles = 0, empties = 0, xtiles = 0;
     for (int e = lo; e < hi; ++e) {
       const int c = sm->grp_cnt[e];
       const int kb = (c + BK - 1) / BK;
@@ -345,19 +374,21 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tiles += tiles_of(sm->grp_cnt[sm->order[e]]);
       units += static_cast<int64_t>(tiles_of(c)) * kb;
       empties += (c == 0);
+      if (MODE == GMM_BWD) xtiles += xtiles_of(c);
     }
     int64_t rows_incl = rows, units_incl = units;
-    int32_t tiles_incl = tiles, empties_incl = empties;
+    int32_t tiles_incl = tiles, empties_incl = empties, xtiles_incl = xtiles;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int64_t r2 = __shfl_up_sync(0xffffffffu, rows_incl, d);
       const int64_t u2 = __shfl_up_sync(0xffffffffu, units_incl, d);
       const int32_t t2 = __shfl_up_sync(0xffffffffu, tiles_incl, d);
       const int32_t e2 = __shfl_up_sync(0xffffffffu, empties_incl, d);
-      if (lane >= d) { rows_incl += r2; units_incl += u2; tiles_incl += t2; empties_incl += e2; }
+      const int32_t x2 = __shfl_up_sync(0xffffffffu, xtiles_incl, d);
+      if (lane >= d) { rows_incl += r2; units_incl += u2; tiles_incl += t2; empties_incl += e2; xtiles_incl += x2; }
     }
     int64_t rb = rows_incl - rows;
-    int32_t tb = tiles_incl - tiles, eb = empties_incl - empties;
+    int32_t tb = tiles_incl - tiles, eb = empties_incl - empties, xb = xtiles_incl - xtiles;
     for (int e = lo; e < hi; ++e) {
       const int c = sm->grp_cnt[e];
       sm->grp_off[e] = rb;
@@ -365,10 +396,15 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       rb += c;
       tb += tiles_of(sm->grp_cnt[sm->order[e]]);
       if (c == 0) sm->empty_ids[eb++] = e;
+      if (MODE == GMM_BWD) {
+        sm->xtile_start[e] = xb;
+        xb += xtiles_of(c);
+      }
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
       sm->tile_start[E] = tiles_incl;
+      if (MODE == GMM_BWD) sm->xtile_start[E] = xtiles_incl;
       sm->n_empty = empties_incl;
       sm->n_live = E - empties_incl;
       sm->units = units_incl;
@@ -377,28 +413,40 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   }
   __syncthreads();
-  if (MODE == GMM_DW) {
+  if (DW_SCHED) {
     // Few groups whose operands fit in L2: warp 0 searches the smallest
     // per-cluster load L for which every group j gets a run of
-    // ceil(tiles / floor(L / cost_j)) clusters within the grid, cost_j the
+    // ceil(tiles_j / floor(L / cost_j)) clusters within the grid, cost_j the
     // tile's blocks of 64 but at least kEpilogueBlocks (a tile's epilogue
     // takes about that long, and it bounds short tiles).  Two rounds of 32
     // candidates (one per lane), the first over [lb, 2 lb), lb the larger of
     // the costliest tile and the average load.  Taken when L is within 15% of
     // the average.
+    // With dX and dW together, all of dX's tiles (N/64 blocks each) are one
+    // more "group" after dW's, and the costs weigh a block of each by its speed.
     const int nl = sm->n_live;
-    const int64_t bytes = sm->grp_off[E] * (static_cast<int64_t>(p.out_rows) + p.out_cols) * 2;
-    if (warp == 0 && !sm->bad && nl >= 1 && nl <= kByGroupMaxGroups && nl <= ncl && bytes <= kByGroupMaxBytes &&
-        sm->units < (1ll << 18) && dw_tiles < (1 << 12)) {
-      // Lane j holds the tile cost of visiting position j; with dW visiting
-      // the groups largest first, positions [0, nl) are the groups with rows.
-      const uint32_t my_cost = lane < nl ? tile_cost(sm->grp_cnt[sm->order[lane]]) : 0;
+    const int32_t xt = (MODE == GMM_BWD) ? sm->xtile_start[E] : 0;
+    const int npos = nl + (xt > 0 ? 1 : 0);
+    const int64_t units_x = static_cast<int64_t>(xt) * p.kblocks;
+    const int64_t bytes = sm->grp_off[E] * (static_cast<int64_t>(pd.out_rows) + pd.out_cols) * 2;
+    if (warp == 0 && !sm->bad && npos >= 1 && npos <= kByGroupMaxGroups && npos <= ncl &&
+        bytes <= kByGroupMaxBytes && sm->units + units_x < (1ll << 18) && dw_tiles < (1 << 12) && xt < (1 << 12)) {
+      // Lane j holds the tile count and cost of visiting position j; with the
+      // groups visited largest first, positions [0, nl) are the groups with
+      // rows, and position nl is dX's tiles.
+      const uint32_t my_tiles = lane < nl ? static_cast<uint32_t>(dw_tiles)
+                                          : (lane == nl && xt > 0 ? static_cast<uint32_t>(xt) : 0u);
+      const uint32_t wdw = (MODE == GMM_BWD) ? kBlockCostDw : 1u;
+      const uint32_t my_cost = lane < nl ? wdw * tile_cost(sm->grp_cnt[sm->order[lane]])
+                                         : (lane == nl && xt > 0 ? kBlockCostDx * max(static_cast<uint32_t>(p.kblocks),
+                                                                                      kEpilogueBlocks) : 0u);
       const uint32_t cost_max = __reduce_max_sync(0xffffffffu, my_cost);
-      const uint32_t cost_sum = __reduce_add_sync(0xffffffffu, my_cost) * static_cast<uint32_t>(dw_tiles);
+      const uint32_t cost_sum = __reduce_add_sync(0xffffffffu, my_cost * my_tiles);
       auto need = [&](uint32_t L) -> uint32_t {  // clusters for load L (every lane takes part)
         uint32_t n = 0;
 #pragma unroll 1
-        for (int i = 0; i < nl; ++i) n += group_clusters(dw_tiles, __shfl_sync(0xffffffffu, my_cost, i), L, ncl);
+        for (int i = 0; i < npos; ++i)
+          n += group_clusters(__shfl_sync(0xffffffffu, my_tiles, i), __shfl_sync(0xffffffffu, my_cost, i), L, ncl);
         return n;
       };
       uint32_t best = 0;
@@ -417,7 +465,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
       }
       if (best != 0 && static_cast<uint64_t>(best) * ncl * 100 <= static_cast<uint64_t>(cost_sum) * 115) {
-        const int32_t runs = lane < nl ? static_cast<int32_t>(group_clusters(dw_tiles, my_cost, best, ncl)) : 0;
+        const int32_t runs = lane < npos ? static_cast<int32_t>(group_clusters(my_tiles, my_cost, best, ncl)) : 0;
         int32_t incl = runs;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -425,32 +473,81 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (lane >= d) incl += r2;
         }
         const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
-        if (lane < nl) sm->run_start[lane] = incl - runs;
-        for (int j = nl + lane; j <= E; j += 32) sm->run_start[j] = total;
+        if (lane < npos) sm->run_start[lane] = incl - runs;
+        for (int j = npos + lane; j <= E; j += 32) sm->run_start[j] = total;
         if (lane == 0) sm->by_group = 1;
       }
+    }
+    if (MODE == GMM_BWD && tid == 0) {
+      // without the by-group schedule: the clusters split between dX and dW in
+      // proportion to their blocks of 64
+      const int64_t uw = sm->units;
+      int nx;
+      if (units_x == 0) nx = 0;
+      else if (uw == 0) nx = ncl;
+      else {
+        nx = static_cast<int>((static_cast<double>(units_x) * ncl) / static_cast<double>(units_x + uw) + 0.5);
+        nx = nx < 1 ? 1 : (nx > ncl - 1 ? ncl - 1 : nx);
+      }
+      sm->ncl_x = nx;
     }
     __syncthreads();
   }
   if (sm->bad && tid == 0 && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
   const bool no_work = sm->bad != 0;  // both CTAs of the pair read the same group_list: no tiles for either
 
+  // This cluster's tiles and their mode (both CTAs of the pair agree: they
+  // read the same group_list and make the same choices).
+  int mode = (MODE == GMM_BWD) ? GMM_DX : MODE;
+  Walk wk;
+  if (MODE == GMM_BWD) {
+    const int nl = sm->n_live;
+    if (sm->by_group) {
+      const int xr0 = sm->run_start[nl], xr1 = sm->run_start[nl + 1];
+      if (cid < xr0) {
+        mode = GMM_DW;
+        wk = Walk{sm->tile_start, sm->run_start, nl, cid, 0, true, no_work};
+      } else {
+        wk = Walk{sm->xtile_start, nullptr, E, cid - xr0, max(xr1 - xr0, 1), false, no_work || cid >= xr1};
+      }
+    } else {
+      const int nx = sm->ncl_x;
+      if (cid < nx) {
+        wk = Walk{sm->xtile_start, nullptr, E, cid, nx, false, no_work};
+      } else {
+        mode = GMM_DW;
+        wk = Walk{sm->tile_start, nullptr, E, cid - nx, ncl - nx, false, no_work};
+      }
+    }
+  } else {
+    wk = Walk{sm->tile_start, sm->run_start, E, cid, ncl, sm->by_group != 0, no_work};
+  }
+  const PairParams& q = (mode == GMM_DW) ? pd : p;
+  const bool A_MN = (mode == GMM_DW);
+  // B is MN-major (output columns contiguous) for dW (dy rows), for the forward
+  // over [K, N] weights and for dX over transposed [N, K] weights.
+  const bool B_MN = (mode == GMM_DW) || ((mode == GMM_FWD) != (p.wt != 0));
+  const uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+  const CUtensorMap* mC = (MODE == GMM_BWD && mode == GMM_DW) ? &tmC2 : &tmC;
+  // tile reference -> group: dW walks visit positions (largest group first), the others groups
+  auto group_of = [&](const TileRef& r) -> int { return mode == GMM_DW ? sm->order[r.g] : r.g; };
+
   const uint32_t tmem_base = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (warp == 0 && MODE == GMM_DW) {
+  if (warp == 0 && mode == GMM_DW) {
     // ---------------------------------------------------------------- dW TMA producer (both CTAs)
     // The whole warp walks the tiles (it rewrites descriptors together); lane 0 copies.
-    uint8_t* slots = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlots * 256;
+    uint8_t* slots = pd.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlots * 256;
     const uint32_t edit_a = smem_u32(sm->map_edit[0]), edit_b = smem_u32(sm->map_edit[1]);
     uint32_t it = 0;
     int ok = 1, cur_g = -1, slot = -1;
     const void* map_a = nullptr;
     const void* map_b = nullptr;
-    ClusterTiles tiles(sm, E, ncl, cid, no_work);
+    ClusterTiles tiles(wk);
     TileRef tr;
     while (ok && tiles.next(tr)) {
-      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
+      const PairTile ti = decode_pair_tile<EPI>(sm, pd, GMM_DW, group_of(tr), tr.local, rank);
       if (ti.g != cur_g) {
         // a new group: descriptors whose row 0 is the group's first row and
         // whose row extent is the group's row count
@@ -459,14 +556,14 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint8_t* ga = slots + slot * 256;
         uint8_t* gb = ga + 128;
         if (lane < 8) {
-          reinterpret_cast<uint4*>(sm->map_edit[0])[lane] = reinterpret_cast<const uint4*>(&tmA)[lane];
-          reinterpret_cast<uint4*>(sm->map_edit[1])[lane] = reinterpret_cast<const uint4*>(&tmB)[lane];
+          reinterpret_cast<uint4*>(sm->map_edit[0])[lane] = reinterpret_cast<const uint4*>(dwA)[lane];
+          reinterpret_cast<uint4*>(sm->map_edit[1])[lane] = reinterpret_cast<const uint4*>(dwB)[lane];
         }
         __syncwarp();
         if (lane == 0) {
-          tmap_set_address(edit_a, reinterpret_cast<uint64_t>(p.a_base + ti.m0 * p.a_pitch));
+          tmap_set_address(edit_a, reinterpret_cast<uint64_t>(pd.a_base + ti.m0 * pd.a_pitch));
           tmap_set_rows(edit_a, static_cast<uint32_t>(ti.depth));
-          tmap_set_address(edit_b, reinterpret_cast<uint64_t>(p.b_base + ti.m0 * p.b_pitch));
+          tmap_set_address(edit_b, reinterpret_cast<uint64_t>(pd.b_base + ti.m0 * pd.b_pitch));
           tmap_set_rows(edit_b, static_cast<uint32_t>(ti.depth));
         }
         __syncwarp();
@@ -510,10 +607,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      ClusterTiles tiles(sm, E, ncl, cid, no_work);
+      ClusterTiles tiles(wk);
       TileRef tr;
       while (ok && tiles.next(tr)) {
-        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
+        const PairTile ti = decode_pair_tile<EPI>(sm, p, mode, group_of(tr), tr.local, rank);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
@@ -550,10 +647,10 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (rank == 0 && lane == 0) {
       uint32_t it = 0, local = 0;
       bool ok = true;
-      ClusterTiles tiles(sm, E, ncl, cid, no_work);
+      ClusterTiles tiles(wk);
       TileRef tr;
       while (ok && tiles.next(tr)) {
-        const int kblocks = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, 0).kblocks;
+        const int kblocks = decode_pair_tile<EPI>(sm, q, mode, group_of(tr), tr.local, 0).kblocks;
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm->tmem_empty[acc]), aph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
         tc_fence_after();
@@ -585,34 +682,34 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   } else if (warp <= 5) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp & 3;
-    uint8_t* ebuf = ebuf_all + q * EPI_WARP_BYTES;
-    if (MODE == GMM_DW && !no_work) {
+    const int qw = warp & 3;   // TMEM lane quarter of this warp
+    uint8_t* ebuf = ebuf_all + qw * EPI_WARP_BYTES;
+    if (DW_SCHED && !no_work) {
       // an empty group's weight gradient is zero: one 512-byte row per instruction
       const int nz = sm->n_empty * dw_tiles;
       for (int z = cid; z < nz; z += ncl) {
-        const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->empty_ids[z / dw_tiles], z % dw_tiles, rank);
-        uint16_t* obase = p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out;
-        const int rows_valid = ti.rows_valid - q * 32;
-        const int ncols = min(BN, p.out_cols - ti.col0);
+        const PairTile ti = decode_pair_tile<EPI>(sm, pd, GMM_DW, sm->empty_ids[z / dw_tiles], z % dw_tiles, rank);
+        uint16_t* obase = pd.out + static_cast<int64_t>(ti.g) * pd.out_rows * pd.ld_out;
+        const int rows_valid = ti.rows_valid - qw * 32;
+        const int ncols = min(BN, pd.out_cols - ti.col0);
         for (int r = 0; r < 32 && r < rows_valid; ++r)
           if (lane * 8 < ncols)
-            *reinterpret_cast<uint4*>(obase + (ti.row0 + q * 32 + r) * p.ld_out + ti.col0 + lane * 8) =
+            *reinterpret_cast<uint4*>(obase + (ti.row0 + qw * 32 + r) * pd.ld_out + ti.col0 + lane * 8) =
                 make_uint4(0, 0, 0, 0);
       }
     }
     uint32_t local = 0;
-    ClusterTiles tiles(sm, E, ncl, cid, no_work);
+    ClusterTiles tiles(wk);
     TileRef tr;
     while (tiles.next(tr)) {
-      const PairTile ti = decode_pair_tile<MODE, EPI>(sm, p, sm->order[tr.g], tr.local, rank);
-      uint16_t* obase = (MODE == GMM_DW) ? p.out + static_cast<int64_t>(ti.g) * p.out_rows * p.ld_out : p.out;
+      const PairTile ti = decode_pair_tile<EPI>(sm, q, mode, group_of(tr), tr.local, rank);
+      uint16_t* obase = (mode == GMM_DW) ? q.out + static_cast<int64_t>(ti.g) * q.out_rows * q.ld_out : q.out;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int rows_valid = ti.rows_valid - q * 32;  // rows of this warp's 32 that are in the group
-      const int64_t wrow0 = ti.row0 + q * 32;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;
+      const int rows_valid = ti.rows_valid - qw * 32;  // rows of this warp's 32 that are in the group
+      const int64_t wrow0 = ti.row0 + qw * 32;
       const uint32_t release = mapa_shared(smem_u32(&sm->tmem_empty[acc]), 0);
       auto release_tmem = [&]() {
         tc_fence_before();
@@ -735,7 +832,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // loaded from TMEM two 32-column chunks per wait; all of half 1 is
         // loaded (and the accumulator released) before waiting for the
         // staging buffer to be read by half 0's stores.
-        const int64_t grow0 = (MODE == GMM_DW) ? static_cast<int64_t>(ti.g) * p.out_rows + wrow0 : wrow0;
+        const int64_t grow0 = (mode == GMM_DW) ? static_cast<int64_t>(ti.g) * q.out_rows + wrow0 : wrow0;
         auto store_half = [&](int half) {
           const int col = ti.col0 + half * (BN / 2);
           if (rows_valid >= 32) {
@@ -743,13 +840,13 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             __syncwarp();
             if (lane == 0) {
               for (int b = 0; b < 2; ++b)
-                if (col + 64 * b < p.out_cols)
-                  tma_store_2d(&tmC, smem_u32(ebuf + b * BOX_STAGE), col + 64 * b, static_cast<int32_t>(grow0));
+                if (col + 64 * b < q.out_cols)
+                  tma_store_2d(mC, smem_u32(ebuf + b * BOX_STAGE), col + 64 * b, static_cast<int32_t>(grow0));
               bulk_commit();
             }
           } else if (rows_valid > 0) {
             __syncwarp();
-            flush_rows_box(ebuf, lane, obase + wrow0 * p.ld_out + col, p.ld_out, rows_valid, p.out_cols - col);
+            flush_rows_box(ebuf, lane, obase + wrow0 * q.ld_out + col, q.ld_out, rows_valid, q.out_cols - col);
           }
           __syncwarp();
         };
@@ -804,7 +901,8 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
 template <int MODE, int EPI>
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const PairParams& p,
-                         cudaStream_t s, int max_ctas) {
+                         cudaStream_t s, int max_ctas, const CUtensorMap* ta2 = nullptr, const CUtensorMap* tb2 = nullptr,
+                         const CUtensorMap* tc2 = nullptr, const PairParams* pw = nullptr) {
   auto kern = gmm_pair_kernel<MODE, EPI>;
   static int configured_dev = -1;
   static int grid = 0;
@@ -833,9 +931,27 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
     configured_dev = dev;
   }
   const int g = (max_ctas >= 2 && max_ctas < grid) ? (max_ctas & ~1) : grid;
-  if (launch_pdl(kern, dim3(g), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, tc, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(g), dim3(NUM_THREADS), kSmemBytes, s, 2, ta, tb, tc, ta2 ? *ta2 : ta, tb2 ? *tb2 : tb,
+                 tc2 ? *tc2 : tc, p, pw ? *pw : p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+// dW parameters and maps: a [M, Ka] and b [M, Nb] contracted over each group's
+// rows into out [E, Ka, Nb].
+bool setup_dw(PairParams& p, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tc, const uint16_t* a, const uint16_t* b,
+              int64_t M, int64_t Ka, int64_t Nb, int64_t E, uint16_t* out, void* gmm_scratch) {
+  p.a_base = reinterpret_cast<const uint8_t*>(a);
+  p.b_base = reinterpret_cast<const uint8_t*>(b);
+  p.a_pitch = Ka * 2;
+  p.b_pitch = Nb * 2;
+  p.map_slots = static_cast<uint8_t*>(gmm_scratch);
+  p.out = out;
+  p.out_rows = static_cast<int>(Ka);
+  p.out_cols = static_cast<int>(Nb);
+  p.ld_out = Nb;
+  p.tile_cols = static_cast<int>((Nb + BN - 1) / BN);
+  return make_map_2d(&ta, a, M, Ka, 64) && make_map_2d(&tb, b, M, Nb, 64) && make_map_2d(&tc, out, E * Ka, Nb, 32);
 }
 
 }  // namespace
@@ -886,18 +1002,38 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
   }
   // DW: a = x [M, K], b = dy [M, N]; output dw [E, K, N]
   if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
-  p.a_base = reinterpret_cast<const uint8_t*>(a);
-  p.b_base = reinterpret_cast<const uint8_t*>(b);
-  p.a_pitch = K * 2;
-  p.b_pitch = N * 2;
-  p.map_slots = static_cast<uint8_t*>(gmm_scratch);
-  p.out_rows = static_cast<int>(K);
-  p.out_cols = static_cast<int>(N);
-  p.ld_out = N;
-  p.tile_cols = static_cast<int>((N + BN - 1) / BN);
-  if (!make_map_2d(&ta, a, M, K, 64) || !make_map_2d(&tb, b, M, N, 64) || !make_map_2d(&tc, out, E * K, N, 32))
-    return MOE_ERR_CUDA;
+  if (!setup_dw(p, ta, tb, tc, a, b, M, K, N, E, out, gmm_scratch)) return MOE_ERR_CUDA;
   return launch_pair<GMM_DW, EPI_PLAIN>(ta, tb, tc, p, s, how.max_ctas);
+}
+
+// dX and dW of one grouped matmul in one launch (plain dX epilogue).
+//   dX: dy [M, N] x w -> dx [M, K] (w [E, K, N], or [E, N, K] when transposed);
+//   dW: x [M, K], dy [M, N] -> dw [E, K, N] (transposed: dy, x -> dw [E, N, K]).
+moe_status_t launch_gmm_pair_bwd(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, uint16_t* dx, uint16_t* dw,
+                                 uint32_t* status, void* gmm_scratch, cudaStream_t s, bool w_transposed) {
+  if (gmm_scratch == nullptr) return MOE_ERR_INVALID;
+  PairParams p{}, pw{};
+  p.wt = w_transposed ? 1 : 0;
+  p.group_list = pw.group_list = group_list;
+  p.E = pw.E = static_cast<int>(E);
+  p.rows_cap = pw.rows_cap = M;
+  p.status = pw.status = status;
+  p.out = dx;
+  p.out_cols = static_cast<int>(K);
+  p.ld_out = K;
+  p.act_cols = static_cast<int>(K);
+  p.tile_cols = static_cast<int>((K + BN - 1) / BN);
+  p.kblocks = static_cast<int>(N / BK);
+  CUtensorMap ta, tb, tc, ta2, tb2, tc2;
+  if (!make_map_2d(&ta, dy, M, N, BM) ||
+      !(w_transposed ? make_map_3d(&tb, w, E, N, K, 64) : make_map_3d(&tb, w, E, K, N, BNH)) ||
+      !make_map_2d(&tc, dx, M, K, 32))
+    return MOE_ERR_CUDA;
+  const bool ok = w_transposed ? setup_dw(pw, ta2, tb2, tc2, dy, x, M, N, K, E, dw, gmm_scratch)
+                               : setup_dw(pw, ta2, tb2, tc2, x, dy, M, K, N, E, dw, gmm_scratch);
+  if (!ok) return MOE_ERR_CUDA;
+  return launch_pair<GMM_BWD, EPI_PLAIN>(ta, tb, tc, p, s, 0, &ta2, &tb2, &tc2, &pw);
 }
 
 }  // namespace moe

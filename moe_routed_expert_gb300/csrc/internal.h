@@ -75,7 +75,7 @@ bool make_map_2d_u8(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t
 bool make_map_3d_u8(::CUtensorMap_st* m, const void* base, int64_t E, int64_t R, int64_t C, int box_rows);
 
 // ---- grouped matmul (gmm.cu, gmm_pair.cu)
-enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2 };
+enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2, GMM_BWD = 3 /* dX and dW in one launch (pairs) */ };
 // Epilogues: 0 plain store; 1 (forward) SwiGLU of the [gate | up] product, H
 // saved to h; 2 (dX) SwiGLU gradient: out = dH from dA = this product and the
 // saved pre-activation passed in h.
@@ -97,6 +97,12 @@ moe_status_t launch_gmm_pair(int mode, int epilogue, const uint16_t* a, const ui
                              int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                              uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                              const GmmLaunch& how = GmmLaunch());
+// dX (plain) and dW of one grouped matmul in one CTA-pair launch: each cluster
+// takes tiles of one of the two, the split chosen on the device from the
+// group sizes.  x [M, K], w [E, K, N] (or [E, N, K] transposed), dy [M, N].
+moe_status_t launch_gmm_pair_bwd(const uint16_t* x, const uint16_t* w, const int64_t* group_list, const uint16_t* dy,
+                                 int64_t M, int64_t K, int64_t N, int64_t E, uint16_t* dx, uint16_t* dw,
+                                 uint32_t* status, void* gmm_scratch, cudaStream_t s, bool w_transposed);
 // gmm_scratch: kGmmScratchBytes of workspace (used by dW).  h: SwiGLU forward
 // output of H, or the saved H read by the SwiGLU-gradient epilogue.
 moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_t* b, const int64_t* group_list,

@@ -76,12 +76,17 @@ def test_forward_and_dx_pair_path(counts, K, N):
 
 
 # Weight gradients whose groups have unequal depths, small enough for the
-# CTA-pair kernel to give each group its own run of clusters, and a single
-# group of deep tiles; one workspace serves every call, a permute included.
+# CTA-pair kernel to give each group its own run of clusters (with dX's tiles
+# as one more run when dX and dW share a launch), and a single group of deep
+# tiles; one workspace serves every call, a permute included.
 BALANCE_CASES = [
     ([512], 4096, 256),
     ([3803, 2000, 1000, 0], 1024, 2048),
     ([551, 443, 1656, 1018, 721, 0, 0, 3803], 1024, 2048),
+    # dX and dW in one launch without the by-group schedule: more than 31 groups
+    # with rows, and operands past the L2 budget; the clusters split between the two
+    ([0, 0] + [520 + 7 * i for i in range(38)], 256, 256),
+    ([30000, 20000, 15000, 5000], 256, 256),
 ]
 
 

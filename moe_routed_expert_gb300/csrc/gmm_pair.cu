@@ -486,7 +486,7 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (units_x == 0) nx = 0;
       else if (uw == 0) nx = ncl;
       else {
-        nx = static_cast<int>((static_cast<double>(units_x) * ncl) / static_cast<double>(units_x + uw) + 0.5);
+        nx = static_cast<int>((units_x * ncl + (units_x + uw) / 2) / (units_x + uw));  // rounded; no FP64
         nx = nx < 1 ? 1 : (nx > ncl - 1 ? ncl - 1 : nx);
       }
       sm->ncl_x = nx;

@@ -43,11 +43,11 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # (profiles/gmm_traffic_layer_train_t16384.md); reported only while they match.
 GMM_TRAFFIC = {
     "workload": "layer_train_t16384",
-    "bytes_per_launch": 2.701e9,
+    "bytes_per_launch": 2.662e9,
     "sources": {
-        "gmm.cu": "8f092e0c820c31ae2a56b27adbf7b485b2e1a0a8e4d6144f6f6405ab023d9d3d",
-        "gmm_pair.cu": "e61019121dca19823bf8cf149c8d79f2c6104c43e39d2e48d9600a0f1744fc46",
-        "common.cuh": "5875786d34cd16a168ad7ac538a7c0270e46c1f3c2714e657ae6e42705aeeada",
+        "gmm.cu": "117c05934dbd56a5bd1f49ae969a92b8cb8c935318e38a6d472f6606b410e6b1",
+        "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
+        "common.cuh": "fbc79d491f1538425ee1b3279a36f2a75d6c88e0db0afb369ee31a45eddc731f",
         "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365",
     },
 }

@@ -130,6 +130,12 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
 
 
+def permute_launches(nslots):
+    """Kernels one permute launches: a one-block index kernel and the gather up to
+    1024 routed slots, else count, scan, rank and the gather."""
+    return 2 if nslots <= 1024 else 4
+
+
 def bf16_dev(bits, dev):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -168,7 +174,7 @@ class LayerTrainStep:
         Rr = int(counts.sum())
         f_up, f_dn = 2.0 * Rr * H * 2 * I, 2.0 * Rr * I * H
         self.stages = [
-            ("permute", self.permute, 0.0, 4),
+            ("permute", self.permute, 0.0, permute_launches(T * k)),
             ("gmm_fwd_gate_up_swiglu", self.gmm1, f_up, 1),
             ("gmm_fwd_down", self.gmm2, f_dn, 1),
             ("combine", self.combine, 0.0, 1),
@@ -245,7 +251,6 @@ class LayerTrainStep:
         M.moe_layer_backward(i["dy"], i["topk_w"], self.w1, self.w2, self.saved, wl.clip, dx=o["dx"], dw1=self.dw1,
                              dw2=self.dw2, dprobs=o["dprobs"], ws=self.ws)
 
-    e2e_launches = 4 + 2 + 1 + 1 + 4 + 1
     e2e_api = "moe_layer_forward/moe_layer_backward"
 
 
@@ -277,7 +282,6 @@ class LayerFwdStep(LayerTrainStep):
         self.M.moe_layer_forward(i["x"], i["topk_ids"], i["topk_w"], self.w1, self.w2, self.wl.clip, y=o["y"],
                                  ws=self.ws)
 
-    e2e_launches = 4 + 2 + 1
     e2e_api = "moe_layer_forward"
 
 
@@ -316,7 +320,7 @@ class LayerMxStep:
         Rr = int(counts.sum())
         f_up, f_dn = 2.0 * Rr * H * 2 * I, 2.0 * Rr * I * H
         self.stages = [
-            ("permute_mx", self.permute, 0.0, 4),
+            ("permute_mx", self.permute, 0.0, permute_launches(R)),
             ("gmm_mx_gate_up_act_quant", self.gmm1, f_up, 1),
             ("gmm_mx_down", self.gmm2, f_dn, 1),
             ("combine", self.combine, 0.0, 1),
@@ -356,7 +360,6 @@ class LayerMxStep:
         self.M.moe_layer_forward_mx(i["x"], i["topk_ids"], i["topk_w"], self.w1q, self.w1s, self.w2q, self.w2s,
                                     x_fmt=self.wl.mx, w_fmt=self.wl.mx, activation=self.act, y=o["y"], ws=self.ws)
 
-    e2e_launches = 4 + 2 + 1
     e2e_api = "moe_layer_forward_mx"
 
 
@@ -400,7 +403,6 @@ class GmmStep:
         self.M.gmm_forward(i["x"], self.w, self.gl, y=o["y"], ws=self.ws)
         self.M.gmm_backward(i["x"], self.w, self.gl, i["dy"], dx=o["dx"], dw=self.dw, ws=self.ws)
 
-    e2e_launches = 3
     e2e_api = "gmm_forward/gmm_backward"
 
 

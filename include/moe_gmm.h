@@ -128,6 +128,16 @@ MOE_API moe_status_t moe_read_status(const void* ws, moe_stream_t stream);
 /* Human-readable name of a status code (static string). */
 MOE_API const char* moe_status_string(moe_status_t status);
 
+/* Failure-detection check: runs one small kernel whose pipeline wait nothing
+ * ever completes, using the same bounded mbarrier wait and shared abort flag
+ * as the grouped-matmul kernels.  The waiting thread gives up after
+ * timeout_ns (1 us .. 10 s) and raises the abort flag; a second warp waiting
+ * on another barrier stops when it sees the flag; the kernel then writes
+ * MOE_ERR_TIMEOUT to the workspace's status word and returns.  Expected
+ * result: moe_read_status(ws) == MOE_ERR_TIMEOUT with the CUDA context still
+ * usable.  ws: at least MOE_STATUS_BYTES, zeroed by moe_workspace_init. */
+MOE_API moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- dispatch */
 
 /* Workspace bytes for moe_permute. */

@@ -41,6 +41,7 @@ SIGNATURES = {
     "moe_workspace_init": (ST, [P, SZ, P]),
     "moe_read_status": (ST, [P, P]),
     "moe_status_string": (C.c_char_p, [ST]),
+    "moe_check_wait_timeout": (ST, [P, SZ, C.c_uint64, P]),
     "moe_permute_workspace_size": (SZ, [I64, I64, I64]),
     "moe_permute": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, SZ, P]),
     "moe_permute_no_alloc": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, P]),

@@ -91,6 +91,13 @@ def status_string(status: int) -> str:
     return _lib().moe_status_string(status).decode()
 
 
+def check_wait_timeout(ws: Workspace, timeout_ns: int = 1000000, stream=None):
+    """Run the library's bounded-wait failure check (see moe_check_wait_timeout):
+    afterwards read_status(ws) is MOE_ERR_TIMEOUT (6)."""
+    _check(_lib().moe_check_wait_timeout(ws.ptr, ws.nbytes, int(timeout_ns), _stream(stream)),
+           "moe_check_wait_timeout")
+
+
 # ------------------------------------------------------------------ sizes
 def moe_permute_workspace_size(T, k, E) -> int:
     return int(_lib().moe_permute_workspace_size(T, k, E))

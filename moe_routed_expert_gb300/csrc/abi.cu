@@ -144,6 +144,13 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) 
              ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {
+  moe_status_t st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES);
+  if (st != MOE_OK) return st;
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return MOE_ERR_INVALID;
+  return launch_wait_timeout_check(status_of(ws), timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_read_status(const void* ws, moe_stream_t stream) {
   if (ws == nullptr) return MOE_ERR_NULLPTR;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -39,6 +39,9 @@ inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255);
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// ---- failure-detection check (selfcheck.cu)
+moe_status_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+
 // ---- MX quantisation (mx.cu): fp8 codes + E8M0 scales, 32-element groups
 struct MxOut {
   int fmt;           // MOE_FP8_E4M3 / MOE_FP8_E5M2

@@ -19,6 +19,9 @@
 //           the flat order (stable).  Writes row_id_map and sorted_flat.
 //   gather  warp per (slot, 2 KB segment of the row), in slot order so the k
 //           copies of one token read it once from HBM: x_perm[row] = x[t].
+// Up to kSmallSlots slots (decode batches), one block does count, scan and
+// rank (permute_small_kernel) and the gather follows: two launches instead of
+// four, for index work that is all latency at that size.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,6 +36,80 @@ constexpr int CHUNK = 1024;          // slots per block (count and rank)
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;  // 8
 constexpr int SUB = CHUNK / WARPS;   // 128 slots per warp in the rank kernel
+constexpr int kSmallSlots = 1024;    // one-block index path up to this many slots
+
+// Count, scan and rank of up to kSmallSlots slots in one block of 1024
+// threads: a shared-memory histogram, an exclusive scan over the experts (one
+// per thread), then warp 0 walks the slots 32 at a time in flat order and
+// ranks equal ids with __match_any_sync (stable), advancing a running row per
+// expert.  Same outputs and status as count + scan + rank.
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int nslots, int E,
+                                                             int64_t* __restrict__ group_list,
+                                                             int32_t* __restrict__ row_id_map,
+                                                             int32_t* __restrict__ sorted_flat, uint32_t* status) {
+  __shared__ int32_t cnt[kMaxExperts];
+  __shared__ int32_t next_row[kMaxExperts];
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t R_sh;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += 1024) cnt[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < nslots; f += 1024) {
+    const int e = ids[f];
+    if (e < -1 || e >= E) set_status(status, MOE_ERR_DEVICE);
+    else if (e >= 0) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  const int32_t v = tid < E ? cnt[tid] : 0;
+  int32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t w = warp_sum[lane];
+    int32_t wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += o;
+    }
+    warp_sum[lane] = wi - w;
+    if (lane == 31) R_sh = wi;
+  }
+  __syncthreads();
+  if (tid < E) {
+    group_list[tid] = v;
+    next_row[tid] = warp_sum[warp] + incl - v;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll 1
+    for (int c = 0; c < nslots; c += 32) {
+      const int f = c + lane;
+      int e = f < nslots ? ids[f] : -1;
+      if (e < -1 || e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int32_t row = next_row[e] + __popc(peers & lt);
+        row_id_map[f] = row;
+        sorted_flat[row] = f;
+      } else if (f < nslots) {
+        row_id_map[f] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) next_row[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  for (int r = R_sh + tid; r < nslots; r += 1024) sorted_flat[r] = -1;   // rows past R own no slot
+}
 
 __global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* __restrict__ ids, int64_t nslots,
                                                                 int E, int nchunks, int32_t* __restrict__ chunk_counts,
@@ -230,16 +307,22 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
   const int nchunks = static_cast<int>((nslots + CHUNK - 1) / CHUNK);
   int32_t* chunk_counts = static_cast<int32_t*>(scratch);
   const int e = static_cast<int>(E);
-  if (launch_pdl(permute_count_kernel, dim3(nchunks), dim3(THREADS), e * sizeof(int32_t), s, 1, ids, nslots, e,
-                 nchunks, chunk_counts, status) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, 1, e, nchunks, nslots, chunk_counts, group_list,
-                 sorted_flat) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  const size_t rank_smem = static_cast<size_t>(WARPS) * e * sizeof(int32_t);
-  if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
-                 static_cast<const int32_t*>(chunk_counts), row_id_map, sorted_flat) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (nslots <= kSmallSlots) {
+    if (launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, 1, ids, static_cast<int>(nslots), e, group_list,
+                   row_id_map, sorted_flat, status) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_pdl(permute_count_kernel, dim3(nchunks), dim3(THREADS), e * sizeof(int32_t), s, 1, ids, nslots, e,
+                   nchunks, chunk_counts, status) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, 1, e, nchunks, nslots, chunk_counts, group_list,
+                   sorted_flat) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    const size_t rank_smem = static_cast<size_t>(WARPS) * e * sizeof(int32_t);
+    if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
+                   static_cast<const int32_t*>(chunk_counts), row_id_map, sorted_flat) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (mx != nullptr && x != nullptr && H > 0) {
     if (launch_mx_gather(x, nslots, H, static_cast<int>(k), row_id_map, *mx, s) != MOE_OK) return MOE_ERR_CUDA;
   } else if (x != nullptr && x_perm != nullptr && H > 0) {

@@ -152,6 +152,14 @@ def test_python_binding_refuses_cpu_tensors(lib):
         M.gmm_forward(x, w, gl)
 
 
+def test_wait_timeout_check_arguments(lib):
+    assert lib.moe_check_wait_timeout(None, 256, 1000000, None) == 1
+    assert lib.moe_check_wait_timeout(MIS, 256, 1000000, None) == 2
+    assert lib.moe_check_wait_timeout(FAKE, 128, 1000000, None) == 2       # workspace too small
+    assert lib.moe_check_wait_timeout(FAKE, 256, 10, None) == 2            # limit below 1 us
+    assert lib.moe_check_wait_timeout(FAKE, 256, 20 * 10**9, None) == 2    # limit above 10 s
+
+
 def test_mx_entry_points_check_their_arguments(lib):
     ws, nws = FAKE, 1 << 20
     a = _abi_act(0)

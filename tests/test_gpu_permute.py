@@ -1,6 +1,7 @@
 """Parity of the CUDA permute (histogram, scan, stable counting-sort scatter,
 row gather) with the oracle: bit-exact for every integer output and for the
-permuted rows (a copy)."""
+permuted rows (a copy).  Cases up to 1024 slots take the one-block index
+kernel, larger ones the four-kernel path."""
 import json
 import os
 
@@ -54,6 +55,8 @@ def test_worked_example():
 @pytest.mark.parametrize("T,k,E,H,p_unused", [
     (1, 1, 1, 64, 0.0), (7, 3, 5, 72, 0.3), (33, 2, 4, 128, 0.5), (1000, 8, 256, 2048, 0.05),
     (3000, 4, 1024, 64, 0.1), (5000, 8, 64, 136, 0.0), (2049, 1, 3, 8, 0.0), (129, 64, 64, 64, 0.2),
+    # either side of the one-block index path (up to 1024 slots), with 1024 experts
+    (128, 8, 1024, 64, 0.1), (1025, 1, 7, 16, 0.2), (100, 8, 1024, 32, 0.0),
 ])
 def test_random_ragged(T, k, E, H, p_unused):
     rng = np.random.default_rng(T * 7 + k)

@@ -25,11 +25,16 @@ Sources (page title, then section):
   weightScales1 is (E, 2I, ceil(H/64), 2) and weightScales2 is
   (E, H, ceil(I/64), 2), both E8M0, i.e. one scale per 32 elements of K; the
   scales of a pre-quantised x are (BS, ceil(H/32)).
+* [MegaMoE] "A8W4-FP 量化场景": the same four stages with MXFP4 (FLOAT4_E2M1)
+  weights for both matmuls and E4M3 tokens / activations (the data flow BF16 ->
+  MXFP8 E4M3 -> A8W4 GMM1 -> MXFP8 E4M3 -> A8W4 GMM2 -> BF16).
 * The element and scale formats are the ones the pages name by type:
   FLOAT8_E4M3FN (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
   infinities, S.1111.111 is NaN, largest finite 448), FLOAT8_E5M2 (bias 15,
-  2 mantissa bits, IEEE-style infinities and NaNs, largest finite 57344) and
-  FLOAT8_E8M0 (an unsigned biased exponent: 2^(code - 127), 0xFF is NaN).
+  2 mantissa bits, IEEE-style infinities and NaNs, largest finite 57344),
+  FLOAT4_E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no
+  infinities or NaNs: 0, 0.5, 1, 1.5, 2, 3, 4, 6) and FLOAT8_E8M0 (an
+  unsigned biased exponent: 2^(code - 127), 0xFF is NaN).
 
 Readings taken where the pages leave a step open (also listed in the design
 notes of the repository):
@@ -47,6 +52,10 @@ M3. The gate / up pre-activations are rounded to bf16 before the activation
     (as in the A16W16 path); the activation's fp output is quantised directly.
 M4. O_e is stored in bf16 and combined like the A16W16 path's expert outputs.
 M5. K of both matmuls (H and I) is a multiple of 128.
+M6. E2M1 has no NaN: a NaN value encodes as the largest magnitude (code 7,
+    or 15 with its sign); emax = 2 (the largest power of two, 4).  Codes are
+    held one per array element here; the CUDA path takes them packed two per
+    byte (a layout, see workloads.pack_fp4).
 """
 from __future__ import annotations
 
@@ -63,8 +72,9 @@ MX_BLOCK = 32
 
 # ebits, mbits, bias; emax = exponent of the largest finite power of two.
 FP8_FORMATS = {
-    "e4m3": dict(ebits=4, mbits=3, bias=7, emax=8, max=448.0, nan_code=0x7F),
-    "e5m2": dict(ebits=5, mbits=2, bias=15, emax=15, max=57344.0, nan_code=0x7F),
+    "e4m3": dict(bits=8, ebits=4, mbits=3, bias=7, emax=8, max=448.0, nan_code=0x7F),
+    "e5m2": dict(bits=8, ebits=5, mbits=2, bias=15, emax=15, max=57344.0, nan_code=0x7F),
+    "e2m1": dict(bits=4, ebits=2, mbits=1, bias=1, emax=2, max=6.0, nan_code=0x7),
 }
 
 
@@ -75,17 +85,20 @@ def _fmt(fmt):
 
 
 def fp8_decode(codes, fmt) -> np.ndarray:
-    """Value of each 8-bit code, from its sign / exponent / mantissa fields."""
+    """Value of each code (8 bits, or the low 4 bits for e2m1), from its sign /
+    exponent / mantissa fields."""
     f = _fmt(fmt)
     c = np.asarray(codes, dtype=np.int64)
     eb, mb, bias = f["ebits"], f["mbits"], f["bias"]
-    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    sign = np.where((c >> (f["bits"] - 1)) & 1, -1.0, 1.0)
     e = (c >> mb) & ((1 << eb) - 1)
     m = c & ((1 << mb) - 1)
     frac = m / float(1 << mb)
     val = np.where(e == 0, frac * 2.0 ** (1 - bias), (1.0 + frac) * np.exp2(e.astype(np.float64) - bias))
     top = (1 << eb) - 1
-    if fmt == "e4m3":
+    if fmt == "e2m1":
+        pass                                             # every code is finite
+    elif fmt == "e4m3":
         val = np.where((e == top) & (m == (1 << mb) - 1), np.nan, val)
     else:
         val = np.where((e == top) & (m == 0), np.inf, val)
@@ -95,7 +108,7 @@ def fp8_decode(codes, fmt) -> np.ndarray:
 
 def fp8_finite_values(fmt):
     """(codes, values) of the non-negative finite codes, ascending."""
-    codes = np.arange(128)
+    codes = np.arange(1 << (_fmt(fmt)["bits"] - 1))
     vals = fp8_decode(codes, fmt)
     keep = np.isfinite(vals)
     return codes[keep], vals[keep]
@@ -117,7 +130,7 @@ def fp8_encode(v, fmt) -> np.ndarray:
     exact = vals[hi] == mag
     pick_hi = exact | (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0))
     out = np.where(pick_hi, codes[hi], codes[lo])
-    out = out | np.where(np.signbit(v), 0x80, 0)
+    out = out | np.where(np.signbit(v), 1 << (f["bits"] - 1), 0)
     out = np.where(np.isnan(v), f["nan_code"], out)
     return out.astype(np.uint8)
 

@@ -1,4 +1,5 @@
-"""Pins of the MXFP8 oracle (oracle/mx_oracle.py) to things other than itself.
+"""Pins of the MX oracle (oracle/mx_oracle.py: MXFP8, and MXFP4 weights) to
+things other than itself.
 
 - The fp8 element formats: every code's value against torch's own float8
   dtypes (a library decode), and the format constants the pages' type names
@@ -12,6 +13,10 @@
 - The MX grouped matmul against a torch float64 matmul of torch-dequantised
   operands, and the MX layer against a per-token evaluation of the four stages
   that takes no permute at all.
+- FLOAT4_E2M1 ("MegaMoE", A8W4-FP 量化场景): the 16 codes against the type's
+  eight magnitudes, ties to the even code, saturation at 6, hand-computed Q_MX
+  groups, and the same error bound, exactness, GMM and per-token layer pins
+  with the weights decoded from that value table.
 """
 import numpy as np
 import pytest
@@ -23,6 +28,8 @@ from oracle import mx_oracle as X
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
 TORCH_FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+# FLOAT4_E2M1's eight magnitudes (the type's definition: no infinities, no NaN)
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
 
 def torch_decode(codes, fmt):
@@ -111,7 +118,26 @@ def test_mx_quantize_hand_groups_e5m2():
     assert q[0, 0] == 0x78 and q[0, 1] == 0x76 and q[1, 0] == 0x7B
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_e2m1_codes_values_and_rounding():
+    codes = np.arange(16)
+    assert X.fp8_decode(codes, "e2m1").tolist() == E2M1_VALUES + [-v for v in E2M1_VALUES]
+    assert X.FP8_FORMATS["e2m1"]["emax"] == 2 and 2.0 ** 2 <= 6.0 < 2.0 ** 3
+    # ties go to the even code; beyond 6 saturates; signed zero and NaN per the readings
+    v = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 1e9, -0.0, -1.5, np.nan, 0.26, 5.01]
+    want = [0, 2, 2, 4, 4, 6, 6, 7, 7, 8, 11, 7, 1, 7]
+    assert X.fp8_encode(v, "e2m1").tolist() == want
+    vals = X.fp8_decode(codes, "e2m1")
+    assert np.array_equal(X.fp8_encode(vals, "e2m1"), codes)
+    g = np.zeros((3, 32))
+    g[0, :2] = [1.0, 0.3]      # X = 2^(0-2): 4 -> code 6, 1.2 -> 1.0 (code 2)
+    g[1, 0] = 1.5              # 6 -> code 7
+    g[2, :2] = [1.9, -0.1]     # 7.6 saturates to 6; -0.4 -> -0.5 (code 9)
+    q, sc = X.mx_quantize(g, "e2m1")
+    assert sc.tolist() == [[125], [125], [125]]
+    assert q[0, :2].tolist() == [6, 2] and q[1, 0] == 7 and q[2, :2].tolist() == [7, 9]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
 def test_mx_quantize_error_bound(fmt):
     """Each element lies within half a step of its dequantised value, the step
     being that of the element format's binade of |x| / X (or the subnormal step
@@ -133,7 +159,7 @@ def test_mx_quantize_error_bound(fmt):
     assert np.all(np.abs(dq[sat]) == f["max"] * scale[sat])
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m1"])
 def test_mx_quantize_is_exact_on_representable_groups(fmt):
     rng = np.random.default_rng(11)
     codes, vals = X.fp8_finite_values(fmt)
@@ -145,9 +171,31 @@ def test_mx_quantize_is_exact_on_representable_groups(fmt):
 
 
 def _torch_dequant(q, s, fmt):
-    v = torch_decode(q, fmt)
+    """Dequantise with an independent element decode: torch's float8 dtypes, or
+    the E2M1 value table."""
+    if fmt == "e2m1":
+        c = np.asarray(q, np.int64)
+        v = np.array(E2M1_VALUES)[c & 7] * np.where(c & 8, -1.0, 1.0)
+    else:
+        v = torch_decode(q, fmt)
     sc = np.exp2(np.asarray(s, np.float64) - 127)
     return (v.reshape(v.shape[:-1] + (-1, 32)) * sc[..., None]).reshape(v.shape)
+
+
+def test_mx_gmm_with_e2m1_weights():
+    rng = np.random.default_rng(6)
+    E, K, N = 2, 128, 32
+    counts = np.array([7, 4])
+    xq = rng.integers(0, 256, (11, K)).astype(np.uint8)
+    xq[(xq & 0x7F) == 0x7F] = 0x11
+    wq = rng.integers(0, 16, (E, N, K)).astype(np.uint8)
+    xs = rng.integers(115, 130, (11, K // 32)).astype(np.uint8)
+    ws = rng.integers(115, 130, (E, N, K // 32)).astype(np.uint8)
+    got = X.mx_gmm(xq, xs, wq, ws, counts, "e4m3", "e2m1", store=None)
+    xd = _torch_dequant(xq, xs, "e4m3")
+    wd = _torch_dequant(wq, ws, "e2m1")
+    want = np.concatenate([xd[:7] @ wd[0].T, xd[7:] @ wd[1].T])
+    assert np.allclose(got, want, rtol=1e-12, atol=0)
 
 
 def test_mx_gmm_against_torch_dequant_matmul():
@@ -170,7 +218,8 @@ def test_mx_gmm_against_torch_dequant_matmul():
         assert np.allclose(got[off[g]:off[g + 1]], want, rtol=1e-12, atol=0)
 
 
-def test_mx_layer_matches_per_token_stages():
+@pytest.mark.parametrize("w_fmt", ["e4m3", "e2m1"])
+def test_mx_layer_matches_per_token_stages(w_fmt):
     """Stage by stage for each token on its own: quantise the token's row, the
     gate_up product with expert e's weights, bf16, the activation, quantise,
     the down product, bf16, then the weighted sum over its k slots."""
@@ -181,12 +230,12 @@ def test_mx_layer_matches_per_token_stages():
     tw = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
     w1 = rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)
     w2 = rng.standard_normal((E, H, I)) / np.sqrt(I)
-    w1q, w1s = X.mx_quantize(w1, "e4m3")
-    w2q, w2s = X.mx_quantize(w2, "e4m3")
+    w1q, w1s = X.mx_quantize(w1, w_fmt)
+    w2q, w2s = X.mx_quantize(w2, w_fmt)
     act = O.activation("swiglu", [7.0])
-    y, _ = X.mx_layer_forward(x, ids, tw, w1q, w1s, w2q, w2s, "e4m3", "e4m3", act)
-    w1d = _torch_dequant(w1q, w1s, "e4m3")
-    w2d = _torch_dequant(w2q, w2s, "e4m3")
+    y, _ = X.mx_layer_forward(x, ids, tw, w1q, w1s, w2q, w2s, "e4m3", w_fmt, act)
+    w1d = _torch_dequant(w1q, w1s, w_fmt)
+    w2d = _torch_dequant(w2q, w2s, w_fmt)
     want = np.zeros((T, H))
     for t in range(T):
         acc = np.zeros(H)

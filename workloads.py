@@ -32,12 +32,18 @@ layer_train_t16384       MoE layer fwd+bwd, T=16384, H=4096, E=64, k=8,
                          I=1024, SwiGLU clip 7, one hot expert (+2 logit)
 layer_prefill_mx_t4096   the prefill layer in MXFP8 (E4M3 tokens and weights)
 layer_decode_mx_t64      the decode layer in MXFP8 (E4M3 tokens and weights)
+layer_prefill_a8w4_t4096 the prefill layer with E4M3 tokens, MXFP4 (E2M1)
+                         weights
+layer_decode_a8w4_t64    the decode layer with E4M3 tokens, MXFP4 weights
 =======================  ====================================================
 
 MXFP8 weights are drawn directly as codes: N(0, 16^2) draws cast to the fp8
 type by torch's CPU conversion (a library cast, not the method's Q_MX), with
 E8M0 scale codes drawn uniformly from three values centred so that the
-dequantised weights have a standard deviation near 1/sqrt(K).
+dequantised weights have a standard deviation near 1/sqrt(K).  MXFP4 weights
+are codes drawn uniformly from the 16 E2M1 codes (values up to +-6), with
+scales centred the same way; the CUDA path takes them packed two per byte,
+element 2i in the low nibble (pack_fp4).
 """
 from __future__ import annotations
 
@@ -49,7 +55,7 @@ import numpy as np
 __all__ = [
     "GmmWorkload", "LayerWorkload", "WORKLOADS", "f32_to_bf16_bits",
     "gmm_inputs", "layer_inputs", "routing", "zipf_counts", "normal_bf16",
-    "fp8_codes", "e8m0_codes", "mx_weight", "mx_layer_weights",
+    "fp8_codes", "e8m0_codes", "mx_weight", "mx_layer_weights", "pack_fp4",
 ]
 
 
@@ -83,6 +89,7 @@ class LayerWorkload:
     hot_bias: float
     backward: bool
     mx: str = ""   # "" (bf16 path) or the fp8 element type of the MXFP8 forward
+    w_mx: str = ""  # the weights' element type when it differs from mx ("e2m1": MXFP4)
 
     @property
     def R(self) -> int:
@@ -105,6 +112,10 @@ WORKLOADS = {
                                             clip=0.0, hot_bias=0.0, backward=False, mx="e4m3"),
     "layer_decode_mx_t64": LayerWorkload("layer_decode_mx_t64", 4, T=64, H=2048, E=256, k=8, I=512,
                                          clip=0.0, hot_bias=0.0, backward=False, mx="e4m3"),
+    "layer_prefill_a8w4_t4096": LayerWorkload("layer_prefill_a8w4_t4096", 3, T=4096, H=2048, E=256, k=8, I=512,
+                                              clip=0.0, hot_bias=0.0, backward=False, mx="e4m3", w_mx="e2m1"),
+    "layer_decode_a8w4_t64": LayerWorkload("layer_decode_a8w4_t64", 4, T=64, H=2048, E=256, k=8, I=512,
+                                           clip=0.0, hot_bias=0.0, backward=False, mx="e4m3", w_mx="e2m1"),
 }
 
 
@@ -225,14 +236,27 @@ def e8m0_codes(rng: np.random.Generator, shape, centre: int) -> np.ndarray:
 
 def mx_weight(rng: np.random.Generator, E: int, N: int, K: int, fmt: str = "e4m3"):
     """(codes [E, N, K], scales [E, N, K/32]) of an MX weight whose dequantised
-    values have a standard deviation near 1/sqrt(K) (codes ~ N(0, 16^2))."""
+    values have a standard deviation near 1/sqrt(K): fp8 codes ~ N(0, 16^2)
+    cast by torch, or e2m1 codes uniform over all 16 (one code per byte here;
+    see pack_fp4 for the CUDA layout)."""
+    if fmt == "e2m1":
+        centre = 127 - 1 - int(round(0.5 * np.log2(K)))
+        codes = rng.integers(0, 16, size=(E, N, K)).astype(np.uint8)
+        return codes, e8m0_codes(rng, (E, N, K // 32), centre)
     centre = 127 - 4 - int(round(0.5 * np.log2(K)))
     return fp8_codes(rng, (E, N, K), fmt), e8m0_codes(rng, (E, N, K // 32), centre)
 
 
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    """4-bit codes [..., K] (one per byte) -> bytes [..., K/2], element 2i in the
+    low nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.ascontiguousarray((c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)).astype(np.uint8)
+
+
 def mx_layer_weights(wl: LayerWorkload, seed: Optional[int] = None, fmt: Optional[str] = None) -> dict:
     """w1_q [E, 2I, H], w1_s [E, 2I, H/32], w2_q [E, H, I], w2_s [E, H, I/32] (uint8)."""
-    fmt = fmt or wl.mx or "e4m3"
+    fmt = fmt or wl.w_mx or wl.mx or "e4m3"
     wrng = np.random.default_rng((wl.seed if seed is None else seed) + 2000)
     w1q, w1s = mx_weight(wrng, wl.E, 2 * wl.I, wl.H, fmt)
     w2q, w2s = mx_weight(wrng, wl.E, wl.H, wl.I, fmt)

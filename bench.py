@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from workloads import WORKLOADS, gmm_inputs, layer_inputs, mx_layer_weights  # noqa: E402
+from workloads import WORKLOADS, gmm_inputs, layer_inputs, mx_layer_weights, pack_fp4  # noqa: E402
 
 METRIC = "GMM fwd+bwd TFLOP/s and MoE-layer tokens/s on 1 GB300; % of bf16 peak / HBM BW"
 DEFAULT_WORKLOAD = "layer_train_t16384"
@@ -300,8 +300,10 @@ class LayerMxStep:
         self.x = bf16_dev(inp["x"], dev)
         self.ids = torch.from_numpy(inp["topk_ids"]).to(dev)
         self.tw = torch.from_numpy(inp["topk_w"]).to(dev)
-        self.w1q, self.w1s = (torch.from_numpy(inp[n]).to(dev) for n in ("w1_q", "w1_s"))
-        self.w2q, self.w2s = (torch.from_numpy(inp[n]).to(dev) for n in ("w2_q", "w2_s"))
+        self.wfmt = wl.w_mx or wl.mx
+        pk = (lambda a: pack_fp4(a)) if self.wfmt == "e2m1" else (lambda a: a)   # E2M1: two codes per byte
+        self.w1q, self.w2q = (torch.from_numpy(pk(inp[n])).to(dev) for n in ("w1_q", "w2_q"))
+        self.w1s, self.w2s = (torch.from_numpy(inp[n]).to(dev) for n in ("w1_s", "w2_s"))
         self.xq = torch.empty(R, H, dtype=u8, device=dev)
         self.xs = torch.empty(R, H // 32, dtype=u8, device=dev)
         self.gl = torch.empty(E, dtype=torch.int64, device=dev)
@@ -325,13 +327,15 @@ class LayerMxStep:
             ("gmm_mx_down", self.gmm2, f_dn, 1),
             ("combine", self.combine, 0.0, 1),
         ]
-        # algorithmic bytes: fp8 weights and their scales of the non-empty experts, operands in and results out once
-        self.gmm_bytes = {"gmm_mx_gate_up_act_quant": live * 2 * I * (H + H // 32) + Rr * (H + H // 32)
+        # algorithmic bytes: weights (fp8, or E2M1 at half a byte) and their scales of the
+        # non-empty experts, operands in and results out once
+        wb = 0.5 if self.wfmt == "e2m1" else 1.0
+        self.gmm_bytes = {"gmm_mx_gate_up_act_quant": live * 2 * I * (wb * H + H // 32) + Rr * (H + H // 32)
                           + Rr * (I + I // 32),
-                          "gmm_mx_down": live * H * (I + I // 32) + Rr * (I + I // 32) + Rr * H * 2}
+                          "gmm_mx_down": live * H * (wb * I + I // 32) + Rr * (I + I // 32) + Rr * H * 2}
         self.units = T
         self.unit = "tokens/s"
-        self.dtype = "mxfp8_" + wl.mx
+        self.dtype = "mxfp8_" + wl.mx + ("_w" + self.wfmt if self.wfmt != wl.mx else "")
         self.kernel = "gmm_mx_kernel (both block-scaled GMM launches of a step)"
 
     def permute(self):
@@ -339,11 +343,11 @@ class LayerMxStep:
                               out=(self.xq, self.xs, self.gl, self.rmap, self.sflat), ws=self.ws)
 
     def gmm1(self):
-        self.M.gmm_forward_mx(self.xq, self.xs, self.w1q, self.w1s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wl.mx,
+        self.M.gmm_forward_mx(self.xq, self.xs, self.w1q, self.w1s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wfmt,
                               activation=self.act, a_q=self.aq, a_scales=self.as_, ws=self.ws)
 
     def gmm2(self):
-        self.M.gmm_forward_mx(self.aq, self.as_, self.w2q, self.w2s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wl.mx,
+        self.M.gmm_forward_mx(self.aq, self.as_, self.w2q, self.w2s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wfmt,
                               y=self.o, ws=self.ws)
 
     def combine(self):
@@ -358,7 +362,7 @@ class LayerMxStep:
 
     def e2e_compute(self, i, o):
         self.M.moe_layer_forward_mx(i["x"], i["topk_ids"], i["topk_w"], self.w1q, self.w1s, self.w2q, self.w2s,
-                                    x_fmt=self.wl.mx, w_fmt=self.wl.mx, activation=self.act, y=o["y"], ws=self.ws)
+                                    x_fmt=self.wl.mx, w_fmt=self.wfmt, activation=self.act, y=o["y"], ws=self.ws)
 
     e2e_api = "moe_layer_forward_mx"
 
@@ -492,7 +496,7 @@ def oracle_mx_layer_step(wl, inp_sub):
     import oracle as O
     from oracle import mx_oracle as X
     X.mx_layer_forward(O.bf16_bits_to_f64(inp_sub["x"]), inp_sub["topk_ids"], inp_sub["topk_w"], inp_sub["w1_q"],
-                       inp_sub["w1_s"], inp_sub["w2_q"], inp_sub["w2_s"], wl.mx, wl.mx,
+                       inp_sub["w1_s"], inp_sub["w2_q"], inp_sub["w2_s"], wl.mx, wl.w_mx or wl.mx,
                        O.activation("swiglu", [wl.clip]))
 
 
@@ -725,7 +729,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": getattr(step, "dtype", "bf16"), "data": "synthetic",
             "config": {"workload": args.workload, **{k_: v_ for k_, v_ in vars(step.wl).items() if k_ != "name"},
                        "l2": "inputs larger than L2" if not args.workload.startswith("layer_decode")
-                       else "weights (%s touched) larger than L2" % ("0.7 GB" if step.wl.mx else "1.4 GB"), "parallelism": "replicas" if world > 1 else "1 GPU"},
+                       else "weights (%s touched) larger than L2" % (
+                           "0.35 GB" if step.wl.w_mx == "e2m1" else ("0.7 GB" if step.wl.mx else "1.4 GB")), "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": roof, "kernels": kernels,
             "kernels_timing": "CUDA events after every launch, in a second pass of the same steps",
             "gpu_launches": launches * args.steps,

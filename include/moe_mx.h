@@ -1,5 +1,6 @@
 /*
- * moe_mx.h -- C ABI of the MXFP8 (A8W8-FP) routed-expert forward.
+ * moe_mx.h -- C ABI of the MX-quantised routed-expert forward: MXFP8 tokens
+ * with MXFP8 weights (A8W8-FP) or MXFP4 weights (A8W4-FP).
  *
  * What the calls compute ("MegaMoE", ops-transformer operator doc):
  *  - "A8W8-FP 量化场景", stage 1: the tokens gathered per expert are quantised
@@ -13,6 +14,8 @@
  *  - stage 3: O_e = DQ(A_e) DQ(W2_e), bf16 (gmm_forward_mx, no activation);
  *  - stage 4: Y[i] = sum_k W[i, k] O[pi(i, k)] (the A16W16 combine,
  *    moe_unpermute).  moe_layer_forward_mx runs the four stages.
+ *  - "A8W4-FP 量化场景": the same stages with FLOAT4_E2M1 weights for both
+ *    matmuls (w_format MOE_FP4_E2M1) and E4M3 tokens and activations.
  *  - "约束说明", MXFP: weight1 is (E, 2I, H) and weight2 (E, H, I): each
  *    output channel is a row of K contiguous elements; weightScales1 is
  *    (E, 2I, ceil(H/64), 2) and weightScales2 (E, H, ceil(I/64), 2), i.e. one
@@ -43,8 +46,11 @@
 extern "C" {
 #endif
 
-/* FP8 element formats (FLOAT8_E4M3FN, FLOAT8_E5M2). */
-typedef enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 } moe_fp8_format_t;
+/* Element formats: FLOAT8_E4M3FN, FLOAT8_E5M2, and FLOAT4_E2M1 for weights
+ * only ("MegaMoE", A8W4-FP 量化场景: MXFP4 weights, E4M3 tokens).  E2M1 weight
+ * codes are packed two per byte, element 2i in the low nibble: w_q is
+ * [E, N, K/2] bytes, 32-byte aligned. */
+typedef enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1, MOE_FP4_E2M1 = 5 } moe_fp8_format_t;
 
 /* Workspace bytes for moe_mx_quantize (the status block only). */
 MOE_API size_t moe_mx_quantize_workspace_size(void);
@@ -68,7 +74,8 @@ MOE_API size_t gmm_mx_workspace_size(int64_t M, int64_t K, int64_t N, int64_t E)
 
 /* Block-scaled grouped matmul per expert e with rows [off_e, off_e + group_list[e]):
  *   P = DQ(x_q, x_scales)[rows] @ DQ(w_q[e], w_scales[e])^T
- *   x_q [M, K] fp8 (x_format), x_scales [M, K/32]; w_q [E, N, K] fp8 (w_format),
+ *   x_q [M, K] fp8 (x_format), x_scales [M, K/32]; w_q [E, N, K] fp8 or
+ *   [E, N, K/2] packed E2M1 (w_format),
  *   w_scales [E, N, K/32]; group_list [E] int64 counts summing to M.
  *   activation NULL: y [M, N] bf16 = P.
  *   activation given (N = 2I): H = bf16(P), A = activation(H[:, :I], H[:, I:]),
@@ -84,7 +91,8 @@ MOE_API moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales,
 /* Workspace bytes for moe_layer_forward_mx. */
 MOE_API size_t moe_layer_mx_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 
-/* The A8W8-FP layer forward: moe_permute_mx (x_format) -> gmm_forward_mx with
+/* The A8W8-FP / A8W4-FP layer forward (w_format an fp8 type, or MOE_FP4_E2M1
+ * with the weights packed as gmm_forward_mx describes): moe_permute_mx (x_format) -> gmm_forward_mx with
  * the activation (w1_q [E, 2I, H], w1_scales [E, 2I, H/32]) -> gmm_forward_mx
  * (w2_q [E, H, I], w2_scales [E, H, I/32]) -> combine with topk_w into
  * y [T, H] bf16.  Intermediates live in ws. */

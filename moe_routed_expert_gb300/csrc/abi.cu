@@ -478,6 +478,11 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
 namespace moe {
 namespace {
 bool bad_fmt(int32_t f) { return f != MOE_FP8_E4M3 && f != MOE_FP8_E5M2; }
+bool bad_wfmt(int32_t f) { return bad_fmt(f) && f != MOE_FP4_E2M1; }
+// the 4-bit TMA map wants a 32-byte-aligned base
+bool w_aligned(const void* w, int32_t f) {
+  return (reinterpret_cast<uintptr_t>(w) & (f == MOE_FP4_E2M1 ? 31u : 15u)) == 0;
+}
 
 size_t layer_mx_acts_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const size_t R = static_cast<size_t>(T * k);
@@ -539,14 +544,14 @@ moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales, const u
                             uint8_t* a_scales, moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x_q || !x_scales || !w_q || !w_scales || !group_list) return MOE_ERR_NULLPTR;
   if (activation ? (!a_q || !a_scales) : !y) return MOE_ERR_NULLPTR;
-  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
+  if (bad_fmt(x_format) || bad_wfmt(w_format)) return MOE_ERR_INVALID;
   Act act;
   moe_status_t st = activation ? resolve_act(activation, &act) : MOE_OK;
   if (st != MOE_OK) return st;
   if ((st = check_mx_gmm(M, K, N, E)) != MOE_OK) return st;
   if (activation && N % 256) return MOE_ERR_UNSUPPORTED;
   if (!activation && h_save) return MOE_ERR_INVALID;
-  if (!aligned16(x_q) || !aligned16(x_scales) || !aligned16(w_q) || !aligned16(w_scales) ||
+  if (!aligned16(x_q) || !aligned16(x_scales) || !w_aligned(w_q, w_format) || !aligned16(w_scales) ||
       (y && !aligned16(y)) || (a_q && !aligned16(a_q)) || (a_scales && !aligned16(a_scales)) ||
       (h_save && !aligned16(h_save)) || (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
@@ -571,14 +576,14 @@ moe_status_t moe_layer_forward_mx(const moe_bf16* x, const int32_t* topk_ids, co
                                   int32_t x_format, int32_t w_format, const moe_activation_t* activation,
                                   moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !topk_ids || !topk_w || !w1_q || !w1_scales || !w2_q || !w2_scales || !y) return MOE_ERR_NULLPTR;
-  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
+  if (bad_fmt(x_format) || bad_wfmt(w_format)) return MOE_ERR_INVALID;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
   if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
   if (H % 128) return MOE_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(w1_q) || !aligned16(w1_scales) || !aligned16(w2_q) || !aligned16(w2_scales) ||
-      !aligned16(y))
+  if (!aligned16(x) || !w_aligned(w1_q, w_format) || !aligned16(w1_scales) || !w_aligned(w2_q, w_format) ||
+      !aligned16(w2_scales) || !aligned16(y))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, moe_layer_mx_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
   if (T == 0) return MOE_OK;

@@ -80,4 +80,20 @@ bool make_map_3d_u8(CUtensorMap* m, const void* base, int64_t E, int64_t R, int6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed 4-bit codes (two per byte) [E, R, C elements], expanded by the TMA
+// unit into 16-byte granules of 16 codes and 8 bytes of gap in shared memory:
+// the layout tcgen05's kind::mxf8f6f4 reads for E2M1 operands, with the same
+// footprint as an fp8 tile.  box = 128 (c) x box_rows (r) x 1 (e).
+bool make_map_3d_fp4(CUtensorMap* m, const void* base, int64_t E, int64_t R, int64_t C, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(C / 2), static_cast<cuuint64_t>(R) * (C / 2)};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe

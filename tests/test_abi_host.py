@@ -193,6 +193,11 @@ def test_mx_entry_points_check_their_arguments(lib):
     assert lib.gmm_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, 3, 0, None, FAKE, None, None, None,
                               ws, nws, None) == 2                    # format
     assert gm(0, 128, 256, None, FAKE, None, None, None) == 0        # no rows: nothing to do
+    # E2M1 is a weight format only, and its packed weights want a 32-byte-aligned base
+    e2m1 = lambda xf, w: lib.gmm_forward_mx(FAKE, FAKE, w, FAKE, FAKE, 64, 128, 256, 4, xf, 5, None, FAKE, None,
+                                            None, None, ws, nws, None)
+    assert e2m1(5, FAKE) == 2
+    assert e2m1(0, C.c_void_p(0x10010)) == 2
     # layer
     lay = lambda H, I, xf, act: lib.moe_layer_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, H, I, 4, 2,
                                                          xf, 0, act, FAKE, ws, nws, None)

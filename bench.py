@@ -610,6 +610,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph (the per-kernel split stays eager)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the first T tokens of the layer workload (smaller captures; not a bench line)")
     args = ap.parse_args()
@@ -657,10 +659,24 @@ def main():
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    run_step = lambda: [fn() for _, fn, _, _ in step.stages]
+    if args.graph:
+        # one step captured into a CUDA graph (every call is stream-ordered, with no host
+        # synchronisation and no allocation), replayed on the timed stream
+        graph = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(graph, stream=cs):
+                run_step()
+        stream.wait_stream(cs)
+        graph.replay()
+        barrier()
+        assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
+        run_step = graph.replay
     t_start.record(stream)
     for s in range(args.steps):
-        for _, fn, _, _ in step.stages:
-            fn()
+        run_step()
     t_end.record(stream)
     barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -732,6 +748,7 @@ def main():
                        else "weights (%s touched) larger than L2" % (
                            "0.35 GB" if step.wl.w_mx == "e2m1" else ("0.7 GB" if step.wl.mx else "1.4 GB")), "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": roof, "kernels": kernels,
+            "launch": "one CUDA graph per step (replayed)" if args.graph else "stream launches, programmatic serialisation",
             "kernels_timing": "CUDA events after every launch, in a second pass of the same steps",
             "gpu_launches": launches * args.steps,
             "gmm_tflops": round(gmm_flops / (gmm_ms / 1e3) / 1e12, 1) if gmm_ms else None}

@@ -18,14 +18,17 @@
 // of 128 fp8 elements = one 128-byte swizzle row):
 //   warp 0      producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
-//               4-stage ring.  All 32 lanes copy the stage's scales 4 stages
-//               ahead with cp.async (4 bytes each: the 4 scales of one row),
-//               into an 8-slot ring, in the order the tensor core reads them:
+//               4-stage ring.  All 32 lanes copy the stage's scales with
+//               cp.async (4 bytes each: the 4 scales of one row) into the
+//               stage's scale slot, in the order the tensor core reads them:
 //               per 128 rows a 512-byte block in which row r's word sits at
-//               word 4 (r % 32) + r / 32.  Before a stage's TMA copies are
-//               issued the warp waits for its own copies of that stage
-//               (cp.async.wait_group) and fences them for the async proxy.
-//   warp 1      TMEM allocator; one thread copies the stage's scales into TMEM
+//               word 4 (r % 32) + r / 32, and each lane's copies arrive on the
+//               stage's full barrier when they land (cp.async.mbarrier.arrive),
+//               so the barrier completes with the TMA bytes and all 32 lanes'
+//               scales and the producer never waits for its copies.
+//   warp 1      TMEM allocator; one thread, after the stage's full barrier and
+//               a proxy fence (the scales were written by the generic proxy),
+//               copies the stage's scales into TMEM
 //               (tcgen05.cp 32x128b, replicated to all four lane quarters:
 //               4 columns for A, 8 for B) and issues four
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32)
@@ -33,8 +36,8 @@
 //   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half
 //               of the tile's columns: tcgen05.ld -> registers (bf16) ->
 //               release the accumulator -> activation / Q_MX -> global stores.
-// TMEM: one 256-column fp32 accumulator (the scales of the 8 scale slots
-// take 96 more columns, so a second accumulator does not fit in 512); the
+// TMEM: one 256-column fp32 accumulator (the scales of the stages take 48
+// more columns, and a second accumulator does not fit in 512 with them); the
 // epilogue releases it as soon as the tile is in registers.
 // Group structure, tile order, bounded waits and the abort path are those of
 // the bf16 kernel (gmm.cu).
@@ -64,16 +67,13 @@ constexpr int SFB_BYTES = BN * 4;
 constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr int SF_COLS = 12;                 // TMEM columns per scale slot: 4 (A) + 8 (B)
-constexpr int SF_SLOTS = 8;                 // scale ring (shared memory and TMEM)
-constexpr int SF_AHEAD = 4;                 // stages between a scale copy and its use
+constexpr int SF_SLOTS = STAGES;            // one scale slot per stage (shared memory and TMEM)
+constexpr int FULL_ARRIVALS = 1 + 32;       // the TMA arrival and each producer lane's scale copies
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 static_assert(ACC_COLS + SF_SLOTS * SF_COLS <= TMEM_COLS, "TMEM budget");
-// the scale slot written at stage i + SF_AHEAD was last read at stage i + SF_AHEAD - SF_SLOTS,
-// which the wait for the data slot of stage i has already seen finish
-static_assert(SF_AHEAD + STAGES <= SF_SLOTS, "scale ring reuse");
 
 enum { MX_PLAIN = 0, MX_ACT = 1 };
 
@@ -108,7 +108,7 @@ struct __align__(16) MxSmem {
   uint32_t abort;
   int32_t bad;
   int32_t ntiles;
-  int64_t grp_off[kMaxExperts + 1];
+  int32_t grp_off[kMaxExperts + 1];    // M < 2^31 (checked by the ABI)
   int32_t grp_cnt[kMaxExperts];
   int32_t tile_start[kMaxExperts + 1];
 };
@@ -227,7 +227,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     sm->bad = 0;
     sm->abort = 0;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->full[s]), FULL_ARRIVALS);
       mbar_init(smem_u32(&sm->empty[s]), 1);
     }
     mbar_init(smem_u32(&sm->tmem_full), 1);
@@ -272,13 +272,13 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     int64_t rb = rows_incl - rows;
     int32_t tb = tiles_incl - tiles;
     for (int e = lo; e < hi; ++e) {
-      sm->grp_off[e] = rb;
+      sm->grp_off[e] = static_cast<int32_t>(rb);
       sm->tile_start[e] = tb;
       rb += sm->grp_cnt[e];
       tb += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
     }
     if (lane == 31) {
-      sm->grp_off[E] = rows_incl;
+      sm->grp_off[E] = static_cast<int32_t>(rows_incl);
       sm->tile_start[E] = tiles_incl;
       sm->ntiles = tiles_incl;
       if (rows_incl > p.rows_cap) sm->bad = 1;
@@ -294,28 +294,15 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // ---------------------------------------------------------------- producer (whole warp)
     uint32_t it = 0;
     bool ok = true;
-    StageIter cur, pre;
+    StageIter cur;
     stage_iter_start<EPI>(cur, sm, p, ntiles);
-    pre = cur;
-#pragma unroll 1
-    for (int d = 0; d < SF_AHEAD; ++d) {   // scales of the first SF_AHEAD stages (one group each)
-      if (pre.valid) copy_sf<EPI>(p, pre.ti, pre.kb, lane, sf_base + d * SF_STAGE_BYTES);
-      cp_async_commit();
-      stage_iter_next<EPI>(pre, sm, p, ntiles);
-    }
     while (cur.valid) {
       const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
       if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
-      // scales of stage it + SF_AHEAD (their slot's last reader, stage it + SF_AHEAD - SF_SLOTS,
-      // finished before the data slot of stage it was released)
-      if (pre.valid) copy_sf<EPI>(p, pre.ti, pre.kb, lane, sf_base + ((it + SF_AHEAD) % SF_SLOTS) * SF_STAGE_BYTES);
-      cp_async_commit();
-      stage_iter_next<EPI>(pre, sm, p, ntiles);
-      cp_async_wait<SF_AHEAD>();           // this lane's copies of stage it have landed
-      fence_proxy_async_smem();            // ... and are visible to tcgen05.cp
-      __syncwarp();
+      const uint32_t bar = smem_u32(&sm->full[s]);
+      copy_sf<EPI>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
+      cp_async_arrive_noinc(bar);          // arrives when this lane's copies have landed
       if (lane == 0) {
-        const uint32_t bar = smem_u32(&sm->full[s]);
         const uint32_t a_dst = stage_base + s * STAGE_BYTES;
         const uint32_t b_dst = a_dst + A_BYTES;
         const TileInfo& ti = cur.ti;
@@ -351,9 +338,10 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
           tc_fence_after();
+          fence_proxy_async_smem();        // the scales came through the generic proxy (cp.async)
           const uint32_t a_addr = stage_base + s * STAGE_BYTES;
           const uint32_t b_addr = a_addr + A_BYTES;
-          const uint32_t sf_slot = it % SF_SLOTS;
+          const uint32_t sf_slot = s;
           const uint32_t sfa_smem = sf_base + sf_slot * SF_STAGE_BYTES;
           const uint32_t sf_col = tmem_base + ACC_COLS + sf_slot * SF_COLS;
           tc_cp_32x128b_x4(sf_col, smem_desc_plain(sfa_smem, 128, 128));
@@ -502,6 +490,7 @@ moe_status_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const M
 }  // namespace
 
 moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s) {
+  // a few rows per expert (decode): the 128-row activation tile would be mostly padding
   MxParams p{};
   p.group_list = x.group_list;
   p.a_sf = x.a_sf;

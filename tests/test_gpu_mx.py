@@ -130,6 +130,42 @@ def test_gmm_forward_mx_plain(case):
     assert_close("y", y, want)
 
 
+# Groups of a few rows, as in decode: many 128-row tiles that hold 0-12 rows,
+# one group over 32 rows, empty groups; N = 384 leaves a ragged 256-column tile.
+SMALL_COUNTS = [3, 0, 1, 40, 2, 0, 7, 1, 0, 5, 2, 2, 0, 9, 1, 1, 0, 3, 4, 0, 1, 1, 6, 0, 2, 3, 0, 1, 2, 0, 0, 12]
+SWAP_CASES = [("e4m3", "e4m3", 384), ("e5m2", "e5m2", 256), ("e4m3", "e2m1", 384)]
+
+
+@pytest.mark.parametrize("xf,wf,N", SWAP_CASES)
+def test_gmm_forward_mx_small_groups_plain(xf, wf, N):
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(51)
+    E, K = len(SMALL_COUNTS), 512
+    xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, N, SMALL_COUNTS, xf, wf)
+    wsp = M.Workspace(256)
+    y = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
+    assert M.read_status(wsp) == 0
+    assert_close("y", y, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
+
+
+@pytest.mark.parametrize("xf,wf", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1")])
+@pytest.mark.parametrize("act", [("swiglu", (7.0,)), ("situglu", (1.0, 2.0))], ids=lambda a: a[0])
+def test_gmm_forward_mx_small_groups_activation(act, xf, wf):
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(52)
+    E, K, I = len(SMALL_COUNTS), 256, 256
+    xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, 2 * I, SMALL_COUNTS, xf, wf)
+    Mr = int(sum(SMALL_COUNTS))
+    h = torch.empty(Mr, 2 * I, dtype=torch.bfloat16, device="cuda")
+    wsp = M.Workspace(256)
+    aq, as_ = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf,
+                               activation=(act[0], list(act[1])), h_save=h, ws=wsp)
+    assert M.read_status(wsp) == 0
+    assert_close("h", h, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
+    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation(act[0], act[1]), xf)
+
+
 def check_act_codes(aq, as_, h_gpu, act, fmt, rel=1e-5, abs_a=2e-6):
     """Codes and scales against Q_MX(activation(H)) of the GPU's own H: a
     decision may differ only where the exact value sits within the fp32

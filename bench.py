@@ -38,31 +38,44 @@ from workloads import WORKLOADS, gmm_inputs, layer_inputs, mx_layer_weights, pac
 METRIC = "GMM fwd+bwd TFLOP/s and MoE-layer tokens/s on 1 GB300; % of bf16 peak / HBM BW"
 DEFAULT_WORKLOAD = "layer_train_t16384"
 
-# DRAM bytes per GMM launch (mean of the six launches of one training step),
-# from one ncu capture of the GMM sources with these hashes
-# (profiles/gmm_traffic_layer_train_t16384.md); reported only while they match.
-GMM_TRAFFIC = {
-    "workload": "layer_train_t16384",
-    "bytes_per_launch": 2.662e9,
-    "sources": {
-        "gmm.cu": "117c05934dbd56a5bd1f49ae969a92b8cb8c935318e38a6d472f6606b410e6b1",
-        "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
-        "common.cuh": "fbc79d491f1538425ee1b3279a36f2a75d6c88e0db0afb369ee31a45eddc731f",
-        "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365",
-    },
-}
+# DRAM bytes per GMM launch (the mean over one step's GMM launches), each from
+# one ncu capture of the sources with these hashes; reported only while they
+# match.  Training step: profiles/gmm_traffic_layer_train_t16384.md; MXFP8
+# layers: profiles/gmm_mx_kernel_layer_mx.md.
+GMM_TRAFFIC = [
+    {"workload": "layer_train_t16384", "bytes_per_launch": 2.662e9,
+     "sources": {
+         "gmm.cu": "117c05934dbd56a5bd1f49ae969a92b8cb8c935318e38a6d472f6606b410e6b1",
+         "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
+         "common.cuh": "fbc79d491f1538425ee1b3279a36f2a75d6c88e0db0afb369ee31a45eddc731f",
+         "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
+    {"workload": "layer_prefill_mx_t4096", "bytes_per_launch": 0.5175e9,
+     "sources": {
+         "gmm_mx.cu": "0c22e9589e9b48e4f61b983120a0aa205bffc132289c0713d2fcdfa71f5a22ef",
+         "common.cuh": "0e8e1d6ccc0f617f923f19edeb534bb6c5a39f113db927aaf3ef9c7640e44a17",
+         "mx.cuh": "4caee62e9ee7559f559d88b7d1888a53a079990c60f159099528049978f1af23",
+         "tmap.cu": "114b607e1a16bc20a94fdeaa36498f25731956da5ecab16f303468d3ce0e9d49"}},
+    {"workload": "layer_decode_mx_t64", "bytes_per_launch": 0.3665e9,
+     "sources": {
+         "gmm_mx.cu": "0c22e9589e9b48e4f61b983120a0aa205bffc132289c0713d2fcdfa71f5a22ef",
+         "common.cuh": "0e8e1d6ccc0f617f923f19edeb534bb6c5a39f113db927aaf3ef9c7640e44a17",
+         "mx.cuh": "4caee62e9ee7559f559d88b7d1888a53a079990c60f159099528049978f1af23",
+         "tmap.cu": "114b607e1a16bc20a94fdeaa36498f25731956da5ecab16f303468d3ce0e9d49"}},
+]
 
 
 def measured_gmm_traffic(workload):
     import hashlib
-    if workload != GMM_TRAFFIC["workload"]:
-        return None
     csrc = os.path.join(ROOT, "moe_routed_expert_gb300", "csrc")
-    for name, digest in GMM_TRAFFIC["sources"].items():
-        with open(os.path.join(csrc, name), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != digest:
-                return None
-    return GMM_TRAFFIC["bytes_per_launch"]
+    for entry in GMM_TRAFFIC:
+        if entry["workload"] != workload:
+            continue
+        for name, digest in entry["sources"].items():
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        return entry["bytes_per_launch"]
+    return None
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -727,7 +740,8 @@ def main():
         achieved = gbytes / (gmm_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_gmm_traffic(args.workload) if args.tokens is None else None,
                 "kernel": getattr(step, "kernel", "gmm_kernel (all GMM launches of a step)"),
                 "peak_kind": "hbm copy, %s" % peaks["source"]}
     else:

@@ -28,6 +28,11 @@ Sources (page title, then section):
 * [MegaMoE] "A8W4-FP 量化场景": the same four stages with MXFP4 (FLOAT4_E2M1)
   weights for both matmuls and E4M3 tokens / activations (the data flow BF16 ->
   MXFP8 E4M3 -> A8W4 GMM1 -> MXFP8 E4M3 -> A8W4 GMM2 -> BF16).
+* [MegaMoE] "A4W4-FP 量化场景": the tokens are quantised to MXFP4 (E2M1
+  elements, E8M0 scales, groups of 32), GMM1 multiplies MXFP4 tokens by MXFP4
+  weights, the activation is quantised to MXFP8 E4M3 (not E2M1, to keep the
+  second matmul's precision), so GMM2 is A8W4 (the data flow BF16 -> MXFP4
+  E2M1 -> A4W4 GMM1 -> MXFP8 E4M3 -> A8W4 GMM2 -> BF16).
 * The element and scale formats are the ones the pages name by type:
   FLOAT8_E4M3FN (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
   infinities, S.1111.111 is NaN, largest finite 448), FLOAT8_E5M2 (bias 15,
@@ -56,6 +61,10 @@ M6. E2M1 has no NaN: a NaN value encodes as the largest magnitude (code 7,
     or 15 with its sign); emax = 2 (the largest power of two, 4).  Codes are
     held one per array element here; the CUDA path takes them packed two per
     byte (a layout, see workloads.pack_fp4).
+M7. The activation is quantised in the tokens' element type when that is an
+    fp8 type, and in E4M3 when the tokens are E2M1 (the A4W4-FP rule above).
+    Other pairings of token and weight types than the pages' four scenarios
+    follow the same stages (the matmul takes any pair).
 """
 from __future__ import annotations
 
@@ -65,7 +74,7 @@ from .moe_oracle import (activation, gated_activation, gmm_forward, moe_permute,
 
 __all__ = [
     "FP8_FORMATS", "fp8_decode", "fp8_encode", "fp8_finite_values", "e8m0_decode",
-    "mx_quantize", "mx_dequantize", "mx_gmm", "mx_layer_forward", "MX_BLOCK",
+    "mx_quantize", "mx_dequantize", "mx_gmm", "mx_layer_forward", "activation_format", "MX_BLOCK",
 ]
 
 MX_BLOCK = 32
@@ -181,9 +190,14 @@ def mx_gmm(xq, xs, wq, ws, group_list, x_fmt, w_fmt, store=round_to_bf16):
     return gmm_forward(x, np.ascontiguousarray(np.transpose(w, (0, 2, 1))), group_list, store)
 
 
+def activation_format(x_fmt):
+    """The element type of the quantised activation (reading M7)."""
+    return "e4m3" if x_fmt == "e2m1" else x_fmt
+
+
 def mx_layer_forward(x, topk_ids, topk_w, w1q, w1s, w2q, w2s, x_fmt="e4m3", w_fmt="e4m3", act=None,
                      store=round_to_bf16):
-    """The four stages of the A8W8-FP forward on one device.
+    """The four stages of the A8W8-FP / A8W4-FP / A4W4-FP forward on one device.
 
     x: bf16-valued [T, H]; w1q [E, 2I, H] / w1s [E, 2I, H/32]; w2q [E, H, I] /
     w2s [E, H, I/32].  Returns (y [T, H], saved) with the intermediates."""
@@ -196,8 +210,9 @@ def mx_layer_forward(x, topk_ids, topk_w, w1q, w1s, w2q, w2s, x_fmt="e4m3", w_fm
     xq, xs = mx_quantize(x_perm, x_fmt)                                   # stage 1
     h = mx_gmm(xq, xs, w1q, w1s, group_list, x_fmt, w_fmt, store=round_to_bf16)  # G | U, bf16 (M3)
     a = gated_activation(h, act, store=None)                              # stage 2
-    aq, as_ = mx_quantize(a, x_fmt)
-    o = mx_gmm(aq, as_, w2q, w2s, group_list, x_fmt, w_fmt, store=store)  # stage 3 (M4)
+    a_fmt = activation_format(x_fmt)
+    aq, as_ = mx_quantize(a, a_fmt)
+    o = mx_gmm(aq, as_, w2q, w2s, group_list, a_fmt, w_fmt, store=store)  # stage 3 (M4)
     y = moe_unpermute(o, row_id_map, topk_w, T, k, store=store)           # stage 4
     saved = dict(x_perm=x_perm, group_list=group_list, row_id_map=row_id_map, xq=xq, xs=xs,
                  h=h, a=a, aq=aq, as_=as_, o=o)

@@ -13,6 +13,7 @@ things other than itself.
 - The MX grouped matmul against a torch float64 matmul of torch-dequantised
   operands, and the MX layer against a per-token evaluation of the four stages
   that takes no permute at all.
+- A4W4-FP: the per-token layer pin with E2M1 tokens and an E4M3 activation.
 - FLOAT4_E2M1 ("MegaMoE", A8W4-FP 量化场景): the 16 codes against the type's
   eight magnitudes, ties to the even code, saturation at 6, hand-computed Q_MX
   groups, and the same error bound, exactness, GMM and per-token layer pins
@@ -218,8 +219,14 @@ def test_mx_gmm_against_torch_dequant_matmul():
         assert np.allclose(got[off[g]:off[g + 1]], want, rtol=1e-12, atol=0)
 
 
-@pytest.mark.parametrize("w_fmt", ["e4m3", "e2m1"])
-def test_mx_layer_matches_per_token_stages(w_fmt):
+# (token type, weight type, activation type): A8W8-FP, A8W4-FP, A4W4-FP, whose
+# activation is E4M3 although its tokens are E2M1 ("MegaMoE", A4W4-FP 量化场景)
+LAYER_FORMATS = [("e4m3", "e4m3", "e4m3"), ("e5m2", "e5m2", "e5m2"), ("e4m3", "e2m1", "e4m3"),
+                 ("e2m1", "e2m1", "e4m3")]
+
+
+@pytest.mark.parametrize("x_fmt,w_fmt,a_fmt", LAYER_FORMATS)
+def test_mx_layer_matches_per_token_stages(x_fmt, w_fmt, a_fmt):
     """Stage by stage for each token on its own: quantise the token's row, the
     gate_up product with expert e's weights, bf16, the activation, quantise,
     the down product, bf16, then the weighted sum over its k slots."""
@@ -233,7 +240,7 @@ def test_mx_layer_matches_per_token_stages(w_fmt):
     w1q, w1s = X.mx_quantize(w1, w_fmt)
     w2q, w2s = X.mx_quantize(w2, w_fmt)
     act = O.activation("swiglu", [7.0])
-    y, _ = X.mx_layer_forward(x, ids, tw, w1q, w1s, w2q, w2s, "e4m3", w_fmt, act)
+    y, saved = X.mx_layer_forward(x, ids, tw, w1q, w1s, w2q, w2s, x_fmt, w_fmt, act)
     w1d = _torch_dequant(w1q, w1s, w_fmt)
     w2d = _torch_dequant(w2q, w2s, w_fmt)
     want = np.zeros((T, H))
@@ -243,17 +250,19 @@ def test_mx_layer_matches_per_token_stages(w_fmt):
             e = ids[t, j]
             if e < 0:
                 continue
-            xq, xs = X.mx_quantize(x[t:t + 1], "e4m3")
-            xr = _torch_dequant(xq, xs, "e4m3")
+            xq, xs = X.mx_quantize(x[t:t + 1], x_fmt)
+            xr = _torch_dequant(xq, xs, x_fmt)
             h = O.round_to_bf16(xr @ w1d[e].T)
             g, u = h[:, :I], h[:, I:]
             gc = np.minimum(g, 7.0)
             a = gc / (1 + np.exp(-gc)) * np.clip(u, -7.0, 7.0)
-            aq, as_ = X.mx_quantize(a, "e4m3")
-            o = O.round_to_bf16(_torch_dequant(aq, as_, "e4m3") @ w2d[e].T)
+            aq, as_ = X.mx_quantize(a, a_fmt)
+            o = O.round_to_bf16(_torch_dequant(aq, as_, a_fmt) @ w2d[e].T)
             acc += float(tw[t, j]) * o[0]
         want[t] = O.round_to_bf16(acc)
     assert np.array_equal(y, want)
+    # the quantised activation holds codes of a_fmt: E2M1 codes stop at 15
+    assert saved["aq"].max() > 15 or a_fmt == "e2m1"
 
 
 def test_mx_layer_close_to_unquantised_layer():

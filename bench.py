@@ -299,9 +299,9 @@ class LayerFwdStep(LayerTrainStep):
 
 
 class LayerMxStep:
-    """The MXFP8 (A8W8-FP) layer forward as the calls moe_layer_forward_mx makes:
-    quantising permute, block-scaled gate_up GMM with the activation and Q_MX in
-    its epilogue, block-scaled down GMM, combine."""
+    """The MX layer forward (A8W8-FP, A8W4-FP, A4W4-FP) as the calls
+    moe_layer_forward_mx makes: quantising permute, block-scaled gate_up GMM with
+    the activation and Q_MX in its epilogue, block-scaled down GMM, combine."""
 
     def __init__(self, wl, dev, inp):
         import torch
@@ -314,10 +314,12 @@ class LayerMxStep:
         self.ids = torch.from_numpy(inp["topk_ids"]).to(dev)
         self.tw = torch.from_numpy(inp["topk_w"]).to(dev)
         self.wfmt = wl.w_mx or wl.mx
+        self.afmt = M.activation_format(wl.mx)
         pk = (lambda a: pack_fp4(a)) if self.wfmt == "e2m1" else (lambda a: a)   # E2M1: two codes per byte
         self.w1q, self.w2q = (torch.from_numpy(pk(inp[n])).to(dev) for n in ("w1_q", "w2_q"))
         self.w1s, self.w2s = (torch.from_numpy(inp[n]).to(dev) for n in ("w1_s", "w2_s"))
-        self.xq = torch.empty(R, H, dtype=u8, device=dev)
+        xb = 0.5 if wl.mx == "e2m1" else 1.0
+        self.xq = torch.empty(R, int(H * xb), dtype=u8, device=dev)
         self.xs = torch.empty(R, H // 32, dtype=u8, device=dev)
         self.gl = torch.empty(E, dtype=torch.int64, device=dev)
         self.rmap = torch.empty(R, dtype=torch.int32, device=dev)
@@ -343,12 +345,14 @@ class LayerMxStep:
         # algorithmic bytes: weights (fp8, or E2M1 at half a byte) and their scales of the
         # non-empty experts, operands in and results out once
         wb = 0.5 if self.wfmt == "e2m1" else 1.0
-        self.gmm_bytes = {"gmm_mx_gate_up_act_quant": live * 2 * I * (wb * H + H // 32) + Rr * (H + H // 32)
+        self.gmm_bytes = {"gmm_mx_gate_up_act_quant": live * 2 * I * (wb * H + H // 32) + Rr * (xb * H + H // 32)
                           + Rr * (I + I // 32),
                           "gmm_mx_down": live * H * (wb * I + I // 32) + Rr * (I + I // 32) + Rr * H * 2}
         self.units = T
         self.unit = "tokens/s"
-        self.dtype = "mxfp8_" + wl.mx + ("_w" + self.wfmt if self.wfmt != wl.mx else "")
+        self.dtype = (("mxfp4_" if wl.mx == "e2m1" else "mxfp8_") + wl.mx
+                      + ("_w" + self.wfmt if self.wfmt != wl.mx else "")
+                      + ("_a" + self.afmt if self.afmt != wl.mx else ""))
         self.kernel = "gmm_mx_kernel (both block-scaled GMM launches of a step)"
 
     def permute(self):
@@ -360,7 +364,7 @@ class LayerMxStep:
                               activation=self.act, a_q=self.aq, a_scales=self.as_, ws=self.ws)
 
     def gmm2(self):
-        self.M.gmm_forward_mx(self.aq, self.as_, self.w2q, self.w2s, self.gl, x_fmt=self.wl.mx, w_fmt=self.wfmt,
+        self.M.gmm_forward_mx(self.aq, self.as_, self.w2q, self.w2s, self.gl, x_fmt=self.afmt, w_fmt=self.wfmt,
                               y=self.o, ws=self.ws)
 
     def combine(self):
@@ -574,7 +578,8 @@ def cpu_sample(name, inp, target_s=15.0):
     desc = ("first %d of %d tokens, slots of experts 0..%d of %d kept (%d routed rows = %.0f token-equivalents "
             "at k=%d), layer fwd%s%s in float64" % (T_s, wl.T, E_s - 1, wl.E, rows, tok_eq, wl.k,
                                                     "+bwd" if wl.backward else "",
-                                                    " (MXFP8 %s, quantisation included)" % wl.mx if wl.mx else ""))
+                                                    " (MX tokens %s, weights %s, quantisation included)" % (wl.mx, wl.w_mx or wl.mx)
+                                                    if wl.mx else ""))
     return tok_eq / dt, "tokens/s", desc, dt, (lambda: run(wl, sub)), tok_eq
 
 

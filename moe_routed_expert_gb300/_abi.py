@@ -23,7 +23,7 @@ STATUS_NAMES = {
 }
 
 
-FP8_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 5}  # moe_fp8_format_t (e2m1: weights only)
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 5}  # moe_fp8_format_t (e2m1: packed two per byte)
 
 ACTIVATIONS = {"swiglu": 0, "swiglustep": 1, "swigluoai": 2, "situglu": 3}  # moe_act_kind_t
 

@@ -395,16 +395,27 @@ U8 = torch.uint8
 
 def _fmt(name):
     if name not in _abi.FP8_FORMATS:
-        raise ValueError("unknown fp8 format %r (e4m3 or e5m2)" % (name,))
+        raise ValueError("unknown MX element format %r (e4m3, e5m2 or e2m1)" % (name,))
     return _abi.FP8_FORMATS[name]
 
 
+def _code_cols(K: int, fmt: str) -> int:
+    """Bytes per row of K codes: E2M1 packs two per byte."""
+    return K // 2 if fmt == "e2m1" else K
+
+
+def activation_format(x_fmt: str) -> str:
+    """The element type gmm_forward_mx quantises the activation to: the tokens'
+    fp8 type, or E4M3 after E2M1 tokens ("MegaMoE", A4W4-FP 量化场景)."""
+    return "e4m3" if x_fmt == "e2m1" else x_fmt
+
+
 def moe_mx_quantize(x, fmt: str = "e4m3", *, q=None, scales=None, ws: Optional[Workspace] = None, stream=None):
-    """Q_MX of each row of x [rows, K] bf16: (q [rows, K] uint8 codes,
-    scales [rows, K/32] uint8 E8M0 codes)."""
+    """Q_MX of each row of x [rows, K] bf16: (q [rows, K] uint8 codes, or
+    [rows, K/2] packed E2M1, scales [rows, K/32] uint8 E8M0 codes)."""
     _dtype(x, BF16, "x")
     rows, K = x.shape
-    q = torch.empty(rows, K, dtype=U8, device=x.device) if q is None else q
+    q = torch.empty(rows, _code_cols(K, fmt), dtype=U8, device=x.device) if q is None else q
     scales = torch.empty(rows, K // 32, dtype=U8, device=x.device) if scales is None else scales
     _dtype(q, U8, "q")
     _dtype(scales, U8, "scales")
@@ -415,15 +426,17 @@ def moe_mx_quantize(x, fmt: str = "e4m3", *, q=None, scales=None, ws: Optional[W
 
 
 def moe_permute_mx(x, topk_ids, E: int, fmt: str = "e4m3", *, out=None, ws: Optional[Workspace] = None, stream=None):
-    """moe_permute whose gathered rows leave quantised: returns (x_q [T*k, H] uint8,
-    x_scales [T*k, H/32] uint8, group_list, row_id_map, sorted_flat)."""
+    """moe_permute whose gathered rows leave quantised: returns (x_q [T*k, H] uint8
+    ([T*k, H/2] packed E2M1), x_scales [T*k, H/32] uint8, group_list, row_id_map,
+    sorted_flat)."""
     _dtype(x, BF16, "x")
     _dtype(topk_ids, torch.int32, "topk_ids")
     T, k = topk_ids.shape
     H = x.shape[1]
     dev = topk_ids.device
     if out is None:
-        out = (torch.empty(T * k, H, dtype=U8, device=dev), torch.empty(T * k, H // 32, dtype=U8, device=dev),
+        out = (torch.empty(T * k, _code_cols(H, fmt), dtype=U8, device=dev),
+               torch.empty(T * k, H // 32, dtype=U8, device=dev),
                torch.empty(E, dtype=torch.int64, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
                torch.empty(T * k, dtype=torch.int32, device=dev))
     x_q, x_s, group_list, row_id_map, sorted_flat = out
@@ -438,9 +451,11 @@ def gmm_forward_mx(x_q, x_scales, w_q, w_scales, group_list, *, x_fmt: str = "e4
                    activation=None, y=None, a_q=None, a_scales=None, h_save=None, ws: Optional[Workspace] = None,
                    stream=None):
     """Block-scaled grouped matmul: x_q [M, K] / x_scales [M, K/32], w_q [E, N, K] /
-    w_scales [E, N, K/32] (uint8 codes).  Without an activation returns y [M, N]
-    bf16; with one returns (a_q [M, N/2], a_scales [M, N/64]) in x_fmt."""
-    M, K = x_q.shape
+    w_scales [E, N, K/32] (uint8 codes; E2M1 operands packed, K/2 bytes a row).
+    Without an activation returns y [M, N] bf16; with one returns
+    (a_q [M, N/2], a_scales [M, N/64]) in activation_format(x_fmt)."""
+    M = x_q.shape[0]
+    K = x_scales.shape[1] * 32
     E, N, _ = w_q.shape
     for t, n in ((x_q, "x_q"), (x_scales, "x_scales"), (w_q, "w_q"), (w_scales, "w_scales")):
         _dtype(t, U8, n)
@@ -466,8 +481,9 @@ def moe_layer_mx_workspace_size(T, H, I, E, k) -> int:
 def moe_layer_forward_mx(x, topk_ids, topk_w, w1_q, w1_scales, w2_q, w2_scales, *, x_fmt: str = "e4m3",
                          w_fmt: str = "e4m3", activation="swiglu", y=None, ws: Optional[Workspace] = None,
                          stream=None):
-    """A8W8-FP layer forward: w1_q [E, 2I, H], w2_q [E, H, I] fp8 codes with their
-    [.., K/32] E8M0 scales; returns y [T, H] bf16."""
+    """MX layer forward (A8W8-FP, A8W4-FP with w_fmt "e2m1", A4W4-FP with x_fmt and
+    w_fmt "e2m1"): w1_q [E, 2I, H], w2_q [E, H, I] codes (E2M1 packed, half the
+    last dimension) with their [.., K/32] E8M0 scales; returns y [T, H] bf16."""
     T, H = x.shape
     E, I2, _ = w1_q.shape
     I = I2 // 2

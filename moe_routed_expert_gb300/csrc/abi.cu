@@ -477,10 +477,11 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
 // ------------------------------------------------------------------ MXFP8 forward (moe_mx.h)
 namespace moe {
 namespace {
-bool bad_fmt(int32_t f) { return f != MOE_FP8_E4M3 && f != MOE_FP8_E5M2; }
-bool bad_wfmt(int32_t f) { return bad_fmt(f) && f != MOE_FP4_E2M1; }
+bool bad_fmt(int32_t f) { return f != MOE_FP8_E4M3 && f != MOE_FP8_E5M2 && f != MOE_FP4_E2M1; }
+// the activation's element type: the tokens' fp8 type, E4M3 after E2M1 tokens (A4W4-FP)
+int32_t act_fmt(int32_t x_format) { return x_format == MOE_FP4_E2M1 ? MOE_FP8_E4M3 : x_format; }
 // the 4-bit TMA map wants a 32-byte-aligned base
-bool w_aligned(const void* w, int32_t f) {
+bool q_aligned(const void* w, int32_t f) {
   return (reinterpret_cast<uintptr_t>(w) & (f == MOE_FP4_E2M1 ? 31u : 15u)) == 0;
 }
 
@@ -544,14 +545,14 @@ moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales, const u
                             uint8_t* a_scales, moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x_q || !x_scales || !w_q || !w_scales || !group_list) return MOE_ERR_NULLPTR;
   if (activation ? (!a_q || !a_scales) : !y) return MOE_ERR_NULLPTR;
-  if (bad_fmt(x_format) || bad_wfmt(w_format)) return MOE_ERR_INVALID;
+  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
   Act act;
   moe_status_t st = activation ? resolve_act(activation, &act) : MOE_OK;
   if (st != MOE_OK) return st;
   if ((st = check_mx_gmm(M, K, N, E)) != MOE_OK) return st;
   if (activation && N % 256) return MOE_ERR_UNSUPPORTED;
   if (!activation && h_save) return MOE_ERR_INVALID;
-  if (!aligned16(x_q) || !aligned16(x_scales) || !w_aligned(w_q, w_format) || !aligned16(w_scales) ||
+  if (!q_aligned(x_q, x_format) || !aligned16(x_scales) || !q_aligned(w_q, w_format) || !aligned16(w_scales) ||
       (y && !aligned16(y)) || (a_q && !aligned16(a_q)) || (a_scales && !aligned16(a_scales)) ||
       (h_save && !aligned16(h_save)) || (reinterpret_cast<uintptr_t>(group_list) & 7u))
     return MOE_ERR_INVALID;
@@ -561,7 +562,7 @@ moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales, const u
   a.a = x_q; a.a_sf = x_scales; a.b = w_q; a.b_sf = w_scales; a.group_list = group_list;
   a.M = M; a.K = K; a.N = N; a.E = E; a.a_fmt = x_format; a.b_fmt = w_format;
   a.act = activation ? &act : nullptr;
-  a.out = y; a.aq = a_q; a.as = a_scales; a.out_fmt = x_format; a.h_save = h_save;
+  a.out = y; a.aq = a_q; a.as = a_scales; a.out_fmt = act_fmt(x_format); a.h_save = h_save;
   return launch_gmm_mx(a, status_of(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -576,16 +577,17 @@ moe_status_t moe_layer_forward_mx(const moe_bf16* x, const int32_t* topk_ids, co
                                   int32_t x_format, int32_t w_format, const moe_activation_t* activation,
                                   moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!x || !topk_ids || !topk_w || !w1_q || !w1_scales || !w2_q || !w2_scales || !y) return MOE_ERR_NULLPTR;
-  if (bad_fmt(x_format) || bad_wfmt(w_format)) return MOE_ERR_INVALID;
+  if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
   if (st != MOE_OK) return st;
   if ((st = check_layer(T, H, I, E, k)) != MOE_OK) return st;
   if (H % 128) return MOE_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !w_aligned(w1_q, w_format) || !aligned16(w1_scales) || !w_aligned(w2_q, w_format) ||
+  if (!aligned16(x) || !q_aligned(w1_q, w_format) || !aligned16(w1_scales) || !q_aligned(w2_q, w_format) ||
       !aligned16(w2_scales) || !aligned16(y))
     return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, moe_layer_mx_workspace_size(T, H, I, E, k))) != MOE_OK) return st;
+  if (!q_aligned(ws, x_format)) return MOE_ERR_INVALID;  // the packed E2M1 tokens live in ws
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t* status = status_of(ws);
@@ -606,11 +608,11 @@ moe_status_t moe_layer_forward_mx(const moe_bf16* x, const int32_t* topk_ids, co
   MxGmmArgs g1{};
   g1.a = xq; g1.a_sf = xs; g1.b = w1_q; g1.b_sf = w1_scales; g1.group_list = gl;
   g1.M = R; g1.K = H; g1.N = 2 * I; g1.E = E; g1.a_fmt = x_format; g1.b_fmt = w_format;
-  g1.act = &act; g1.aq = aq; g1.as = as; g1.out_fmt = x_format;
+  g1.act = &act; g1.aq = aq; g1.as = as; g1.out_fmt = act_fmt(x_format);
   if ((st = launch_gmm_mx(g1, status, s)) != MOE_OK) return st;
   MxGmmArgs g2{};
   g2.a = aq; g2.a_sf = as; g2.b = w2_q; g2.b_sf = w2_scales; g2.group_list = gl;
-  g2.M = R; g2.K = I; g2.N = H; g2.E = E; g2.a_fmt = x_format; g2.b_fmt = w_format;
+  g2.M = R; g2.K = I; g2.N = H; g2.E = E; g2.a_fmt = act_fmt(x_format); g2.b_fmt = w_format;
   g2.out = o;
   if ((st = launch_gmm_mx(g2, status, s)) != MOE_OK) return st;
   return launch_unpermute(o, rmap, topk_w, T, H, k, y, status, s);

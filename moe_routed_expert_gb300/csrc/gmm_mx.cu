@@ -5,16 +5,17 @@
 //   P_e = DQ_MX(X_e) DQ_MX(W_e)^T
 // with W_e = weight[e] stored [N, K] (one output channel per row) and one E8M0
 // scale per 32 elements of K on both sides, as the page's MXFP constraints lay
-// out weight1 / weight2 and weightScales1 / weightScales2.  The weights may be
-// FLOAT4_E2M1 ("A8W4-FP 量化场景"): packed two per byte in HBM, expanded by the
-// TMA unit to the 16-byte-granule form the MMA reads, so a stage of B has the
-// same shared-memory footprint and descriptors as with fp8.  Epilogues:
+// out weight1 / weight2 and weightScales1 / weightScales2.  The weights
+// ("A8W4-FP 量化场景") and the tokens ("A4W4-FP 量化场景") may be FLOAT4_E2M1:
+// packed two per byte in HBM, expanded by the TMA unit to the 16-byte-granule
+// form the MMA reads, so a stage has the same shared-memory footprint and
+// descriptors as with fp8.  Epilogues:
 //   plain  (stage 3)  O_e = bf16(P_e);
 //   ACT    (stage 2)  H = bf16(P_e) split into gate (first N/2 channels) and
 //                     up (last N/2), A = Activation(G, U), then Q_MX(A): fp8
 //                     codes and scales of the next matmul's operand.
 //
-// Design (one CTA per SM, 192 threads; 128 x 256 output tiles, K in blocks
+// Design (one CTA per SM, 320 threads; 128 x 256 output tiles, K in blocks
 // of 128 fp8 elements = one 128-byte swizzle row):
 //   warp 0      producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
@@ -94,7 +95,7 @@ struct MxParams {
   uint16_t* h_save;      // ACT: optional bf16 [M, N]
   Act act;
   uint32_t idesc;
-  uint32_t b_bytes;      // bytes a stage's B copy delivers: E2M1 weights count their packed size
+  uint32_t tx_bytes;     // bytes a stage's A and B copies deliver: E2M1 operands count their packed size
   uint32_t* status;
 };
 
@@ -306,7 +307,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const uint32_t a_dst = stage_base + s * STAGE_BYTES;
         const uint32_t b_dst = a_dst + A_BYTES;
         const TileInfo& ti = cur.ti;
-        mbar_expect_tx(bar, A_BYTES + p.b_bytes);
+        mbar_expect_tx(bar, p.tx_bytes);
         tma_load_2d(a_dst, &tmA, bar, cur.kb * BK, static_cast<int32_t>(ti.row0));
         if (EPI == MX_ACT) {  // 128 gate channels, then the 128 matching up channels
           tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
@@ -502,8 +503,9 @@ moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s)
   p.kblocks = static_cast<int>(x.K / BK);
   p.status = status;
   p.idesc = idesc_mxf8(BM, BN, x.a_fmt, x.b_fmt);
-  // the 4-bit map fills the same 32 KB of shared memory but counts the packed bytes it read
-  p.b_bytes = x.b_fmt == MOE_FP4_E2M1 ? B_BYTES / 2 : B_BYTES;
+  // a 4-bit map fills the same shared memory as an fp8 one but counts the packed bytes it read
+  const bool a_fp4 = (x.a_fmt == MOE_FP4_E2M1), b_fp4 = (x.b_fmt == MOE_FP4_E2M1);
+  p.tx_bytes = (a_fp4 ? A_BYTES / 2 : A_BYTES) + (b_fp4 ? B_BYTES / 2 : B_BYTES);
   const bool act = x.act != nullptr;
   p.out_cols = static_cast<int>(act ? x.N / 2 : x.N);
   p.tile_cols = act ? static_cast<int>((x.N / 2) / (BN / 2)) : static_cast<int>((x.N + BN - 1) / BN);
@@ -513,8 +515,7 @@ moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s)
   p.h_save = x.h_save;
   if (act) p.act = *x.act;
   CUtensorMap ta, tb;
-  const bool b_fp4 = (x.b_fmt == MOE_FP4_E2M1);
-  if (!make_map_2d_u8(&ta, x.a, x.M, x.K, BM) ||
+  if (!(a_fp4 ? make_map_2d_fp4(&ta, x.a, x.M, x.K, BM) : make_map_2d_u8(&ta, x.a, x.M, x.K, BM)) ||
       !(b_fp4 ? make_map_3d_fp4(&tb, x.b, x.E, x.N, x.K, act ? BN / 2 : BN)
               : make_map_3d_u8(&tb, x.b, x.E, x.N, x.K, act ? BN / 2 : BN)))
     return MOE_ERR_CUDA;

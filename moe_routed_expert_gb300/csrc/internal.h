@@ -78,6 +78,7 @@ bool make_map_2d_u8(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t
 bool make_map_3d_u8(::CUtensorMap_st* m, const void* base, int64_t E, int64_t R, int64_t C, int box_rows);
 // packed 4-bit codes, expanded to the 16-byte-granule shared-memory form
 bool make_map_3d_fp4(::CUtensorMap_st* m, const void* base, int64_t E, int64_t R, int64_t C, int box_rows);
+bool make_map_2d_fp4(::CUtensorMap_st* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
 // ---- grouped matmul (gmm.cu, gmm_pair.cu)
 enum GmmMode { GMM_FWD = 0, GMM_DX = 1, GMM_DW = 2, GMM_BWD = 3 /* dX and dW in one launch (pairs) */ };

@@ -1,11 +1,12 @@
-// Q_MX of bf16 rows ("MegaMoE", "A8W8-FP 量化场景", stage 1): the standalone
-// row quantiser and the permute's quantising gather, which writes the rows of
-// each expert straight into fp8 codes and E8M0 scales.  HBM-bound: per row,
-// K*2 bytes read, K + K/32 bytes written.
+// Q_MX of bf16 rows ("MegaMoE", "A8W8-FP 量化场景" and "A4W4-FP 量化场景",
+// stage 1): the standalone row quantiser and the permute's quantising gather,
+// which writes the rows of each expert straight into fp8 / fp4 codes and E8M0
+// scales.  HBM-bound: per row, K*2 bytes read, K (fp4: K/2) + K/32 written.
 //
 // One warp per (row, 1024-element segment): lane l quantises group l of the
 // segment from its 64 contiguous bytes, writes its 32 codes as two 16-byte
-// stores and its scale byte (the warp's 32 scale bytes are contiguous).
+// stores (E2M1: one, two codes per byte, rows of K/2 bytes) and its scale byte
+// (the warp's 32 scale bytes are contiguous).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,11 +56,18 @@ __global__ void __launch_bounds__(THREADS) mx_rows_kernel(const uint16_t* __rest
         v[8 * u + 2 * i + 1] = bf16_hi(ws[i]);
       }
     }
-    uint32_t c[8];
-    const uint32_t sc = mx_quant32<FMT>(v, c);
-    uint4* d = reinterpret_cast<uint4*>(q + dst_row * K + grp * 32);
-    d[0] = make_uint4(c[0], c[1], c[2], c[3]);
-    d[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    uint32_t sc;
+    if constexpr (FMT == MOE_FP4_E2M1) {
+      uint32_t c[4];
+      sc = mx_quant32_fp4(v, c);
+      *reinterpret_cast<uint4*>(q + dst_row * (K / 2) + grp * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+    } else {
+      uint32_t c[8];
+      sc = mx_quant32<FMT>(v, c);
+      uint4* d = reinterpret_cast<uint4*>(q + dst_row * K + grp * 32);
+      d[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      d[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    }
     scales[dst_row * groups + grp] = static_cast<uint8_t>(sc);
   }
 }
@@ -73,11 +81,16 @@ moe_status_t launch_rows(const uint16_t* x, int64_t n, int64_t K, const int32_t*
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const dim3 grid(static_cast<unsigned>(blocks));
-  cudaError_t e = fmt == MOE_FP8_E5M2
-                      ? launch_pdl(mx_rows_kernel<MOE_FP8_E5M2, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K,
-                                   row_id_map, k, q, scales)
-                      : launch_pdl(mx_rows_kernel<MOE_FP8_E4M3, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K,
-                                   row_id_map, k, q, scales);
+  cudaError_t e;
+  if (fmt == MOE_FP8_E5M2)
+    e = launch_pdl(mx_rows_kernel<MOE_FP8_E5M2, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
+                   scales);
+  else if (fmt == MOE_FP4_E2M1)
+    e = launch_pdl(mx_rows_kernel<MOE_FP4_E2M1, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
+                   scales);
+  else
+    e = launch_pdl(mx_rows_kernel<MOE_FP8_E4M3, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
+                   scales);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -1,14 +1,16 @@
 // MX (microscaling) quantisation of 32-element groups, as "MegaMoE",
-// "A8W8-FP 量化场景" uses it: a shared E8M0 exponent per group and FP8
-// (E4M3FN or E5M2) elements.
+// "A8W8-FP 量化场景" and "A4W4-FP 量化场景" use it: a shared E8M0 exponent per
+// group and FP8 (E4M3FN or E5M2) or FP4 (E2M1) elements.
 //
-// Shared exponent: X = 2^(floor(log2 amax) - emax), emax = 8 (E4M3) or 15
-// (E5M2), clamped below at 2^-127; a group holding an infinity or a NaN gets
-// the NaN scale 0xFF.  Elements: x / X rounded to nearest even with
-// saturation to the largest finite value (the hardware's satfinite convert).
+// Shared exponent: X = 2^(floor(log2 amax) - emax), emax = 8 (E4M3), 15
+// (E5M2) or 2 (E2M1), clamped below at 2^-127; a group holding an infinity or
+// a NaN gets the NaN scale 0xFF.  Elements: x / X rounded to nearest even with
+// saturation to the largest finite value (the hardware's satfinite convert;
+// E2M1 has no NaN, and a NaN converts to the largest positive code, 7).
 // floor(log2 amax) is read off amax's exponent field, so the decision is exact.
 #pragma once
 
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -27,6 +29,11 @@ template <>
 struct Fp8Fmt<MOE_FP8_E5M2> {
   static constexpr int emax = 15;
   static constexpr __nv_fp8_interpretation_t kind = __NV_E5M2;
+};
+
+template <>
+struct Fp8Fmt<MOE_FP4_E2M1> {
+  static constexpr int emax = 2;
 };
 
 // E8M0 code of a group whose largest magnitude has bit pattern `amax_bits`
@@ -63,6 +70,27 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
 #pragma unroll
   for (int w = 0; w < 8; ++w)
     q[w] = fp8x2<FMT>(v[4 * w] * inv, v[4 * w + 1] * inv) | (fp8x2<FMT>(v[4 * w + 2] * inv, v[4 * w + 3] * inv) << 16);
+  return sc;
+}
+
+// Quantise 32 values to E2M1: element i in nibble i % 8 of word i / 8 (two
+// elements per byte, the first in the low nibble); returns the scale code.
+__device__ __forceinline__ uint32_t mx_quant32_fp4(const float (&v)[32], uint32_t (&q)[4]) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  float inv;
+  const uint32_t sc = mx_scale_code<MOE_FP4_E2M1>(amax, inv);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 pr = make_float2(v[8 * w + 2 * b] * inv, v[8 * w + 2 * b + 1] * inv);
+      word |= static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(pr, __NV_E2M1, cudaRoundNearest)) << (8 * b);
+    }
+    q[w] = word;
+  }
   return sc;
 }
 

@@ -177,7 +177,7 @@ def test_mx_entry_points_check_their_arguments(lib):
     assert lib.moe_mx_quantize(None, 0, 64, 1, None, None, ws, nws, None) == 0
     # permute_mx
     assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 2, 4, 0, None, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 1
-    assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 2, 4, 5, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2
+    assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 2, 4, 7, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2
     assert lib.moe_permute_mx(FAKE, FAKE, 4, 48, 2, 4, 0, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 3
     assert lib.moe_permute_mx(FAKE, FAKE, 4, 64, 5, 4, 0, FAKE, FAKE, FAKE, FAKE, FAKE, ws, nws, None) == 2
     # gmm_forward_mx: plain needs y, activation needs a_q / a_scales; K and N multiples of 128
@@ -193,11 +193,12 @@ def test_mx_entry_points_check_their_arguments(lib):
     assert lib.gmm_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 256, 4, 3, 0, None, FAKE, None, None, None,
                               ws, nws, None) == 2                    # format
     assert gm(0, 128, 256, None, FAKE, None, None, None) == 0        # no rows: nothing to do
-    # E2M1 is a weight format only, and its packed weights want a 32-byte-aligned base
-    e2m1 = lambda xf, w: lib.gmm_forward_mx(FAKE, FAKE, w, FAKE, FAKE, 64, 128, 256, 4, xf, 5, None, FAKE, None,
-                                            None, None, ws, nws, None)
-    assert e2m1(5, FAKE) == 2
-    assert e2m1(0, C.c_void_p(0x10010)) == 2
+    # packed E2M1 operands (weights, or A4W4 tokens) want a 32-byte-aligned base
+    e2m1 = lambda xf, x, w: lib.gmm_forward_mx(x, FAKE, w, FAKE, FAKE, 64, 128, 256, 4, xf, 5, None, FAKE, None,
+                                               None, None, ws, nws, None)
+    assert e2m1(0, FAKE, C.c_void_p(0x10010)) == 2
+    assert e2m1(5, C.c_void_p(0x10010), FAKE) == 2
+    assert e2m1(6, FAKE, FAKE) == 2                                  # E2M3 is not a format here
     # layer
     lay = lambda H, I, xf, act: lib.moe_layer_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, H, I, 4, 2,
                                                          xf, 0, act, FAKE, ws, nws, None)
@@ -205,6 +206,9 @@ def test_mx_entry_points_check_their_arguments(lib):
     assert lay(128, 128, 9, a) == 2
     assert lay(192, 128, 0, a) == 3                                   # H % 128
     assert lay(128, 64, 0, a) == 3                                    # I % 128
+    # A4W4: the packed tokens live in the workspace, which must then be 32-byte aligned
+    assert lib.moe_layer_forward_mx(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 128, 128, 4, 2, 5, 5, a, FAKE,
+                                    C.c_void_p(0x10010), 1 << 40, None) == 2
 
 
 def _abi_act(kind, *params):
@@ -214,3 +218,13 @@ def _abi_act(kind, *params):
     for i, v in enumerate(params):
         x.params[i] = v
     return C.byref(x)
+
+
+def test_fp4_packing_layout():
+    """E2M1 codes travel two per byte, element 2i in the low nibble (moe_mx.h)."""
+    import numpy as np
+    from workloads import pack_fp4, unpack_fp4
+    c = np.arange(16, dtype=np.uint8).reshape(1, 16)
+    p = pack_fp4(c)
+    assert p.tolist() == [[0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]]
+    assert np.array_equal(unpack_fp4(p), c)

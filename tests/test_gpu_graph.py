@@ -17,7 +17,8 @@ def _inputs(wl, seed):
     return layer_inputs(wl, seed=seed, with_weights=False)
 
 
-@pytest.mark.parametrize("name", ["layer_decode_t64", "layer_decode_mx_t64", "layer_decode_a8w4_t64"])
+@pytest.mark.parametrize("name", ["layer_decode_t64", "layer_decode_mx_t64", "layer_decode_a8w4_t64",
+                                  "layer_decode_a4w4_t64"])
 def test_layer_forward_replays_from_a_cuda_graph(name):
     import torch
     import moe_routed_expert_gb300 as M

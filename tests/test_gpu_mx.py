@@ -1,4 +1,5 @@
-"""Parity of the MXFP8 forward (include/moe_mx.h) with the oracle.
+"""Parity of the MX forward (include/moe_mx.h: A8W8-FP, A8W4-FP, A4W4-FP) with
+the oracle.
 
 - Q_MX of bf16 rows is exact arithmetic (an exponent read off amax, a scaling
   by a power of two, one rounding), so codes and scales must match the oracle
@@ -24,11 +25,11 @@ import oracle as O
 from oracle import mx_oracle as X
 from tests._util import assert_close, dev, dev_bf16, f64, host_f64
 from workloads import (WORKLOADS, fp8_codes, e8m0_codes, layer_inputs, mx_layer_weights, mx_weight, normal_bf16,
-                       pack_fp4)
+                       pack_fp4, unpack_fp4)
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["e4m3", "e5m2"]
+FMTS = ["e4m3", "e5m2", "e2m1"]
 
 
 def np_u8(t):
@@ -36,8 +37,13 @@ def np_u8(t):
 
 
 def w_dev(codes, fmt):
-    """Weight codes as the CUDA path takes them: E2M1 packed two per byte."""
+    """Codes as the CUDA path takes them: E2M1 packed two per byte."""
     return dev(pack_fp4(codes) if fmt == "e2m1" else codes)
+
+
+def codes_of(t, fmt):
+    """A device tensor of codes as one code per byte."""
+    return unpack_fp4(np_u8(t)) if fmt == "e2m1" else np_u8(t)
 
 
 def special_rows(fmt, K=256):
@@ -60,6 +66,9 @@ def special_rows(fmt, K=256):
 def compare_quant(q_gpu, s_gpu, x, fmt):
     q, s = X.mx_quantize(x, fmt)
     assert np.array_equal(s_gpu, s)
+    if fmt == "e2m1":        # no NaN code: every code of a NaN-scaled group is 7 on both sides
+        assert np.array_equal(q_gpu, q)
+        return
     nan_group = np.repeat(s == 255, 32, axis=-1)
     assert np.array_equal(q_gpu[~nan_group], q[~nan_group])
     assert np.all(np.isnan(X.fp8_decode(q_gpu[nan_group], fmt)))
@@ -75,7 +84,7 @@ def test_mx_quantize_bit_exact(fmt):
     for arr in (x, xs):
         bits = O.f64_to_bf16_bits(arr)
         q, s = M.moe_mx_quantize(dev_bf16(bits), fmt)
-        compare_quant(np_u8(q), np_u8(s), arr, fmt)
+        compare_quant(codes_of(q, fmt), np_u8(s), arr, fmt)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -92,7 +101,7 @@ def test_permute_mx(fmt):
     assert np.array_equal(host_f64(gl), counts)
     assert np.array_equal(host_f64(rmap), rmap_o)
     assert np.array_equal(host_f64(sflat)[:R], sflat_o)
-    compare_quant(np_u8(xq)[:R], np_u8(xs)[:R], x_perm, fmt)
+    compare_quant(codes_of(xq, fmt)[:R], np_u8(xs)[:R], x_perm, fmt)
 
 
 def mx_gmm_case(rng, E, K, N, counts, x_fmt, w_fmt):
@@ -114,6 +123,10 @@ GMM_CASES = [
     (4, 256, 384, [37, 0, 200, 91], "e4m3", "e2m1"),
     (3, 640, 512, [129, 64, 0], "e5m2", "e2m1"),
     (8, 1024, 768, [300, 0, 17, 512, 1, 0, 90, 256], "e4m3", "e2m1"),
+    # MXFP4 tokens, "A4W4-FP 量化场景" (and E2M1 tokens with fp8 weights)
+    (4, 256, 384, [37, 0, 200, 91], "e2m1", "e2m1"),
+    (3, 640, 512, [129, 64, 0], "e2m1", "e4m3"),
+    (8, 1024, 768, [300, 0, 17, 512, 1, 0, 90, 256], "e2m1", "e2m1"),
 ]
 
 
@@ -124,7 +137,7 @@ def test_gmm_forward_mx_plain(case):
     rng = np.random.default_rng(31)
     xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, N, counts, xf, wf)
     wsp = M.Workspace(256)
-    y = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
+    y = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
     assert M.read_status(wsp) == 0
     want = X.mx_gmm(xq, xs, wq, ws, gl, xf, wf)
     assert_close("y", y, want)
@@ -133,7 +146,7 @@ def test_gmm_forward_mx_plain(case):
 # Groups of a few rows, as in decode: many 128-row tiles that hold 0-12 rows,
 # one group over 32 rows, empty groups; N = 384 leaves a ragged 256-column tile.
 SMALL_COUNTS = [3, 0, 1, 40, 2, 0, 7, 1, 0, 5, 2, 2, 0, 9, 1, 1, 0, 3, 4, 0, 1, 1, 6, 0, 2, 3, 0, 1, 2, 0, 0, 12]
-SWAP_CASES = [("e4m3", "e4m3", 384), ("e5m2", "e5m2", 256), ("e4m3", "e2m1", 384)]
+SWAP_CASES = [("e4m3", "e4m3", 384), ("e5m2", "e5m2", 256), ("e4m3", "e2m1", 384), ("e2m1", "e2m1", 384)]
 
 
 @pytest.mark.parametrize("xf,wf,N", SWAP_CASES)
@@ -143,12 +156,12 @@ def test_gmm_forward_mx_small_groups_plain(xf, wf, N):
     E, K = len(SMALL_COUNTS), 512
     xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, N, SMALL_COUNTS, xf, wf)
     wsp = M.Workspace(256)
-    y = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
+    y = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
     assert M.read_status(wsp) == 0
     assert_close("y", y, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
 
 
-@pytest.mark.parametrize("xf,wf", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1")])
+@pytest.mark.parametrize("xf,wf", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1"), ("e2m1", "e2m1")])
 @pytest.mark.parametrize("act", [("swiglu", (7.0,)), ("situglu", (1.0, 2.0))], ids=lambda a: a[0])
 def test_gmm_forward_mx_small_groups_activation(act, xf, wf):
     import torch
@@ -159,11 +172,11 @@ def test_gmm_forward_mx_small_groups_activation(act, xf, wf):
     Mr = int(sum(SMALL_COUNTS))
     h = torch.empty(Mr, 2 * I, dtype=torch.bfloat16, device="cuda")
     wsp = M.Workspace(256)
-    aq, as_ = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf,
+    aq, as_ = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf,
                                activation=(act[0], list(act[1])), h_save=h, ws=wsp)
     assert M.read_status(wsp) == 0
     assert_close("h", h, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
-    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation(act[0], act[1]), xf)
+    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation(act[0], act[1]), X.activation_format(xf))
 
 
 def check_act_codes(aq, as_, h_gpu, act, fmt, rel=1e-5, abs_a=2e-6):
@@ -203,7 +216,7 @@ ACT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1")])
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1"), ("e2m1", "e2m1")])
 @pytest.mark.parametrize("act", ACT_CASES, ids=lambda a: a[0] + "".join("_%g" % v for v in a[1]))
 def test_gmm_forward_mx_activation(act, fmt, wfmt):
     import torch
@@ -215,12 +228,12 @@ def test_gmm_forward_mx_activation(act, fmt, wfmt):
     Mr = int(sum(counts))
     h = torch.empty(Mr, 2 * I, dtype=torch.bfloat16, device="cuda")
     wsp = M.Workspace(256)
-    aq, as_ = M.gmm_forward_mx(dev(xq), dev(xs), w_dev(wq, wfmt), dev(ws), dev(gl), x_fmt=fmt, w_fmt=wfmt,
+    aq, as_ = M.gmm_forward_mx(w_dev(xq, fmt), dev(xs), w_dev(wq, wfmt), dev(ws), dev(gl), x_fmt=fmt, w_fmt=wfmt,
                                activation=(act[0], list(act[1])), h_save=h, ws=wsp)
     assert M.read_status(wsp) == 0
     want_h = X.mx_gmm(xq, xs, wq, ws, gl, fmt, wfmt)
     assert_close("h", h, want_h)
-    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation(act[0], act[1]), fmt)
+    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation(act[0], act[1]), X.activation_format(fmt))
 
 
 def gpu_mx_chain(inp, wts, wl, fmt, act, wfmt=None):
@@ -234,13 +247,14 @@ def gpu_mx_chain(inp, wts, wl, fmt, act, wfmt=None):
     h = torch.empty(xq.shape[0], 2 * wl.I, dtype=torch.bfloat16, device="cuda")
     aq, as_ = M.gmm_forward_mx(xq, xs, w_dev(wts["w1_q"], wfmt), dev(wts["w1_s"]), gl, x_fmt=fmt, w_fmt=wfmt,
                                activation=act, h_save=h, ws=wsc)
-    o = M.gmm_forward_mx(aq, as_, w_dev(wts["w2_q"], wfmt), dev(wts["w2_s"]), gl, x_fmt=fmt, w_fmt=wfmt, ws=wsc)
+    o = M.gmm_forward_mx(aq, as_, w_dev(wts["w2_q"], wfmt), dev(wts["w2_s"]), gl, x_fmt=X.activation_format(fmt),
+                         w_fmt=wfmt, ws=wsc)
     y = M.moe_unpermute(o, rmap, tw, wl.T, wl.k, ws=wsc)
     assert M.read_status(wsc) == 0
     return dict(xq=xq, xs=xs, gl=gl, rmap=rmap, h=h, aq=aq, as_=as_, o=o, y=y)
 
 
-@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1")])
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1"), ("e2m1", "e2m1")])
 def test_layer_mx_small(fmt, wfmt):
     import moe_routed_expert_gb300 as M
     wl = WORKLOADS["layer_prefill_mx_t4096"]
@@ -259,10 +273,12 @@ def test_layer_mx_small(fmt, wfmt):
     oa = O.activation(*act)
     x_perm, counts, rmap_o, _ = O.moe_permute(f64(inp["x"]), inp["topk_ids"], wl.E)
     R = int(counts.sum())
-    compare_quant(np_u8(ch["xq"])[:R], np_u8(ch["xs"])[:R], x_perm, fmt)
-    assert_close("h", ch["h"], X.mx_gmm(np_u8(ch["xq"]), np_u8(ch["xs"]), wts["w1_q"], wts["w1_s"], counts, fmt, wfmt))
-    check_act_codes(np_u8(ch["aq"]), np_u8(ch["as_"]), host_f64(ch["h"]), oa, fmt)
-    o_want = X.mx_gmm(np_u8(ch["aq"]), np_u8(ch["as_"]), wts["w2_q"], wts["w2_s"], counts, fmt, wfmt)
+    xq = codes_of(ch["xq"], fmt)
+    compare_quant(xq[:R], np_u8(ch["xs"])[:R], x_perm, fmt)
+    assert_close("h", ch["h"], X.mx_gmm(xq, np_u8(ch["xs"]), wts["w1_q"], wts["w1_s"], counts, fmt, wfmt))
+    afmt = X.activation_format(fmt)
+    check_act_codes(np_u8(ch["aq"]), np_u8(ch["as_"]), host_f64(ch["h"]), oa, afmt)
+    o_want = X.mx_gmm(np_u8(ch["aq"]), np_u8(ch["as_"]), wts["w2_q"], wts["w2_s"], counts, afmt, wfmt)
     assert_close("o", ch["o"], o_want)
     # end to end
     y_want, _ = X.mx_layer_forward(f64(inp["x"]), inp["topk_ids"], inp["topk_w"], wts["w1_q"], wts["w1_s"],
@@ -271,7 +287,7 @@ def test_layer_mx_small(fmt, wfmt):
 
 
 @pytest.mark.parametrize("name", ["layer_prefill_mx_t4096", "layer_decode_mx_t64", "layer_prefill_a8w4_t4096",
-                                  "layer_decode_a8w4_t64"])
+                                  "layer_decode_a8w4_t64", "layer_prefill_a4w4_t4096", "layer_decode_a4w4_t64"])
 def test_layer_mx_full_size_sampled_tokens(name):
     """The bench's workloads through moe_layer_forward_mx; y of a sample of
     tokens against the oracle run on those tokens alone (a token's output

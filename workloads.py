@@ -35,6 +35,9 @@ layer_decode_mx_t64      the decode layer in MXFP8 (E4M3 tokens and weights)
 layer_prefill_a8w4_t4096 the prefill layer with E4M3 tokens, MXFP4 (E2M1)
                          weights
 layer_decode_a8w4_t64    the decode layer with E4M3 tokens, MXFP4 weights
+layer_prefill_a4w4_t4096 the prefill layer with MXFP4 tokens and weights
+                         (E4M3 activation)
+layer_decode_a4w4_t64    the decode layer with MXFP4 tokens and weights
 =======================  ====================================================
 
 MXFP8 weights are drawn directly as codes: N(0, 16^2) draws cast to the fp8
@@ -88,7 +91,7 @@ class LayerWorkload:
     clip: float
     hot_bias: float
     backward: bool
-    mx: str = ""   # "" (bf16 path) or the fp8 element type of the MXFP8 forward
+    mx: str = ""   # "" (bf16 path) or the tokens' element type in the MX forward
     w_mx: str = ""  # the weights' element type when it differs from mx ("e2m1": MXFP4)
 
     @property
@@ -116,6 +119,10 @@ WORKLOADS = {
                                               clip=0.0, hot_bias=0.0, backward=False, mx="e4m3", w_mx="e2m1"),
     "layer_decode_a8w4_t64": LayerWorkload("layer_decode_a8w4_t64", 4, T=64, H=2048, E=256, k=8, I=512,
                                            clip=0.0, hot_bias=0.0, backward=False, mx="e4m3", w_mx="e2m1"),
+    "layer_prefill_a4w4_t4096": LayerWorkload("layer_prefill_a4w4_t4096", 3, T=4096, H=2048, E=256, k=8, I=512,
+                                              clip=0.0, hot_bias=0.0, backward=False, mx="e2m1", w_mx="e2m1"),
+    "layer_decode_a4w4_t64": LayerWorkload("layer_decode_a4w4_t64", 4, T=64, H=2048, E=256, k=8, I=512,
+                                           clip=0.0, hot_bias=0.0, backward=False, mx="e2m1", w_mx="e2m1"),
 }
 
 
@@ -222,7 +229,10 @@ def layer_inputs(wl: LayerWorkload, seed: Optional[int] = None, tokens: Optional
 
 def fp8_codes(rng: np.random.Generator, shape, fmt: str = "e4m3", std: float = 16.0) -> np.ndarray:
     """N(0, std^2) draws cast to an fp8 type by torch's CPU conversion, as raw
-    uint8 codes (fmt "e4m3" = float8_e4m3fn or "e5m2")."""
+    uint8 codes (fmt "e4m3" = float8_e4m3fn or "e5m2"); for "e2m1", codes
+    uniform over all 16 (one per byte)."""
+    if fmt == "e2m1":
+        return rng.integers(0, 16, size=shape).astype(np.uint8)
     import torch
     dt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[fmt]
     a = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std)
@@ -252,6 +262,15 @@ def pack_fp4(codes: np.ndarray) -> np.ndarray:
     low nibble of byte i."""
     c = np.asarray(codes, dtype=np.uint8)
     return np.ascontiguousarray((c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)).astype(np.uint8)
+
+
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    """The inverse of pack_fp4: bytes [..., K/2] -> 4-bit codes [..., K]."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
 
 
 def mx_layer_weights(wl: LayerWorkload, seed: Optional[int] = None, fmt: Optional[str] = None) -> dict:

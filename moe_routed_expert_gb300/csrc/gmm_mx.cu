@@ -15,18 +15,21 @@
 //                     up (last N/2), A = Activation(G, U), then Q_MX(A): fp8
 //                     codes and scales of the next matmul's operand.
 //
-// Design (one CTA per SM, 320 threads; 128 x 256 output tiles, K in blocks
+// Design (one CTA per SM, 352 threads; 128 x 256 output tiles, K in blocks
 // of 128 fp8 elements = one 128-byte swizzle row):
-//   warp 0      producer.  Lane 0 issues the TMA copies of the A tile
+//   warp 0      tile producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
-//               4-stage ring.  All 32 lanes copy the stage's scales with
+//               4-stage ring.
+//   warp 10     scale producer.  All 32 lanes copy the stage's scales with
 //               cp.async (4 bytes each: the 4 scales of one row) into the
 //               stage's scale slot, in the order the tensor core reads them:
 //               per 128 rows a 512-byte block in which row r's word sits at
 //               word 4 (r % 32) + r / 32, and each lane's copies arrive on the
 //               stage's full barrier when they land (cp.async.mbarrier.arrive),
 //               so the barrier completes with the TMA bytes and all 32 lanes'
-//               scales and the producer never waits for its copies.
+//               scales and no producer waits for its copies.  Issuing the
+//               scale copies takes about as long as issuing the tile copies,
+//               so the two run side by side in separate warps.
 //   warp 1      TMEM allocator; one thread, after the stage's full barrier and
 //               a proxy fence (the scales were written by the generic proxy),
 //               copies the stage's scales into TMEM
@@ -69,10 +72,11 @@ constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr int SF_COLS = 12;                 // TMEM columns per scale slot: 4 (A) + 8 (B)
 constexpr int SF_SLOTS = STAGES;            // one scale slot per stage (shared memory and TMEM)
-constexpr int FULL_ARRIVALS = 1 + 32;       // the TMA arrival and each producer lane's scale copies
+constexpr int FULL_ARRIVALS = 1 + 32;       // the TMA arrival and each scale-warp lane's copies
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SF_WARP = 2 + EPI_WARPS;      // the last warp copies the scales
+constexpr int NUM_THREADS = 32 * (SF_WARP + 1);
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 static_assert(ACC_COLS + SF_SLOTS * SF_COLS <= TMEM_COLS, "TMEM budget");
 
@@ -292,18 +296,16 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   volatile uint32_t* abort_flag = &sm->abort;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer (whole warp)
-    uint32_t it = 0;
-    bool ok = true;
-    StageIter cur;
-    stage_iter_start<EPI>(cur, sm, p, ntiles);
-    while (cur.valid) {
-      const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-      if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
-      const uint32_t bar = smem_u32(&sm->full[s]);
-      copy_sf<EPI>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
-      cp_async_arrive_noinc(bar);          // arrives when this lane's copies have landed
-      if (lane == 0) {
+    // ---------------------------------------------------------------- tile producer (one thread)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      StageIter cur;
+      stage_iter_start<EPI>(cur, sm, p, ntiles);
+      while (cur.valid) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+        const uint32_t bar = smem_u32(&sm->full[s]);
         const uint32_t a_dst = stage_base + s * STAGE_BYTES;
         const uint32_t b_dst = a_dst + A_BYTES;
         const TileInfo& ti = cur.ti;
@@ -315,15 +317,28 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         } else {
           tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
         }
+        ++it;
+        stage_iter_next<EPI>(cur, sm, p, ntiles);
       }
+      if (!ok) {  // copies still in flight land before the CTA exits (bounded: the scale warp may have stopped)
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
+      }
+    }
+  } else if (warp == SF_WARP) {
+    // ---------------------------------------------------------------- scale producer (whole warp)
+    uint32_t it = 0;
+    StageIter cur;
+    stage_iter_start<EPI>(cur, sm, p, ntiles);
+    while (cur.valid) {
+      const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+      if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) break;
+      copy_sf<EPI>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
+      cp_async_arrive_noinc(smem_u32(&sm->full[s]));   // arrives when this lane's copies have landed
       ++it;
       stage_iter_next<EPI>(cur, sm, p, ntiles);
     }
     cp_async_wait_all();                   // no copy of this CTA outlives it
-    if (!ok && lane == 0) {
-      const uint32_t first = it > STAGES ? it - STAGES : 0;
-      for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
-    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
     if (lane == 0) {

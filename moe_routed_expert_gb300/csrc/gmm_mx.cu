@@ -15,21 +15,22 @@
 //                     up (last N/2), A = Activation(G, U), then Q_MX(A): fp8
 //                     codes and scales of the next matmul's operand.
 //
-// Design (one CTA per SM, 352 threads; 128 x 256 output tiles, K in blocks
+// Design (one CTA per SM, 384 threads; 128 x 256 output tiles, K in blocks
 // of 128 fp8 elements = one 128-byte swizzle row):
 //   warp 0      tile producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
 //               4-stage ring.
-//   warp 10     scale producer.  All 32 lanes copy the stage's scales with
+//   warps 10-11 scale producers.  Their lanes copy the stage's scales with
 //               cp.async (4 bytes each: the 4 scales of one row) into the
 //               stage's scale slot, in the order the tensor core reads them:
 //               per 128 rows a 512-byte block in which row r's word sits at
 //               word 4 (r % 32) + r / 32, and each lane's copies arrive on the
 //               stage's full barrier when they land (cp.async.mbarrier.arrive),
-//               so the barrier completes with the TMA bytes and all 32 lanes'
+//               so the barrier completes with the TMA bytes and all 64 lanes'
 //               scales and no producer waits for its copies.  Issuing the
-//               scale copies takes about as long as issuing the tile copies,
-//               so the two run side by side in separate warps.
+//               384 scale copies of a stage takes longer than issuing its
+//               tile copies, so they are spread over two warps that run
+//               beside the TMA thread.
 //   warp 1      TMEM allocator; one thread, after the stage's full barrier and
 //               a proxy fence (the scales were written by the generic proxy),
 //               copies the stage's scales into TMEM
@@ -72,11 +73,12 @@ constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr int SF_COLS = 12;                 // TMEM columns per scale slot: 4 (A) + 8 (B)
 constexpr int SF_SLOTS = STAGES;            // one scale slot per stage (shared memory and TMEM)
-constexpr int FULL_ARRIVALS = 1 + 32;       // the TMA arrival and each scale-warp lane's copies
+constexpr int SF_WARPS = 2;                // warps copying the scales
+constexpr int FULL_ARRIVALS = 1 + 32 * SF_WARPS;  // the TMA arrival and each scale-warp lane's copies
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int SF_WARP = 2 + EPI_WARPS;      // the last warp copies the scales
-constexpr int NUM_THREADS = 32 * (SF_WARP + 1);
+constexpr int SF_WARP = 2 + EPI_WARPS;      // the first scale warp; the others follow it
+constexpr int NUM_THREADS = 32 * (SF_WARP + SF_WARPS);
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 static_assert(ACC_COLS + SF_SLOTS * SF_COLS <= TMEM_COLS, "TMEM budget");
 
@@ -160,20 +162,24 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // Copy one stage's scales into a scale slot: lane l copies the words of rows
 // l + 32 j of the A tile (j < 4) and of channels l + 32 j of the B tile
-// (j < 8) to the tensor core's order.  Rows past M and channels past N copy
-// zeros (their data arrive as zeros from the TMA unit).
-template <int EPI>
+// (j < 8) to the tensor core's order, split in two halves of six words, one
+// per scale warp (PART 0: the A words and B's j < 2; PART 1: B's j >= 2).
+// Rows past M and channels past N copy zeros (their data arrive as zeros from
+// the TMA unit).
+template <int EPI, int PART>
 __device__ __forceinline__ void copy_sf(const MxParams& p, const TileInfo& ti, int kb, int lane, uint32_t slot) {
   const int64_t ld = p.sf_ld;
+  if (PART == 0) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int64_t r = ti.row0 + lane + 32 * j;
-    const bool in = r < p.rows_cap;
-    cp_async4(slot + 16 * lane + 4 * j, p.a_sf + (in ? r * ld + 4 * kb : 0), in ? 4u : 0u);
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = ti.row0 + lane + 32 * j;
+      const bool in = r < p.rows_cap;
+      cp_async4(slot + 16 * lane + 4 * j, p.a_sf + (in ? r * ld + 4 * kb : 0), in ? 4u : 0u);
+    }
   }
   const uint8_t* bsf = p.b_sf + static_cast<int64_t>(ti.g) * p.N * ld + 4 * kb;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = PART == 0 ? 0 : 2; j < (PART == 0 ? 2 : 8); ++j) {
     int n;
     if (EPI == MX_ACT)  // channels [0, 128) of the tile: gate; [128, 256): the matching up channels
       n = (j < 4 ? ti.col0 : p.out_cols + ti.col0) + lane + 32 * (j & 3);
@@ -325,15 +331,18 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
       }
     }
-  } else if (warp == SF_WARP) {
-    // ---------------------------------------------------------------- scale producer (whole warp)
+  } else if (warp >= SF_WARP) {
+    // ---------------------------------------------------------------- scale producers (whole warps)
     uint32_t it = 0;
     StageIter cur;
     stage_iter_start<EPI>(cur, sm, p, ntiles);
     while (cur.valid) {
       const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
       if (!warp_wait(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, lane)) break;
-      copy_sf<EPI>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
+      if (warp == SF_WARP)
+        copy_sf<EPI, 0>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
+      else
+        copy_sf<EPI, 1>(p, cur.ti, cur.kb, lane, sf_base + s * SF_STAGE_BYTES);
       cp_async_arrive_noinc(smem_u32(&sm->full[s]));   // arrives when this lane's copies have landed
       ++it;
       stage_iter_next<EPI>(cur, sm, p, ntiles);

@@ -99,6 +99,8 @@ struct MxParams {
   uint8_t* aq;           // ACT: fp8 [M, N/2]
   uint8_t* as;           // ACT: [M, N/64]
   uint16_t* h_save;      // ACT: optional bf16 [M, N]
+  uint32_t out32;        // the outputs (plain: out; ACT: aq and h_save) are 32-byte aligned, so
+                         // rows are written in 32-byte pieces
   Act act;
   uint32_t idesc;
   uint32_t tx_bytes;     // bytes a stage's A and B copies deliver: E2M1 operands count their packed size
@@ -147,6 +149,13 @@ __device__ __forceinline__ TileInfo decode_tile(const MxSmem* sm, const MxParams
   ti.row0 = sm->grp_off[lo] + static_cast<int64_t>(rt) * BM;
   ti.rows_valid = min(BM, sm->grp_cnt[lo] - rt * BM);
   return ti;
+}
+
+// One 32-byte store: a whole sector, where two 16-byte stores would each fill half of one.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int lane) {
@@ -429,26 +438,38 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               a[i] = act_forward(bf16_lo(gu[32 * cc + i]), bf16_hi(gu[32 * cc + i]), p.act);
             uint32_t c8[8];
             scales |= mx_quant32<OUT_FMT>(a, c8) << (8 * cc);
-            uint4* dq = reinterpret_cast<uint4*>(p.aq + row * I + c0 + 32 * cc);
-            dq[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
-            dq[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
+            if (p.out32) {
+              st_global_v8(p.aq + row * I + c0 + 32 * cc, c8);
+            } else {
+              uint4* dq = reinterpret_cast<uint4*>(p.aq + row * I + c0 + 32 * cc);
+              dq[0] = make_uint4(c8[0], c8[1], c8[2], c8[3]);
+              dq[1] = make_uint4(c8[4], c8[5], c8[6], c8[7]);
+            }
           }
           *reinterpret_cast<uint16_t*>(p.as + row * (I / 32) + c0 / 32) = static_cast<uint16_t>(scales);
           if (p.h_save) {
             uint16_t* hg = p.h_save + row * (2 * static_cast<int64_t>(I)) + c0;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              uint4 gq, uq;
-              uint32_t* gw = &gq.x;
-              uint32_t* uw = &uq.x;
+            for (int v = 0; v < 4; ++v) {   // 16 columns of gate and of up at a time
+              uint32_t gw[8], uw[8];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const uint32_t p0 = gu[8 * v + 2 * w], p1 = gu[8 * v + 2 * w + 1];
+              for (int w = 0; w < 8; ++w) {
+                const uint32_t p0 = gu[16 * v + 2 * w], p1 = gu[16 * v + 2 * w + 1];
                 gw[w] = (p0 & 0xFFFFu) | (p1 << 16);
                 uw[w] = (p0 >> 16) | (p1 & 0xFFFF0000u);
               }
-              reinterpret_cast<uint4*>(hg)[v] = gq;
-              reinterpret_cast<uint4*>(hg + I)[v] = uq;
+              if (p.out32) {
+                st_global_v8(hg + 16 * v, gw);
+                st_global_v8(hg + I + 16 * v, uw);
+              } else {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  reinterpret_cast<uint4*>(hg + 16 * v)[h2] = make_uint4(gw[4 * h2], gw[4 * h2 + 1], gw[4 * h2 + 2],
+                                                                         gw[4 * h2 + 3]);
+                  reinterpret_cast<uint4*>(hg + I + 16 * v)[h2] = make_uint4(uw[4 * h2], uw[4 * h2 + 1],
+                                                                             uw[4 * h2 + 2], uw[4 * h2 + 3]);
+                }
+              }
             }
           }
         }
@@ -472,14 +493,23 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (row_ok) {
           const int c0 = ti.col0 + 128 * half;
           uint16_t* dst = p.out + row * p.out_cols + c0;
+          if (p.out32) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            if (c0 + 32 * cc < p.out_cols) {
-              uint4* d = reinterpret_cast<uint4*>(dst + 32 * cc);
+            for (int cc = 0; cc < 4; ++cc)
+              if (c0 + 32 * cc < p.out_cols) {
+                st_global_v8(dst + 32 * cc, &packed[16 * cc]);
+                st_global_v8(dst + 32 * cc + 16, &packed[16 * cc + 8]);
+              }
+          } else {
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                d[v] = make_uint4(packed[16 * cc + 4 * v], packed[16 * cc + 4 * v + 1], packed[16 * cc + 4 * v + 2],
-                                  packed[16 * cc + 4 * v + 3]);
+            for (int cc = 0; cc < 4; ++cc) {
+              if (c0 + 32 * cc < p.out_cols) {
+                uint4* d = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  d[v] = make_uint4(packed[16 * cc + 4 * v], packed[16 * cc + 4 * v + 1], packed[16 * cc + 4 * v + 2],
+                                    packed[16 * cc + 4 * v + 3]);
+              }
             }
           }
         }
@@ -537,6 +567,8 @@ moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s)
   p.aq = x.aq;
   p.as = x.as;
   p.h_save = x.h_save;
+  const auto a32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+  p.out32 = (act ? a32(x.aq) && a32(x.h_save) : a32(x.out)) ? 1u : 0u;
   if (act) p.act = *x.act;
   CUtensorMap ta, tb;
   if (!(a_fp4 ? make_map_2d_fp4(&ta, x.a, x.M, x.K, BM) : make_map_2d_u8(&ta, x.a, x.M, x.K, BM)) ||

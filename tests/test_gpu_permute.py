@@ -57,6 +57,8 @@ def test_worked_example():
     (3000, 4, 1024, 64, 0.1), (5000, 8, 64, 136, 0.0), (2049, 1, 3, 8, 0.0), (129, 64, 64, 64, 0.2),
     # either side of the one-block index path (up to 1024 slots), with 1024 experts
     (128, 8, 1024, 64, 0.1), (1025, 1, 7, 16, 0.2), (100, 8, 1024, 32, 0.0),
+    # the prefill batch size (32768 slots) and around it: full, ragged, 1024 experts
+    (4096, 8, 256, 32, 0.0), (32769, 1, 5, 16, 0.1), (4000, 8, 1024, 32, 0.3), (1057, 31, 40, 8, 0.05),
 ])
 def test_random_ragged(T, k, E, H, p_unused):
     rng = np.random.default_rng(T * 7 + k)
@@ -90,6 +92,19 @@ def test_bad_ids_raise_device_status():
     ids = np.array([[0, -2]], np.int32)
     _, st = run_permute(None, ids, 4)
     assert st == 5
+
+
+@pytest.mark.parametrize("T,k", [(2000, 4), (10000, 4)])
+def test_bad_ids_raise_device_status_larger_batches(T, k):
+    """The four-kernel index path flags a bad id too, and treats it as an
+    unused slot."""
+    rng = np.random.default_rng(T)
+    E = 16
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids[T // 2, 1] = E
+    (_, _, rmap, _), st = run_permute(None, ids, E)
+    assert st == 5  # MOE_ERR_DEVICE
+    assert rmap.cpu().numpy()[(T // 2) * k + 1] == -1
 
 
 def test_empty_tokens():

@@ -49,15 +49,15 @@ GMM_TRAFFIC = [
          "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
          "common.cuh": "0e8e1d6ccc0f617f923f19edeb534bb6c5a39f113db927aaf3ef9c7640e44a17",
          "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
-    {"workload": "layer_prefill_mx_t4096", "bytes_per_launch": 0.5153e9,
+    {"workload": "layer_prefill_mx_t4096", "bytes_per_launch": 0.5163e9,
      "sources": {
-         "gmm_mx.cu": "9a88d70eb17c72c1fc284efea5d5a113ada35d0439dc6a1cf39edf5eb68237f6",
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
          "common.cuh": "0e8e1d6ccc0f617f923f19edeb534bb6c5a39f113db927aaf3ef9c7640e44a17",
          "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
          "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
     {"workload": "layer_decode_mx_t64", "bytes_per_launch": 0.3650e9,
      "sources": {
-         "gmm_mx.cu": "9a88d70eb17c72c1fc284efea5d5a113ada35d0439dc6a1cf39edf5eb68237f6",
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
          "common.cuh": "0e8e1d6ccc0f617f923f19edeb534bb6c5a39f113db927aaf3ef9c7640e44a17",
          "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
          "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},

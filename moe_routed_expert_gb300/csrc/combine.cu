@@ -46,6 +46,80 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
   return q;
 }
 
+// Rows of the slots [j0, j0 + JB) of token t; a row outside [-1, rows_cap)
+// raises MOE_ERR_DEVICE and counts as unused.
+__device__ __forceinline__ void slot_rows(const int32_t* __restrict__ row_id_map, int64_t t, int j0, int k,
+                                          int64_t rows_cap, uint32_t* status, int32_t (&r)[JB]) {
+#pragma unroll
+  for (int jj = 0; jj < JB; ++jj) {
+    const int j = j0 + jj;
+    r[jj] = j < k ? row_id_map[t * k + j] : -1;
+    if (r[jj] < -1 || r[jj] >= rows_cap) {
+      set_status(status, MOE_ERR_DEVICE);
+      r[jj] = -1;
+    }
+  }
+}
+
+// Slots [j0, j0 + JB) of token t whose rows are r into acc, in slot order.
+template <bool HAS_W>
+__device__ __forceinline__ void add_slots(float (&acc)[8], const uint16_t* __restrict__ y_perm,
+                                          const float* __restrict__ topk_w, const int32_t (&r)[JB], int64_t t,
+                                          int j0, int k, int64_t H, int64_t col, const int32_t* __restrict__ row_id_map,
+                                          int64_t rows_cap, uint32_t* status, int64_t t_next, int32_t (&r_next)[JB]) {
+  uint4 v[JB];
+  float w[JB];
+  uint32_t live = 0;
+#pragma unroll
+  for (int jj = 0; jj < JB; ++jj) {
+    if (r[jj] >= 0) {
+      v[jj] = ld_nc_v4(y_perm + static_cast<int64_t>(r[jj]) * H + col);
+      live |= 1u << jj;
+    }
+    w[jj] = (HAS_W && j0 + jj < k) ? topk_w[t * k + j0 + jj] : 1.0f;
+  }
+  if (t_next >= 0) slot_rows(row_id_map, t_next, 0, k, rows_cap, status, r_next);   // while the rows load
+#pragma unroll
+  for (int jj = 0; jj < JB; ++jj)
+    if ((live >> jj) & 1u) add8(acc, v[jj], w[jj]);
+}
+
+// The token gradient (unit weights, large batches): grid (min(T, 3 x SMs),
+// ceil(H / 2048)), three blocks per SM; each thread owns 8 consecutive columns
+// and walks the tokens t = blockIdx.x, + gridDim.x, ...  The rows of the next
+// token's first JB slots load while the current token's rows are in flight.
+// Slots are summed in order j = 0, 1, ... as in unpermute_kernel, so both give
+// the same bits.  (With the weights as well, this loop spills and is slower
+// than unpermute_kernel.)
+template <bool HAS_W>
+__global__ void __launch_bounds__(THREADS, 3) token_sum_kernel(const uint16_t* __restrict__ y_perm,
+                                                               const int32_t* __restrict__ row_id_map,
+                                                               const float* __restrict__ topk_w, int64_t T, int64_t H,
+                                                               int k, int64_t rows_cap, uint16_t* __restrict__ y,
+                                                               uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t col = static_cast<int64_t>(blockIdx.y) * COLS_PER_BLOCK + threadIdx.x * 8;
+  int64_t t = blockIdx.x;
+  if (col >= H || t >= T) return;
+  int32_t rn[JB];
+  slot_rows(row_id_map, t, 0, k, rows_cap, status, rn);
+  for (; t < T; t += gridDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int32_t r[JB];
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) r[jj] = rn[jj];
+    const int64_t t_next = t + gridDim.x < T ? t + gridDim.x : -1;
+    add_slots<HAS_W>(acc, y_perm, topk_w, r, t, 0, k, H, col, row_id_map, rows_cap, status, t_next, rn);
+    for (int j0 = JB; j0 < k; j0 += JB) {   // more than JB slots: the rest without a prefetch
+      int32_t rb[JB], unused[JB];
+      slot_rows(row_id_map, t, j0, k, rows_cap, status, rb);
+      add_slots<HAS_W>(acc, y_perm, topk_w, rb, t, j0, k, H, col, row_id_map, rows_cap, status, -1, unused);
+    }
+    *reinterpret_cast<uint4*>(y + t * H + col) = pack8(acc);
+  }
+}
+
 // grid (T, ceil(H / 2048)); each thread owns 8 consecutive columns of one token.
 template <bool HAS_W>
 __global__ void __launch_bounds__(THREADS) unpermute_kernel(const uint16_t* __restrict__ y_perm,
@@ -188,11 +262,19 @@ __global__ void __launch_bounds__(THREADS) act_backward_kernel(const uint16_t* _
 moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
                               int64_t T, int64_t H, int64_t k, uint16_t* y, uint32_t* status, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H + COLS_PER_BLOCK - 1) / COLS_PER_BLOCK));
-  const cudaError_t e =
-      topk_w ? launch_pdl(unpermute_kernel<true>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map, topk_w, H,
-                          static_cast<int>(k), T * k, y, status)
-             : launch_pdl(unpermute_kernel<false>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map,
-                          static_cast<const float*>(nullptr), H, static_cast<int>(k), T * k, y, status);
+  const int64_t loop_blocks = 3 * static_cast<int64_t>(num_sms());
+  cudaError_t e;
+  if (topk_w) {
+    e = launch_pdl(unpermute_kernel<true>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map, topk_w, H,
+                   static_cast<int>(k), T * k, y, status);
+  } else if (T > loop_blocks) {   // the token gradient of a large batch
+    const dim3 g2(static_cast<unsigned>(loop_blocks), grid.y);
+    e = launch_pdl(token_sum_kernel<false>, g2, dim3(THREADS), 0, s, 1, y_perm, row_id_map,
+                   static_cast<const float*>(nullptr), T, H, static_cast<int>(k), T * k, y, status);
+  } else {
+    e = launch_pdl(unpermute_kernel<false>, grid, dim3(THREADS), 0, s, 1, y_perm, row_id_map,
+                   static_cast<const float*>(nullptr), H, static_cast<int>(k), T * k, y, status);
+  }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -17,8 +17,10 @@
 //           slots.  Per-warp expert counts -> per-warp base rows; then every
 //           32-slot step ranks equal ids with __match_any_sync, which keeps
 //           the flat order (stable).  Writes row_id_map and sorted_flat.
-//   gather  warp per (slot, 2 KB segment of the row), in slot order so the k
-//           copies of one token read it once from HBM: x_perm[row] = x[t].
+//   gather  warp per (token, 2 KB segment of its row): read once, stored to
+//           the permuted row of each of the token's k slots: x_perm[row] = x[t].
+//           Small batches take a warp per (slot, segment) instead, for more
+//           warps in flight.
 // Up to kSmallSlots slots (decode batches), one block does count, scan and
 // rank (permute_small_kernel) and the gather follows: two launches instead of
 // four, for index work that is all latency at that size.
@@ -258,7 +260,49 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
 
 constexpr int SEG = 1024;  // bf16 elements per warp item (2 KB)
 
-__global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t* __restrict__ x, int64_t nslots,
+// Warp per (token, 2 KB segment of its row): the segment is read once and
+// stored to the permuted row of each of the token's k slots.
+__global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t* __restrict__ x, int64_t T,
+                                                                 int64_t H, int k,
+                                                                 const int32_t* __restrict__ row_id_map,
+                                                                 uint16_t* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nseg = (H + SEG - 1) / SEG;
+  const int64_t items = T * nseg;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
+  for (int64_t item = gw; item < items; item += nw) {   // the whole warp takes each item
+    const int64_t t = item / nseg;
+    const int64_t seg = item - t * nseg;
+    const uint16_t* src = x + t * H + seg * SEG;
+    const int64_t n = (H - seg * SEG) < SEG ? (H - seg * SEG) : static_cast<int64_t>(SEG);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = (u * 32 + lane) * 8;
+      if (c < n) v[u] = ld_nc_v4(src + c);
+    }
+    for (int j0 = 0; j0 < k; j0 += 32) {   // lane l fetches slot j0 + l's row, then the warp walks them
+      const int32_t rl = j0 + lane < k ? row_id_map[t * k + j0 + lane] : -1;
+      const int m = min(32, k - j0);
+      for (int jj = 0; jj < m; ++jj) {
+        const int32_t row = __shfl_sync(0xffffffffu, rl, jj);
+        if (row < 0) continue;
+        uint16_t* dst = x_perm + static_cast<int64_t>(row) * H + seg * SEG;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t c = (u * 32 + lane) * 8;
+          if (c < n) *reinterpret_cast<uint4*>(dst + c) = v[u];
+        }
+      }
+    }
+  }
+}
+
+// Warp per (slot, 2 KB segment): more warps than tokens, for small batches.
+__global__ void __launch_bounds__(THREADS) permute_gather_slots_kernel(const uint16_t* __restrict__ x, int64_t nslots,
                                                                  int64_t H, int k,
                                                                  const int32_t* __restrict__ row_id_map,
                                                                  uint16_t* __restrict__ x_perm) {
@@ -326,14 +370,20 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
   if (mx != nullptr && x != nullptr && H > 0) {
     if (launch_mx_gather(x, nslots, H, static_cast<int>(k), row_id_map, *mx, s) != MOE_OK) return MOE_ERR_CUDA;
   } else if (x != nullptr && x_perm != nullptr && H > 0) {
-    const int64_t items = nslots * ((H + SEG - 1) / SEG);
-    const int64_t warps_needed = items;
-    int64_t blocks = (warps_needed + WARPS - 1) / WARPS;
+    const int64_t nseg = (H + SEG - 1) / SEG;
     const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+    // token-major once there are enough tokens to fill the GPU's warps a few times over
+    const bool by_token = T * nseg >= 4 * static_cast<int64_t>(num_sms()) * WARPS;
+    const int64_t items = (by_token ? T : nslots) * nseg;
+    int64_t blocks = (items + WARPS - 1) / WARPS;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, x, nslots, H,
-                   static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm) != cudaSuccess)
+    const cudaError_t ge =
+        by_token ? launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, x,
+                              T, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm)
+                 : launch_pdl(permute_gather_slots_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s,
+                              1, x, nslots, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm);
+    if (ge != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

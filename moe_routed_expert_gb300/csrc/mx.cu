@@ -80,16 +80,16 @@ __global__ void __launch_bounds__(THREADS) mx_rows_kernel(const uint16_t* __rest
       else
         g.sc = mx_quant32<FMT>(v, g.c);
     }
-    if (!GATHER) {
+    if constexpr (!GATHER) {
       if (active) store_group<FMT>(g, q, scales, t, K, grp);
-      continue;
-    }
-    for (int j0 = 0; j0 < k; j0 += 32) {   // lane l fetches slot j0 + l's row, then the warp walks them
-      const int32_t rl = j0 + lane < k ? row_id_map[t * k + j0 + lane] : -1;
-      const int n = min(32, k - j0);
-      for (int jj = 0; jj < n; ++jj) {
-        const int32_t r = __shfl_sync(0xffffffffu, rl, jj);
-        if (r >= 0 && active) store_group<FMT>(g, q, scales, r, K, grp);
+    } else {
+      for (int j0 = 0; j0 < k; j0 += 32) {   // lane l fetches slot j0 + l's row, then the warp walks them
+        const int32_t rl = j0 + lane < k ? row_id_map[t * k + j0 + lane] : -1;
+        const int n = min(32, k - j0);
+        for (int jj = 0; jj < n; ++jj) {
+          const int32_t r = __shfl_sync(0xffffffffu, rl, jj);
+          if (r >= 0 && active) store_group<FMT>(g, q, scales, r, K, grp);
+        }
       }
     }
   }

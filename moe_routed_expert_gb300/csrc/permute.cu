@@ -41,16 +41,18 @@ constexpr int SUB = CHUNK / WARPS;   // 128 slots per warp in the rank kernel
 constexpr int kSmallSlots = 1024;    // one-block index path up to this many slots
 
 // Count, scan and rank of up to kSmallSlots slots in one block of 1024
-// threads: a shared-memory histogram, an exclusive scan over the experts (one
-// per thread), then warp 0 walks the slots 32 at a time in flat order and
-// ranks equal ids with __match_any_sync (stable), advancing a running row per
-// expert.  Same outputs and status as count + scan + rank.
+// threads: a shared-memory histogram (the ids stay in shared memory), an
+// exclusive scan over the experts (one per thread), then warp 0 walks the
+// slots 32 at a time in flat order and ranks equal ids with __match_any_sync
+// (stable), advancing a running row per expert.  Same outputs and status as
+// count + scan + rank.
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int nslots, int E,
                                                              int64_t* __restrict__ group_list,
                                                              int32_t* __restrict__ row_id_map,
                                                              int32_t* __restrict__ sorted_flat, uint32_t* status) {
   __shared__ int32_t cnt[kMaxExperts];
   __shared__ int32_t next_row[kMaxExperts];
+  __shared__ int32_t id_sh[kSmallSlots];   // each slot's expert, -1 when unused or invalid
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t R_sh;
   pdl_wait();
@@ -59,9 +61,14 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   for (int e = tid; e < E; e += 1024) cnt[e] = 0;
   __syncthreads();
   for (int f = tid; f < nslots; f += 1024) {
-    const int e = ids[f];
-    if (e < -1 || e >= E) set_status(status, MOE_ERR_DEVICE);
-    else if (e >= 0) atomicAdd(&cnt[e], 1);
+    int e = ids[f];
+    if (e < -1 || e >= E) {
+      set_status(status, MOE_ERR_DEVICE);
+      e = -1;
+    } else if (e >= 0) {
+      atomicAdd(&cnt[e], 1);
+    }
+    id_sh[f] = e;
   }
   __syncthreads();
   const int32_t v = tid < E ? cnt[tid] : 0;
@@ -95,8 +102,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
 #pragma unroll 1
     for (int c = 0; c < nslots; c += 32) {
       const int f = c + lane;
-      int e = f < nslots ? ids[f] : -1;
-      if (e < -1 || e >= E) e = -1;
+      const int e = f < nslots ? id_sh[f] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       if (e >= 0) {
         const int32_t row = next_row[e] + __popc(peers & lt);

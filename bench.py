@@ -145,8 +145,8 @@ class ClockSampler:
 
 def permute_launches(nslots):
     """Kernels one permute launches: a one-block index kernel and the gather up to
-    1024 routed slots, else count, scan, rank and the gather."""
-    return 2 if nslots <= 1024 else 4
+    1024 routed slots, else count, rank and the gather."""
+    return 2 if nslots <= 1024 else 3
 
 
 def bf16_dev(bits, dev):

@@ -7,23 +7,24 @@
 // owns one row row(i,k) of its expert's block, rows stacked in a fixed order.
 // The order used here is ascending flat slot f = t*k + j within an expert.
 //
-// Kernels (four launches, no host sync):
+// Kernels (three launches, no host sync):
 //   count   one block per chunk of 1024 slots: shared-memory histogram,
 //           written as chunk_counts[e][chunk]; ids outside [-1, E) raise
 //           MOE_ERR_DEVICE and are skipped.
-//   scan    one block: per expert (one warp each) exclusive scan over chunks,
-//           block scan over experts -> group_list and each chunk's first row.
-//   rank    one block per chunk; each of its 8 warps owns 128 consecutive
-//           slots.  Per-warp expert counts -> per-warp base rows; then every
-//           32-slot step ranks equal ids with __match_any_sync, which keeps
-//           the flat order (stable).  Writes row_id_map and sorted_flat.
+//   rank    one block per chunk.  From all chunk counts, its chunk's first
+//           row per expert (earlier chunks, then the exclusive scan over the
+//           experts' totals; block 0 writes group_list).  Each of its 8 warps
+//           owns 128 consecutive slots: per-warp expert counts -> per-warp
+//           base rows; then every 32-slot step ranks equal ids with
+//           __match_any_sync, which keeps the flat order (stable).  Writes
+//           row_id_map and sorted_flat.
 //   gather  warp per (token, 2 KB segment of its row): read once, stored to
 //           the permuted row of each of the token's k slots: x_perm[row] = x[t].
 //           Small batches take a warp per (slot, segment) instead, for more
 //           warps in flight.
 // Up to kSmallSlots slots (decode batches), one block does count, scan and
 // rank (permute_small_kernel) and the gather follows: two launches instead of
-// four, for index work that is all latency at that size.
+// three, for index work that is all latency at that size.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -45,7 +46,7 @@ constexpr int kSmallSlots = 1024;    // one-block index path up to this many slo
 // exclusive scan over the experts (one per thread), then warp 0 walks the
 // slots 32 at a time in flat order and ranks equal ids with __match_any_sync
 // (stable), advancing a running row per expert.  Same outputs and status as
-// count + scan + rank.
+// count + rank.
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int nslots, int E,
                                                              int64_t* __restrict__ group_list,
                                                              int32_t* __restrict__ row_id_map,
@@ -141,40 +142,43 @@ __global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* _
     chunk_counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
 }
 
-// One block of 1024 threads.
-__global__ void __launch_bounds__(1024) permute_scan_kernel(int E, int nchunks, int64_t nslots,
-                                                            int32_t* __restrict__ chunk_counts,
-                                                            int64_t* __restrict__ group_list,
-                                                            int32_t* __restrict__ sorted_flat) {
-  __shared__ int32_t total[kMaxExperts];
-  __shared__ int32_t warp_sum[32];
+// Rank kernel, one block per chunk.  It first turns the chunk counts of all
+// chunks into this chunk's first row per expert: rows of expert e in earlier
+// chunks plus the rows of all earlier experts (an exclusive scan over the
+// experts of their totals).  Block 0 writes group_list; the blocks share the
+// rows past R, which own no slot (-1 in sorted_flat).
+__global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __restrict__ ids, int64_t nslots,
+                                                               int E, int nchunks,
+                                                               const int32_t* __restrict__ chunk_counts,
+                                                               int64_t* __restrict__ group_list,
+                                                               int32_t* __restrict__ row_id_map,
+                                                               int32_t* __restrict__ sorted_flat) {
+  extern __shared__ int32_t wbase[];  // [WARPS][E], then the chunk's first row per expert [E]
+  int32_t* cbase = wbase + WARPS * E;
+  __shared__ int32_t warp_sum[WARPS];
   __shared__ int32_t R_sh;
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1) per expert: exclusive scan of its chunk counts (in place), total rows
-  for (int e = warp; e < E; e += 32) {
-    int32_t* row = chunk_counts + static_cast<int64_t>(e) * nchunks;
-    int32_t run = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int32_t v = c < nchunks ? row[c] : 0;
-      int32_t incl = v;
+  for (int i = threadIdx.x; i < WARPS * E; i += THREADS) wbase[i] = 0;
+  // this thread's experts: ept consecutive ones (E <= 4 x THREADS)
+  const int ept = (E + THREADS - 1) / THREADS;
+  int32_t tot[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
+  int32_t mine_tot = 0;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
+  for (int i = 0; i < 4; ++i) {
+    const int e = threadIdx.x * ept + i;
+    if (i < ept && e < E) {
+      const int32_t* row = chunk_counts + static_cast<int64_t>(e) * nchunks;
+      for (int c = 0; c < nchunks; ++c) {
+        const int32_t v = row[c];
+        tot[i] += v;
+        if (c < static_cast<int>(blockIdx.x)) pre[i] += v;
       }
-      if (c < nchunks) row[c] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      mine_tot += tot[i];
     }
-    if (lane == 0) total[e] = run;
   }
-  __syncthreads();
-  // 2) exclusive scan over experts (E <= 1024 = one element per thread)
-  const int e = threadIdx.x;
-  const int32_t v = e < E ? total[e] : 0;
-  int32_t incl = v;
+  int32_t incl = mine_tot;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
@@ -182,44 +186,29 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int E, int nchunks, 
   }
   if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int32_t w = warp_sum[lane];
-    int32_t wi = w;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
-      if (lane >= d) wi += o;
+  if (threadIdx.x == 0) {
+    int32_t run = 0;
+    for (int w = 0; w < WARPS; ++w) {
+      const int32_t v = warp_sum[w];
+      warp_sum[w] = run;
+      run += v;
     }
-    warp_sum[lane] = wi - w;
-    if (lane == 31) R_sh = wi;
+    R_sh = run;
   }
   __syncthreads();
-  const int32_t off = warp_sum[warp] + incl - v;
-  if (e < E) {
-    group_list[e] = v;
-    total[e] = off;
+  int32_t off = warp_sum[warp] + incl - mine_tot;   // rows of all experts before this thread's first
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = threadIdx.x * ept + i;
+    if (i < ept && e < E) {
+      cbase[e] = off + pre[i];
+      if (blockIdx.x == 0) group_list[e] = tot[i];
+      off += tot[i];
+    }
   }
-  __syncthreads();
-  // 3) chunk bases become absolute first rows
-  for (int ee = warp; ee < E; ee += 32) {
-    int32_t* row = chunk_counts + static_cast<int64_t>(ee) * nchunks;
-    const int32_t base = total[ee];
-    for (int c = lane; c < nchunks; c += 32) row[c] += base;
-  }
-  // 4) rows past R own no slot
-  for (int64_t r = R_sh + threadIdx.x; r < nslots; r += 1024) sorted_flat[r] = -1;
-}
-
-__global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __restrict__ ids, int64_t nslots,
-                                                               int E, int nchunks,
-                                                               const int32_t* __restrict__ chunk_base,
-                                                               int32_t* __restrict__ row_id_map,
-                                                               int32_t* __restrict__ sorted_flat) {
-  extern __shared__ int32_t wbase[];  // [WARPS][E]
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < WARPS * E; i += THREADS) wbase[i] = 0;
+  for (int64_t r = R_sh + static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x; r < nslots;
+       r += static_cast<int64_t>(gridDim.x) * THREADS)
+    sorted_flat[r] = -1;
   __syncthreads();
   const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK + warp * SUB;
   int32_t* mine = wbase + warp * E;
@@ -235,7 +224,7 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
   __syncthreads();
   // per-expert scan over the warps of this chunk, starting at the chunk's first row
   for (int e = threadIdx.x; e < E; e += THREADS) {
-    int32_t run = chunk_base[static_cast<int64_t>(e) * nchunks + blockIdx.x];
+    int32_t run = cbase[e];
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) {
       const int32_t c = wbase[w * E + e];
@@ -365,12 +354,9 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
     if (launch_pdl(permute_count_kernel, dim3(nchunks), dim3(THREADS), e * sizeof(int32_t), s, 1, ids, nslots, e,
                    nchunks, chunk_counts, status) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, 1, e, nchunks, nslots, chunk_counts, group_list,
-                   sorted_flat) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    const size_t rank_smem = static_cast<size_t>(WARPS) * e * sizeof(int32_t);
+    const size_t rank_smem = static_cast<size_t>(WARPS + 1) * e * sizeof(int32_t);
     if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
-                   static_cast<const int32_t*>(chunk_counts), row_id_map, sorted_flat) != cudaSuccess)
+                   static_cast<const int32_t*>(chunk_counts), group_list, row_id_map, sorted_flat) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if (mx != nullptr && x != nullptr && H > 0) {

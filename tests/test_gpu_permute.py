@@ -1,7 +1,7 @@
 """Parity of the CUDA permute (histogram, scan, stable counting-sort scatter,
 row gather) with the oracle: bit-exact for every integer output and for the
 permuted rows (a copy).  Cases up to 1024 slots take the one-block index
-kernel, larger ones the four-kernel path."""
+kernel, larger ones the three-kernel path (count, rank, gather)."""
 import json
 import os
 
@@ -96,7 +96,7 @@ def test_bad_ids_raise_device_status():
 
 @pytest.mark.parametrize("T,k", [(2000, 4), (10000, 4)])
 def test_bad_ids_raise_device_status_larger_batches(T, k):
-    """The four-kernel index path flags a bad id too, and treats it as an
+    """The multi-block index path flags a bad id too, and treats it as an
     unused slot."""
     rng = np.random.default_rng(T)
     E = 16

@@ -146,6 +146,9 @@ def test_gmm_forward_mx_plain(case):
 # Groups of a few rows, as in decode: many 128-row tiles that hold 0-12 rows,
 # one group over 32 rows, empty groups; N = 384 leaves a ragged 256-column tile.
 SMALL_COUNTS = [3, 0, 1, 40, 2, 0, 7, 1, 0, 5, 2, 2, 0, 9, 1, 1, 0, 3, 4, 0, 1, 1, 6, 0, 2, 3, 0, 1, 2, 0, 0, 12]
+# A sparse batch (about 6 rows per expert) with one group of 300 rows among 63
+# small ones: three 128-row tiles for the big group, the last ragged.
+SPARSE_BIG_GROUP = [300] + [2, 0, 1, 3] * 15 + [0, 5, 1]
 SWAP_CASES = [("e4m3", "e4m3", 384), ("e5m2", "e5m2", 256), ("e4m3", "e2m1", 384), ("e2m1", "e2m1", 384)]
 
 
@@ -312,3 +315,23 @@ def test_layer_mx_full_size_sampled_tokens(name):
     y_want, _ = X.mx_layer_forward(f64(inp["x"][toks]), remap[ids], inp["topk_w"][toks], sub(wts["w1_q"]),
                                    sub(wts["w1_s"]), sub(wts["w2_q"]), sub(wts["w2_s"]), wl.mx, wf)
     assert_close("y", host_f64(y)[toks], y_want)
+
+
+@pytest.mark.parametrize("xf,wf", [("e4m3", "e4m3"), ("e2m1", "e2m1")])
+def test_gmm_forward_mx_sparse_batch_with_a_big_group(xf, wf):
+    import torch
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(53)
+    counts = SPARSE_BIG_GROUP
+    E, K, I = len(counts), 256, 256
+    xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, 2 * I, counts, xf, wf)
+    wsp = M.Workspace(256)
+    y = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
+    assert M.read_status(wsp) == 0
+    assert_close("y", y, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
+    h = torch.empty(int(sum(counts)), 2 * I, dtype=torch.bfloat16, device="cuda")
+    aq, as_ = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf,
+                               activation=("swiglu", [7.0]), h_save=h, ws=wsp)
+    assert M.read_status(wsp) == 0
+    assert_close("h", h, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
+    check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation("swiglu", [7.0]), X.activation_format(xf))

@@ -618,6 +618,24 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of every rank's x: the job ends when its slowest rank does
+    (all ranks call it; NCCL on the GPU, any backend the group was made with)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: the units all ranks processed in a step (replicas,
+    each with the same work) over the slowest rank's step time."""
+    return units_per_rank_step * world / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -697,11 +715,7 @@ def main():
         run_step()
     t_end.record(stream)
     barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
 
     # Per-kernel breakdown: the same K steps again with an event after every launch.
@@ -724,7 +738,7 @@ def main():
             stage_ms[i] += events[s][i].elapsed_time(events[s][i + 1])
     stage_ms = [v / args.steps for v in stage_ms]
     ms_per_step = elapsed_ms / args.steps
-    value = step.units * world / (ms_per_step / 1e3)
+    value = job_throughput(step.units, world, ms_per_step)
 
     kernels = {}
     gmm_flops, gmm_ms, gmm_launches = 0.0, 0.0, 0
@@ -787,12 +801,8 @@ def main():
         pipe.run(args.steps)
         b.record(stream)
         barrier()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        line["e2e"] = {"value": round(step.units * world / (e_ms / args.steps / 1e3), 3), "unit": step.unit,
+        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        line["e2e"] = {"value": round(job_throughput(step.units, world, e_ms / args.steps), 3), "unit": step.unit,
                        "h2d_bytes_per_step": int(pipe.h2d_bytes), "d2h_bytes_per_step": int(pipe.d2h_bytes),
                        "ms_per_step": round(e_ms / args.steps, 4), "api": step.e2e_api,
                        "copies": "pinned host buffers; two buffer sets, H2D and D2H on their own streams"}

@@ -234,6 +234,28 @@ def test_backward_ragged(M_, K, N, E, n_empty, seed):
         assert np.all(host_f64(dw[e]) == 0)
 
 
+def test_max_experts_forward_and_backward():
+    """1024 experts, the most the library takes (its per-expert shared-memory
+    tables are then full): a decode-like spread of 0-4 rows each, most empty,
+    one group of 300 rows, and the last expert holding the final rows."""
+    rng = np.random.default_rng(31)
+    E, K, N = 1024, 128, 256
+    gl = rng.choice([0, 0, 0, 1, 2, 4], size=E).astype(np.int64)
+    gl[517] = 300
+    gl[E - 1] = 3
+    M_ = int(gl.sum())
+    x = normal_bf16(rng, (M_, K))
+    w = normal_bf16(rng, (E, K, N), 1 / np.sqrt(K))
+    dy = normal_bf16(rng, (M_, N))
+    y, _ = gpu_forward(x, w, gl)
+    assert_close("y", y, O.gmm_forward(f64(x), f64(w), gl))
+    dx, dw = gpu_backward(x, w, gl, dy)
+    dx_o, dw_o = O.gmm_backward(f64(x), f64(w), gl, f64(dy))
+    assert_close("dx", dx, dx_o)
+    assert_close("dw", dw, dw_o)
+    assert np.all(host_f64(dw)[gl == 0] == 0)
+
+
 def test_workload_gmm_zipf_e8():
     wl = WORKLOADS["gmm_zipf_e8"]
     inp = gmm_inputs(wl)

@@ -335,3 +335,18 @@ def test_gmm_forward_mx_sparse_batch_with_a_big_group(xf, wf):
     assert M.read_status(wsp) == 0
     assert_close("h", h, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))
     check_act_codes(np_u8(aq), np_u8(as_), host_f64(h), O.activation("swiglu", [7.0]), X.activation_format(xf))
+
+
+@pytest.mark.parametrize("xf,wf", [("e4m3", "e4m3"), ("e4m3", "e2m1")])
+def test_gmm_forward_mx_max_experts(xf, wf):
+    """1024 experts (the library's limit), most of them empty."""
+    import moe_routed_expert_gb300 as M
+    rng = np.random.default_rng(54)
+    E, K, N = 1024, 128, 256
+    counts = rng.choice([0, 0, 0, 1, 2, 4], size=E).astype(np.int64)
+    counts[700] = 200
+    xq, xs, wq, ws, gl, _ = mx_gmm_case(rng, E, K, N, counts, xf, wf)
+    wsp = M.Workspace(256)
+    y = M.gmm_forward_mx(w_dev(xq, xf), dev(xs), w_dev(wq, wf), dev(ws), dev(gl), x_fmt=xf, w_fmt=wf, ws=wsp)
+    assert M.read_status(wsp) == 0
+    assert_close("y", y, X.mx_gmm(xq, xs, wq, ws, gl, xf, wf))

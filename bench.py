@@ -102,8 +102,10 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % self.gpu)
+            import tempfile
+            out_dir = os.environ.get("MOE_BENCH_CLOCKS_DIR", tempfile.gettempdir())
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, "moe_bench_clocks_rank%d.csv" % self.gpu)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
                                           "--format=csv,noheader,nounits", "-lms", "200"],

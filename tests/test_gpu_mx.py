@@ -200,7 +200,7 @@ def check_act_codes(aq, as_, h_gpu, act, fmt, rel=1e-5, abs_a=2e-6):
     near_pow2 = np.abs(amax / np.exp2(np.round(np.log2(np.maximum(amax, 1e-300)))) - 1.0) < rel
     bad_s = (as_ != s_ref) & ~near_pow2
     assert not np.any(bad_s), "scale mismatch away from a power of two at %s" % (np.argwhere(bad_s)[:5],)
-    # codes, judged against the GPU's own scale: the GPU's value must be the
+    # codes, checked against the GPU's own scale: the GPU's value must be the
     # nearest one, or tie with it within rel
     X_gpu = np.repeat(X.e8m0_decode(as_), 32, axis=1)
     r = np.clip(a / X_gpu, -f["max"], f["max"])

@@ -40,7 +40,7 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 
 # DRAM bytes per GMM launch (the mean over one step's GMM launches), each from
 # one ncu capture of the sources with these hashes; reported only while they
-# match.  Training step: profiles/gmm_traffic_layer_train_t16384.md; MXFP8
+# match.  Training step: profiles/gmm_traffic_layer_train_t16384.md; MX
 # layers: profiles/gmm_mx_kernel_layer_mx.md.
 GMM_TRAFFIC = [
     {"workload": "layer_train_t16384", "bytes_per_launch": 2.701e9,
@@ -56,6 +56,30 @@ GMM_TRAFFIC = [
          "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
          "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
     {"workload": "layer_decode_mx_t64", "bytes_per_launch": 0.3652e9,
+     "sources": {
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
+         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
+         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
+         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
+    {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 0.3088e9,
+     "sources": {
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
+         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
+         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
+         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
+    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 0.1883e9,
+     "sources": {
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
+         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
+         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
+         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
+    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 0.2914e9,
+     "sources": {
+         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
+         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
+         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
+         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
+    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 0.1881e9,
      "sources": {
          "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
          "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",

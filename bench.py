@@ -7,7 +7,7 @@ whole backward (combine gradients, dX and dW of both GMMs, SwiGLU gradient,
 token gradient).  One step = one forward + backward over one batch.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                        [--impl reference]
+                        [--extra default|none|mx|all] [--impl reference]
 
 Prints one JSON line.  ``value`` is tokens/s of the whole job with inputs
 resident in HBM, timed with CUDA events on the launching stream between a
@@ -17,6 +17,11 @@ outputs copied inside the timed region.  Under torchrun every rank runs its
 own replica (the layer shards by batch with no data-path exchange), so the
 scaling is weak.  ``--impl reference`` times the CPU oracle on a bounded
 token sample of the same workload.
+
+With the default workload the line also carries ``workloads``: the Zipf
+grouped matmul forward + backward (E=8, K=1024, N=2048, M=8192; tensor-bound)
+and the prefill (T=4096) and decode (T=64) layer forwards (HBM-bound), each
+timed the same way with its own per-launch split, roofline, clocks and e2e.
 """
 from __future__ import annotations
 
@@ -40,8 +45,7 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 
 # DRAM bytes per GMM launch (the mean over one step's GMM launches), each from
 # one ncu capture of the sources with these hashes; reported only while they
-# match.  Training step: profiles/gmm_traffic_layer_train_t16384.md; MX
-# layers: profiles/gmm_mx_kernel_layer_mx.md.
+# match (the captures' commands sit beside their summaries).
 GMM_TRAFFIC = [
     {"workload": "layer_train_t16384", "bytes_per_launch": 2.701e9,
      "sources": {
@@ -411,33 +415,53 @@ class LayerMxStep:
 
 
 class GmmStep:
-    """Standalone grouped matmul forward + dX + dW (the Zipf GMM workload)."""
+    """Standalone grouped matmul forward + dX + dW (the Zipf GMM workload).
 
-    def __init__(self, wl, dev, inp):
+    Its inputs (x 16.8 MB, W 33.5 MB, dY 33.5 MB) fit in L2, so the steps
+    rotate through ``nsets`` copies of every input and output: a step reads
+    inputs last touched ``nsets`` steps earlier, with more than L2's capacity
+    of other traffic in between."""
+
+    def __init__(self, wl, dev, inp, nsets=1):
         import torch
         import moe_routed_expert_gb300 as M
         self.M, self.wl, self.dev = M, wl, dev
-        self.x = bf16_dev(inp["x"], dev)
-        self.w = bf16_dev(inp["w"], dev)
-        self.dyv = bf16_dev(inp["dy"], dev) if "dy" in inp else None
-        self.gl = torch.from_numpy(inp["group_list"]).to(dev)
-        self.y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=dev)
-        self.dx = torch.empty_like(self.x)
-        self.dw = torch.empty_like(self.w)
+        self.sets = []
+        for _ in range(nsets):
+            b = {"x": bf16_dev(inp["x"], dev), "w": bf16_dev(inp["w"], dev),
+                 "dy": bf16_dev(inp["dy"], dev) if "dy" in inp else None,
+                 "gl": torch.from_numpy(inp["group_list"]).to(dev),
+                 "y": torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=dev)}
+            b["dx"] = torch.empty_like(b["x"])
+            b["dw"] = torch.empty_like(b["w"])
+            self.sets.append(b)
+        self.cur = self.sets[0]
+        self.nstep = 0
+        # the e2e leg keeps the weights of set 0 resident and copies x and dY in
+        self.w, self.gl, self.y, self.dx, self.dw = (self.cur[n] for n in ("w", "gl", "y", "dx", "dw"))
         self.ws = M.Workspace(256, dev)
         f = 2.0 * wl.M * wl.K * wl.N
         self.stages = [("gmm_fwd", self.fwd, f, 1)]
         if wl.backward:
-            # one gmm_backward call: dX and dW (two launches, side by side when small)
+            # one gmm_backward call: dX and dW (one CTA-pair launch, or two side by side)
             self.stages += [("gmm_bwd_dx_dw", self.bwd, 2 * f, 2)]
         self.units = sum(s[2] for s in self.stages) / 1e12
         self.unit = "TFLOP/s"
+        set_bytes = sum(t.numel() * t.element_size() for t in self.sets[0].values() if t is not None)
+        self.l2 = ("%d rotating sets of inputs and outputs (%.0f MB each), more than L2 between reuses"
+                   % (nsets, set_bytes / 1e6)) if nsets > 1 else "inputs smaller than L2, not rotated"
+
+    def advance(self):
+        self.cur = self.sets[self.nstep % len(self.sets)]
+        self.nstep += 1
 
     def fwd(self):
-        self.M.gmm_forward(self.x, self.w, self.gl, y=self.y, ws=self.ws)
+        c = self.cur
+        self.M.gmm_forward(c["x"], c["w"], c["gl"], y=c["y"], ws=self.ws)
 
     def bwd(self):
-        self.M.gmm_backward(self.x, self.w, self.gl, self.dyv, dx=self.dx, dw=self.dw, ws=self.ws)
+        c = self.cur
+        self.M.gmm_backward(c["x"], c["w"], c["gl"], c["dy"], dx=c["dx"], dw=c["dw"], ws=self.ws)
 
     def e2e_host_inputs(self, inp):
         return {"x": pinned_bf16(inp["x"]), "dy": pinned_bf16(inp["dy"])}
@@ -508,11 +532,11 @@ class E2EPipeline:
             comp.wait_event(self.out_free[b])
 
 
-def make_step(name, dev, tokens=None):
+def make_step(name, dev, tokens=None, nsets=1):
     wl = WORKLOADS[name]
     if name.startswith("gmm"):
         inp = gmm_inputs(wl)
-        return GmmStep(wl, dev, inp), inp
+        return GmmStep(wl, dev, inp, nsets=nsets), inp
     if wl.mx:
         inp = layer_inputs(wl, tokens=tokens, with_weights=False)
         inp.update(mx_layer_weights(wl))
@@ -523,6 +547,33 @@ def make_step(name, dev, tokens=None):
     if tokens is not None:   # a smaller batch of the same workload (profiling captures)
         wl = wl.with_tokens(tokens)
     return (LayerTrainStep(wl, dev, inp) if wl.backward else LayerFwdStep(wl, dev, inp)), inp
+
+
+def layer_bytes(wl, inp):
+    """Algorithmic HBM bytes of one layer forward (the roofline's numerator):
+    the weights of every expert that holds a row, read once, plus the tokens,
+    the routing (ids and weights) and the output, once each.  MX weights count
+    their codes (E2M1 at half a byte) and E8M0 scales."""
+    ids = inp["topk_ids"]
+    counts = np.bincount(ids[ids >= 0].ravel(), minlength=wl.E)
+    live = int((counts > 0).sum())
+    T, H, I, k = wl.T, wl.H, wl.I, wl.k
+    if wl.mx:
+        wb = 0.5 if (wl.w_mx or wl.mx) == "e2m1" else 1.0
+        w = live * (2 * I * (wb * H + H // 32) + H * (wb * I + I // 32))
+    else:
+        w = live * 3 * H * I * 2
+    return w + T * H * 2 * 2 + T * k * 8
+
+
+# The workloads the default run measures beside its headline: the standalone
+# Zipf GMM forward + backward (tensor-bound), and the prefill and decode
+# layer forwards (HBM-bound), each with its own split, roofline, clocks and e2e.
+EXTRA_WORKLOADS = ["gmm_zipf_e8", "layer_prefill_t4096", "layer_decode_t64"]
+MX_WORKLOADS = ["layer_prefill_mx_t4096", "layer_decode_mx_t64", "layer_prefill_a8w4_t4096",
+                "layer_decode_a8w4_t64", "layer_prefill_a4w4_t4096", "layer_decode_a4w4_t64"]
+GMM_SETS = 4            # rotating input sets of the Zipf GMM (4 x 168 MB)
+MIN_TIMED_MS = 200.0    # the extra workloads run at least this long in their timed region
 
 
 # ---------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
@@ -576,37 +627,76 @@ def oracle_gmm_step(wl, inp, rows):
         O.gmm_backward(x, w, gl, f(inp["dy"][:rows]))
 
 
-def cpu_sample(name, inp, target_s=15.0):
-    """Time the oracle, as it stands, on a bounded sample of the workload.
-    Returns (value, unit, sample description, seconds, runner) where runner()
-    repeats the same sample and value is the sample's work per second."""
+def cpu_sample(name, inp):
+    """The oracle's bounded sample of a workload, the same one for the bench's
+    cpu_baseline leg and for the reference arm: the first eighth of the tokens
+    with the slots and weights of the first eighth of the experts (every kept
+    expert does its full-problem work over those tokens), or the first 1024
+    rows of a grouped matmul.  Returns (runner, units per run, unit, description)."""
     wl = WORKLOADS[name]
     if name.startswith("gmm"):
         per_row = (3 if wl.backward else 1) * 2.0 * wl.K * wl.N / 1e12
-        rows = min(wl.M, 512)
-        t0 = time.perf_counter(); oracle_gmm_step(wl, inp, rows); dt = time.perf_counter() - t0
-        if dt < target_s / 3 and rows < wl.M:
-            rows = int(min(wl.M, rows * max(1.0, target_s / max(dt, 1e-3))))
-            t0 = time.perf_counter(); oracle_gmm_step(wl, inp, rows); dt = time.perf_counter() - t0
-        desc = "first %d of %d rows (groups trimmed from the end), fwd%s" % (rows, wl.M, "+dX+dW" if wl.backward else "")
-        return rows * per_row / dt, "TFLOP/s", desc, dt, (lambda: oracle_gmm_step(wl, inp, rows)), rows * per_row
-    # token-equivalents: a token owns k routed rows
+        rows = min(wl.M, 1024)
+        desc = "first %d of %d rows (groups trimmed from the end), fwd%s in float64" % (
+            rows, wl.M, "+dX+dW" if wl.backward else "")
+        return (lambda: oracle_gmm_step(wl, inp, rows)), rows * per_row, "TFLOP/s", desc
     E_s = max(1, wl.E // 8)
     T_s = max(1, wl.T // 8)
     run = oracle_mx_layer_step if wl.mx else oracle_layer_step
     sub, rows = layer_sample(inp, T_s, E_s)
-    t0 = time.perf_counter(); run(wl, sub); dt = time.perf_counter() - t0
-    if dt < target_s / 3 and T_s < wl.T:
-        T_s = int(min(wl.T, T_s * max(1.0, target_s / max(dt, 1e-3))))
-        sub, rows = layer_sample(inp, T_s, E_s)
-        t0 = time.perf_counter(); run(wl, sub); dt = time.perf_counter() - t0
-    tok_eq = rows / wl.k
+    tok_eq = rows / wl.k   # token-equivalents: a token owns k routed rows
     desc = ("first %d of %d tokens, slots of experts 0..%d of %d kept (%d routed rows = %.0f token-equivalents "
             "at k=%d), layer fwd%s%s in float64" % (T_s, wl.T, E_s - 1, wl.E, rows, tok_eq, wl.k,
                                                     "+bwd" if wl.backward else "",
-                                                    " (MX tokens %s, weights %s, quantisation included)" % (wl.mx, wl.w_mx or wl.mx)
-                                                    if wl.mx else ""))
-    return tok_eq / dt, "tokens/s", desc, dt, (lambda: run(wl, sub)), tok_eq
+                                                    " (MX tokens %s, weights %s, quantisation included)"
+                                                    % (wl.mx, wl.w_mx or wl.mx) if wl.mx else ""))
+    return (lambda: run(wl, sub)), tok_eq, "tokens/s", desc
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def cpu_threads():
+    """Threads the oracle's numpy/BLAS calls use (OMP/OpenBLAS limits, else every core)."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    return os.cpu_count()
+
+
+def time_cpu_sample(name, inp, runs=None, min_s=10.0, max_runs=8):
+    """Time the oracle sample: `runs` runs, or repeat until min_s (at most max_runs).
+    Returns (value, unit, sample, seconds, runs)."""
+    fn, units, unit, desc = cpu_sample(name, inp)
+    times = []
+    while True:
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+        if runs is not None:
+            if len(times) >= runs:
+                break
+        elif sum(times) >= min_s or len(times) >= max_runs:
+            break
+    total = sum(times)
+    return units * len(times) / total, unit, desc, total, len(times)
 
 
 def run_reference(args):
@@ -622,9 +712,8 @@ def run_reference(args):
         inp.update(mx_layer_weights(wl))
     else:
         inp = layer_inputs(wl)
-    # one bounded sample per step, sized so the whole run stays within a few minutes
-    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
-    _, unit, sample, _, fn, units = cpu_sample(name, inp, target_s=per_step)
+    # each step runs the same bounded sample the cpu_baseline leg times
+    fn, units, unit, sample = cpu_sample(name, inp)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -633,12 +722,12 @@ def run_reference(args):
             times.append(time.perf_counter() - t0)
     total = sum(times)
     v = units * len(times) / total
-    cores = os.cpu_count()
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": name, "sample": sample},
-            "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": cpu_threads(), "cpu": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -662,6 +751,195 @@ def job_throughput(units_per_rank_step, world, ms_per_step):
     return units_per_rank_step * world / (ms_per_step / 1e3)
 
 
+def l2_note(name, step):
+    if hasattr(step, "l2"):
+        return step.l2
+    wl = step.wl
+    if name.startswith("layer_decode"):
+        return "weights (%s touched) larger than L2" % (
+            "0.35 GB" if wl.w_mx == "e2m1" else ("0.7 GB" if wl.mx else "1.4 GB"))
+    return "inputs larger than L2"
+
+
+# ---------------------------------------------------------------------------- one workload on the GPU
+def measure(name, step, inp, args, steps, warmup, world, dev, peaks, with_e2e=True):
+    """Time `steps` steps of one workload (after `warmup`), then the same steps
+    again with an event after every launch for the per-kernel split, then
+    (with_e2e) the e2e pipeline.  Returns the workload's JSON fields."""
+    import torch
+    import moe_routed_expert_gb300 as M
+    stream = torch.cuda.current_stream()
+    advance = getattr(step, "advance", lambda: None)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def check():
+        st = M.read_status(step.ws)
+        assert st == 0, "device status %s" % M.status_string(st)
+
+    run_step = lambda: (advance(), [fn() for _, fn, _, _ in step.stages])
+    # the sampler starts before the warm-up: nvidia-smi's start-up must not land in the timed region
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    for _ in range(warmup):
+        run_step()
+    check()
+
+    # The headline region records events only at its two ends: an event between
+    # two launches would stop the second one's prologue from overlapping the
+    # first one's tail (programmatic dependent launch).
+    barrier()
+    if args.graph:
+        # one step captured into a CUDA graph (every call is stream-ordered, with no host
+        # synchronisation and no allocation), replayed on the timed stream
+        graph = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(graph, stream=cs):
+                [fn() for _, fn, _, _ in step.stages]
+        stream.wait_stream(cs)
+        graph.replay()
+        barrier()
+        check()
+        run_step = graph.replay
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(steps):
+        run_step()
+    t_end.record(stream)
+    barrier()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    check()
+
+    # Per-kernel breakdown: the same steps again with an event after every launch.
+    ns = len(step.stages)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(steps)]
+    barrier()
+    for s in range(steps):
+        ev = events[s]
+        advance()
+        ev[0].record(stream)
+        for i, (_, fn, _, _) in enumerate(step.stages):
+            fn()
+            ev[i + 1].record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    check()
+
+    stage_ms = [0.0] * ns
+    for s in range(steps):
+        for i in range(ns):
+            stage_ms[i] += events[s][i].elapsed_time(events[s][i + 1])
+    stage_ms = [v / steps for v in stage_ms]
+    ms_per_step = elapsed_ms / steps
+    value = job_throughput(step.units, world, ms_per_step)
+
+    kernels = {}
+    gmm_flops, gmm_ms, gmm_launches = 0.0, 0.0, 0
+    launches = 0
+    for (sname, _, flops, nl), ms in zip(step.stages, stage_ms):
+        entry = {"ms": round(ms, 4), "launches": nl}
+        if flops:
+            entry["tflops"] = round(flops / (ms / 1e3) / 1e12, 1)
+            gmm_flops += flops
+            gmm_ms += ms
+            gmm_launches += nl
+        if hasattr(step, "gmm_bytes") and sname in step.gmm_bytes:
+            entry["gbs"] = round(step.gmm_bytes[sname] / (ms / 1e3) / 1e9, 1)
+        launches += nl
+        kernels[sname] = entry
+
+    if hasattr(step, "gmm_bytes"):
+        gbytes = sum(step.gmm_bytes.values())
+        achieved = gbytes / (gmm_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_gmm_traffic(name) if args.tokens is None else None,
+                "kernel": getattr(step, "kernel", "gmm_kernel (all GMM launches of a step)"),
+                "peak_kind": "hbm copy, %s" % peaks["source"]}
+    else:
+        achieved = gmm_flops / (gmm_ms / 1e3) / 1e12
+        long_step = ms_per_step * steps > 500.0
+        peak = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_gmm_traffic(name) if args.tokens is None else None,
+                "kernel": "gmm_pair_kernel / gmm_kernel (all %d GMM launches of a step)" % gmm_launches,
+                "peak_kind": "bf16 dense %s, %s" % ("sustained" if long_step else "burst", peaks["source"])}
+
+    out = {"value": round(value, 3), "unit": step.unit, "steps": steps, "warmup": warmup,
+           "ms_per_step": round(ms_per_step, 4), "dtype": getattr(step, "dtype", "bf16"),
+           "config": {"workload": name, **{k_: v_ for k_, v_ in vars(step.wl).items() if k_ != "name"},
+                      "l2": l2_note(name, step), "parallelism": "replicas" if world > 1 else "1 GPU"},
+           "roofline": roof, "kernels": kernels,
+           "launch": "one CUDA graph per step (replayed)" if args.graph else "stream launches, programmatic serialisation",
+           "kernels_timing": "CUDA events after every launch, in a second pass of the same steps",
+           "gpu_launches": launches * steps,
+           "gmm_tflops": round(gmm_flops / (gmm_ms / 1e3) / 1e12, 1) if gmm_ms else None}
+    if not name.startswith("gmm") and not getattr(step.wl, "backward", False):
+        lb = layer_bytes(step.wl, inp)
+        t_roof = lb / (peaks["hbm_gbs"] * 1e9) * 1e3
+        out["layer_roofline"] = {"bound": "hbm", "bytes": int(lb), "time_ms": round(t_roof, 4),
+                                 "achieved": round(lb / (ms_per_step / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": round(t_roof / ms_per_step, 4),
+                                 "what": "whole layer step: weights of the experts with rows, tokens, routing and "
+                                         "output once each, against the measured copy rate"}
+    if clock_info is not None:
+        out["clocks"] = clock_info
+
+    # end to end through the public entry points, host buffers, copies inside the timed region
+    if with_e2e:
+        pipe = E2EPipeline(step, inp)
+        pipe.run(2)
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pipe.h2d.wait_stream(stream)
+        pipe.d2h.wait_stream(stream)
+        pipe.run(steps)
+        b.record(stream)
+        barrier()
+        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        out["e2e"] = {"value": round(job_throughput(step.units, world, e_ms / steps), 3), "unit": step.unit,
+                      "h2d_bytes_per_step": int(pipe.h2d_bytes), "d2h_bytes_per_step": int(pipe.d2h_bytes),
+                      "ms_per_step": round(e_ms / steps, 4), "api": step.e2e_api,
+                      "copies": "pinned host buffers; two buffer sets, H2D and D2H on their own streams"}
+        check()
+        del pipe
+    return out
+
+
+def extra_steps(step, args, world, dev):
+    """Steps for an extra workload: the headline's count, or more, so that its
+    timed region lasts at least MIN_TIMED_MS (clock samples land inside it)."""
+    import torch
+    advance = getattr(step, "advance", lambda: None)
+    for _ in range(2):
+        advance()
+        [fn() for _, fn, _, _ in step.stages]
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        advance()
+        [fn() for _, fn, _, _ in step.stages]
+    b.record()
+    torch.cuda.synchronize()
+    est = max(a.elapsed_time(b) / 3, 1e-3)
+    n = max(args.steps, int(np.ceil(MIN_TIMED_MS / est)))
+    return int(max_over_ranks(n, world, dev))
+
+
 # ---------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -672,6 +950,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--extra", default="default", choices=["default", "none", "mx", "all"],
+                    help="workloads timed beside the headline: the Zipf GMM and the prefill / decode layers "
+                         "(default, with the default workload), none, the MX layers, or all of them")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph (the per-kernel split stays eager)")
     ap.add_argument("--tokens", type=int, default=None,
@@ -695,151 +976,41 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    import moe_routed_expert_gb300 as M
 
-    step, inp = make_step(args.workload, dev, args.tokens)
     peaks = load_peaks()
-    stream = torch.cuda.current_stream()
-
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    # the sampler starts before the warm-up: nvidia-smi's start-up must not land in the timed region
-    clocks = ClockSampler(local)
-    clocks.start()
-    for _ in range(args.warmup):
-        for _, fn, _, _ in step.stages:
-            fn()
-    assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
-
-    # The headline region records events only at its two ends: an event between
-    # two launches would stop the second one's prologue from overlapping the
-    # first one's tail (programmatic dependent launch).
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    run_step = lambda: [fn() for _, fn, _, _ in step.stages]
-    if args.graph:
-        # one step captured into a CUDA graph (every call is stream-ordered, with no host
-        # synchronisation and no allocation), replayed on the timed stream
-        graph = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(device=dev)
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(graph, stream=cs):
-                run_step()
-        stream.wait_stream(cs)
-        graph.replay()
-        barrier()
-        assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
-        run_step = graph.replay
-    t_start.record(stream)
-    for s in range(args.steps):
-        run_step()
-    t_end.record(stream)
-    barrier()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
-
-    # Per-kernel breakdown: the same K steps again with an event after every launch.
-    ns = len(step.stages)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
-    barrier()
-    for s in range(args.steps):
-        ev = events[s]
-        ev[0].record(stream)
-        for i, (_, fn, _, _) in enumerate(step.stages):
-            fn()
-            ev[i + 1].record(stream)
-    barrier()
-    clock_info = clocks.stop()
-    assert M.read_status(step.ws) == 0, "device status %s" % M.status_string(M.read_status(step.ws))
-
-    stage_ms = [0.0] * ns
-    for s in range(args.steps):
-        for i in range(ns):
-            stage_ms[i] += events[s][i].elapsed_time(events[s][i + 1])
-    stage_ms = [v / args.steps for v in stage_ms]
-    ms_per_step = elapsed_ms / args.steps
-    value = job_throughput(step.units, world, ms_per_step)
-
-    kernels = {}
-    gmm_flops, gmm_ms, gmm_launches = 0.0, 0.0, 0
-    launches = 0
-    for (name, _, flops, nl), ms in zip(step.stages, stage_ms):
-        entry = {"ms": round(ms, 4), "launches": nl}
-        if flops:
-            entry["tflops"] = round(flops / (ms / 1e3) / 1e12, 1)
-            gmm_flops += flops
-            gmm_ms += ms
-            gmm_launches += nl
-        launches += nl
-        kernels[name] = entry
-
-    hbm_bound = hasattr(step, "gmm_bytes")
-    if hbm_bound:
-        gbytes = sum(step.gmm_bytes.values())
-        achieved = gbytes / (gmm_ms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": measured_gmm_traffic(args.workload) if args.tokens is None else None,
-                "kernel": getattr(step, "kernel", "gmm_kernel (all GMM launches of a step)"),
-                "peak_kind": "hbm copy, %s" % peaks["source"]}
-    else:
-        achieved = gmm_flops / (gmm_ms / 1e3) / 1e12
-        long_step = ms_per_step * args.steps > 500.0
-        peak = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
-        traffic = measured_gmm_traffic(args.workload) if args.tokens is None else None
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "gmm_pair_kernel / gmm_kernel (all %d GMM launches of a step)" % gmm_launches,
-                "peak_kind": "bf16 dense %s, %s" % ("sustained" if long_step else "burst", peaks["source"])}
-
-    line = {"metric": METRIC, "value": round(value, 3), "unit": step.unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": getattr(step, "dtype", "bf16"), "data": "synthetic",
-            "config": {"workload": args.workload, **{k_: v_ for k_, v_ in vars(step.wl).items() if k_ != "name"},
-                       "l2": "inputs larger than L2" if not args.workload.startswith("layer_decode")
-                       else "weights (%s touched) larger than L2" % (
-                           "0.35 GB" if step.wl.w_mx == "e2m1" else ("0.7 GB" if step.wl.mx else "1.4 GB")), "parallelism": "replicas" if world > 1 else "1 GPU"},
-            "roofline": roof, "kernels": kernels,
-            "launch": "one CUDA graph per step (replayed)" if args.graph else "stream launches, programmatic serialisation",
-            "kernels_timing": "CUDA events after every launch, in a second pass of the same steps",
-            "gpu_launches": launches * args.steps,
-            "gmm_tflops": round(gmm_flops / (gmm_ms / 1e3) / 1e12, 1) if gmm_ms else None}
-    if clock_info is not None:
-        line["clocks"] = clock_info
-
-    # end to end through the public entry points, host buffers, copies inside the timed region
-    if not args.no_e2e:
-        pipe = E2EPipeline(step, inp)
-        pipe.run(2)
-        barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        pipe.h2d.wait_stream(stream)
-        pipe.d2h.wait_stream(stream)
-        pipe.run(args.steps)
-        b.record(stream)
-        barrier()
-        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
-        line["e2e"] = {"value": round(job_throughput(step.units, world, e_ms / args.steps), 3), "unit": step.unit,
-                       "h2d_bytes_per_step": int(pipe.h2d_bytes), "d2h_bytes_per_step": int(pipe.d2h_bytes),
-                       "ms_per_step": round(e_ms / args.steps, 4), "api": step.e2e_api,
-                       "copies": "pinned host buffers; two buffer sets, H2D and D2H on their own streams"}
-        assert M.read_status(step.ws) == 0
-
+    nsets = GMM_SETS if args.workload.startswith("gmm") and WORKLOADS[args.workload].M >= 1024 else 1
+    step, inp = make_step(args.workload, dev, args.tokens, nsets=nsets)
+    res = measure(args.workload, step, inp, args, args.steps, args.warmup, world, dev, peaks,
+                  with_e2e=not args.no_e2e)
+    line = {"metric": METRIC, "value": res["value"], "unit": res["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": res["dtype"], "data": "synthetic"}
+    line.update({k_: v_ for k_, v_ in res.items() if k_ not in line and k_ not in ("steps", "warmup")})
     if args.tokens is not None:
         line["config"]["note"] = "first %d tokens only: a profiling run, not the workload's bench line" % args.tokens
     if rank == 0 and not args.no_cpu_baseline:
-        v, unit, sample, secs, _, _ = cpu_sample(args.workload, inp)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": sample, "seconds": round(secs, 2)}
+        v, unit, sample, secs, runs = time_cpu_sample(args.workload, inp)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": unit, "cores": cpu_threads(), "cpu": cpu_model(),
+                                "kind": "oracle", "sample": sample, "runs": runs, "seconds": round(secs, 2)}
+
+    extras = []
+    if args.tokens is None and not args.graph:
+        if args.extra in ("default", "all") and (args.workload == DEFAULT_WORKLOAD or args.extra == "all"):
+            extras += [w for w in EXTRA_WORKLOADS if w != args.workload]
+        if args.extra in ("mx", "all"):
+            extras += [w for w in MX_WORKLOADS if w != args.workload]
+    if extras:
+        del step, inp
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in extras:
+            nsets = GMM_SETS if name.startswith("gmm") else 1
+            st, ip = make_step(name, dev, nsets=nsets)
+            n = extra_steps(st, args, world, dev)
+            line["workloads"][name] = measure(name, st, ip, args, n, args.warmup, world, dev, peaks,
+                                              with_e2e=not args.no_e2e)
+            del st, ip
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

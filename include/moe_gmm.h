@@ -170,13 +170,17 @@ MOE_API moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids,
  * it exists for those callers.
  *
  * Same arguments, outputs and results as moe_permute, with no workspace:
- *   device_status  NULL, or a device word the caller owns and zeroes; bad ids
- *                  set it to MOE_ERR_DEVICE (sticky, like the workspace word).
+ *   device_status  NULL, or a 4-byte-aligned device word the caller owns and
+ *                  zeroes; bad ids set it to MOE_ERR_DEVICE (sticky, like the
+ *                  workspace word).  A misaligned word gives MOE_ERR_INVALID.
  * Scratch: one fixed device array inside the library, 512 KiB of int32
  * counters, held by every device that loads the library until the process
  * exits.  Sizes with ceil(T*k / 1024) * E > 131072 return MOE_ERR_UNSUPPORTED.
- * The first call on a device looks up that array's device address (with the
- * device current); make that first call before any stream capture.  It calls
+ * The first call in each CUDA context of a device looks up that array's
+ * device address (with the device current), so a context rebuilt after
+ * cudaDeviceReset gets its own; make that first call before any stream
+ * capture.  Each rank block of the index pass reads every chunk's counters:
+ * about (T*k / 1024)^2 * E * 4 bytes of L2 reads, 8 GB at the size limit.  It calls
  * no allocator.  All calls share the array, so calls whose kernels overlap on
  * the GPU race: order them on one stream. */
 MOE_API moe_status_t moe_permute_no_alloc(const moe_bf16* x, const int32_t* topk_ids,

@@ -118,6 +118,22 @@ moe_status_t check_tokens(int64_t T, int64_t H, int64_t k) {
 }
 
 }  // namespace
+
+// Argument checks of the permute, shared by moe_permute and moe_permute_no_alloc.
+moe_status_t check_permute_args(const uint16_t* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k,
+                                int64_t E, const uint16_t* x_perm, const int64_t* group_list,
+                                const int32_t* row_id_map, const int32_t* sorted_flat) {
+  if (!group_list) return MOE_ERR_NULLPTR;
+  if (T != 0 && (!topk_ids || !row_id_map || !sorted_flat)) return MOE_ERR_NULLPTR;  // T == 0: nothing to read or write
+  if (T != 0 && (x == nullptr) != (x_perm == nullptr)) return MOE_ERR_NULLPTR;
+  if (E <= 0 || k > E) return MOE_ERR_INVALID;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = check_tokens(T, x ? H : 8, k);
+  if (st != MOE_OK) return st;
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -169,14 +185,8 @@ size_t moe_permute_workspace_size(int64_t T, int64_t k, int64_t E) {
 moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k, int64_t E,
                          moe_bf16* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!group_list) return MOE_ERR_NULLPTR;
-  if (T != 0 && (!topk_ids || !row_id_map || !sorted_flat)) return MOE_ERR_NULLPTR;  // T == 0: nothing to read or write
-  if (T != 0 && (x == nullptr) != (x_perm == nullptr)) return MOE_ERR_NULLPTR;
-  if (E <= 0 || k > E) return MOE_ERR_INVALID;
-  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
-  moe_status_t st = check_tokens(T, x ? H : 8, k);
+  moe_status_t st = check_permute_args(x, topk_ids, T, H, k, E, x_perm, group_list, row_id_map, sorted_flat);
   if (st != MOE_OK) return st;
-  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID;
   if ((st = check_ws(ws, ws_bytes, moe_permute_workspace_size(T, k, E))) != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T == 0)

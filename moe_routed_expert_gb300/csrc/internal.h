@@ -55,6 +55,10 @@ moe_status_t launch_mx_gather(const uint16_t* x, int64_t nslots, int64_t H, int 
                               const MxOut& out, cudaStream_t s);
 
 // ---- dispatch (permute.cu)
+// Argument checks shared by the permute entry points (abi.cu).
+moe_status_t check_permute_args(const uint16_t* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k,
+                                int64_t E, const uint16_t* x_perm, const int64_t* group_list,
+                                const int32_t* row_id_map, const int32_t* sorted_flat);
 size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E);
 // With `mx`, the gathered rows leave quantised into mx->q / mx->scales (x_perm unused).
 moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,

@@ -8,6 +8,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -105,3 +106,31 @@ def test_reference_arm_json_line():
 def test_reference_arm_other_ranks_exit_quietly():
     out = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
     assert not [l for l in out.splitlines() if l.startswith("{")]
+
+
+def test_layer_roofline_bytes_of_the_prefill_layer():
+    """Weights of every expert with rows once, tokens in and out once, routing once:
+    256 live experts x 3 H I bf16 + 2 T H bf16 + T k (int32 + fp32) = 1.644 GB."""
+    from workloads import WORKLOADS as W
+    wl = W["layer_prefill_t4096"]
+    ids = np.tile(np.arange(8, dtype=np.int32), (wl.T, 1))
+    ids[:, :] = (np.arange(wl.T * 8).reshape(wl.T, 8) % wl.E).astype(np.int32)   # every expert holds rows
+    b = bench.layer_bytes(wl, {"topk_ids": ids})
+    assert b == 256 * 3 * 2048 * 512 * 2 + 2 * 4096 * 2048 * 2 + 4096 * 8 * 8
+    assert abs(b / 1e9 - 1.644) < 0.001
+    ids[:, :] = 0   # one expert: only its weights count
+    assert bench.layer_bytes(wl, {"topk_ids": ids}) == 3 * 2048 * 512 * 2 + 2 * 4096 * 2048 * 2 + 4096 * 8 * 8
+
+
+def test_cpu_baseline_and_reference_arm_share_one_sample():
+    """Both CPU arms time the same oracle sample of the same workload."""
+    from workloads import WORKLOADS as W, layer_inputs
+    wl = W["layer_decode_t64"]
+    inp = {"topk_ids": np.zeros((wl.T, wl.k), np.int32), "topk_w": np.zeros((wl.T, wl.k), np.float32),
+           "x": np.zeros((wl.T, wl.H), np.uint16)}
+    _, units_a, unit_a, desc_a = bench.cpu_sample("layer_decode_t64", inp)
+    _, units_b, unit_b, desc_b = bench.cpu_sample("layer_decode_t64", inp)
+    assert (units_a, unit_a, desc_a) == (units_b, unit_b, desc_b)
+    assert "first 8 of 64 tokens" in desc_a and "experts 0..31 of 256" in desc_a
+    assert bench.cpu_model()
+    assert bench.cpu_threads() >= 1

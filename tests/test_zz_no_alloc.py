@@ -74,3 +74,38 @@ def test_no_alloc_permute_rejects_sizes_beyond_its_scratch(lib):
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     assert lib.moe_permute_no_alloc(None, fake, 1 << 20, 0, 8, 1024, None, fake, fake, fake, None, stream) == 3
     assert lib.moe_permute_no_alloc(None, None, 16, 0, 2, 8, None, fake, fake, fake, None, stream) == 1
+
+
+def test_no_alloc_permute_bad_id_null_status_empty_batch_and_binding(lib):
+    import torch
+    import moe_routed_expert_gb300 as M
+    dev = "cuda"
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    T, H, k, E = 40, 64, 2, 8
+    ids = torch.from_numpy(np.stack([np.arange(k) + (t % (E - k)) for t in range(T)]).astype(np.int32)).to(dev)
+    x = torch.randn(T, H, device=dev).to(torch.bfloat16)
+    # an id equal to E: the device status word records MOE_ERR_DEVICE
+    bad = ids.clone()
+    bad[3, 1] = E
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    M.moe_permute_no_alloc(x, bad, E, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    # no status word at all: the same call runs and the good ids are ranked as moe_permute ranks them
+    got = M.moe_permute_no_alloc(x, ids, E, device_status=None)
+    want = M.moe_permute(x, ids, E)
+    torch.cuda.synchronize()
+    R = int(want[1].sum().item())
+    assert R == T * k
+    for a, b in zip(want[1:], got[1:]):
+        assert torch.equal(a, b)
+    assert torch.equal(want[0][:R], got[0][:R])
+    # an empty batch: every expert gets zero rows, and the row tensors may be NULL
+    gl = torch.full((E,), -7, dtype=torch.int64, device=dev)
+    assert lib.moe_permute_no_alloc(None, None, 0, H, k, E, None, _p(gl), None, None, None, stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(gl, torch.zeros(E, dtype=torch.int64, device=dev))
+    # a status word that is not 4-byte aligned is refused on the host
+    odd = C.c_void_p(status.data_ptr() + 2)
+    assert lib.moe_permute_no_alloc(None, _p(ids), T, 0, k, E, None, _p(gl), _p(got[2]), _p(got[3]), odd,
+                                    stream) == 2

@@ -226,6 +226,54 @@ MOE_API moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const
                              const moe_activation_t* activation, int w_flags, moe_bf16* y, moe_bf16* h_save,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Dispatch fused into the gate_up grouped matmul ([MegaMoE] "算子功能": the
+ * dispatch and the first expert matmul with its activation in one operator;
+ * the GMM of [GMM] "算子语义" over the permuted rows of [GMM] "Qwen3.5 MoE 路径").
+ * Computes gmm_forward_act(x_perm, w, ...) with an activation, where the
+ * permuted rows are never stored: row r of the grouped operand is token
+ * sorted_flat[r] / k of x, fetched from x by the kernel (TMA gather of four
+ * rows per copy).
+ *   x           [T, K] bf16 tokens
+ *   sorted_flat [M] int32 from moe_permute (row -> flat slot t * k + j); rows
+ *               at and past sum(group_list) are not read
+ *   w           [E, K, N] bf16 (or [E, N, K] with MOE_W_TRANSPOSED), N = 2I,
+ *               a multiple of 256
+ *   group_list  [E] int64 counts (device), sum <= M
+ *   activation  required (the gated activation of the [gate | up] product)
+ *   y           [M, N/2] bf16 out
+ * Workspace: gmm_workspace_size(M, K, N, E).  A slot outside [0, T*k) in the
+ * rows read sets MOE_ERR_DEVICE (the row reads token 0).  128-row tiles. */
+MOE_API moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* sorted_flat, int64_t T, int64_t k,
+                             const moe_bf16* w, const int64_t* group_list,
+                             int64_t M, int64_t K, int64_t N, int64_t E,
+                             const moe_activation_t* activation, int w_flags, moe_bf16* y,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Workspace bytes for gmm_forward_combine: the status block, T * ceil(N/256)
+ * int32 arrival counts and an [M, N] bf16 scratch for the expert outputs. */
+MOE_API size_t gmm_forward_combine_workspace_size(int64_t T, int64_t k, int64_t M, int64_t N);
+
+/* The down grouped matmul fused with the weighted top-k combine ([MegaMoE]
+ * "算子功能" and "Token Combine": y_i = sum_k w_k Y_{e_ik}[row(i,k)]):
+ *   Y = gmm_forward(a, w) over the groups of group_list (never returned), and
+ *   y[t] = sum over j in 0..k-1 with row_id_map[t*k+j] >= 0 of
+ *          topk_w[t*k+j] * Y[row_id_map[t*k+j]],
+ * summed in fp32 in slot order and rounded once to bf16: the same arithmetic,
+ * and so the same bits, as gmm_forward followed by moe_unpermute.  Each token
+ * is summed as soon as the last of its k rows is stored, while the rows are
+ * still in L2; the rows are then dropped from L2 unwritten.
+ *   a           [M, K] bf16, rows grouped by expert; w [E, K, N] (or [E, N, K]
+ *               with MOE_W_TRANSPOSED); group_list [E] int64 counts
+ *   row_id_map, sorted_flat  [T*k] / [M] int32 from moe_permute
+ *   topk_w      [T, k] fp32;  y [T, N] bf16 out (tokens without a routed slot
+ *               get zeros)
+ * Workspace: gmm_forward_combine_workspace_size(T, k, M, N).  Out-of-range
+ * rows or slots set MOE_ERR_DEVICE.  128-row tiles. */
+MOE_API moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int64_t* group_list,
+                             const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
+                             int64_t T, int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, int w_flags,
+                             moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Grouped matmul backward: [GMM] "算子语义" backward formulas
  *   dx[s:e] = dy[s:e] @ w[g]^T            (dx [M, K], NULL to skip)
  *   dw[g]   = x[s:e]^T @ dy[s:e]          (dw [E, K, N], NULL to skip;
@@ -328,7 +376,13 @@ MOE_API size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t
  * permute -> GMM(w1 [E, H, 2I]) with SwiGLU(clip) -> GMM(w2 [E, I, H]) -> combine.
  *   x [T, H] bf16, topk_ids [T, k] int32, topk_w [T, k] fp32, y [T, H] bf16 out.
  *   saved: NULL for inference (intermediates live in ws), or the buffers that
- *   moe_layer_backward will read. */
+ *   moe_layer_backward will read.
+ * Inference with T*k < 512*E (groups that average under 512 rows) runs fused
+ * ([MegaMoE] "算子功能"): the permute's index pass, gmm_forward_gather_act and
+ * gmm_forward_combine, three launches (four above 1024 routed slots); the
+ * permuted tokens and the expert outputs are never written to HBM.  The result
+ * is bit-identical to the unfused chain (moe_permute, gmm_forward with the
+ * activation, gmm_forward, moe_unpermute), which the other cases run. */
 MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
                                const moe_bf16* w1, const moe_bf16* w2,
                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,

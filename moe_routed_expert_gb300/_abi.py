@@ -50,6 +50,10 @@ SIGNATURES = {
     "gmm_backward": (ST, [P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
     "gmm_backward_ex": (ST, [P, P, P, P, I64, I64, I64, I64, INT, P, P, P, SZ, P]),
     "gmm_forward_act": (ST, [P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P, P, P, SZ, P]),
+    "gmm_forward_gather_act": (ST, [P, P, I64, I64, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P,
+                                    P, SZ, P]),
+    "gmm_forward_combine_workspace_size": (SZ, [I64, I64, I64, I64]),
+    "gmm_forward_combine": (ST, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, INT, P, P, SZ, P]),
     "gmm_backward_dx_swiglu": (ST, [P, P, P, P, I64, I64, I64, I64, F32, P, P, SZ, P]),
     "gmm_backward_dx_act": (ST, [P, P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P, P, SZ, P]),
     "moe_unpermute_workspace_size": (SZ, []),

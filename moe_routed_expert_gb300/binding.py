@@ -214,6 +214,61 @@ def gmm_forward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, *, e
     return y
 
 
+def gmm_forward_gather_act(x: torch.Tensor, sorted_flat: torch.Tensor, k: int, w: torch.Tensor,
+                           group_list: torch.Tensor, activation=("swiglu", ()), *, M: Optional[int] = None,
+                           y: Optional[torch.Tensor] = None, w_transposed: bool = False,
+                           ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """The gate_up GMM with its activation over rows gathered from x: row r of
+    the grouped operand is token sorted_flat[r] // k (M rows, default
+    len(sorted_flat)); returns y [M, N/2]."""
+    _dtype(x, BF16, "x")
+    _dtype(sorted_flat, torch.int32, "sorted_flat")
+    _dtype(w, BF16, "w")
+    _dtype(group_list, torch.int64, "group_list")
+    T, K = x.shape
+    M = sorted_flat.shape[0] if M is None else M
+    E, K2, N = w.shape
+    if w_transposed:
+        K2, N = N, K2
+    if K2 != K:
+        raise ValueError("x and w disagree on K")
+    if y is None:
+        y = torch.empty(M, N // 2, dtype=BF16, device=x.device)
+    wsp = _ws(ws, gmm_workspace_size(M, K, N, E), x.device)
+    _check(_lib().gmm_forward_gather_act(_ptr(x), _ptr(sorted_flat), T, k, _ptr(w), _ptr(group_list), M, K, N, E,
+                                         C.byref(_act(activation)), int(bool(w_transposed)), _ptr(y), wsp.ptr,
+                                         wsp.nbytes, _stream(stream)), "gmm_forward_gather_act")
+    return y
+
+
+def gmm_forward_combine_workspace_size(T, k, M, N) -> int:
+    return int(_lib().gmm_forward_combine_workspace_size(T, k, M, N))
+
+
+def gmm_forward_combine(a: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, row_id_map: torch.Tensor,
+                        sorted_flat: torch.Tensor, topk_w: torch.Tensor, *, y: Optional[torch.Tensor] = None,
+                        w_transposed: bool = False, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """The down GMM fused with the weighted top-k combine: y [T, N] =
+    moe_unpermute(gmm_forward(a, w), row_id_map, topk_w), bit for bit."""
+    _dtype(a, BF16, "a")
+    _dtype(w, BF16, "w")
+    _dtype(group_list, torch.int64, "group_list")
+    _dtype(row_id_map, torch.int32, "row_id_map")
+    _dtype(sorted_flat, torch.int32, "sorted_flat")
+    _dtype(topk_w, torch.float32, "topk_w")
+    M, K = a.shape
+    T, k = topk_w.shape
+    E = w.shape[0]
+    N = w.shape[1] if w_transposed else w.shape[2]
+    if y is None:
+        y = torch.empty(T, N, dtype=BF16, device=a.device)
+    wsp = _ws(ws, gmm_forward_combine_workspace_size(T, k, M, N), a.device)
+    _check(_lib().gmm_forward_combine(_ptr(a), _ptr(w), _ptr(group_list), _ptr(row_id_map), _ptr(sorted_flat),
+                                      _ptr(topk_w), T, k, M, K, N, E, int(bool(w_transposed)), _ptr(y), wsp.ptr,
+                                      wsp.nbytes, _stream(stream)), "gmm_forward_combine")
+    return y
+
+
 def gmm_backward(x: torch.Tensor, w: torch.Tensor, group_list: torch.Tensor, dy: torch.Tensor, *,
                  need_dx: bool = True, need_dw: bool = True, dx=None, dw=None, w_transposed: bool = False,
                  ws: Optional[Workspace] = None, stream=None):

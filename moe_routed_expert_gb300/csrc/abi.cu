@@ -230,6 +230,60 @@ moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* gr
                          ws, ws_bytes, stream);
 }
 
+moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* sorted_flat, int64_t T, int64_t k,
+                                    const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K, int64_t N,
+                                    int64_t E, const moe_activation_t* activation, int w_flags, moe_bf16* y,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !sorted_flat || !w || !group_list || !y || !activation) return MOE_ERR_NULLPTR;
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
+  if (st != MOE_OK) return st;
+  if ((st = check_gmm_dims(M, K, N, E)) != MOE_OK) return st;
+  if ((st = check_tokens(T, K, k)) != MOE_OK) return st;
+  if (w_flags & ~MOE_W_TRANSPOSED) return MOE_ERR_INVALID;
+  if (N % 256) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(group_list) & 7u) ||
+      (reinterpret_cast<uintptr_t>(sorted_flat) & 3u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_workspace_size(M, K, N, E))) != MOE_OK) return st;
+  if (M == 0 || T == 0) return MOE_OK;
+  return launch_gmm_gather_act(x, sorted_flat, T, k, w, group_list, M, K, N, E, act, (w_flags & MOE_W_TRANSPOSED) != 0,
+                               y, nullptr, 0, status_of(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gmm_forward_combine_workspace_size(int64_t T, int64_t k, int64_t M, int64_t N) {
+  (void)k;
+  if (T <= 0 || M < 0 || N <= 0) return MOE_STATUS_BYTES;
+  return MOE_STATUS_BYTES + fused_counter_bytes(T, N) + align256(static_cast<size_t>(M) * N * 2);
+}
+
+moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int64_t* group_list,
+                                 const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
+                                 int64_t T, int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, int w_flags,
+                                 moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!w || !group_list || !y) return MOE_ERR_NULLPTR;
+  if (T != 0 && (!row_id_map || !topk_w)) return MOE_ERR_NULLPTR;
+  if (M != 0 && (!a || !sorted_flat)) return MOE_ERR_NULLPTR;
+  moe_status_t st = check_gmm_dims(M, K, N, E);
+  if (st != MOE_OK) return st;
+  if ((st = check_tokens(T, N, k)) != MOE_OK) return st;
+  if (w_flags & ~MOE_W_TRANSPOSED) return MOE_ERR_INVALID;
+  if ((a && !aligned16(a)) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(group_list) & 7u) ||
+      (reinterpret_cast<uintptr_t>(row_id_map) & 3u) || (reinterpret_cast<uintptr_t>(sorted_flat) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, gmm_forward_combine_workspace_size(T, k, M, N))) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0)  // no expert rows: every token's sum is empty
+    return cudaMemsetAsync(y, 0, static_cast<size_t>(T) * N * 2, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  int32_t* counters = reinterpret_cast<int32_t*>(after_status(ws));
+  moe_bf16* y2 = reinterpret_cast<moe_bf16*>(after_status(ws) + fused_counter_bytes(T, N));
+  if (cudaMemsetAsync(counters, 0, fused_counter_bytes(T, N), s) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_gmm_combine(a, w, group_list, row_id_map, sorted_flat, topk_w, T, k, M, K, N, E,
+                            (w_flags & MOE_W_TRANSPOSED) != 0, y2, counters, y, status_of(ws), s);
+}
+
 moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
                              int64_t M, int64_t K, int64_t N, int64_t E, int w_flags, moe_bf16* dx, moe_bf16* dw,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -407,6 +461,17 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
     sflat = reinterpret_cast<int32_t*>(p);   p += align256(R * 4);
     gl = reinterpret_cast<int64_t*>(p);
     h = nullptr;
+  }
+  if (!saved && R < kPairMinRowsPerGroup * E) {
+    // Inference with groups that average under 512 rows (the 128-row kernel's
+    // regime): the fused forward.  The permute only ranks the slots; gate_up
+    // reads its rows straight from x, and down combines each token as soon as
+    // its k rows are stored, so neither x_perm nor the expert outputs make a
+    // round trip through HBM.  The arrival counts sit where x_perm would.
+    if ((st = launch_permute(nullptr, topk_ids, T, H, k, E, nullptr, gl, rmap, sflat, status, scratch, s)) != MOE_OK)
+      return st;
+    return launch_layer_fused(x, w1, w2, gl, rmap, sflat, topk_w, T, H, I, E, k, act, w_flags, a, y2,
+                              reinterpret_cast<int32_t*>(x_perm), y, status, s);
   }
   if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
   GmmLaunch how1, how2;

@@ -26,26 +26,6 @@ constexpr int THREADS = 256;
 constexpr int COLS_PER_BLOCK = THREADS * 8;  // 2048 bf16 per block row segment
 constexpr int JB = 8;                         // slots loaded together
 
-__device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
-  acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
-  acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
-  acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
-  acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
-  acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
-  acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
-  acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
-  acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
-  uint4 q;
-  q.x = pack_bf16x2(a[0], a[1]);
-  q.y = pack_bf16x2(a[2], a[3]);
-  q.z = pack_bf16x2(a[4], a[5]);
-  q.w = pack_bf16x2(a[6], a[7]);
-  return q;
-}
-
 // Rows of the slots [j0, j0 + JB) of token t; a row outside [-1, rows_cap)
 // raises MOE_ERR_DEVICE and counts as unused.
 __device__ __forceinline__ void slot_rows(const int32_t* __restrict__ row_id_map, int64_t t, int j0, int k,

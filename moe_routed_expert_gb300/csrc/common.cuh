@@ -32,6 +32,30 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// acc[i] += w * (bf16 element i of v), one fused multiply-add each: the
+// combine's per-slot step (the standalone kernel and the fused down GMM share
+// it, so both give the same bits).
+__device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
+  acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+  acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+  acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+  acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+  acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
+  acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
+  acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
+  acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+}
+
+// Eight floats rounded to bf16 (nearest even) and packed.
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+  uint4 q;
+  q.x = pack_bf16x2(a[0], a[1]);
+  q.y = pack_bf16x2(a[2], a[3]);
+  q.z = pack_bf16x2(a[4], a[5]);
+  q.w = pack_bf16x2(a[6], a[7]);
+  return q;
+}
+
 // sigma(z) = 1 / (1 + e^-z) with the hardware exponential and an approximate
 // reciprocal (2 ulp): every use rounds its result to bf16 (8 significant bits).
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
@@ -216,6 +240,49 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       " [%0], [%1, {%3, %4, %5}], [%2];"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Four rows of a 2D tensor whose map has a one-row box (64 bf16 columns), rows
+// r0..r3 at column c0, written to consecutive 128-byte rows at dst (with the
+// map's swizzle, which follows the shared-memory address like a tile copy's).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
+// An L2 policy under which lines are the first to be evicted (for data read
+// once, such as streamed weights, so it does not push out data read again).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+// 16-byte load cached in L2 only (data another SM wrote during this kernel).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+
+// Drop a 128-byte line from L2 without writing it back: for scratch that is
+// dead once read (its memory then holds undefined values).
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
 }
 
 // ----------------------------------------------------------------- TMA descriptors edited on the device

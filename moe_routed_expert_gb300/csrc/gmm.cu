@@ -28,6 +28,23 @@
 // columns in L2.
 // Every wait is bounded; on a timeout the kernel drains its own copies and
 // MMAs, writes MOE_ERR_TIMEOUT to the status word and returns.
+//
+// The fused layer forward ("MegaMoE", 算子功能: dispatch, the two expert
+// matmuls with the activation between them, and the combine as one operator)
+// runs two variants of this kernel, and neither the permuted tokens nor the
+// expert outputs ever make a round trip through HBM:
+//   FUSE_GATHER   gate_up: A rows are fetched straight from the tokens x by
+//                 TMA gather4 (four rows per copy), row r of a group being
+//                 token sorted_flat[r] / k; x stays in L2 (read k times).
+//   FUSE_COMBINE  down: tiles are visited column tile slowest, so the expert
+//                 outputs of one 256-column slice stay in L2 while it lasts.
+//                 After storing its rows, each epilogue thread counts its
+//                 token's slot in for this slice; the thread whose count
+//                 completes the token hands it to its warp, which sums the
+//                 token's k rows in slot order j = 0, 1, ... with the routing
+//                 weights (fp32, one bf16 rounding: the same arithmetic as the
+//                 standalone combine, so the same bits) and can drop the rows
+//                 from L2 unwritten.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -69,7 +86,21 @@ struct GmmParams {
   uint32_t* status;
   int concurrent;      // see GmmLaunch
   int wt;              // each expert's weight stored transposed, [N, K]
+  // fused layer forward
+  const int32_t* sorted_flat;  // GATHER, COMBINE: permuted row -> flat slot t * k + j
+  const int32_t* row_id_map;   // COMBINE, GATHER set-up: flat slot -> row (-1: unused)
+  const float* topk_w;         // COMBINE: routing weights [T, k]
+  int k;                       // slots per token
+  int64_t T;                   // tokens
+  uint16_t* y;                 // COMBINE: the combined output [T, out_cols]
+  int32_t* counters;           // per-token arrival counts of the down GMM, [its tile_cols][T]
+  int64_t n_counters;          // GATHER: counts to zero for the down GMM that follows
+  int cols_slow;               // tiles visited column tile slowest
+  int discard;                 // COMBINE: expert rows dropped from L2 once combined
+  int w_evict_first;           // weight tiles loaded under an L2 evict-first policy
 };
+
+enum GmmFuse { FUSE_NONE = 0, FUSE_GATHER = 1, FUSE_COMBINE = 2 };
 
 struct __align__(16) GmmSmem {
   uint64_t full[STAGES];
@@ -81,9 +112,10 @@ struct __align__(16) GmmSmem {
   uint32_t abort;
   int32_t bad;
   int32_t ntiles;
+  int32_t row_tiles;                  // row tiles of all experts
   int64_t grp_off[kMaxExperts + 1];   // row offset of each expert (by id)
   int32_t grp_cnt[kMaxExperts];       // rows of each expert (by id)
-  int32_t tile_start[kMaxExperts + 1];  // tile prefix over experts
+  int32_t tile_start[kMaxExperts + 1];  // tile prefix over experts (row tiles only when cols_slow)
 };
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(GmmSmem);
@@ -97,6 +129,13 @@ struct TileInfo {
 
 template <int MODE, int EPI>
 __device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmParams& p, int t) {
+  // column tile fastest: t runs over (expert, row tile, column tile); slowest:
+  // over (column tile, expert, row tile)
+  int ct = 0;
+  if (p.cols_slow) {
+    ct = t / sm->row_tiles;
+    t -= ct * sm->row_tiles;
+  }
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -105,8 +144,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GmmSmem* sm, const GmmPara
   TileInfo ti;
   const int g = lo;
   const int local = t - sm->tile_start[lo];
-  const int rt = local / p.tile_cols;
-  const int ct = local - rt * p.tile_cols;
+  int rt = local;
+  if (!p.cols_slow) {
+    rt = local / p.tile_cols;
+    ct = local - rt * p.tile_cols;
+  }
   ti.g = g;
   ti.col0 = ct * (EPI == EPI_SWIGLU ? BN / 2 : BN);
   ti.row0 = sm->grp_off[g] + static_cast<int64_t>(rt) * BM;
@@ -141,10 +183,82 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&r)[3
   }
 }
 
-template <int MODE, int EPI>
+// FUSE_COMBINE, after this thread stored its row of the tile: count the row's
+// slot into its token's arrivals for this column slice; the warp then sums
+// every token whose count completed here, over the slice's 256 columns (8
+// per lane), its slots in order j = 0, 1, ... (fp32, one bf16 rounding).
+__device__ __forceinline__ void combine_slice(const GmmParams& p, const TileInfo& ti, bool row_ok, int64_t row,
+                                              int lane) {
+  const int ct = ti.col0 / BN;
+  const int64_t nslots = p.T * p.k;
+  int64_t tok = -1;
+  bool last = false;
+  __threadfence();   // the stored row is visible GPU-wide before it is counted
+  if (row_ok) {
+    const int64_t f = p.sorted_flat[row];
+    if (f >= 0 && f < nslots) {
+      tok = f / p.k;
+      int nvalid = 0;
+      for (int j = 0; j < p.k; ++j) nvalid += p.row_id_map[tok * p.k + j] >= 0 ? 1 : 0;
+      const int old = atomicAdd(&p.counters[static_cast<int64_t>(ct) * p.T + tok], 1);
+      last = (old + 1 == nvalid);
+    } else {
+      set_status(p.status, MOE_ERR_DEVICE);
+    }
+  }
+  unsigned m = __ballot_sync(0xffffffffu, last);
+  if (m == 0) return;
+  if (last) __threadfence();   // the token's other rows are read after their counts were seen
+  __syncwarp();
+  const int64_t c = ti.col0 + lane * 8;
+  const bool col_ok = c < p.out_cols;
+  while (m) {
+    const int src = __ffs(m) - 1;
+    m &= m - 1;
+    const int64_t t = __shfl_sync(0xffffffffu, tok, src);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+      int32_t r[8];
+      float w[8];
+      uint4 v[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        r[jj] = j < p.k ? p.row_id_map[t * p.k + j] : -1;
+        if (r[jj] < -1 || r[jj] >= p.rows_cap) {
+          set_status(p.status, MOE_ERR_DEVICE);
+          r[jj] = -1;
+        }
+        w[jj] = j < p.k ? p.topk_w[t * p.k + j] : 0.0f;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (r[jj] >= 0 && col_ok) v[jj] = ld_cg_v4(p.out + static_cast<int64_t>(r[jj]) * p.ld_out + c);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (r[jj] >= 0 && col_ok) add8(acc, v[jj], w[jj]);
+    }
+    if (col_ok) *reinterpret_cast<uint4*>(p.y + t * p.out_cols + c) = pack8(acc);
+    if (p.discard) {
+      // the token's rows of this slice are dead: drop their lines (four of
+      // 128 bytes per row) from L2 without writing them back
+      __syncwarp();
+      for (int i = lane; i < p.k * 4; i += 32) {
+        const int j = i >> 2;
+        const int64_t cl = ti.col0 + (i & 3) * 64;
+        const int32_t r = p.row_id_map[t * p.k + j];
+        if (r >= 0 && r < p.rows_cap && cl < p.out_cols) discard_l2_line(p.out + static_cast<int64_t>(r) * p.ld_out + cl);
+      }
+    }
+  }
+}
+
+template <int MODE, int EPI, int FUSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
   static_assert(MODE == GMM_FWD || MODE == GMM_DX, "dW runs on CTA pairs");
+  static_assert(FUSE == FUSE_NONE || (MODE == GMM_FWD && (FUSE == FUSE_GATHER) == (EPI == EPI_SWIGLU)),
+                "fused forms: the gate_up forward with the gather, the down forward with the combine");
   // B is MN-major (output columns contiguous) for the forward over [K, N]
   // weights and for dX over transposed [N, K] weights.
   const bool B_MN = (MODE == GMM_FWD) != (p.wt != 0);
@@ -193,9 +307,10 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int64_t rows = 0;
     int32_t tiles = 0;
+    const int per_rt = p.cols_slow ? 1 : p.tile_cols;   // prefix entries per row tile
     for (int e = lo; e < hi; ++e) {
       rows += sm->grp_cnt[e];
-      tiles += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
+      tiles += ((sm->grp_cnt[e] + BM - 1) / BM) * per_rt;
     }
     int64_t rows_incl = rows;
     int32_t tiles_incl = tiles;
@@ -211,12 +326,13 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       sm->grp_off[e] = rb;
       sm->tile_start[e] = tb;
       rb += sm->grp_cnt[e];
-      tb += ((sm->grp_cnt[e] + BM - 1) / BM) * p.tile_cols;
+      tb += ((sm->grp_cnt[e] + BM - 1) / BM) * per_rt;
     }
     if (lane == 31) {
       sm->grp_off[E] = rows_incl;
       sm->tile_start[E] = tiles_incl;
-      sm->ntiles = tiles_incl;
+      sm->row_tiles = tiles_incl;
+      sm->ntiles = p.cols_slow ? tiles_incl * p.tile_cols : tiles_incl;
       if (rows_incl > p.rows_cap) sm->bad = 1;
     }
   }
@@ -239,34 +355,66 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
+    // One thread copies; with the gather, the whole warp walks the tiles and
+    // lane l copies rows 4l .. 4l+3 of A (one gather4 each), lane 0 the rest.
+    const bool active = (FUSE == FUSE_GATHER) || lane == 0;
+    if (active) {
+      const uint64_t pol = p.w_evict_first ? l2_policy_evict_first() : 0ull;
+      auto load_b = [&](uint32_t dst, uint32_t bar, int32_t c0, int32_t c1, int32_t g) {
+        if (p.w_evict_first) tma_load_3d_hint(dst, &tmB, bar, c0, c1, g, pol);
+        else tma_load_3d(dst, &tmB, bar, c0, c1, g);
+      };
       uint32_t it = 0;
-      bool ok = true;
+      int ok = 1;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
+        int32_t tok[4] = {0, 0, 0, 0};
+        if (FUSE == FUSE_GATHER) {
+          // the tokens of this lane's four rows (rows past the group end repeat the tile's first)
+          const int64_t nslots = p.T * p.k;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = 4 * lane + q;
+            const int64_t f = p.sorted_flat[ti.row0 + (r < ti.rows_valid ? r : 0)];
+            if (f < 0 || f >= nslots) {
+              set_status(p.status, MOE_ERR_DEVICE);
+              tok[q] = 0;
+            } else {
+              tok[q] = static_cast<int32_t>(f / p.k);
+            }
+          }
+        }
         for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
+          if (lane == 0) ok = mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs) ? 1 : 0;
+          if (FUSE == FUSE_GATHER) ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
           const uint32_t bar = smem_u32(&sm->full[s]);
           const uint32_t a_dst = stage_base + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
-          mbar_expect_tx(bar, STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          if (lane == 0) mbar_expect_tx(bar, STAGE_BYTES);
+          if (FUSE == FUSE_GATHER) {
+            __syncwarp();   // the expected bytes are set before any copy can complete
+            tma_gather4(a_dst + lane * 4 * 128, &tmA, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
+            if (lane != 0) continue;
+          } else {
+            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+          }
           // output columns [0, 128) and [128, 256) of the tile: the gate and the up half with SwiGLU
           const int c0 = ti.col0, c1 = EPI == EPI_SWIGLU ? p.act_cols + ti.col0 : ti.col0 + BN / 2;
           if (B_MN) {  // weight rows hold output columns: four 64-column boxes
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(b_dst + j * BOX_BYTES, &tmB, bar, (j < 2 ? c0 : c1) + 64 * (j & 1), kb * BK, ti.g);
+              load_b(b_dst + j * BOX_BYTES, bar, (j < 2 ? c0 : c1) + 64 * (j & 1), kb * BK, ti.g);
           } else if (MODE == GMM_FWD) {  // transposed weights: two boxes of 128 rows
-            tma_load_3d(b_dst, &tmB, bar, kb * BK, c0, ti.g);
-            tma_load_3d(b_dst + (BN / 2) * 128, &tmB, bar, kb * BK, c1, ti.g);
+            load_b(b_dst, bar, kb * BK, c0, ti.g);
+            load_b(b_dst + (BN / 2) * 128, bar, kb * BK, c1, ti.g);
           } else {     // dX over [K, N] weights: one box of 256 rows
-            tma_load_3d(b_dst, &tmB, bar, kb * BK, ti.col0, ti.g);
+            load_b(b_dst, bar, kb * BK, ti.col0, ti.g);
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // let every copy already issued land before the CTA can exit
         const uint32_t first = it > STAGES ? it - STAGES : 0;
         for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
@@ -310,6 +458,23 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int row_in_tile = q * 32 + lane;
+    // while the first tile's stages fill (epilogue threads, spread over the grid):
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * (NUM_THREADS - 64);
+    const int64_t gthr = static_cast<int64_t>(blockIdx.x) * (NUM_THREADS - 64) + (tid - 64);
+    if (FUSE == FUSE_GATHER) {
+      // zero the arrival counts of the down GMM that follows
+      for (int64_t i = gthr; i < p.n_counters; i += nthr) p.counters[i] = 0;
+    }
+    if (FUSE == FUSE_COMBINE) {
+      // the output rows of tokens without a routed slot: no tile counts them in
+      for (int64_t t = gthr; t < p.T; t += nthr) {
+        bool any = false;
+        for (int j = 0; j < p.k; ++j) any |= p.row_id_map[t * p.k + j] >= 0;
+        if (!any)
+          for (int c = 0; c < p.out_cols; c += 8)
+            *reinterpret_cast<uint4*>(p.y + t * p.out_cols + c) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
@@ -393,10 +558,19 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             store_row32(dst, r);
           }
         }
+        if (FUSE == FUSE_COMBINE) {
+          // the accumulator is free before the combine: the next tile's MMAs can start
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty[acc]));
+          combine_slice(p, ti, row_ok, row, lane);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty[acc]));
+      if (FUSE != FUSE_COMBINE) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty[acc]));
+      }
       ++local;
     }
   }
@@ -411,10 +585,10 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 }
 
 // ------------------------------------------------------------------ host side
-template <int MODE, int EPI>
+template <int MODE, int EPI, int FUSE = FUSE_NONE>
 moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s,
                          int max_ctas) {
-  auto kern = gmm_kernel<MODE, EPI>;
+  auto kern = gmm_kernel<MODE, EPI, FUSE>;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -479,6 +653,97 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
     return MOE_ERR_CUDA;
   return dsw ? launch_mode<GMM_DX, EPI_DSWIGLU>(ta, tb, p, s, how.max_ctas)
              : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
+}
+
+size_t fused_counter_bytes(int64_t T, int64_t H) {
+  return align256(static_cast<size_t>((H + BN - 1) / BN) * static_cast<size_t>(T) * sizeof(int32_t));
+}
+
+// Fused dispatch + gate_up: rows of A gathered from x [T, K] (row r of the
+// permuted order is token sorted_flat[r] / k), w [E, K, N], the gated
+// activation of the [gate | up] product into out [M, N/2].  With counters,
+// the kernel also zeroes n_counters arrival counts for a down GMM that follows.
+moe_status_t launch_gmm_gather_act(const uint16_t* x, const int32_t* sorted_flat, int64_t T, int64_t k,
+                                   const uint16_t* w, const int64_t* group_list, int64_t M, int64_t K, int64_t N,
+                                   int64_t E, const Act& act, bool w_transposed, uint16_t* out, int32_t* counters,
+                                   int64_t n_counters, uint32_t* status, cudaStream_t s, const FusedOptions& opt) {
+  GmmParams p{};
+  p.group_list = group_list;
+  p.E = static_cast<int>(E);
+  p.rows_cap = M;
+  p.status = status;
+  p.act = act;
+  p.sorted_flat = sorted_flat;
+  p.k = static_cast<int>(k);
+  p.T = T;
+  p.counters = counters;
+  p.n_counters = counters ? n_counters : 0;
+  p.w_evict_first = opt.evict_first ? 1 : 0;
+  p.wt = w_transposed ? 1 : 0;
+  p.out = out;
+  p.out_cols = static_cast<int>(N / 2);
+  p.ld_out = N / 2;
+  p.act_cols = static_cast<int>(N / 2);
+  p.tile_cols = static_cast<int>((N / 2) / (BN / 2));
+  p.kblocks = static_cast<int>(K / BK);
+  CUtensorMap ta, tb;
+  if (!make_map_2d(&ta, x, T, K, 1) ||
+      !(w_transposed ? make_map_3d(&tb, w, E, N, K, BN / 2) : make_map_3d(&tb, w, E, K, N, 64)))
+    return MOE_ERR_CUDA;
+  return launch_mode<GMM_FWD, EPI_SWIGLU, FUSE_GATHER>(ta, tb, p, s, 0);
+}
+
+// Fused down + combine: a [M, K] @ w [E, K, N] into the scratch y2 [M, N],
+// each token's k rows summed with the routing weights into y [T, N] once the
+// last of them is stored.  counters: fused_counter_bytes(T, N), zero on entry.
+moe_status_t launch_gmm_combine(const uint16_t* a, const uint16_t* w, const int64_t* group_list,
+                                const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w, int64_t T,
+                                int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, bool w_transposed,
+                                uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status, cudaStream_t s,
+                                const FusedOptions& opt) {
+  GmmParams p{};
+  p.group_list = group_list;
+  p.E = static_cast<int>(E);
+  p.rows_cap = M;
+  p.status = status;
+  p.sorted_flat = sorted_flat;
+  p.row_id_map = row_id_map;
+  p.topk_w = topk_w;
+  p.k = static_cast<int>(k);
+  p.T = T;
+  p.counters = counters;
+  p.w_evict_first = opt.evict_first ? 1 : 0;
+  p.wt = w_transposed ? 1 : 0;
+  p.out = y2;
+  p.out_cols = static_cast<int>(N);
+  p.ld_out = N;
+  p.tile_cols = static_cast<int>((N + BN - 1) / BN);
+  p.kblocks = static_cast<int>(K / BK);
+  p.y = y;
+  p.cols_slow = 1;
+  p.discard = opt.discard ? 1 : 0;
+  CUtensorMap ta, tb;
+  if (!make_map_2d(&ta, a, M, K, BM) ||
+      !(w_transposed ? make_map_3d(&tb, w, E, N, K, BN / 2) : make_map_3d(&tb, w, E, K, N, 64)))
+    return MOE_ERR_CUDA;
+  return launch_mode<GMM_FWD, EPI_PLAIN, FUSE_COMBINE>(ta, tb, p, s, 0);
+}
+
+// The two expert matmuls of the fused layer forward: gate_up with the token
+// gather and the activation (a [R, I] out; it also zeroes the arrival counts),
+// then down with the combine into y.
+moe_status_t launch_layer_fused(const uint16_t* x, const uint16_t* w1, const uint16_t* w2, const int64_t* group_list,
+                                const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
+                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, const Act& act, int w_flags,
+                                uint16_t* a, uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status,
+                                cudaStream_t s, const FusedOptions& opt) {
+  const int64_t R = T * k;
+  const int64_t n_counters = ((H + BN - 1) / BN) * T;
+  moe_status_t st = launch_gmm_gather_act(x, sorted_flat, T, k, w1, group_list, R, H, 2 * I, E, act,
+                                          (w_flags & MOE_W1_TRANSPOSED) != 0, a, counters, n_counters, status, s, opt);
+  if (st != MOE_OK) return st;
+  return launch_gmm_combine(a, w2, group_list, row_id_map, sorted_flat, topk_w, T, k, R, I, H, E,
+                            (w_flags & MOE_W2_TRANSPOSED) != 0, y2, counters, y, status, s, opt);
 }
 
 }  // namespace moe

@@ -101,6 +101,32 @@ def test_null_and_invalid_arguments_fail_on_the_host(lib):
     assert lib.moe_workspace_init(FAKE, 16, None) == 2
 
 
+def test_fused_entry_points_check_their_arguments(lib):
+    from moe_routed_expert_gb300 import _abi
+    ws, nws = FAKE, 1 << 30
+    act = _abi.MoeActivation(0, 0)
+    a = C.byref(act)
+    # gmm_forward_gather_act(x, sorted_flat, T, k, w, gl, M, K, N, E, act, flags, y, ws, n, s)
+    g = lib.gmm_forward_gather_act
+    assert g(FAKE, FAKE, 64, 2, FAKE, FAKE, 128, 256, 512, 4, None, 0, FAKE, ws, nws, None) == 1  # activation required
+    assert g(FAKE, None, 64, 2, FAKE, FAKE, 128, 256, 512, 4, a, 0, FAKE, ws, nws, None) == 1
+    assert g(FAKE, FAKE, 64, 2, FAKE, FAKE, 128, 256, 384, 4, a, 0, FAKE, ws, nws, None) == 3   # N % 256
+    assert g(FAKE, FAKE, 64, 2, FAKE, FAKE, 128, 256, 512, 4, a, 4, FAKE, ws, nws, None) == 2   # flags
+    assert g(FAKE, C.c_void_p(0x10002), 64, 2, FAKE, FAKE, 128, 256, 512, 4, a, 0, FAKE, ws, nws, None) == 2
+    assert g(FAKE, FAKE, 64, 0, FAKE, FAKE, 128, 256, 512, 4, a, 0, FAKE, ws, nws, None) == 2   # k
+    assert g(FAKE, FAKE, 64, 2, FAKE, FAKE, 128, 256, 512, 4, a, 0, FAKE, ws, 16, None) == 2   # workspace
+    # gmm_forward_combine(a, w, gl, rmap, sflat, topk_w, T, k, M, K, N, E, flags, y, ws, n, s)
+    c = lib.gmm_forward_combine
+    assert c(FAKE, FAKE, FAKE, None, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, nws, None) == 1
+    assert c(None, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, nws, None) == 1
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 100, 512, 4, 0, FAKE, ws, nws, None) == 3  # K % 64
+    assert c(MIS, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, nws, None) == 2
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, 256, None) == 2
+    # status + counts (T x ceil(N/256) int32) + the [M, N] bf16 scratch
+    assert lib.gmm_forward_combine_workspace_size(4096, 8, 32768, 2048) == 256 + 4096 * 8 * 4 + 32768 * 2048 * 2
+    assert lib.gmm_forward_combine_workspace_size(0, 8, 0, 2048) == 256
+
+
 def test_activation_descriptor_checks(lib):
     """The (activation, activation_params) pair is checked on the host with the
     pages' rules: parameter counts per kind, clamp >= 0 and not NaN, finite

@@ -299,12 +299,11 @@ class LayerTrainStep:
 
 class LayerFwdStep(LayerTrainStep):
     """Forward only (prefill / decode layer workloads).  Where the layer entry
-    point runs fused (inference, groups averaging under 512 rows), a step is
-    one moe_layer_forward call (three or four launches), and the per-kernel
-    split times its pieces through their own entry points: the permute's
-    index pass, the gate_up GMM gathering its rows from x, and the down GMM
-    with the combine (whose standalone entry also zeroes its arrival counts
-    with a memset, which the layer call leaves to gate_up)."""
+    point fuses the dispatch into gate_up (inference, groups averaging under
+    512 rows), a step is one moe_layer_forward call, and the per-kernel split
+    times the same launches through their own entry points: the permute's
+    index pass, the gate_up GMM gathering its rows from x, the down GMM and
+    the combine."""
 
     def __init__(self, wl, dev, inp):
         import torch
@@ -325,20 +324,20 @@ class LayerFwdStep(LayerTrainStep):
             return
         M = self.M
         self.y_layer = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        self.ws_comb = M.Workspace(M.gmm_forward_combine_workspace_size(T, k, T * k, H), dev)
         f_up, f_dn = 2.0 * R * H * 2 * I, 2.0 * R * I * H
         self.stages = [
             ("permute_index", self.permute_index, 0.0, permute_launches(T * k) - 1),
             ("gmm_gate_up_gather_act", self.gmm1_gather, f_up, 1),
-            ("gmm_down_combine", self.gmm2_combine, f_dn, 1),
+            ("gmm_fwd_down", self.gmm2, f_dn, 1),
+            ("combine", self.combine, 0.0, 1),
         ]
         # algorithmic bytes: weights of the experts with rows once, the tokens
         # once (gathered k times, from L2), the activation out and back in
-        # once, the combined output once
+        # once, the expert outputs once
         self.gmm_bytes = {"gmm_gate_up_gather_act": live * H * 2 * I * 2 + T * H * 2 + R * I * 2,
-                          "gmm_down_combine": live * I * H * 2 + R * I * 2 + T * H * 2}
+                          "gmm_fwd_down": live * I * H * 2 + R * I * 2 + R * H * 2}
         self.headline = self.layer_call
-        self.kernel = "gmm_kernel, fused forms (the gate_up GMM with the token gather, the down GMM with the combine)"
+        self.kernel = "gmm_kernel (the gate_up GMM gathering its rows from the tokens, the down GMM)"
 
     def permute_index(self):
         s = self.saved
@@ -350,10 +349,6 @@ class LayerFwdStep(LayerTrainStep):
         self.M.gmm_forward_gather_act(self.x, s.sorted_flat, self.wl.k, self.w1, s.group_list, ("swiglu", [self.wl.clip]),
                                       y=s.a, ws=self.ws)
 
-    def gmm2_combine(self):
-        s = self.saved
-        self.M.gmm_forward_combine(s.a, self.w2, s.group_list, s.row_id_map, s.sorted_flat, self.tw, y=self.y,
-                                   ws=self.ws_comb)
 
     def layer_call(self):
         self.M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, self.wl.clip, y=self.y_layer,

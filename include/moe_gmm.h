@@ -249,8 +249,9 @@ MOE_API moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* so
                              const moe_activation_t* activation, int w_flags, moe_bf16* y,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Workspace bytes for gmm_forward_combine: the status block, T * ceil(N/256)
- * int32 arrival counts and an [M, N] bf16 scratch for the expert outputs. */
+/* Workspace bytes for gmm_forward_combine: the status block, ceil(N/256)
+ * int32 counts (one per 256-column slice) and an [M, N] bf16 scratch for the
+ * expert outputs. */
 MOE_API size_t gmm_forward_combine_workspace_size(int64_t T, int64_t k, int64_t M, int64_t N);
 
 /* The down grouped matmul fused with the weighted top-k combine ([MegaMoE]
@@ -259,9 +260,12 @@ MOE_API size_t gmm_forward_combine_workspace_size(int64_t T, int64_t k, int64_t 
  *   y[t] = sum over j in 0..k-1 with row_id_map[t*k+j] >= 0 of
  *          topk_w[t*k+j] * Y[row_id_map[t*k+j]],
  * summed in fp32 in slot order and rounded once to bf16: the same arithmetic,
- * and so the same bits, as gmm_forward followed by moe_unpermute.  Each token
- * is summed as soon as the last of its k rows is stored, while the rows are
- * still in L2; the rows are then dropped from L2 unwritten.
+ * and so the same bits, as gmm_forward followed by moe_unpermute.  The
+ * matmul's tiles are visited 256 output columns at a time; once a slice is
+ * stored, the tokens are summed over it while its rows are still in L2, and
+ * the rows are then dropped from L2 unwritten.  The kernel's CTAs wait for one
+ * another's slices (bounded: a wait past 4 s gives MOE_ERR_TIMEOUT), so they
+ * must all be resident at once: one per SM, as launched.
  *   a           [M, K] bf16, rows grouped by expert; w [E, K, N] (or [E, N, K]
  *               with MOE_W_TRANSPOSED); group_list [E] int64 counts
  *   row_id_map, sorted_flat  [T*k] / [M] int32 from moe_permute
@@ -377,12 +381,12 @@ MOE_API size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t
  *   x [T, H] bf16, topk_ids [T, k] int32, topk_w [T, k] fp32, y [T, H] bf16 out.
  *   saved: NULL for inference (intermediates live in ws), or the buffers that
  *   moe_layer_backward will read.
- * Inference with T*k < 512*E (groups that average under 512 rows) runs fused
- * ([MegaMoE] "算子功能"): the permute's index pass, gmm_forward_gather_act and
- * gmm_forward_combine, three launches (four above 1024 routed slots); the
- * permuted tokens and the expert outputs are never written to HBM.  The result
- * is bit-identical to the unfused chain (moe_permute, gmm_forward with the
- * activation, gmm_forward, moe_unpermute), which the other cases run. */
+ * Inference with T*k < 512*E (groups that average under 512 rows) fuses the
+ * dispatch into gate_up ([MegaMoE] "算子功能"): the permute's index pass,
+ * gmm_forward_gather_act, gmm_forward and moe_unpermute, four launches (five
+ * above 1024 routed slots); the permuted tokens are never written to HBM.  The
+ * result is bit-identical to the unfused chain (moe_permute, gmm_forward with
+ * the activation, gmm_forward, moe_unpermute), which the other cases run. */
 MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
                                const moe_bf16* w1, const moe_bf16* w2,
                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,

@@ -254,7 +254,7 @@ moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* sorted_fla
 size_t gmm_forward_combine_workspace_size(int64_t T, int64_t k, int64_t M, int64_t N) {
   (void)k;
   if (T <= 0 || M < 0 || N <= 0) return MOE_STATUS_BYTES;
-  return MOE_STATUS_BYTES + fused_counter_bytes(T, N) + align256(static_cast<size_t>(M) * N * 2);
+  return MOE_STATUS_BYTES + fused_counter_bytes(N) + align256(static_cast<size_t>(M) * N * 2);
 }
 
 moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int64_t* group_list,
@@ -278,8 +278,8 @@ moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int
   if (M == 0)  // no expert rows: every token's sum is empty
     return cudaMemsetAsync(y, 0, static_cast<size_t>(T) * N * 2, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   int32_t* counters = reinterpret_cast<int32_t*>(after_status(ws));
-  moe_bf16* y2 = reinterpret_cast<moe_bf16*>(after_status(ws) + fused_counter_bytes(T, N));
-  if (cudaMemsetAsync(counters, 0, fused_counter_bytes(T, N), s) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_bf16* y2 = reinterpret_cast<moe_bf16*>(after_status(ws) + fused_counter_bytes(N));
+  if (cudaMemsetAsync(counters, 0, fused_counter_bytes(N), s) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_gmm_combine(a, w, group_list, row_id_map, sorted_flat, topk_w, T, k, M, K, N, E,
                             (w_flags & MOE_W_TRANSPOSED) != 0, y2, counters, y, status_of(ws), s);
 }
@@ -464,14 +464,22 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
   }
   if (!saved && R < kPairMinRowsPerGroup * E) {
     // Inference with groups that average under 512 rows (the 128-row kernel's
-    // regime): the fused forward.  The permute only ranks the slots; gate_up
-    // reads its rows straight from x, and down combines each token as soon as
-    // its k rows are stored, so neither x_perm nor the expert outputs make a
-    // round trip through HBM.  The arrival counts sit where x_perm would.
+    // regime): the permute only ranks the slots, and gate_up reads its rows
+    // straight from x, so the permuted tokens never make a round trip through
+    // HBM.  Down and the combine stay two launches: the fused form
+    // (gmm_forward_combine) is slower at these sizes (its column-slice order
+    // re-reads the activation from HBM).
     if ((st = launch_permute(nullptr, topk_ids, T, H, k, E, nullptr, gl, rmap, sflat, status, scratch, s)) != MOE_OK)
       return st;
-    return launch_layer_fused(x, w1, w2, gl, rmap, sflat, topk_w, T, H, I, E, k, act, w_flags, a, y2,
-                              reinterpret_cast<int32_t*>(x_perm), y, status, s);
+    if ((st = launch_gmm_gather_act(x, sflat, T, k, w1, gl, R, H, 2 * I, E, act, (w_flags & MOE_W1_TRANSPOSED) != 0,
+                                    a, nullptr, 0, status, s)) != MOE_OK)
+      return st;
+    GmmLaunch how2;
+    how2.w_transposed = (w_flags & MOE_W2_TRANSPOSED) != 0;
+    if ((st = launch_gmm(GMM_FWD, EPI_PLAIN, a, w2, gl, R, I, H, E, Act(), y2, nullptr, status, gmm_scratch, s,
+                         how2)) != MOE_OK)
+      return st;
+    return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
   }
   if ((st = launch_permute(x, topk_ids, T, H, k, E, x_perm, gl, rmap, sflat, status, scratch, s)) != MOE_OK) return st;
   GmmLaunch how1, how2;

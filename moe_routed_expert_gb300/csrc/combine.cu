@@ -27,18 +27,24 @@ constexpr int COLS_PER_BLOCK = THREADS * 8;  // 2048 bf16 per block row segment
 constexpr int JB = 8;                         // slots loaded together
 
 // Rows of the slots [j0, j0 + JB) of token t; a row outside [-1, rows_cap)
-// raises MOE_ERR_DEVICE and counts as unused.
+// raises MOE_ERR_DEVICE and counts as unused.  Every load is issued before
+// any is checked: a check whose failure path writes the status word would
+// make each load wait for the one before it.
 __device__ __forceinline__ void slot_rows(const int32_t* __restrict__ row_id_map, int64_t t, int j0, int k,
                                           int64_t rows_cap, uint32_t* status, int32_t (&r)[JB]) {
 #pragma unroll
   for (int jj = 0; jj < JB; ++jj) {
     const int j = j0 + jj;
     r[jj] = j < k ? row_id_map[t * k + j] : -1;
-    if (r[jj] < -1 || r[jj] >= rows_cap) {
-      set_status(status, MOE_ERR_DEVICE);
-      r[jj] = -1;
-    }
   }
+  bool bad = false;
+#pragma unroll
+  for (int jj = 0; jj < JB; ++jj) {
+    const bool b = r[jj] < -1 || r[jj] >= rows_cap;
+    bad |= b;
+    if (b) r[jj] = -1;
+  }
+  if (bad) set_status(status, MOE_ERR_DEVICE);
 }
 
 // Slots [j0, j0 + JB) of token t whose rows are r into acc, in slot order.
@@ -113,25 +119,33 @@ __global__ void __launch_bounds__(THREADS) unpermute_kernel(const uint16_t* __re
   const int64_t col = static_cast<int64_t>(blockIdx.y) * COLS_PER_BLOCK + threadIdx.x * 8;
   if (col >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool bad = false;
   for (int j0 = 0; j0 < k; j0 += JB) {
     int32_t r[JB];
+    float w[JB];
     uint4 v[JB];
 #pragma unroll
-    for (int jj = 0; jj < JB; ++jj) {
+    for (int jj = 0; jj < JB; ++jj) {   // every load first, then the checks
       const int j = j0 + jj;
       r[jj] = j < k ? row_id_map[t * k + j] : -1;
-      if (r[jj] < -1 || r[jj] >= rows_cap) {
-        set_status(status, MOE_ERR_DEVICE);
-        r[jj] = -1;
-      }
-      if (r[jj] >= 0) v[jj] = ld_nc_v4(y_perm + static_cast<int64_t>(r[jj]) * H + col);
+      w[jj] = (HAS_W && j < k) ? topk_w[t * k + j] : 1.0f;
     }
 #pragma unroll
     for (int jj = 0; jj < JB; ++jj) {
-      if (r[jj] >= 0) add8(acc, v[jj], HAS_W ? topk_w[t * k + j0 + jj] : 1.0f);
+      const bool b = r[jj] < -1 || r[jj] >= rows_cap;
+      bad |= b;
+      if (b) r[jj] = -1;
+    }
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj)
+      if (r[jj] >= 0) v[jj] = ld_nc_v4(y_perm + static_cast<int64_t>(r[jj]) * H + col);
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
+      if (r[jj] >= 0) add8(acc, v[jj], w[jj]);
     }
   }
   *reinterpret_cast<uint4*>(y + t * H + col) = pack8(acc);
+  if (bad) set_status(status, MOE_ERR_DEVICE);
 }
 
 // One block per token: writes dy_perm rows and reduces the k dot products.
@@ -148,16 +162,20 @@ __global__ void __launch_bounds__(THREADS) unpermute_backward_kernel(
     int32_t r[JB];
     float w[JB], dot[JB];
 #pragma unroll
-    for (int jj = 0; jj < JB; ++jj) {
+    for (int jj = 0; jj < JB; ++jj) {   // every load first, then the checks
       const int j = j0 + jj;
       r[jj] = j < k ? row_id_map[t * k + j] : -1;
-      if (r[jj] < -1 || r[jj] >= rows_cap) {
-        if (threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE);
-        r[jj] = -1;
-      }
       w[jj] = (j < k && topk_w) ? topk_w[t * k + j] : 0.f;
       dot[jj] = 0.f;
     }
+    bool bad = false;
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
+      const bool b = r[jj] < -1 || r[jj] >= rows_cap;
+      bad |= b;
+      if (b) r[jj] = -1;
+    }
+    if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE);
     for (int64_t col = threadIdx.x * 8; col < H; col += COLS_PER_BLOCK) {
       const uint4 g = ld_nc_v4(dy + t * H + col);
       float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),

@@ -33,18 +33,29 @@
 // matmuls with the activation between them, and the combine as one operator)
 // runs two variants of this kernel, and neither the permuted tokens nor the
 // expert outputs ever make a round trip through HBM:
-//   FUSE_GATHER   gate_up: A rows are fetched straight from the tokens x by
-//                 TMA gather4 (four rows per copy), row r of a group being
-//                 token sorted_flat[r] / k; x stays in L2 (read k times).
+//   FUSE_GATHER   gate_up: A rows are copied straight from the tokens x,
+//                 row r of a group being token sorted_flat[r] / k: gather
+//                 warps copy 16-byte pieces of the tile's rows (cp.async,
+//                 into the 128B-swizzled layout the MMA reads) and signal the
+//                 stage barrier when they land; the
+//                 weight tile still comes by TMA.  x stays in L2 (read k times).
+//                 (A TMA gather4 per four rows was tried: the TMA unit's cost
+//                 per row made a stage take twice as long.)  Two gather warps
+//                 copy 64 rows each.
 //   FUSE_COMBINE  down: tiles are visited column tile slowest, so the expert
 //                 outputs of one 256-column slice stay in L2 while it lasts.
-//                 After storing its rows, each epilogue thread counts its
-//                 token's slot in for this slice; the thread whose count
-//                 completes the token hands it to its warp, which sums the
-//                 token's k rows in slot order j = 0, 1, ... with the routing
-//                 weights (fp32, one bf16 rounding: the same arithmetic as the
-//                 standalone combine, so the same bits) and can drop the rows
-//                 from L2 unwritten.
+//                 Once the epilogue warps stored a tile, a signal warp counts
+//                 it in for its slice (a release); four combine warps per
+//                 CTA wait until a slice is complete and then sum their CTA's
+//                 share of the tokens over it: a token's k rows in slot order
+//                 j = 0, 1, ... with the routing weights (fp32, one bf16
+//                 rounding: the same arithmetic as the standalone combine, so
+//                 the same bits), two tokens per warp at a time, dropping the
+//                 rows from L2 unwritten once read.  The combine of one slice
+//                 overlaps the matmuls of the next.  (Per-token completion
+//                 counts, a ring of finished tokens per epilogue warp, and the
+//                 sums done in the epilogue itself were tried: each put
+//                 dependent L2 round trips on every tile's critical path.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -67,7 +78,9 @@ constexpr int B_BYTES = BN * BK * 2;        // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * 64 * 2;      // one 64 x 64 bf16 box = 8 KB
 constexpr int TMEM_COLS = 2 * BN;           // two accumulators
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;                 // producer, MMA, 4 epilogue warps
+constexpr int GATHER_WARPS = 2;                  // FUSE_GATHER: warps copying A rows (64 rows each)
+constexpr int COMBINE_WARPS = 4;                 // FUSE_COMBINE: warps summing tokens (plus one signal warp)
 constexpr uint64_t kTimeoutNs = 4000000000ull;   // 4 s: far above any legal wait
 
 struct GmmParams {
@@ -93,20 +106,28 @@ struct GmmParams {
   int k;                       // slots per token
   int64_t T;                   // tokens
   uint16_t* y;                 // COMBINE: the combined output [T, out_cols]
-  int32_t* counters;           // per-token arrival counts of the down GMM, [its tile_cols][T]
+  int32_t* counters;           // COMBINE: per column tile, epilogue warps that finished a tile of it
   int64_t n_counters;          // GATHER: counts to zero for the down GMM that follows
   int cols_slow;               // tiles visited column tile slowest
   int discard;                 // COMBINE: expert rows dropped from L2 once combined
   int w_evict_first;           // weight tiles loaded under an L2 evict-first policy
+  const uint16_t* gx;          // GATHER: the tokens x [T, gx_ld]
+  int64_t gx_ld;
 };
 
 enum GmmFuse { FUSE_NONE = 0, FUSE_GATHER = 1, FUSE_COMBINE = 2 };
+
+template <int FUSE>
+constexpr int threads_of() {
+  return NUM_THREADS + 32 * (FUSE == FUSE_COMBINE ? COMBINE_WARPS + 1 : (FUSE == FUSE_GATHER ? GATHER_WARPS : 0));
+}
 
 struct __align__(16) GmmSmem {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t stored[2];                 // FUSE_COMBINE: the epilogue warps stored an accumulator's tile
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -183,78 +204,93 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&r)[3
   }
 }
 
-// FUSE_COMBINE, after this thread stored its row of the tile: count the row's
-// slot into its token's arrivals for this column slice; the warp then sums
-// every token whose count completed here, over the slice's 256 columns (8
-// per lane), its slots in order j = 0, 1, ... (fp32, one bf16 rounding).
-__device__ __forceinline__ void combine_slice(const GmmParams& p, const TileInfo& ti, bool row_ok, int64_t row,
-                                              int lane) {
-  const int ct = ti.col0 / BN;
-  const int64_t nslots = p.T * p.k;
-  int64_t tok = -1;
-  bool last = false;
-  __threadfence();   // the stored row is visible GPU-wide before it is counted
-  if (row_ok) {
-    const int64_t f = p.sorted_flat[row];
-    if (f >= 0 && f < nslots) {
-      tok = f / p.k;
-      int nvalid = 0;
-      for (int j = 0; j < p.k; ++j) nvalid += p.row_id_map[tok * p.k + j] >= 0 ? 1 : 0;
-      const int old = atomicAdd(&p.counters[static_cast<int64_t>(ct) * p.T + tok], 1);
-      last = (old + 1 == nvalid);
-    } else {
-      set_status(p.status, MOE_ERR_DEVICE);
-    }
-  }
-  unsigned m = __ballot_sync(0xffffffffu, last);
-  if (m == 0) return;
-  if (last) __threadfence();   // the token's other rows are read after their counts were seen
-  __syncwarp();
-  const int64_t c = ti.col0 + lane * 8;
-  const bool col_ok = c < p.out_cols;
-  while (m) {
-    const int src = __ffs(m) - 1;
-    m &= m - 1;
-    const int64_t t = __shfl_sync(0xffffffffu, tok, src);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < p.k; j0 += 8) {
-      int32_t r[8];
-      float w[8];
-      uint4 v[8];
+__device__ __forceinline__ void store_row32_hint(uint16_t* dst, const uint32_t (&r)[32], uint64_t pol) {
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int j = j0 + jj;
-        r[jj] = j < p.k ? p.row_id_map[t * p.k + j] : -1;
-        if (r[jj] < -1 || r[jj] >= p.rows_cap) {
-          set_status(p.status, MOE_ERR_DEVICE);
-          r[jj] = -1;
-        }
-        w[jj] = j < p.k ? p.topk_w[t * p.k + j] : 0.0f;
-      }
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (r[jj] >= 0 && col_ok) v[jj] = ld_cg_v4(p.out + static_cast<int64_t>(r[jj]) * p.ld_out + c);
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (r[jj] >= 0 && col_ok) add8(acc, v[jj], w[jj]);
-    }
-    if (col_ok) *reinterpret_cast<uint4*>(p.y + t * p.out_cols + c) = pack8(acc);
-    if (p.discard) {
-      // the token's rows of this slice are dead: drop their lines (four of
-      // 128 bytes per row) from L2 without writing them back
-      __syncwarp();
-      for (int i = lane; i < p.k * 4; i += 32) {
-        const int j = i >> 2;
-        const int64_t cl = ti.col0 + (i & 3) * 64;
-        const int32_t r = p.row_id_map[t * p.k + j];
-        if (r >= 0 && r < p.rows_cap && cl < p.out_cols) discard_l2_line(p.out + static_cast<int64_t>(r) * p.ld_out + cl);
-      }
-    }
+  for (int v = 0; v < 4; ++v) {
+    uint4 q;
+    q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+    q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+    q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+    q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+    st_v4_hint(dst + 8 * v, q, pol);
   }
 }
 
+// FUSE_COMBINE, in a combine warp: the sums of token ta over column slice cta
+// and of token tb over slice ctb (tb < 0: none) into y, 8 columns per lane,
+// each token's slots in order j = 0, 1, ... (fp32, one bf16 rounding); the
+// two tokens' loads are in flight together.  Then the tokens' expert rows of
+// those slices are dead: their 128-byte lines are dropped from L2 unwritten.
+__device__ __forceinline__ void combine_tokens(const GmmParams& p, int64_t ta, int cta, int64_t tb, int ctb,
+                                              int lane) {
+  const int64_t ca = static_cast<int64_t>(cta) * BN + lane * 8;
+  const int64_t cb = static_cast<int64_t>(ctb) * BN + lane * 8;
+  const bool oka = ca < p.out_cols;
+  const bool okb = tb >= 0 && cb < p.out_cols;
+  float acca[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float accb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool bad = false;
+  for (int j0 = 0; j0 < p.k; j0 += 8) {
+    int32_t ra[8], rb[8];
+    float wa[8], wb[8];
+    uint4 va[8], vb[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {   // every load first, then the checks
+      const int j = j0 + jj;
+      ra[jj] = j < p.k ? p.row_id_map[ta * p.k + j] : -1;
+      rb[jj] = (tb >= 0 && j < p.k) ? p.row_id_map[tb * p.k + j] : -1;
+      wa[jj] = j < p.k ? p.topk_w[ta * p.k + j] : 0.0f;
+      wb[jj] = (tb >= 0 && j < p.k) ? p.topk_w[tb * p.k + j] : 0.0f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const bool ba = ra[jj] < -1 || ra[jj] >= p.rows_cap, bb = rb[jj] < -1 || rb[jj] >= p.rows_cap;
+      bad |= ba || bb;
+      if (ba) ra[jj] = -1;
+      if (bb) rb[jj] = -1;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (ra[jj] >= 0 && oka) va[jj] = ld_cg_v4(p.out + static_cast<int64_t>(ra[jj]) * p.ld_out + ca);
+      if (rb[jj] >= 0 && okb) vb[jj] = ld_cg_v4(p.out + static_cast<int64_t>(rb[jj]) * p.ld_out + cb);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (ra[jj] >= 0 && oka) add8(acca, va[jj], wa[jj]);
+      if (rb[jj] >= 0 && okb) add8(accb, vb[jj], wb[jj]);
+    }
+  }
+  if (oka) *reinterpret_cast<uint4*>(p.y + ta * p.out_cols + ca) = pack8(acca);
+  if (okb) *reinterpret_cast<uint4*>(p.y + tb * p.out_cols + cb) = pack8(accb);
+  if (p.discard) {
+    __syncwarp();   // every lane holds its values: the lines may go
+    // four 128-byte lines per row of a 256-column slice; the rows are read
+    // first, then the lines dropped
+    const int per = p.k * 4;
+    for (int u0 = lane; u0 < 2 * per; u0 += 4 * 32) {   // k <= 16: one round
+      int32_t r[4];
+      int cl[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = u0 + 32 * u;
+        const bool second = i >= per;
+        const int64_t t = second ? tb : ta;
+        const int ii = second ? i - per : i;
+        r[u] = -1;
+        cl[u] = (second ? ctb : cta) * BN + (ii & 3) * 64;
+        if (i < 2 * per && t >= 0) r[u] = p.row_id_map[t * p.k + (ii >> 2)];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (r[u] >= 0 && r[u] < p.rows_cap && cl[u] < p.out_cols)
+          discard_l2_line(p.out + static_cast<int64_t>(r[u]) * p.ld_out + cl[u]);
+    }
+  }
+  if (bad) set_status(p.status, MOE_ERR_DEVICE);
+}
+
 template <int MODE, int EPI, int FUSE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(threads_of<FUSE>(), 1)
 gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GmmParams p) {
   static_assert(MODE == GMM_FWD || MODE == GMM_DX, "dW runs on CTA pairs");
   static_assert(FUSE == FUSE_NONE || (MODE == GMM_FWD && (FUSE == FUSE_GATHER) == (EPI == EPI_SWIGLU)),
@@ -269,6 +305,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   GmmSmem* sm = reinterpret_cast<GmmSmem*>(smem + STAGES * STAGE_BYTES);
   const uint32_t stage_base = smem_u32(smem);
 
+  constexpr int NT = threads_of<FUSE>();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -279,12 +316,18 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     sm->bad = 0;
     sm->abort = 0;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), 1);
+      // with the gather, each lane of the gather warps also arrives once its
+      // copies of the stage have landed
+      mbar_init(smem_u32(&sm->full[s]), FUSE == FUSE_GATHER ? 1 + 32 * GATHER_WARPS : 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm->tmem_full[a]), 1);
-      mbar_init(smem_u32(&sm->tmem_empty[a]), 4);
+      // with the combine, the signal warp releases the accumulator once the
+      // four epilogue warps have stored its tile (so they can never run two
+      // tiles ahead of it on one barrier)
+      mbar_init(smem_u32(&sm->tmem_empty[a]), FUSE == FUSE_COMBINE ? 1 : 4);
+      mbar_init(smem_u32(&sm->stored[a]), 4);
     }
     mbar_init(smem_u32(&sm->drain), 1);
     fence_barrier_init();
@@ -296,7 +339,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   // it overlaps the tail of the previous kernel on the stream.
   if (!p.concurrent) pdl_wait();
   pdl_trigger();
-  for (int e = tid; e < E; e += NUM_THREADS) {
+  for (int e = tid; e < E; e += NT) {
     const int64_t c = p.group_list[e];
     if (c < 0 || c > p.rows_cap) atomicOr(&sm->bad, 1);
     sm->grp_cnt[e] = static_cast<int32_t>(c < 0 ? 0 : (c > p.rows_cap ? p.rows_cap : c));
@@ -354,51 +397,33 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   volatile uint32_t* abort_flag = &sm->abort;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    // One thread copies; with the gather, the whole warp walks the tiles and
-    // lane l copies rows 4l .. 4l+3 of A (one gather4 each), lane 0 the rest.
-    const bool active = (FUSE == FUSE_GATHER) || lane == 0;
-    if (active) {
+    // ---------------------------------------------------------------- TMA producer (one thread)
+    // With the gather it copies only the weight tile; the gather warps copy A.
+    if (lane == 0) {
       const uint64_t pol = p.w_evict_first ? l2_policy_evict_first() : 0ull;
+      const uint64_t pol_keep = FUSE == FUSE_COMBINE ? l2_policy_evict_last() : 0ull;
       auto load_b = [&](uint32_t dst, uint32_t bar, int32_t c0, int32_t c1, int32_t g) {
         if (p.w_evict_first) tma_load_3d_hint(dst, &tmB, bar, c0, c1, g, pol);
         else tma_load_3d(dst, &tmB, bar, c0, c1, g);
       };
       uint32_t it = 0;
-      int ok = 1;
+      bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
-        int32_t tok[4] = {0, 0, 0, 0};
-        if (FUSE == FUSE_GATHER) {
-          // the tokens of this lane's four rows (rows past the group end repeat the tile's first)
-          const int64_t nslots = p.T * p.k;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = 4 * lane + q;
-            const int64_t f = p.sorted_flat[ti.row0 + (r < ti.rows_valid ? r : 0)];
-            if (f < 0 || f >= nslots) {
-              set_status(p.status, MOE_ERR_DEVICE);
-              tok[q] = 0;
-            } else {
-              tok[q] = static_cast<int32_t>(f / p.k);
-            }
-          }
-        }
         for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (lane == 0) ok = mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs) ? 1 : 0;
-          if (FUSE == FUSE_GATHER) ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          if (!mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs)) { ok = false; break; }
           const uint32_t bar = smem_u32(&sm->full[s]);
           const uint32_t a_dst = stage_base + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
-          if (lane == 0) mbar_expect_tx(bar, STAGE_BYTES);
           if (FUSE == FUSE_GATHER) {
-            __syncwarp();   // the expected bytes are set before any copy can complete
-            tma_gather4(a_dst + lane * 4 * 128, &tmA, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
-            if (lane != 0) continue;
+            mbar_expect_tx(bar, B_BYTES);
           } else {
-            tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
+            mbar_expect_tx(bar, STAGE_BYTES);
+            if (FUSE == FUSE_COMBINE)   // the rows are read again for every column slice
+              tma_load_2d_hint(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0), pol_keep);
+            else
+              tma_load_2d(a_dst, &tmA, bar, kb * BK, static_cast<int32_t>(ti.row0));
           }
           // output columns [0, 128) and [128, 256) of the tile: the gate and the up half with SwiGLU
           const int c0 = ti.col0, c1 = EPI == EPI_SWIGLU ? p.act_cols + ti.col0 : ti.col0 + BN / 2;
@@ -414,7 +439,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           }
         }
       }
-      if (!ok && lane == 0) {
+      if (!ok) {
         // let every copy already issued land before the CTA can exit
         const uint32_t first = it > STAGES ? it - STAGES : 0;
         for (uint32_t i = first; i < it; ++i) drain_wait(smem_u32(&sm->full[i % STAGES]), (i / STAGES) & 1u);
@@ -434,6 +459,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&sm->full[s]), ph, abort_flag, kTimeoutNs)) { ok = false; break; }
           tc_fence_after();
+          if (FUSE == FUSE_GATHER) fence_proxy_async_smem();   // the cp.async rows, for the tensor core
           const uint32_t a_addr = stage_base + s * STAGE_BYTES;
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
@@ -454,27 +480,106 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         drain_wait(smem_u32(&sm->drain), 0);
       }
     }
+  } else if (FUSE == FUSE_GATHER && warp >= NUM_THREADS / 32) {
+    // ---------------------------------------------------------------- gather warps
+    // Warp g copies rows [64 g, 64 g + 64) of each stage's A tile from x with
+    // cp.async, 16 bytes at a time, into the 128B-swizzled K-major layout the
+    // MMA reads: 8 lanes cover one row's 128 bytes, so lane l copies piece
+    // l & 7 of rows 64 g + (l >> 3) + 4 i, i = 0 .. 15.  Rows past the group
+    // end are not copied (the MMA's results for them are never stored).
+    const int gw = warp - NUM_THREADS / 32;
+    const int chunk = lane & 7;
+    constexpr int ROWS = BM / GATHER_WARPS / 4;   // rows per lane
+    const int64_t nslots = p.T * p.k;
+    uint32_t it = 0;
+    int ok = 1;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
+      // the source of each of this lane's rows (all loads first, then the checks)
+      int32_t f[ROWS];
+#pragma unroll
+      for (int i = 0; i < ROWS; ++i) {
+        const int r = gw * (BM / GATHER_WARPS) + (lane >> 3) + 4 * i;
+        f[i] = r < ti.rows_valid ? p.sorted_flat[ti.row0 + r] : 0;
+      }
+      const uint16_t* src[ROWS];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < ROWS; ++i) {
+        const bool b = f[i] < 0 || f[i] >= nslots;
+        bad |= b;
+        src[i] = p.gx + static_cast<int64_t>(b ? 0 : f[i] / p.k) * p.gx_ld + chunk * 8;
+      }
+      if (bad) set_status(p.status, MOE_ERR_DEVICE);
+      const int nrows = ti.rows_valid - gw * (BM / GATHER_WARPS) - (lane >> 3);   // rows i with 4 i < nrows
+      for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (lane == 0) ok = mbar_wait_bounded(smem_u32(&sm->empty[s]), ph ^ 1u, abort_flag, kTimeoutNs) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t a_dst = stage_base + s * STAGE_BYTES;
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i) {
+          const int r = gw * (BM / GATHER_WARPS) + (lane >> 3) + 4 * i;
+          if (4 * i < nrows) cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * BK);
+        }
+        cp_async_arrive_noinc(smem_u32(&sm->full[s]));   // once this lane's copies of the stage land
+      }
+    }
+    cp_async_wait_all();   // no copy of this thread lands after the CTA retires
+  } else if (FUSE == FUSE_COMBINE && warp == NUM_THREADS / 32 + COMBINE_WARPS) {
+    // ---------------------------------------------------------------- signal warp
+    // Once the four epilogue warps have stored a tile of this CTA, frees its
+    // accumulator and counts the tile into its column slice: the wait on their
+    // arrival orders their stores before this thread's GPU-scope fence, which
+    // orders them before the count (the epilogue warps never wait for their
+    // stores to land).
+    if (lane == 0) {
+      uint32_t local = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+        const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
+        if (!mbar_wait_bounded(smem_u32(&sm->stored[local & 1u]), (local >> 1) & 1u, abort_flag, kTimeoutNs)) break;
+        mbar_arrive(smem_u32(&sm->tmem_empty[local & 1u]));
+        __threadfence();
+        red_add_release_gpu(&p.counters[ti.col0 / BN], 1);
+      }
+    }
+  } else if (FUSE == FUSE_COMBINE && warp >= NUM_THREADS / 32) {
+    // ---------------------------------------------------------------- combine warps
+    // Column slice by column slice (the tile order): once every tile of the
+    // slice is stored (the signal warps count them in), this CTA sums its
+    // share of the tokens, two per warp at a time.
+    const int cw = warp - NUM_THREADS / 32;
+    const int64_t tb0 = static_cast<int64_t>(blockIdx.x) * p.T / gridDim.x;
+    const int64_t tb1 = static_cast<int64_t>(blockIdx.x + 1) * p.T / gridDim.x;
+    const int need = sm->row_tiles;   // tiles per slice
+    for (int ct = 0; ct < p.tile_cols; ++ct) {
+      int ok = 1;
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(&p.counters[ct]) < need) {
+          if (*abort_flag) { ok = 0; break; }
+          if (globaltimer_ns() - t0 > kTimeoutNs) { *abort_flag = 1u; ok = 0; break; }
+          __nanosleep(256);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      __threadfence();   // the slice's stored rows are visible to every lane's reads
+      for (int64_t t = tb0 + 2 * cw; t < tb1; t += 2 * COMBINE_WARPS)
+        combine_tokens(p, t, ct, t + 1 < tb1 ? t + 1 : -1, ct, lane);
+    }
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int row_in_tile = q * 32 + lane;
-    // while the first tile's stages fill (epilogue threads, spread over the grid):
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * (NUM_THREADS - 64);
-    const int64_t gthr = static_cast<int64_t>(blockIdx.x) * (NUM_THREADS - 64) + (tid - 64);
     if (FUSE == FUSE_GATHER) {
-      // zero the arrival counts of the down GMM that follows
+      // while the first tile's stages fill: zero the arrival counts of the down
+      // GMM that follows (epilogue threads, spread over the grid)
+      const int64_t nthr = static_cast<int64_t>(gridDim.x) * (NUM_THREADS - 64);
+      const int64_t gthr = static_cast<int64_t>(blockIdx.x) * (NUM_THREADS - 64) + (tid - 64);
       for (int64_t i = gthr; i < p.n_counters; i += nthr) p.counters[i] = 0;
     }
-    if (FUSE == FUSE_COMBINE) {
-      // the output rows of tokens without a routed slot: no tile counts them in
-      for (int64_t t = gthr; t < p.T; t += nthr) {
-        bool any = false;
-        for (int j = 0; j < p.k; ++j) any |= p.row_id_map[t * p.k + j] >= 0;
-        if (!any)
-          for (int c = 0; c < p.out_cols; c += 8)
-            *reinterpret_cast<uint4*>(p.y + t * p.out_cols + c) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+    const uint64_t pol_keep = FUSE == FUSE_COMBINE ? l2_policy_evict_last() : 0ull;
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
@@ -555,15 +660,16 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           tmem_ld_wait();
           if (row_ok) {
             uint16_t* dst = p.out + row * p.ld_out + ti.col0 + cc;
-            store_row32(dst, r);
+            if (FUSE == FUSE_COMBINE) store_row32_hint(dst, r, pol_keep);   // read again soon, by the combine
+            else store_row32(dst, r);
           }
         }
         if (FUSE == FUSE_COMBINE) {
-          // the accumulator is free before the combine: the next tile's MMAs can start
+          // the signal warp frees the accumulator and counts the tile in once
+          // all four warps stored it
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty[acc]));
-          combine_slice(p, ti, row_ok, row, lane);
+          if (lane == 0) mbar_arrive(smem_u32(&sm->stored[acc]));
         }
       }
       if (FUSE != FUSE_COMBINE) {
@@ -589,6 +695,7 @@ template <int MODE, int EPI, int FUSE = FUSE_NONE>
 moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const GmmParams& p, cudaStream_t s,
                          int max_ctas) {
   auto kern = gmm_kernel<MODE, EPI, FUSE>;
+  constexpr int NT = threads_of<FUSE>();
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -598,7 +705,7 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
     configured_dev = dev;
   }
   const int grid = (max_ctas > 0 && max_ctas < num_sms()) ? max_ctas : num_sms();
-  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(grid), dim3(NT), kSmemBytes, s, 1, ta, tb, p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -655,9 +762,7 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
              : launch_mode<GMM_DX, EPI_PLAIN>(ta, tb, p, s, how.max_ctas);
 }
 
-size_t fused_counter_bytes(int64_t T, int64_t H) {
-  return align256(static_cast<size_t>((H + BN - 1) / BN) * static_cast<size_t>(T) * sizeof(int32_t));
-}
+size_t fused_counter_bytes(int64_t N) { return align256(static_cast<size_t>((N + BN - 1) / BN) * sizeof(int32_t)); }
 
 // Fused dispatch + gate_up: rows of A gathered from x [T, K] (row r of the
 // permuted order is token sorted_flat[r] / k), w [E, K, N], the gated
@@ -678,6 +783,8 @@ moe_status_t launch_gmm_gather_act(const uint16_t* x, const int32_t* sorted_flat
   p.T = T;
   p.counters = counters;
   p.n_counters = counters ? n_counters : 0;
+  p.gx = x;
+  p.gx_ld = K;
   p.w_evict_first = opt.evict_first ? 1 : 0;
   p.wt = w_transposed ? 1 : 0;
   p.out = out;
@@ -695,7 +802,8 @@ moe_status_t launch_gmm_gather_act(const uint16_t* x, const int32_t* sorted_flat
 
 // Fused down + combine: a [M, K] @ w [E, K, N] into the scratch y2 [M, N],
 // each token's k rows summed with the routing weights into y [T, N] once the
-// last of them is stored.  counters: fused_counter_bytes(T, N), zero on entry.
+// column slice holding them is stored.  counters: fused_counter_bytes(N),
+// zero on entry.
 moe_status_t launch_gmm_combine(const uint16_t* a, const uint16_t* w, const int64_t* group_list,
                                 const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w, int64_t T,
                                 int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, bool w_transposed,
@@ -727,23 +835,6 @@ moe_status_t launch_gmm_combine(const uint16_t* a, const uint16_t* w, const int6
       !(w_transposed ? make_map_3d(&tb, w, E, N, K, BN / 2) : make_map_3d(&tb, w, E, K, N, 64)))
     return MOE_ERR_CUDA;
   return launch_mode<GMM_FWD, EPI_PLAIN, FUSE_COMBINE>(ta, tb, p, s, 0);
-}
-
-// The two expert matmuls of the fused layer forward: gate_up with the token
-// gather and the activation (a [R, I] out; it also zeroes the arrival counts),
-// then down with the combine into y.
-moe_status_t launch_layer_fused(const uint16_t* x, const uint16_t* w1, const uint16_t* w2, const int64_t* group_list,
-                                const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
-                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, const Act& act, int w_flags,
-                                uint16_t* a, uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status,
-                                cudaStream_t s, const FusedOptions& opt) {
-  const int64_t R = T * k;
-  const int64_t n_counters = ((H + BN - 1) / BN) * T;
-  moe_status_t st = launch_gmm_gather_act(x, sorted_flat, T, k, w1, group_list, R, H, 2 * I, E, act,
-                                          (w_flags & MOE_W1_TRANSPOSED) != 0, a, counters, n_counters, status, s, opt);
-  if (st != MOE_OK) return st;
-  return launch_gmm_combine(a, w2, group_list, row_id_map, sorted_flat, topk_w, T, k, R, I, H, E,
-                            (w_flags & MOE_W2_TRANSPOSED) != 0, y2, counters, y, status, s, opt);
 }
 
 }  // namespace moe

@@ -119,17 +119,18 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
                         int64_t M, int64_t K, int64_t N, int64_t E, const Act& act,
                         uint16_t* out, uint16_t* h_save, uint32_t* status, void* gmm_scratch, cudaStream_t s,
                         const GmmLaunch& how = GmmLaunch());
-// The fused layer forward's two grouped matmuls (gmm.cu, 128-row tiles):
-// gate_up reads its rows straight from the tokens x [T, H] (row r of the
-// permuted order is token sorted_flat[r] / k) and writes the activation
-// a [R, I]; down writes the expert outputs to the scratch y2 [R, H] and
-// combines each token's k rows into y [T, H] as soon as the last of them is
-// stored.  counters: ceil(H / 256) * T int32 of scratch (zeroed by gate_up).
+// Fused grouped matmuls (gmm.cu, 128-row tiles): gate_up reading its rows
+// straight from the tokens x [T, K] (row r of the permuted order is token
+// sorted_flat[r] / k) and writing the activation [M, N/2]; down writing the
+// expert outputs to a scratch y2 [M, N] and combining each token's k rows
+// into y [T, N] once the 256-column slice holding them is stored.  counters:
+// fused_counter_bytes(N) of scratch, zero on entry (gate_up can zero
+// n_counters of them for a down GMM that follows).
 struct FusedOptions {
   bool discard = true;       // drop combined expert rows from L2 unwritten
   bool evict_first = true;   // stream the weights under an L2 evict-first policy
 };
-size_t fused_counter_bytes(int64_t T, int64_t H);
+size_t fused_counter_bytes(int64_t N);
 moe_status_t launch_gmm_gather_act(const uint16_t* x, const int32_t* sorted_flat, int64_t T, int64_t k,
                                    const uint16_t* w, const int64_t* group_list, int64_t M, int64_t K, int64_t N,
                                    int64_t E, const Act& act, bool w_transposed, uint16_t* out, int32_t* counters,
@@ -140,11 +141,6 @@ moe_status_t launch_gmm_combine(const uint16_t* a, const uint16_t* w, const int6
                                 int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, bool w_transposed,
                                 uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status, cudaStream_t s,
                                 const FusedOptions& opt = FusedOptions());
-moe_status_t launch_layer_fused(const uint16_t* x, const uint16_t* w1, const uint16_t* w2, const int64_t* group_list,
-                                const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
-                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, const Act& act, int w_flags,
-                                uint16_t* a, uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status,
-                                cudaStream_t s, const FusedOptions& opt = FusedOptions());
 // Block-scaled grouped matmul (gmm_mx.cu): a [M, K] fp8 with scales [M, K/32];
 // b [E, N, K] fp8 with scales [E, N, K/32].  act == nullptr: bf16 out [M, N];
 // else the activation of the [gate | up] halves, quantised into aq [M, N/2] /

@@ -129,14 +129,19 @@ __global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* _
   for (int e = threadIdx.x; e < E; e += THREADS) hist[e] = 0;
   __syncthreads();
   const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
-  for (int i = threadIdx.x; i < CHUNK; i += THREADS) {
-    const int64_t f = f0 + i;
-    if (f < nslots) {
-      const int e = ids[f];
-      if (e < -1 || e >= E) set_status(status, MOE_ERR_DEVICE);
-      else if (e >= 0) atomicAdd(&hist[e], 1);
-    }
+  int e[CHUNK / THREADS];   // all loads first, then the counting
+#pragma unroll
+  for (int u = 0; u < CHUNK / THREADS; ++u) {
+    const int64_t f = f0 + threadIdx.x + u * THREADS;
+    e[u] = f < nslots ? ids[f] : -1;
   }
+  bool bad = false;
+#pragma unroll
+  for (int u = 0; u < CHUNK / THREADS; ++u) {
+    if (e[u] < -1 || e[u] >= E) bad = true;
+    else if (e[u] >= 0) atomicAdd(&hist[e[u]], 1);
+  }
+  if (bad) set_status(status, MOE_ERR_DEVICE);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += THREADS)
     chunk_counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
@@ -170,10 +175,15 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
     const int e = threadIdx.x * ept + i;
     if (i < ept && e < E) {
       const int32_t* row = chunk_counts + static_cast<int64_t>(e) * nchunks;
-      for (int c = 0; c < nchunks; ++c) {
-        const int32_t v = row[c];
-        tot[i] += v;
-        if (c < static_cast<int>(blockIdx.x)) pre[i] += v;
+      for (int c0 = 0; c0 < nchunks; c0 += 8) {   // eight loads in flight at a time
+        int32_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = c0 + u < nchunks ? row[c0 + u] : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          tot[i] += v[u];
+          if (c0 + u < static_cast<int>(blockIdx.x)) pre[i] += v[u];
+        }
       }
       mine_tot += tot[i];
     }
@@ -212,14 +222,23 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
   __syncthreads();
   const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK + warp * SUB;
   int32_t* mine = wbase + warp * E;
-  // per-warp counts
-#pragma unroll 1
+  // this warp's ids, loaded once for both passes (all loads in flight together)
+  int ev[SUB / 32];
+#pragma unroll
   for (int step = 0; step < SUB / 32; ++step) {
     const int64_t f = f0 + step * 32 + lane;
-    int e = f < nslots ? ids[f] : -1;
-    if (e < -1 || e >= E) e = -1;
+    ev[step] = f < nslots ? ids[f] : -1;
+  }
+#pragma unroll
+  for (int step = 0; step < SUB / 32; ++step)
+    if (ev[step] < -1 || ev[step] >= E) ev[step] = -1;
+  // per-warp counts
+#pragma unroll
+  for (int step = 0; step < SUB / 32; ++step) {
+    const int e = ev[step];
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
   // per-expert scan over the warps of this chunk, starting at the chunk's first row
@@ -234,11 +253,10 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
   }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
-#pragma unroll 1
+#pragma unroll
   for (int step = 0; step < SUB / 32; ++step) {
     const int64_t f = f0 + step * 32 + lane;
-    int e = f < nslots ? ids[f] : -1;
-    if (e < -1 || e >= E) e = -1;
+    const int e = ev[step];
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       const int32_t row = mine[e] + __popc(peers & lt);

@@ -122,8 +122,8 @@ def test_fused_entry_points_check_their_arguments(lib):
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 100, 512, 4, 0, FAKE, ws, nws, None) == 3  # K % 64
     assert c(MIS, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, nws, None) == 2
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, 256, None) == 2
-    # status + counts (T x ceil(N/256) int32) + the [M, N] bf16 scratch
-    assert lib.gmm_forward_combine_workspace_size(4096, 8, 32768, 2048) == 256 + 4096 * 8 * 4 + 32768 * 2048 * 2
+    # status + counts (ceil(N/256) int32, 256-byte aligned) + the [M, N] bf16 scratch
+    assert lib.gmm_forward_combine_workspace_size(4096, 8, 32768, 2048) == 256 + 256 + 32768 * 2048 * 2
     assert lib.gmm_forward_combine_workspace_size(0, 8, 0, 2048) == 256
 
 

@@ -321,6 +321,11 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   return v;
 }
 
+// Bring the 128-byte line holding p into L2 (no value returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 // 16-byte load cached in L2 only (data another SM wrote during this kernel).
 __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 r;

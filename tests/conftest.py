@@ -25,3 +25,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def guarded_outputs(request, monkeypatch):
+    """GPU tests: the binding's device allocations (outputs, workspaces) get
+    canary guard regions, checked after the test (tests/_util.py)."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    import torch
+    if not torch.cuda.is_available():
+        yield
+        return
+    from tests._util import GuardedAlloc, GuardedTorch
+    from moe_routed_expert_gb300 import binding
+    alloc = GuardedAlloc()
+    monkeypatch.setattr(binding, "torch", GuardedTorch(torch, alloc))
+    yield alloc
+    alloc.check()

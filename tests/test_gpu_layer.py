@@ -181,9 +181,16 @@ def test_layer_small_every_output(wl):
     np.testing.assert_array_equal(f64(gs["x_perm"][:R]), so["x_perm"])
     check_steps(o)
     assert_close("y", g["y"], o["y_steps"])
-    # shallow outputs (sums over the k slots of a token) also end to end
+    # the outputs also end to end, the oracle from the inputs alone
+    # ("NPU Training Operators - GMM", 实测表模板: grad_weight per expert).  The
+    # weight gradients only where no activation value is large: in small_b
+    # (clip 7, a hot expert) activations reach about 5, where one bf16 step is
+    # 0.03, so one rounding decision on A taken the other way moves a dW2
+    # element by about 0.02 (5 of 1.57M elements); its weight gradients are
+    # checked on the GPU's own inputs below
     o_pure = oracle_layer(inp, wl, backward=True)
-    for key in ("y", "dx", "dprobs"):
+    keys = ("y", "dx", "dprobs") + (() if wl.name == "small_b" else ("dw1", "dw2"))
+    for key in keys:
         assert_close(key + " (end to end)", g[key], o_pure[key])
     chain = gpu_chain_backward(g["saved"], dev_bf16(inp["dy"]), dev(inp["topk_w"]), dev_bf16(inp["w1"]),
                                dev_bf16(inp["w2"]), wl.clip, wl.T, wl.k)

@@ -705,19 +705,6 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const PairTile ti = decode_pair_tile<EPI>(sm, q, mode, group_of(tr), tr.local, rank);
       uint16_t* obase = (mode == GMM_DW) ? q.out + static_cast<int64_t>(ti.g) * q.out_rows * q.ld_out : q.out;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
-      if (EPI == EPI_DSWIGLU) {
-        // while this tile's MMAs run: bring the saved pre-activation rows the
-        // epilogue will read (gate and up, 256 columns each) into L2
-        const int rv = ti.rows_valid - qw * 32;
-        const int64_t ldh = 2 * static_cast<int64_t>(p.act_cols);
-#pragma unroll
-        for (int i = lane; i < 32 * 8; i += 32) {
-          const int r = i >> 3, seg = i & 7;
-          const int c = ti.col0 + (seg & 3) * 64;
-          if (r < rv && c < p.out_cols)
-            prefetch_l2(p.h_in + (ti.row0 + qw * 32 + r) * ldh + c + (seg >= 4 ? p.act_cols : 0));
-        }
-      }
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;

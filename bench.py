@@ -297,6 +297,9 @@ class LayerTrainStep:
     e2e_api = "moe_layer_forward/moe_layer_backward"
 
 
+fused_combine = False   # --down-combine fused
+
+
 class LayerFwdStep(LayerTrainStep):
     """Forward only (prefill / decode layer workloads).  Where the layer entry
     point fuses the dispatch into gate_up (inference, groups averaging under
@@ -337,6 +340,14 @@ class LayerFwdStep(LayerTrainStep):
         self.gmm_bytes = {"gmm_gate_up_gather_act": live * H * 2 * I * 2 + T * H * 2 + R * I * 2,
                           "gmm_fwd_down": live * I * H * 2 + R * I * 2 + R * H * 2}
         self.headline = self.layer_call
+        if fused_combine:
+            # the down GMM fused with the combine (gmm_forward_combine) in place
+            # of the down GMM and the combine; a step is then the three calls
+            self.ws_comb = M.Workspace(M.gmm_forward_combine_workspace_size(T, k, T * k, H), dev)
+            self.stages = self.stages[:2] + [("gmm_down_combine", self.gmm2_combine, f_dn, 1)]
+            self.gmm_bytes = {"gmm_gate_up_gather_act": self.gmm_bytes["gmm_gate_up_gather_act"],
+                              "gmm_down_combine": live * I * H * 2 + R * I * 2 + T * H * 2}
+            self.headline = None
         self.kernel = "gmm_kernel (the gate_up GMM gathering its rows from the tokens, the down GMM)"
 
     def permute_index(self):
@@ -349,6 +360,11 @@ class LayerFwdStep(LayerTrainStep):
         self.M.gmm_forward_gather_act(self.x, s.sorted_flat, self.wl.k, self.w1, s.group_list, ("swiglu", [self.wl.clip]),
                                       y=s.a, ws=self.ws)
 
+
+    def gmm2_combine(self):
+        s = self.saved
+        self.M.gmm_forward_combine(s.a, self.w2, s.group_list, s.row_id_map, s.sorted_flat, self.tw, y=self.y,
+                                   ws=self.ws_comb)
 
     def layer_call(self):
         self.M.moe_layer_forward(self.x, self.ids, self.tw, self.w1, self.w2, self.wl.clip, y=self.y_layer,
@@ -1008,7 +1024,12 @@ def main():
                     help="time replays of one step captured in a CUDA graph (the per-kernel split stays eager)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the first T tokens of the layer workload (smaller captures; not a bench line)")
+    ap.add_argument("--down-combine", default="split", choices=["split", "fused"],
+                    help="layer forwards: the down GMM and the combine as two calls (the layer entry point's "
+                         "choice), or the fused gmm_forward_combine")
     args = ap.parse_args()
+    global fused_combine
+    fused_combine = args.down_combine == "fused"
     if args.impl == "reference":
         return run_reference(args)
     if args.warmup < 3:

@@ -328,27 +328,27 @@ class LayerFwdStep(LayerTrainStep):
         M = self.M
         self.y_layer = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
         f_up, f_dn = 2.0 * R * H * 2 * I, 2.0 * R * I * H
+        self.ws_mlp = M.Workspace(M.moe_expert_mlp_workspace_size(T, k, wl.E), dev)
         self.stages = [
             ("permute_index", self.permute_index, 0.0, permute_launches(T * k) - 1),
-            ("gmm_gate_up_gather_act", self.gmm1_gather, f_up, 1),
-            ("gmm_fwd_down", self.gmm2, f_dn, 1),
+            ("gmm_expert_mlp", self.expert_mlp, f_up + f_dn, 1),
             ("combine", self.combine, 0.0, 1),
         ]
-        # algorithmic bytes: weights of the experts with rows once, the tokens
-        # once (gathered k times, from L2), the activation out and back in
-        # once, the expert outputs once
-        self.gmm_bytes = {"gmm_gate_up_gather_act": live * H * 2 * I * 2 + T * H * 2 + R * I * 2,
-                          "gmm_fwd_down": live * I * H * 2 + R * I * 2 + R * H * 2}
+        # algorithmic bytes of the one launch of both GMMs: weights of the
+        # experts with rows once, the tokens once (gathered k times, from L2),
+        # the activation out and back in once, the expert outputs once
+        self.gmm_bytes = {"gmm_expert_mlp": live * 3 * H * I * 2 + T * H * 2 + 2 * R * I * 2 + R * H * 2}
         self.headline = self.layer_call
         if fused_combine:
-            # the down GMM fused with the combine (gmm_forward_combine) in place
-            # of the down GMM and the combine; a step is then the three calls
+            # the gathered gate_up GMM, then the down GMM fused with the combine
+            # (gmm_forward_combine) in place of the one launch and the combine
             self.ws_comb = M.Workspace(M.gmm_forward_combine_workspace_size(T, k, T * k, H), dev)
-            self.stages = self.stages[:2] + [("gmm_down_combine", self.gmm2_combine, f_dn, 1)]
-            self.gmm_bytes = {"gmm_gate_up_gather_act": self.gmm_bytes["gmm_gate_up_gather_act"],
+            self.stages = [self.stages[0], ("gmm_gate_up_gather_act", self.gmm1_gather, f_up, 1),
+                           ("gmm_down_combine", self.gmm2_combine, f_dn, 1)]
+            self.gmm_bytes = {"gmm_gate_up_gather_act": live * H * 2 * I * 2 + T * H * 2 + R * I * 2,
                               "gmm_down_combine": live * I * H * 2 + R * I * 2 + T * H * 2}
             self.headline = None
-        self.kernel = "gmm_kernel (the gate_up GMM gathering its rows from the tokens, the down GMM)"
+        self.kernel = "expert_mlp_kernel (gate_up gathering its rows from the tokens, then down, one launch)"
 
     def permute_index(self):
         s = self.saved
@@ -360,6 +360,11 @@ class LayerFwdStep(LayerTrainStep):
         self.M.gmm_forward_gather_act(self.x, s.sorted_flat, self.wl.k, self.w1, s.group_list, ("swiglu", [self.wl.clip]),
                                       y=s.a, ws=self.ws)
 
+
+    def expert_mlp(self):
+        s = self.saved
+        self.M.moe_expert_mlp_forward(self.x, s.sorted_flat, s.group_list, self.w1, self.w2, self.wl.k,
+                                      ("swiglu", [self.wl.clip]), a=s.a, y2=s.y2, ws=self.ws_mlp)
 
     def gmm2_combine(self):
         s = self.saved

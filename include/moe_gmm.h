@@ -249,6 +249,30 @@ MOE_API moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* so
                              const moe_activation_t* activation, int w_flags, moe_bf16* y,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Workspace bytes for moe_expert_mlp_forward: the status block and one int32
+ * readiness count per 128-row tile (T*k/128 + E of them). */
+MOE_API size_t moe_expert_mlp_workspace_size(int64_t T, int64_t k, int64_t E);
+
+/* The routed experts' MLP over the permuted tokens in one launch ([MegaMoE]
+ * "算子功能": the dispatch and the two expert matmuls with the activation
+ * between them as one operator; [MegaMoE] "Expert Compute" 1-3):
+ *   a  = gmm_forward_gather_act(x, sorted_flat, w1, activation)    [T*k, I]
+ *   y2 = gmm_forward(a, w2)                                         [T*k, H]
+ * bit for bit, as one persistent kernel: its CTAs first take the gate_up
+ * tiles (rows gathered from x; row r of group g is token sorted_flat[r] / k),
+ * then the down tiles, each of which waits until its 128 rows of `a` are
+ * stored.  The CTAs wait for one another (bounded: a wait past 4 s gives
+ * MOE_ERR_TIMEOUT), so they must all be resident at once: one per SM, as
+ * launched.  Rows past sum(group_list) of a and y2 are not written.
+ *   x [T, H] bf16; sorted_flat [T*k] int32 and group_list [E] int64 from
+ *   moe_permute; w1 [E, H, 2I], w2 [E, I, H] bf16 (H % 64 == 0, I % 128 == 0);
+ *   activation required; a [T*k, I] and y2 [T*k, H] bf16 out.
+ * Workspace: moe_expert_mlp_workspace_size(T, k, E).  128-row tiles. */
+MOE_API moe_status_t moe_expert_mlp_forward(const moe_bf16* x, const int32_t* sorted_flat, const int64_t* group_list,
+                             const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E,
+                             int64_t k, const moe_activation_t* activation, moe_bf16* a, moe_bf16* y2,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Workspace bytes for gmm_forward_combine: the status block, ceil(N/256)
  * int32 counts (one per 256-column slice) and an [M, N] bf16 scratch for the
  * expert outputs. */
@@ -382,11 +406,13 @@ MOE_API size_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t I, int64_t
  *   saved: NULL for inference (intermediates live in ws), or the buffers that
  *   moe_layer_backward will read.
  * Inference with T*k < 512*E (groups that average under 512 rows) fuses the
- * dispatch into gate_up ([MegaMoE] "算子功能"): the permute's index pass,
- * gmm_forward_gather_act, gmm_forward and moe_unpermute, four launches (five
- * above 1024 routed slots); the permuted tokens are never written to HBM.  The
- * result is bit-identical to the unfused chain (moe_permute, gmm_forward with
- * the activation, gmm_forward, moe_unpermute), which the other cases run. */
+ * dispatch into gate_up and runs both expert matmuls as one launch ([MegaMoE]
+ * "算子功能"): the permute's index pass, moe_expert_mlp_forward and
+ * moe_unpermute, three launches (four above 1024 routed slots; with
+ * transposed weights the two matmuls are gmm_forward_gather_act and
+ * gmm_forward); the permuted tokens are never written to HBM.  The result is
+ * bit-identical to the unfused chain (moe_permute, gmm_forward with the
+ * activation, gmm_forward, moe_unpermute), which the other cases run. */
 MOE_API moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const float* topk_w,
                                const moe_bf16* w1, const moe_bf16* w2,
                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,

@@ -53,6 +53,9 @@ SIGNATURES = {
     "gmm_forward_gather_act": (ST, [P, P, I64, I64, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P,
                                     P, SZ, P]),
     "gmm_forward_combine_workspace_size": (SZ, [I64, I64, I64, I64]),
+    "moe_expert_mlp_workspace_size": (SZ, [I64, I64, I64]),
+    "moe_expert_mlp_forward": (ST, [P, P, P, P, P, I64, I64, I64, I64, I64, C.POINTER(MoeActivation), P, P, P, SZ,
+                                    P]),
     "gmm_forward_combine": (ST, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, INT, P, P, SZ, P]),
     "gmm_backward_dx_swiglu": (ST, [P, P, P, P, I64, I64, I64, I64, F32, P, P, SZ, P]),
     "gmm_backward_dx_act": (ST, [P, P, P, P, I64, I64, I64, I64, C.POINTER(MoeActivation), INT, P, P, SZ, P]),

@@ -241,6 +241,32 @@ def gmm_forward_gather_act(x: torch.Tensor, sorted_flat: torch.Tensor, k: int, w
     return y
 
 
+def moe_expert_mlp_workspace_size(T, k, E) -> int:
+    return int(_lib().moe_expert_mlp_workspace_size(T, k, E))
+
+
+def moe_expert_mlp_forward(x: torch.Tensor, sorted_flat: torch.Tensor, group_list: torch.Tensor, w1: torch.Tensor,
+                           w2: torch.Tensor, k: int, activation=("swiglu", ()), *, a=None, y2=None,
+                           ws: Optional[Workspace] = None, stream=None):
+    """Both expert matmuls in one launch, the gate_up rows gathered from x:
+    returns (a [T*k, I], y2 [T*k, H])."""
+    for t, n in ((x, "x"), (w1, "w1"), (w2, "w2")):
+        _dtype(t, BF16, n)
+    _dtype(sorted_flat, torch.int32, "sorted_flat")
+    _dtype(group_list, torch.int64, "group_list")
+    T, H = x.shape
+    E, I = w2.shape[0], w2.shape[1]
+    if a is None:
+        a = torch.empty(T * k, I, dtype=BF16, device=x.device)
+    if y2 is None:
+        y2 = torch.empty(T * k, H, dtype=BF16, device=x.device)
+    wsp = _ws(ws, moe_expert_mlp_workspace_size(T, k, E), x.device)
+    _check(_lib().moe_expert_mlp_forward(_ptr(x), _ptr(sorted_flat), _ptr(group_list), _ptr(w1), _ptr(w2), T, H, I, E,
+                                         k, C.byref(_act(activation)), _ptr(a), _ptr(y2), wsp.ptr, wsp.nbytes,
+                                         _stream(stream)), "moe_expert_mlp_forward")
+    return a, y2
+
+
 def gmm_forward_combine_workspace_size(T, k, M, N) -> int:
     return int(_lib().gmm_forward_combine_workspace_size(T, k, M, N))
 

@@ -284,6 +284,33 @@ moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int
                             (w_flags & MOE_W_TRANSPOSED) != 0, y2, counters, y, status_of(ws), s);
 }
 
+size_t moe_expert_mlp_workspace_size(int64_t T, int64_t k, int64_t E) {
+  if (T <= 0 || k <= 0 || E <= 0) return MOE_STATUS_BYTES;
+  return MOE_STATUS_BYTES + expert_mlp_ready_bytes(T * k, E);
+}
+
+moe_status_t moe_expert_mlp_forward(const moe_bf16* x, const int32_t* sorted_flat, const int64_t* group_list,
+                                    const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I,
+                                    int64_t E, int64_t k, const moe_activation_t* activation, moe_bf16* a,
+                                    moe_bf16* y2, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !sorted_flat || !group_list || !w1 || !w2 || !a || !y2 || !activation) return MOE_ERR_NULLPTR;
+  Act act;
+  moe_status_t st = resolve_act(activation, &act);
+  if (st != MOE_OK) return st;
+  if (E <= 0 || I <= 0 || k > E) return MOE_ERR_INVALID;
+  if ((st = check_tokens(T, H, k)) != MOE_OK) return st;
+  if (E > kMaxExperts || H % 64 || I % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(a) || !aligned16(y2) ||
+      (reinterpret_cast<uintptr_t>(group_list) & 7u) || (reinterpret_cast<uintptr_t>(sorted_flat) & 3u))
+    return MOE_ERR_INVALID;
+  if ((st = check_ws(ws, ws_bytes, moe_expert_mlp_workspace_size(T, k, E))) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* ready = reinterpret_cast<int32_t*>(after_status(ws));
+  if (cudaMemsetAsync(ready, 0, expert_mlp_ready_bytes(T * k, E), s) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_expert_mlp(x, sorted_flat, w1, w2, group_list, T, H, I, E, k, act, a, y2, ready, status_of(ws), s);
+}
+
 moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
                              int64_t M, int64_t K, int64_t N, int64_t E, int w_flags, moe_bf16* dx, moe_bf16* dw,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -464,13 +491,24 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
   }
   if (!saved && R < kPairMinRowsPerGroup * E) {
     // Inference with groups that average under 512 rows (the 128-row kernel's
-    // regime): the permute only ranks the slots, and gate_up reads its rows
-    // straight from x, so the permuted tokens never make a round trip through
-    // HBM.  Down and the combine stay two launches: the fused form
-    // (gmm_forward_combine) is slower at these sizes (its column-slice order
-    // re-reads the activation from HBM).
-    if ((st = launch_permute(nullptr, topk_ids, T, H, k, E, nullptr, gl, rmap, sflat, status, scratch, s)) != MOE_OK)
+    // regime): the permute only ranks the slots (and zeroes the readiness
+    // counts, which sit where x_perm would), then both expert matmuls run in
+    // one launch whose gate_up reads its rows straight from x, so the permuted
+    // tokens never make a round trip through HBM.  The combine stays its own
+    // launch: the fused form (gmm_forward_combine) is slower at these sizes
+    // (its column-slice order re-reads the activation from HBM).  Transposed
+    // weights take the gathered gate_up and the down GMM as two launches.
+    int32_t* ready = reinterpret_cast<int32_t*>(x_perm);
+    const bool one_launch = w_flags == 0;
+    const int64_t n_ready = one_launch ? static_cast<int64_t>(expert_mlp_ready_bytes(R, E) / sizeof(int32_t)) : 0;
+    if ((st = launch_permute(nullptr, topk_ids, T, H, k, E, nullptr, gl, rmap, sflat, status, scratch, s, nullptr,
+                             ready, n_ready)) != MOE_OK)
       return st;
+    if (one_launch) {
+      if ((st = launch_expert_mlp(x, sflat, w1, w2, gl, T, H, I, E, k, act, a, y2, ready, status, s)) != MOE_OK)
+        return st;
+      return launch_unpermute(y2, rmap, topk_w, T, H, k, y, status, s);
+    }
     if ((st = launch_gmm_gather_act(x, sflat, T, k, w1, gl, R, H, 2 * I, E, act, (w_flags & MOE_W1_TRANSPOSED) != 0,
                                     a, nullptr, 0, status, s)) != MOE_OK)
       return st;

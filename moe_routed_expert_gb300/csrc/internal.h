@@ -61,9 +61,11 @@ moe_status_t check_permute_args(const uint16_t* x, const int32_t* topk_ids, int6
                                 const int32_t* row_id_map, const int32_t* sorted_flat);
 size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E);
 // With `mx`, the gathered rows leave quantised into mx->q / mx->scales (x_perm unused).
+// zero / zero_n: an int32 scratch range the index pass zeroes on the way (or none).
 moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
                             uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
-                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx = nullptr);
+                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx = nullptr,
+                            int32_t* zero = nullptr, int64_t zero_n = 0);
 
 // ---- combine side (combine.cu)
 moe_status_t launch_unpermute(const uint16_t* y_perm, const int32_t* row_id_map, const float* topk_w,
@@ -128,7 +130,8 @@ moe_status_t launch_gmm(int mode, int epilogue, const uint16_t* a, const uint16_
 // n_counters of them for a down GMM that follows).
 struct FusedOptions {
   bool discard = true;       // drop combined expert rows from L2 unwritten
-  bool evict_first = true;   // stream the weights under an L2 evict-first policy
+  bool evict_first = true;   // stream the weights under an L2 evict-first policy (when experts
+                             // average under 64 rows)
 };
 size_t fused_counter_bytes(int64_t N);
 moe_status_t launch_gmm_gather_act(const uint16_t* x, const int32_t* sorted_flat, int64_t T, int64_t k,
@@ -141,6 +144,16 @@ moe_status_t launch_gmm_combine(const uint16_t* a, const uint16_t* w, const int6
                                 int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, bool w_transposed,
                                 uint16_t* y2, int32_t* counters, uint16_t* y, uint32_t* status, cudaStream_t s,
                                 const FusedOptions& opt = FusedOptions());
+// Both expert matmuls of the inference layer in one persistent launch
+// (gmm.cu): gate_up with the activation over rows gathered from x (row r is
+// token sorted_flat[r] / k), then down; a [R, I] and y2 [R, H] out, R = T * k.
+// Weights [E, H, 2I] and [E, I, H].  ready: expert_mlp_ready_bytes(R, E) of
+// scratch, zero at launch (launch_permute can zero it).
+size_t expert_mlp_ready_bytes(int64_t R, int64_t E);
+moe_status_t launch_expert_mlp(const uint16_t* x, const int32_t* sorted_flat, const uint16_t* w1, const uint16_t* w2,
+                               const int64_t* group_list, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                               const Act& act, uint16_t* a, uint16_t* y2, int32_t* ready, uint32_t* status,
+                               cudaStream_t s);
 // Block-scaled grouped matmul (gmm_mx.cu): a [M, K] fp8 with scales [M, K/32];
 // b [E, N, K] fp8 with scales [E, N, K/32].  act == nullptr: bf16 out [M, N];
 // else the activation of the [gate | up] halves, quantised into aq [M, N/2] /

@@ -50,7 +50,8 @@ constexpr int kSmallSlots = 1024;    // one-block index path up to this many slo
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int nslots, int E,
                                                              int64_t* __restrict__ group_list,
                                                              int32_t* __restrict__ row_id_map,
-                                                             int32_t* __restrict__ sorted_flat, uint32_t* status) {
+                                                             int32_t* __restrict__ sorted_flat, uint32_t* status,
+                                                             int32_t* zero, int64_t zero_n) {
   __shared__ int32_t cnt[kMaxExperts];
   __shared__ int32_t next_row[kMaxExperts];
   __shared__ int32_t id_sh[kSmallSlots];   // each slot's expert, -1 when unused or invalid
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int64_t i = tid; i < zero_n; i += 1024) zero[i] = 0;   // a scratch range the caller wants zeroed
   for (int e = tid; e < E; e += 1024) cnt[e] = 0;
   __syncthreads();
   for (int f = tid; f < nslots; f += 1024) {
@@ -122,9 +124,12 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
 
 __global__ void __launch_bounds__(THREADS) permute_count_kernel(const int32_t* __restrict__ ids, int64_t nslots,
                                                                 int E, int nchunks, int32_t* __restrict__ chunk_counts,
-                                                                uint32_t* status) {
+                                                                uint32_t* status, int32_t* zero, int64_t zero_n) {
   pdl_wait();
   pdl_trigger();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x; i < zero_n;
+       i += static_cast<int64_t>(gridDim.x) * THREADS)
+    zero[i] = 0;   // a scratch range the caller wants zeroed
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += THREADS) hist[e] = 0;
   __syncthreads();
@@ -359,18 +364,19 @@ size_t permute_scratch_bytes(int64_t T, int64_t k, int64_t E) {
 
 moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, int64_t H, int64_t k, int64_t E,
                             uint16_t* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
-                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx) {
+                            uint32_t* status, void* scratch, cudaStream_t s, const MxOut* mx, int32_t* zero,
+                            int64_t zero_n) {
   const int64_t nslots = T * k;
   const int nchunks = static_cast<int>((nslots + CHUNK - 1) / CHUNK);
   int32_t* chunk_counts = static_cast<int32_t*>(scratch);
   const int e = static_cast<int>(E);
   if (nslots <= kSmallSlots) {
     if (launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, 1, ids, static_cast<int>(nslots), e, group_list,
-                   row_id_map, sorted_flat, status) != cudaSuccess)
+                   row_id_map, sorted_flat, status, zero, zero_n) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
     if (launch_pdl(permute_count_kernel, dim3(nchunks), dim3(THREADS), e * sizeof(int32_t), s, 1, ids, nslots, e,
-                   nchunks, chunk_counts, status) != cudaSuccess)
+                   nchunks, chunk_counts, status, zero, zero_n) != cudaSuccess)
       return MOE_ERR_CUDA;
     const size_t rank_smem = static_cast<size_t>(WARPS + 1) * e * sizeof(int32_t);
     if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,

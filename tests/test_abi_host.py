@@ -122,6 +122,15 @@ def test_fused_entry_points_check_their_arguments(lib):
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 100, 512, 4, 0, FAKE, ws, nws, None) == 3  # K % 64
     assert c(MIS, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, nws, None) == 2
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 2, 128, 256, 512, 4, 0, FAKE, ws, 256, None) == 2
+    # moe_expert_mlp_forward(x, sorted_flat, gl, w1, w2, T, H, I, E, k, act, a, y2, ws, n, s)
+    f = lib.moe_expert_mlp_forward
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 256, 128, 8, 2, None, FAKE, FAKE, ws, nws, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 256, 96, 8, 2, a, FAKE, FAKE, ws, nws, None) == 3      # I % 128
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 256, 128, 8, 9, a, FAKE, FAKE, ws, nws, None) == 2     # k > E
+    assert f(FAKE, FAKE, FAKE, FAKE, MIS, 64, 256, 128, 8, 2, a, FAKE, FAKE, ws, nws, None) == 2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 256, 128, 8, 2, a, FAKE, FAKE, ws, 256, None) == 2     # workspace
+    # status + one count per 128-row tile (T*k/128 + E), 256-byte aligned
+    assert lib.moe_expert_mlp_workspace_size(4096, 8, 256) == 256 + (256 + 256) * 4
     # status + counts (ceil(N/256) int32, 256-byte aligned) + the [M, N] bf16 scratch
     assert lib.gmm_forward_combine_workspace_size(4096, 8, 32768, 2048) == 256 + 256 + 32768 * 2048 * 2
     assert lib.gmm_forward_combine_workspace_size(0, 8, 0, 2048) == 256

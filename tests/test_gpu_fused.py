@@ -139,3 +139,45 @@ def test_fused_layer_forward_workloads(name):
     y_o, _ = O.moe_layer_forward(f64(inp["x"]), inp["topk_ids"], inp["topk_w"], f64(inp["w1"]), f64(inp["w2"]),
                                  wl.clip)
     assert_close("y (fused, end to end)", y_fused, y_o)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_expert_mlp_one_launch_equals_the_two_gmms(case):
+    """moe_expert_mlp_forward (both expert matmuls in one launch, gate_up rows
+    gathered from x) against gmm_forward with the activation on the permuted
+    rows and gmm_forward: bit for bit, rows past the groups untouched, and the
+    same on a second call (its readiness counts start at zero each time)."""
+    import torch
+    import moe_routed_expert_gb300 as M
+    wl = _wl(case)
+    inp = _inputs(wl, *case[6:])
+    x, ids = dev_bf16(inp["x"]), dev(inp["topk_ids"])
+    w1, w2 = dev_bf16(inp["w1"]), dev_bf16(inp["w2"])
+    x_perm, gl, rmap, sflat = M.moe_permute(x, ids, wl.E)
+    R = int(gl.sum())
+    act = ("swiglu", [3.0])
+    a_ref = M.gmm_forward(x_perm, w1, gl, activation=act)
+    y2_ref = M.gmm_forward(a_ref, w2, gl)
+    a = torch.full_like(a_ref, 7.0)
+    y2 = torch.full_like(y2_ref, 5.0)
+    ws = M.Workspace(M.moe_expert_mlp_workspace_size(wl.T, wl.k, wl.E))
+    for _ in range(2):
+        M.moe_expert_mlp_forward(x, sflat, gl, w1, w2, wl.k, act, a=a, y2=y2, ws=ws)
+        assert M.read_status(ws) == 0
+        assert torch.equal(a[:R], a_ref[:R]) and torch.equal(y2[:R], y2_ref[:R])
+        assert torch.all(a[R:] == 7.0) and torch.all(y2[R:] == 5.0)
+
+
+def test_expert_mlp_one_launch_at_the_prefill_size():
+    import torch
+    import moe_routed_expert_gb300 as M
+    wl = WORKLOADS["layer_prefill_t4096"]
+    inp = layer_inputs(wl)
+    x, ids = dev_bf16(inp["x"]), dev(inp["topk_ids"])
+    w1, w2 = dev_bf16(inp["w1"]), dev_bf16(inp["w2"])
+    x_perm, gl, rmap, sflat = M.moe_permute(x, ids, wl.E)
+    a_ref = M.gmm_forward(x_perm, w1, gl, epilogue=1)
+    y2_ref = M.gmm_forward(a_ref, w2, gl)
+    a, y2 = M.moe_expert_mlp_forward(x, sflat, gl, w1, w2, wl.k)
+    torch.cuda.synchronize()
+    assert torch.equal(a, a_ref) and torch.equal(y2, y2_ref)

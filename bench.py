@@ -19,9 +19,10 @@ scaling is weak.  ``--impl reference`` times the CPU oracle on a bounded
 token sample of the same workload.
 
 With the default workload the line also carries ``workloads``: the Zipf
-grouped matmul forward + backward (E=8, K=1024, N=2048, M=8192; tensor-bound)
-and the prefill (T=4096) and decode (T=64) layer forwards (HBM-bound), each
-timed the same way with its own per-launch split, roofline, clocks and e2e.
+grouped matmul forward + backward (E=8, K=1024, N=2048, M=8192; tensor-bound),
+the prefill (T=4096) and decode (T=64) layer forwards (HBM-bound), and the
+same layers in A8W4-FP and A4W4-FP (MXFP4 weights), each timed the same way
+with its own per-launch split, roofline, clocks and e2e.
 """
 from __future__ import annotations
 
@@ -628,9 +629,11 @@ def layer_bytes(wl, inp):
 
 
 # The workloads the default run measures beside its headline: the standalone
-# Zipf GMM forward + backward (tensor-bound), and the prefill and decode
-# layer forwards (HBM-bound), each with its own split, roofline, clocks and e2e.
-EXTRA_WORKLOADS = ["gmm_zipf_e8", "layer_prefill_t4096", "layer_decode_t64"]
+# Zipf GMM forward + backward (tensor-bound), the prefill and decode layer
+# forwards (HBM-bound), and the same layers with MXFP4 (E2M1) weights and
+# MXFP8 or MXFP4 tokens, each with its own split, roofline, clocks and e2e.
+EXTRA_WORKLOADS = ["gmm_zipf_e8", "layer_prefill_t4096", "layer_decode_t64", "layer_prefill_a8w4_t4096",
+                   "layer_decode_a8w4_t64", "layer_prefill_a4w4_t4096", "layer_decode_a4w4_t64"]
 MX_WORKLOADS = ["layer_prefill_mx_t4096", "layer_decode_mx_t64", "layer_prefill_a8w4_t4096",
                 "layer_decode_a8w4_t64", "layer_prefill_a4w4_t4096", "layer_decode_a4w4_t64"]
 GMM_SETS = 4            # rotating input sets of the Zipf GMM (4 x 168 MB)
@@ -1075,7 +1078,7 @@ def main():
         if args.extra in ("default", "all") and (args.workload == DEFAULT_WORKLOAD or args.extra == "all"):
             extras += [w for w in EXTRA_WORKLOADS if w != args.workload]
         if args.extra in ("mx", "all"):
-            extras += [w for w in MX_WORKLOADS if w != args.workload]
+            extras += [w for w in MX_WORKLOADS if w != args.workload and w not in extras]
     if extras:
         del step, inp
         torch.cuda.empty_cache()

@@ -49,47 +49,12 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # match (the captures' commands sit beside their summaries).
 GMM_TRAFFIC = [
     {"workload": "layer_train_t16384", "bytes_per_launch": 2.701e9,
-     "sources": {
-         "gmm.cu": "117c05934dbd56a5bd1f49ae969a92b8cb8c935318e38a6d472f6606b410e6b1",
-         "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
-    {"workload": "layer_prefill_mx_t4096", "bytes_per_launch": 0.5171e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
-    {"workload": "layer_decode_mx_t64", "bytes_per_launch": 0.3652e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
-    {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 0.3088e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
-    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 0.1883e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
-    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 0.2914e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
-    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 0.1881e9,
-     "sources": {
-         "gmm_mx.cu": "b7cd7e232d90486789ddb23a5f3a75eac463fecb9980ddd618ae69b3e0672b95",
-         "common.cuh": "d0d5b889231fa811707bbc4b591cad061f4c4bbe1fccd03adb1d5f197b2d8e9c",
-         "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd",
-         "tmap.cu": "c9b5bce8eca7d2d76c4f82a7e683a971586ea5a1f5b11a1dd63fe34a7a865b64"}},
+     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
+                 "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5", "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
+    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.912e9,
+     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5"}},
+    {"workload": "layer_decode_t64", "bytes_per_launch": 1.4125e9,
+     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5"}},
 ]
 
 

@@ -19,7 +19,9 @@
 // of 128 fp8 elements = one 128-byte swizzle row):
 //   warp 0      tile producer.  Lane 0 issues the TMA copies of the A tile
 //               (128 rows x 128) and the B tile (256 channels x 128) into a
-//               4-stage ring.
+//               4-stage ring; the B copies take an L2 evict-first policy when
+//               the groups average under 64 rows (each weight tile is then
+//               read once).
 //   warps 10-11 scale producers.  Their lanes copy the stage's scales with
 //               cp.async (4 bytes each: the 4 scales of one row) into the
 //               stage's scale slot, in the order the tensor core reads them:
@@ -41,6 +43,7 @@
 //   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half
 //               of the tile's columns: tcgen05.ld -> registers (bf16) ->
 //               release the accumulator -> activation / Q_MX -> global stores.
+//               A quarter with no row of the tile releases at once.
 // TMEM: one 256-column fp32 accumulator (the scales of the stages take 48
 // more columns, and a second accumulator does not fit in 512 with them); the
 // epilogue releases it as soon as the tile is in registers.
@@ -104,6 +107,7 @@ struct MxParams {
   Act act;
   uint32_t idesc;
   uint32_t tx_bytes;     // bytes a stage's A and B copies deliver: E2M1 operands count their packed size
+  uint32_t w_evict_first;  // weight tiles loaded under an L2 evict-first policy
   uint32_t* status;
 };
 
@@ -316,6 +320,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       uint32_t it = 0;
       bool ok = true;
       StageIter cur;
+      const uint64_t pol = p.w_evict_first ? l2_policy_evict_first() : 0ull;
       stage_iter_start<EPI>(cur, sm, p, ntiles);
       while (cur.valid) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -326,11 +331,14 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const TileInfo& ti = cur.ti;
         mbar_expect_tx(bar, p.tx_bytes);
         tma_load_2d(a_dst, &tmA, bar, cur.kb * BK, static_cast<int32_t>(ti.row0));
-        if (EPI == MX_ACT) {  // 128 gate channels, then the 128 matching up channels
-          tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
-          tma_load_3d(b_dst + (BN / 2) * BK, &tmB, bar, cur.kb * BK, p.out_cols + ti.col0, ti.g);
+        // ACT: 128 gate channels, then the 128 matching up channels
+        const int c1 = EPI == MX_ACT ? p.out_cols + ti.col0 : 0;
+        if (p.w_evict_first) {
+          tma_load_3d_hint(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g, pol);
+          if (EPI == MX_ACT) tma_load_3d_hint(b_dst + (BN / 2) * BK, &tmB, bar, cur.kb * BK, c1, ti.g, pol);
         } else {
           tma_load_3d(b_dst, &tmB, bar, cur.kb * BK, ti.col0, ti.g);
+          if (EPI == MX_ACT) tma_load_3d(b_dst + (BN / 2) * BK, &tmB, bar, cur.kb * BK, c1, ti.g);
         }
         ++it;
         stage_iter_next<EPI>(cur, sm, p, ntiles);
@@ -409,6 +417,11 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const bool row_ok = row_in_tile < ti.rows_valid;
       const int64_t row = ti.row0 + row_in_tile;
       if (!warp_wait(smem_u32(&sm->tmem_full), local & 1u, abort_flag, lane)) break;
+      if (q * 32 >= ti.rows_valid) {   // no row of this lane quarter is stored: release at once
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->tmem_empty));
+        continue;
+      }
       tc_fence_after();
       if (EPI == MX_ACT) {
         // activation columns [64 half, 64 half + 64): gate at TMEM columns 64 half + c,
@@ -545,8 +558,12 @@ moe_status_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const M
 }  // namespace
 
 moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s) {
-  // a few rows per expert (decode): the 128-row activation tile would be mostly padding
   MxParams p{};
+  // weights streamed under an L2 evict-first policy only when experts average
+  // under 64 rows (decode), as in the bf16 grouped matmul: there each weight
+  // tile is read once, while larger groups read it again from L2 for each of
+  // their 128-row tiles
+  p.w_evict_first = x.M < 64 * x.E ? 1u : 0u;
   p.group_list = x.group_list;
   p.a_sf = x.a_sf;
   p.b_sf = x.b_sf;

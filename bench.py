@@ -7,7 +7,7 @@ whole backward (combine gradients, dX and dW of both GMMs, SwiGLU gradient,
 token gradient).  One step = one forward + backward over one batch.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                        [--extra default|none|mx|all] [--impl reference]
+                        [--extra default|none|mx|all] [--impl reference] [--nvtx]
 
 Prints one JSON line.  ``value`` is tokens/s of the whole job with inputs
 resident in HBM, timed with CUDA events on the launching stream between a
@@ -816,6 +816,13 @@ def measure(name, step, inp, args, steps, warmup, world, dev, peaks, with_e2e=Tr
     headline = getattr(step, "headline", None)
     run_step = ((lambda: (advance(), headline())) if headline is not None else
                 (lambda: (advance(), [fn() for _, fn, _, _ in step.stages])))
+    if args.nvtx:   # one range per step around the library's own per-call ranges
+        plain_step = run_step
+
+        def run_step():
+            torch.cuda.nvtx.range_push("%s step" % name)
+            plain_step()
+            torch.cuda.nvtx.range_pop()
     # the sampler starts before the warm-up: nvidia-smi's start-up must not land in the timed region
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
@@ -859,8 +866,12 @@ def measure(name, step, inp, args, steps, warmup, world, dev, peaks, with_e2e=Tr
         ev = events[s]
         advance()
         ev[0].record(stream)
-        for i, (_, fn, _, _) in enumerate(step.stages):
+        for i, (sname, fn, _, _) in enumerate(step.stages):
+            if args.nvtx:
+                torch.cuda.nvtx.range_push(sname)
             fn()
+            if args.nvtx:
+                torch.cuda.nvtx.range_pop()
             ev[i + 1].record(stream)
     barrier()
     clock_info = clocks.stop()
@@ -993,6 +1004,9 @@ def main():
     ap.add_argument("--extra", default="default", choices=["default", "none", "mx", "all"],
                     help="workloads timed beside the headline: the Zipf GMM and the prefill / decode layers "
                          "(default, with the default workload), none, the MX layers, or all of them")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="NVTX ranges around each step and each stage of the per-launch split (every call "
+                         "of the library is also its own range)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph (the per-kernel split stays eager)")
     ap.add_argument("--tokens", type=int, default=None,

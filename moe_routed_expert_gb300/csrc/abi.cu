@@ -154,6 +154,7 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (ws == nullptr) return MOE_ERR_NULLPTR;
   if (ws_bytes < MOE_STATUS_BYTES || !aligned16(ws)) return MOE_ERR_INVALID;
   return cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -161,6 +162,7 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) 
 }
 
 moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES);
   if (st != MOE_OK) return st;
   if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return MOE_ERR_INVALID;
@@ -168,6 +170,7 @@ moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_
 }
 
 moe_status_t moe_read_status(const void* ws, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (ws == nullptr) return MOE_ERR_NULLPTR;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t v = 0;
@@ -185,6 +188,7 @@ size_t moe_permute_workspace_size(int64_t T, int64_t k, int64_t E) {
 moe_status_t moe_permute(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H, int64_t k, int64_t E,
                          moe_bf16* x_perm, int64_t* group_list, int32_t* row_id_map, int32_t* sorted_flat,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_permute_args(x, topk_ids, T, H, k, E, x_perm, group_list, row_id_map, sorted_flat);
   if (st != MOE_OK) return st;
   if ((st = check_ws(ws, ws_bytes, moe_permute_workspace_size(T, k, E))) != MOE_OK) return st;
@@ -201,6 +205,7 @@ size_t gmm_workspace_size(int64_t, int64_t, int64_t, int64_t) { return MOE_STATU
 moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
                              int64_t N, int64_t E, const moe_activation_t* activation, int w_flags, moe_bf16* y,
                              moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !w || !group_list || !y) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = activation ? resolve_act(activation, &act) : MOE_OK;
@@ -223,6 +228,7 @@ moe_status_t gmm_forward_act(const moe_bf16* x, const moe_bf16* w, const int64_t
 moe_status_t gmm_forward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K,
                          int64_t N, int64_t E, int epilogue, float clip, moe_bf16* y, moe_bf16* h_save,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SWIGLU) return MOE_ERR_UNSUPPORTED;
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
@@ -234,6 +240,7 @@ moe_status_t gmm_forward_gather_act(const moe_bf16* x, const int32_t* sorted_fla
                                     const moe_bf16* w, const int64_t* group_list, int64_t M, int64_t K, int64_t N,
                                     int64_t E, const moe_activation_t* activation, int w_flags, moe_bf16* y,
                                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !sorted_flat || !w || !group_list || !y || !activation) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
@@ -261,6 +268,7 @@ moe_status_t gmm_forward_combine(const moe_bf16* a, const moe_bf16* w, const int
                                  const int32_t* row_id_map, const int32_t* sorted_flat, const float* topk_w,
                                  int64_t T, int64_t k, int64_t M, int64_t K, int64_t N, int64_t E, int w_flags,
                                  moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!w || !group_list || !y) return MOE_ERR_NULLPTR;
   if (T != 0 && (!row_id_map || !topk_w)) return MOE_ERR_NULLPTR;
   if (M != 0 && (!a || !sorted_flat)) return MOE_ERR_NULLPTR;
@@ -293,6 +301,7 @@ moe_status_t moe_expert_mlp_forward(const moe_bf16* x, const int32_t* sorted_fla
                                     const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I,
                                     int64_t E, int64_t k, const moe_activation_t* activation, moe_bf16* a,
                                     moe_bf16* y2, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !sorted_flat || !group_list || !w1 || !w2 || !a || !y2 || !activation) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
@@ -314,6 +323,7 @@ moe_status_t moe_expert_mlp_forward(const moe_bf16* x, const int32_t* sorted_fla
 moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
                              int64_t M, int64_t K, int64_t N, int64_t E, int w_flags, moe_bf16* dx, moe_bf16* dw,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !w || !group_list || !dy) return MOE_ERR_NULLPTR;
   moe_status_t st = check_gmm_dims(M, K, N, E);
   if (st != MOE_OK) return st;
@@ -335,6 +345,7 @@ moe_status_t gmm_backward_ex(const moe_bf16* x, const moe_bf16* w, const int64_t
 moe_status_t gmm_backward(const moe_bf16* x, const moe_bf16* w, const int64_t* group_list, const moe_bf16* dy,
                           int64_t M, int64_t K, int64_t N, int64_t E, moe_bf16* dx, moe_bf16* dw,
                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   return gmm_backward_ex(x, w, group_list, dy, M, K, N, E, 0, dx, dw, ws, ws_bytes, stream);
 }
 
@@ -342,6 +353,7 @@ moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const in
                                  const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E,
                                  const moe_activation_t* activation, int w_flags, moe_bf16* dh, void* ws,
                                  size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!dy || !w || !group_list || !h || !dh) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
@@ -362,6 +374,7 @@ moe_status_t gmm_backward_dx_act(const moe_bf16* dy, const moe_bf16* w, const in
 moe_status_t gmm_backward_dx_swiglu(const moe_bf16* dy, const moe_bf16* w, const int64_t* group_list,
                                     const moe_bf16* h, int64_t M, int64_t K, int64_t N, int64_t E, float clip,
                                     moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
   return gmm_backward_dx_act(dy, w, group_list, h, M, K, N, E, &a, 0, dh, ws, ws_bytes, stream);
@@ -372,6 +385,7 @@ size_t moe_unpermute_workspace_size(void) { return MOE_STATUS_BYTES; }
 
 moe_status_t moe_unpermute(const moe_bf16* y_perm, const int32_t* row_id_map, const float* topk_w, int64_t T,
                            int64_t H, int64_t k, moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!y_perm || !row_id_map || !y) return MOE_ERR_NULLPTR;
   moe_status_t st = check_tokens(T, H, k);
   if (st != MOE_OK) return st;
@@ -385,6 +399,7 @@ moe_status_t moe_unpermute(const moe_bf16* y_perm, const int32_t* row_id_map, co
 moe_status_t moe_unpermute_backward(const moe_bf16* dy, const moe_bf16* y_perm, const int32_t* row_id_map,
                                     const float* topk_w, int64_t T, int64_t H, int64_t k, moe_bf16* dy_perm,
                                     float* dprobs, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!dy || !y_perm || !row_id_map || !topk_w || !dy_perm) return MOE_ERR_NULLPTR;
   moe_status_t st = check_tokens(T, H, k);
   if (st != MOE_OK) return st;
@@ -397,6 +412,7 @@ moe_status_t moe_unpermute_backward(const moe_bf16* dy, const moe_bf16* y_perm, 
 
 moe_status_t moe_permute_backward(const moe_bf16* dx_perm, const int32_t* row_id_map, int64_t T, int64_t H,
                                   int64_t k, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!dx_perm || !row_id_map || !dx) return MOE_ERR_NULLPTR;
   moe_status_t st = check_tokens(T, H, k);
   if (st != MOE_OK) return st;
@@ -410,6 +426,7 @@ moe_status_t moe_permute_backward(const moe_bf16* dx_perm, const int32_t* row_id
 moe_status_t moe_activation_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I,
                                      const moe_activation_t* activation, moe_bf16* dh, void* ws, size_t ws_bytes,
                                      moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!h || !da || !dh) return MOE_ERR_NULLPTR;
   Act act;
   moe_status_t st = resolve_act(activation, &act);
@@ -424,6 +441,7 @@ moe_status_t moe_activation_backward(const moe_bf16* h, const moe_bf16* da, int6
 
 moe_status_t moe_swiglu_backward(const moe_bf16* h, const moe_bf16* da, int64_t rows, int64_t I, float clip,
                                  moe_bf16* dh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
   return moe_activation_backward(h, da, rows, I, &a, dh, ws, ws_bytes, stream);
@@ -456,6 +474,7 @@ moe_status_t moe_layer_forward_act(const moe_bf16* x, const int32_t* topk_ids, c
                                    const moe_bf16* w1, const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E,
                                    int64_t k, const moe_activation_t* activation, int w_flags, moe_bf16* y,
                                    const moe_layer_saved_t* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !topk_ids || !topk_w || !w1 || !w2 || !y) return MOE_ERR_NULLPTR;
   if (saved && !saved_ok(saved)) return MOE_ERR_NULLPTR;
   Act act;
@@ -536,6 +555,7 @@ moe_status_t moe_layer_forward(const moe_bf16* x, const int32_t* topk_ids, const
                                const moe_bf16* w2, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float clip,
                                moe_bf16* y, const moe_layer_saved_t* saved, void* ws, size_t ws_bytes,
                                moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
   return moe_layer_forward_act(x, topk_ids, topk_w, w1, w2, T, H, I, E, k, &a, 0, y, saved, ws, ws_bytes, stream);
@@ -546,6 +566,7 @@ moe_status_t moe_layer_backward_act(const moe_bf16* dy, const float* topk_w, con
                                     int64_t I, int64_t E, int64_t k, const moe_activation_t* activation,
                                     int w_flags, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
                                     size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!dy || !topk_w || !w1 || !w2 || !saved || !dx) return MOE_ERR_NULLPTR;
   if (!saved_ok(saved)) return MOE_ERR_NULLPTR;
   Act act;
@@ -587,6 +608,7 @@ moe_status_t moe_layer_backward(const moe_bf16* dy, const float* topk_w, const m
                                 const moe_layer_saved_t* saved, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
                                 float clip, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2, float* dprobs, void* ws,
                                 size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (bad_clip(clip)) return MOE_ERR_INVALID;
   const moe_activation_t a = swiglu_desc(clip);
   return moe_layer_backward_act(dy, topk_w, w1, w2, saved, T, H, I, E, k, &a, 0, dx, dw1, dw2, dprobs, ws, ws_bytes,
@@ -628,6 +650,7 @@ size_t moe_mx_quantize_workspace_size(void) { return MOE_STATUS_BYTES; }
 
 moe_status_t moe_mx_quantize(const moe_bf16* x, int64_t rows, int64_t K, int32_t format, uint8_t* q,
                              uint8_t* scales, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (rows != 0 && (!x || !q || !scales)) return MOE_ERR_NULLPTR;
   if (rows < 0 || K <= 0 || bad_fmt(format)) return MOE_ERR_INVALID;
   if (K % 32) return MOE_ERR_UNSUPPORTED;
@@ -641,6 +664,7 @@ moe_status_t moe_permute_mx(const moe_bf16* x, const int32_t* topk_ids, int64_t 
                             int32_t format, uint8_t* x_q, uint8_t* x_scales, int64_t* group_list,
                             int32_t* row_id_map, int32_t* sorted_flat, void* ws, size_t ws_bytes,
                             moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!group_list) return MOE_ERR_NULLPTR;
   if (T != 0 && (!x || !topk_ids || !x_q || !x_scales || !row_id_map || !sorted_flat)) return MOE_ERR_NULLPTR;
   if (E <= 0 || k > E || bad_fmt(format)) return MOE_ERR_INVALID;
@@ -664,6 +688,7 @@ moe_status_t gmm_forward_mx(const uint8_t* x_q, const uint8_t* x_scales, const u
                             const int64_t* group_list, int64_t M, int64_t K, int64_t N, int64_t E, int32_t x_format,
                             int32_t w_format, const moe_activation_t* activation, moe_bf16* y, uint8_t* a_q,
                             uint8_t* a_scales, moe_bf16* h_save, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x_q || !x_scales || !w_q || !w_scales || !group_list) return MOE_ERR_NULLPTR;
   if (activation ? (!a_q || !a_scales) : !y) return MOE_ERR_NULLPTR;
   if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
@@ -697,6 +722,7 @@ moe_status_t moe_layer_forward_mx(const moe_bf16* x, const int32_t* topk_ids, co
                                   const uint8_t* w2_scales, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
                                   int32_t x_format, int32_t w_format, const moe_activation_t* activation,
                                   moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (!x || !topk_ids || !topk_w || !w1_q || !w1_scales || !w2_q || !w2_scales || !y) return MOE_ERR_NULLPTR;
   if (bad_fmt(x_format) || bad_fmt(w_format)) return MOE_ERR_INVALID;
   Act act;

@@ -5,12 +5,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_gmm.h"
 #include "moe_mx.h"
 
 struct CUtensorMap_st;  // cuda.h
 
 namespace moe {
+
+// An NVTX range named after the C-ABI function it spans (push at entry, pop
+// at any return): a profiler collecting NVTX (ncu --nvtx, nsys) sees each call
+// of the library as one range around its launches; without one attached the
+// push and pop do nothing.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+#define MOE_TRACE_CALL() ::moe::TraceRange moe_trace_range_(__func__)
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 64;

@@ -71,7 +71,9 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 3,  /* sizes outside what the kernels handle (see above) */
   MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
   MOE_ERR_DEVICE = 5,       /* the device found bad data (ids, counts, row ids) */
-  MOE_ERR_TIMEOUT = 6       /* a bounded pipeline wait expired inside a kernel */
+  MOE_ERR_TIMEOUT = 6,      /* a bounded pipeline wait expired inside a kernel */
+  MOE_ERR_BOUNDS = 7        /* bounds-checking build only: a kernel computed an index outside
+                               the tensor it was about to access and skipped the access */
 } moe_status_t;
 
 enum { MOE_EPILOGUE_NONE = 0, MOE_EPILOGUE_SWIGLU = 1 };
@@ -137,6 +139,15 @@ MOE_API const char* moe_status_string(moe_status_t status);
  * result: moe_read_status(ws) == MOE_ERR_TIMEOUT with the CUDA context still
  * usable.  ws: at least MOE_STATUS_BYTES, zeroed by moe_workspace_init. */
 MOE_API moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream);
+
+/* Bounds-check self-check: one kernel thread asks the device-side bounds
+ * check about an index one past the end of a range and accesses nothing.
+ * Built with MOE_BOUNDS_CHECK=1 (libmoe_gb300_bounds.so) the check records
+ * MOE_ERR_BOUNDS in the workspace's status word, as it would for any index a
+ * kernel derives outside the tensor it is about to access (the access is
+ * then skipped); the release library has no such checks and the status stays
+ * MOE_OK.  ws: at least MOE_STATUS_BYTES, zeroed by moe_workspace_init. */
+MOE_API moe_status_t moe_check_bounds(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- dispatch */
 

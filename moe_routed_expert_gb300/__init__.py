@@ -8,7 +8,7 @@ from .binding import (  # noqa: F401
     moe_layer_forward, moe_layer_workspace_size, moe_permute, moe_permute_backward, moe_permute_no_alloc, moe_permute_workspace_size,
     moe_swiglu_backward, moe_unpermute, moe_unpermute_backward, moe_unpermute_workspace_size, read_status,
     status_string, moe_mx_quantize, moe_permute_mx, gmm_forward_mx, moe_layer_forward_mx, moe_layer_mx_workspace_size,
-    check_wait_timeout, activation_format, gmm_forward_gather_act, gmm_forward_combine,
+    check_wait_timeout, check_bounds, activation_format, gmm_forward_gather_act, gmm_forward_combine,
     gmm_forward_combine_workspace_size, moe_expert_mlp_forward, moe_expert_mlp_workspace_size,
 )
-from ._abi import MOE_EPILOGUE_NONE, MOE_EPILOGUE_SWIGLU, STATUS_NAMES, load, lib_path  # noqa: F401
+from ._abi import MOE_EPILOGUE_NONE, MOE_EPILOGUE_SWIGLU, STATUS_NAMES, bounds_checking, load, lib_path  # noqa: F401

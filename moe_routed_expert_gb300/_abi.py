@@ -19,7 +19,7 @@ MOE_EPILOGUE_SWIGLU = 1
 
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_NULLPTR", 2: "MOE_ERR_INVALID", 3: "MOE_ERR_UNSUPPORTED",
-    4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BOUNDS",
 }
 
 
@@ -42,6 +42,7 @@ SIGNATURES = {
     "moe_read_status": (ST, [P, P]),
     "moe_status_string": (C.c_char_p, [ST]),
     "moe_check_wait_timeout": (ST, [P, SZ, C.c_uint64, P]),
+    "moe_check_bounds": (ST, [P, SZ, P]),
     "moe_permute_workspace_size": (SZ, [I64, I64, I64]),
     "moe_permute": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, SZ, P]),
     "moe_permute_no_alloc": (ST, [P, P, I64, I64, I64, I64, P, P, P, P, P, P]),
@@ -89,8 +90,13 @@ SIGNATURES = {
 _lib = None
 
 
+def bounds_checking() -> bool:
+    """MOE_GB300_BOUNDS_CHECK=1 selects the bounds-checking build of the library."""
+    return os.environ.get("MOE_GB300_BOUNDS_CHECK", "") == "1"
+
+
 def lib_path() -> str:
-    return _build.LIB_PATH
+    return _build.BOUNDS_LIB_PATH if bounds_checking() else _build.LIB_PATH
 
 
 def load(build_if_missing: bool = False):
@@ -102,7 +108,7 @@ def load(build_if_missing: bool = False):
     if not os.path.exists(path):
         if not build_if_missing:
             raise RuntimeError("moe_routed_expert_gb300: CUDA library not built (%s); run build()" % path)
-        _build.build()
+        _build.build(bounds=bounds_checking())
     lib = C.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)

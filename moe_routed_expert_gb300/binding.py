@@ -91,6 +91,13 @@ def status_string(status: int) -> str:
     return _lib().moe_status_string(status).decode()
 
 
+def check_bounds(ws: Workspace, stream=None):
+    """Run the library's bounds-check self-check (see moe_check_bounds): afterwards
+    read_status(ws) is MOE_ERR_BOUNDS (7) on the bounds-checking build, MOE_OK on
+    the release build."""
+    _check(_lib().moe_check_bounds(ws.ptr, ws.nbytes, _stream(stream)), "moe_check_bounds")
+
+
 def check_wait_timeout(ws: Workspace, timeout_ns: int = 1000000, stream=None):
     """Run the library's bounded-wait failure check (see moe_check_wait_timeout):
     afterwards read_status(ws) is MOE_ERR_TIMEOUT (6)."""

@@ -149,6 +149,7 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS";
   }
   return "MOE_ERR_UNKNOWN";
 }
@@ -167,6 +168,13 @@ moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_
   if (st != MOE_OK) return st;
   if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return MOE_ERR_INVALID;
   return launch_wait_timeout_check(status_of(ws), timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_check_bounds(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
+  moe_status_t st = check_ws(ws, ws_bytes, MOE_STATUS_BYTES);
+  if (st != MOE_OK) return st;
+  return launch_bounds_check(status_of(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_read_status(const void* ws, moe_stream_t stream) {

@@ -18,6 +18,29 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// Bounds-checking build (MOE_BOUNDS_CHECK=1, the library
+// libmoe_gb300_bounds.so): true when 0 <= i < n; otherwise the status word
+// takes MOE_ERR_BOUNDS and the caller skips the access it guards.  The
+// checks sit where a kernel derives an index from its own arithmetic (a row
+// from group offsets and tile numbers, a permuted row from a rank) rather
+// than reading one that it validates anyway.  Release build: always true, no
+// code.
+#ifndef MOE_BOUNDS_CHECK
+#define MOE_BOUNDS_CHECK 0
+#endif
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, uint32_t* status) {
+#if MOE_BOUNDS_CHECK
+  if (i >= 0 && i < n) return true;
+  set_status(status, MOE_ERR_BOUNDS);
+  return false;
+#else
+  (void)i;
+  (void)n;
+  (void)status;
+  return true;
+#endif
+}
+
 // ----------------------------------------------------------------- bf16 helpers
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

@@ -500,7 +500,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 #pragma unroll
       for (int i = 0; i < ROWS; ++i) {
         const int r = gw * (BM / GATHER_WARPS) + (lane >> 3) + 4 * i;
-        f[i] = r < ti.rows_valid ? p.sorted_flat[ti.row0 + r] : 0;
+        f[i] = r < ti.rows_valid && in_bounds(ti.row0 + r, p.rows_cap, p.status) ? p.sorted_flat[ti.row0 + r] : 0;
       }
       const uint16_t* src[ROWS];
       bool bad = false;
@@ -583,7 +583,7 @@ gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE, EPI>(sm, p, t);
-      const bool row_ok = row_in_tile < ti.rows_valid;
+      const bool row_ok = row_in_tile < ti.rows_valid && in_bounds(ti.row0 + row_in_tile, p.rows_cap, p.status);
       const int64_t row = ti.row0 + row_in_tile;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
@@ -974,7 +974,7 @@ expert_mlp_kernel(const __grid_constant__ CUtensorMap tmB1, const __grid_constan
 #pragma unroll
       for (int i = 0; i < ROWS; ++i) {
         const int r = gw * (BM / GATHER_WARPS) + (lane >> 3) + 4 * i;
-        f[i] = r < ti.rows_valid ? p.sorted_flat[ti.row0 + r] : 0;
+        f[i] = r < ti.rows_valid && in_bounds(ti.row0 + r, p.rows_cap, p.status) ? p.sorted_flat[ti.row0 + r] : 0;
       }
       const uint16_t* src[ROWS];
       bool bad = false;
@@ -1025,7 +1025,7 @@ expert_mlp_kernel(const __grid_constant__ CUtensorMap tmB1, const __grid_constan
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
       const LTile ti = decode_layer_tile(sm, p, n1, t);
-      const bool row_ok = row_in_tile < ti.rows_valid;
+      const bool row_ok = row_in_tile < ti.rows_valid && in_bounds(ti.row0 + row_in_tile, p.rows_cap, p.status);
       const int64_t row = ti.row0 + row_in_tile;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;

@@ -414,7 +414,7 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint32_t local = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
       const TileInfo ti = decode_tile<EPI>(sm, p, t);
-      const bool row_ok = row_in_tile < ti.rows_valid;
+      const bool row_ok = row_in_tile < ti.rows_valid && in_bounds(ti.row0 + row_in_tile, p.rows_cap, p.status);
       const int64_t row = ti.row0 + row_in_tile;
       if (!warp_wait(smem_u32(&sm->tmem_full), local & 1u, abort_flag, lane)) break;
       if (q * 32 >= ti.rows_valid) {   // no row of this lane quarter is stored: release at once

@@ -708,8 +708,15 @@ gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!warp_wait(smem_u32(&sm->tmem_full[acc]), aph, abort_flag, lane)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;
-      const int rows_valid = ti.rows_valid - qw * 32;  // rows of this warp's 32 that are in the group
+      int rows_valid = ti.rows_valid - qw * 32;  // rows of this warp's 32 that are in the group
       const int64_t wrow0 = ti.row0 + qw * 32;
+      {  // bounds-checking build: the warp's first and last rows lie in the output (dW: in the group's gradient)
+        const int64_t rcap = mode == GMM_DW ? q.out_rows : q.rows_cap;
+        if (rows_valid > 0 &&
+            !(in_bounds(wrow0, rcap, q.status) && in_bounds(wrow0 + min(rows_valid, 32) - 1, rcap, q.status) &&
+              (mode != GMM_DW || in_bounds(ti.g, q.E, q.status))))
+          rows_valid = 0;
+      }
       const uint32_t release = mapa_shared(smem_u32(&sm->tmem_empty[acc]), 0);
       auto release_tmem = [&]() {
         tc_fence_before();

@@ -55,6 +55,7 @@ int num_sms();  // SM count of the current device (cached per device)
 
 // ---- failure-detection check (selfcheck.cu)
 moe_status_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+moe_status_t launch_bounds_check(uint32_t* status, cudaStream_t s);
 
 // ---- MX quantisation (mx.cu): fp8 codes + E8M0 scales, 32-element groups
 struct MxOut {
@@ -66,7 +67,7 @@ moe_status_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, int 
                                 cudaStream_t s);
 // The permute's gather, quantising: slot f's token row of x -> row row_id_map[f].
 moe_status_t launch_mx_gather(const uint16_t* x, int64_t nslots, int64_t H, int k, const int32_t* row_id_map,
-                              const MxOut& out, cudaStream_t s);
+                              const MxOut& out, uint32_t* status, cudaStream_t s);
 
 // ---- dispatch (permute.cu)
 // Argument checks shared by the permute entry points (abi.cu).

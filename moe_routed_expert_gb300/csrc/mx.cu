@@ -48,7 +48,8 @@ __device__ __forceinline__ void store_group(const GroupCodes<FMT>& g, uint8_t* q
 template <int FMT, bool GATHER>
 __global__ void __launch_bounds__(THREADS) mx_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                           const int32_t* __restrict__ row_id_map, int k,
-                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales) {
+                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
+                                                          uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int64_t groups = K / 32;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(THREADS) mx_rows_kernel(const uint16_t* __rest
         const int n = min(32, k - j0);
         for (int jj = 0; jj < n; ++jj) {
           const int32_t r = __shfl_sync(0xffffffffu, rl, jj);
-          if (r >= 0 && active) store_group<FMT>(g, q, scales, r, K, grp);
+          if (r >= 0 && active && in_bounds(r, rows * k, status)) store_group<FMT>(g, q, scales, r, K, grp);
         }
       }
     }
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(THREADS) mx_rows_kernel(const uint16_t* __rest
 
 template <bool GATHER>
 moe_status_t launch_rows(const uint16_t* x, int64_t n, int64_t K, const int32_t* row_id_map, int k, int fmt,
-                         uint8_t* q, uint8_t* scales, cudaStream_t s) {
+                         uint8_t* q, uint8_t* scales, uint32_t* status, cudaStream_t s) {
   const int64_t items = n * ((K / 32 + 31) / 32);
   int64_t blocks = (items + THREADS / 32 - 1) / (THREADS / 32);
   const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
@@ -107,13 +108,13 @@ moe_status_t launch_rows(const uint16_t* x, int64_t n, int64_t K, const int32_t*
   cudaError_t e;
   if (fmt == MOE_FP8_E5M2)
     e = launch_pdl(mx_rows_kernel<MOE_FP8_E5M2, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
-                   scales);
+                   scales, status);
   else if (fmt == MOE_FP4_E2M1)
     e = launch_pdl(mx_rows_kernel<MOE_FP4_E2M1, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
-                   scales);
+                   scales, status);
   else
     e = launch_pdl(mx_rows_kernel<MOE_FP8_E4M3, GATHER>, grid, dim3(THREADS), 0, s, 1, x, n, K, row_id_map, k, q,
-                   scales);
+                   scales, status);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -121,12 +122,12 @@ moe_status_t launch_rows(const uint16_t* x, int64_t n, int64_t K, const int32_t*
 
 moe_status_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, int fmt, uint8_t* q, uint8_t* scales,
                                 cudaStream_t s) {
-  return launch_rows<false>(x, rows, K, nullptr, 1, fmt, q, scales, s);
+  return launch_rows<false>(x, rows, K, nullptr, 1, fmt, q, scales, nullptr, s);
 }
 
 moe_status_t launch_mx_gather(const uint16_t* x, int64_t nslots, int64_t H, int k, const int32_t* row_id_map,
-                              const MxOut& out, cudaStream_t s) {
-  return launch_rows<true>(x, nslots / k, H, row_id_map, k, out.fmt, out.q, out.scales, s);
+                              const MxOut& out, uint32_t* status, cudaStream_t s) {
+  return launch_rows<true>(x, nslots / k, H, row_id_map, k, out.fmt, out.q, out.scales, status, s);
 }
 
 }  // namespace moe

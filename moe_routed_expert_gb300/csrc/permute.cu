@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
       if (e >= 0) {
         const int32_t row = next_row[e] + __popc(peers & lt);
         row_id_map[f] = row;
-        sorted_flat[row] = f;
+        if (in_bounds(row, nslots, status)) sorted_flat[row] = f;
       } else if (f < nslots) {
         row_id_map[f] = -1;
       }
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
                                                                const int32_t* __restrict__ chunk_counts,
                                                                int64_t* __restrict__ group_list,
                                                                int32_t* __restrict__ row_id_map,
-                                                               int32_t* __restrict__ sorted_flat) {
+                                                               int32_t* __restrict__ sorted_flat, uint32_t* status) {
   extern __shared__ int32_t wbase[];  // [WARPS][E], then the chunk's first row per expert [E]
   int32_t* cbase = wbase + WARPS * E;
   __shared__ int32_t warp_sum[WARPS];
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(THREADS) permute_rank_kernel(const int32_t* __
     if (e >= 0) {
       const int32_t row = mine[e] + __popc(peers & lt);
       row_id_map[f] = row;
-      sorted_flat[row] = static_cast<int32_t>(f);
+      if (in_bounds(row, nslots, status)) sorted_flat[row] = static_cast<int32_t>(f);
     } else if (f < nslots) {
       row_id_map[f] = -1;
     }
@@ -283,7 +283,7 @@ constexpr int SEG = 1024;  // bf16 elements per warp item (2 KB)
 __global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t* __restrict__ x, int64_t T,
                                                                  int64_t H, int k,
                                                                  const int32_t* __restrict__ row_id_map,
-                                                                 uint16_t* __restrict__ x_perm) {
+                                                                 uint16_t* __restrict__ x_perm, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int64_t nseg = (H + SEG - 1) / SEG;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t*
       const int m = min(32, k - j0);
       for (int jj = 0; jj < m; ++jj) {
         const int32_t row = __shfl_sync(0xffffffffu, rl, jj);
-        if (row < 0) continue;
+        if (row < 0 || !in_bounds(row, T * k, status)) continue;
         uint16_t* dst = x_perm + static_cast<int64_t>(row) * H + seg * SEG;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(THREADS) permute_gather_kernel(const uint16_t*
 __global__ void __launch_bounds__(THREADS) permute_gather_slots_kernel(const uint16_t* __restrict__ x, int64_t nslots,
                                                                  int64_t H, int k,
                                                                  const int32_t* __restrict__ row_id_map,
-                                                                 uint16_t* __restrict__ x_perm) {
+                                                                 uint16_t* __restrict__ x_perm, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int64_t nseg = (H + SEG - 1) / SEG;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(THREADS) permute_gather_slots_kernel(const uin
     const int64_t f = item / nseg;
     const int64_t seg = item - f * nseg;
     const int32_t row = row_id_map[f];
-    if (row < 0) continue;
+    if (row < 0 || !in_bounds(row, nslots, status)) continue;
     const int64_t t = f / k;
     const uint16_t* src = x + t * H + seg * SEG;
     uint16_t* dst = x_perm + static_cast<int64_t>(row) * H + seg * SEG;
@@ -380,11 +380,13 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
       return MOE_ERR_CUDA;
     const size_t rank_smem = static_cast<size_t>(WARPS + 1) * e * sizeof(int32_t);
     if (launch_pdl(permute_rank_kernel, dim3(nchunks), dim3(THREADS), rank_smem, s, 1, ids, nslots, e, nchunks,
-                   static_cast<const int32_t*>(chunk_counts), group_list, row_id_map, sorted_flat) != cudaSuccess)
+                   static_cast<const int32_t*>(chunk_counts), group_list, row_id_map, sorted_flat, status) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if (mx != nullptr && x != nullptr && H > 0) {
-    if (launch_mx_gather(x, nslots, H, static_cast<int>(k), row_id_map, *mx, s) != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_mx_gather(x, nslots, H, static_cast<int>(k), row_id_map, *mx, status, s) != MOE_OK)
+      return MOE_ERR_CUDA;
   } else if (x != nullptr && x_perm != nullptr && H > 0) {
     const int64_t nseg = (H + SEG - 1) / SEG;
     const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
@@ -396,9 +398,10 @@ moe_status_t launch_permute(const uint16_t* x, const int32_t* ids, int64_t T, in
     if (blocks < 1) blocks = 1;
     const cudaError_t ge =
         by_token ? launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s, 1, x,
-                              T, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm)
+                              T, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm, status)
                  : launch_pdl(permute_gather_slots_kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s,
-                              1, x, nslots, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm);
+                              1, x, nslots, H, static_cast<int>(k), static_cast<const int32_t*>(row_id_map), x_perm,
+                              status);
     if (ge != cudaSuccess)
       return MOE_ERR_CUDA;
   }

@@ -48,9 +48,34 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_abi.SIGNATURES) == set(declared_functions())
 
 
+def test_bounds_checking_build_exports_the_same_symbols():
+    """The bounds-checking variant (-DMOE_BOUNDS_CHECK=1) builds from the same
+    sources and exports the same entry points; the binding picks it only when
+    MOE_GB300_BOUNDS_CHECK=1."""
+    import subprocess
+    from moe_routed_expert_gb300 import _abi, build
+    path = build.build(bounds=True)
+    assert path.endswith("libmoe_gb300_bounds.so") and path != build.LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(declared_functions()) <= exported
+    assert all(not e.startswith("_ZN3moe") for e in exported)
+    old = os.environ.get("MOE_GB300_BOUNDS_CHECK")
+    try:
+        os.environ["MOE_GB300_BOUNDS_CHECK"] = "1"
+        assert _abi.bounds_checking() and _abi.lib_path() == path
+        os.environ["MOE_GB300_BOUNDS_CHECK"] = "0"
+        assert not _abi.bounds_checking() and _abi.lib_path() == build.LIB_PATH
+    finally:
+        if old is None:
+            os.environ.pop("MOE_GB300_BOUNDS_CHECK", None)
+        else:
+            os.environ["MOE_GB300_BOUNDS_CHECK"] = old
+
+
 def test_status_strings(lib):
     for code, name in {0: "MOE_OK", 1: "MOE_ERR_NULLPTR", 2: "MOE_ERR_INVALID", 3: "MOE_ERR_UNSUPPORTED",
-                       4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT"}.items():
+                       4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BOUNDS"}.items():
         assert lib.moe_status_string(code).decode() == name
 
 
@@ -193,6 +218,12 @@ def test_wait_timeout_check_arguments(lib):
     assert lib.moe_check_wait_timeout(FAKE, 128, 1000000, None) == 2       # workspace too small
     assert lib.moe_check_wait_timeout(FAKE, 256, 10, None) == 2            # limit below 1 us
     assert lib.moe_check_wait_timeout(FAKE, 256, 20 * 10**9, None) == 2    # limit above 10 s
+
+
+def test_bounds_check_arguments(lib):
+    assert lib.moe_check_bounds(None, 256, None) == 1
+    assert lib.moe_check_bounds(MIS, 256, None) == 2
+    assert lib.moe_check_bounds(FAKE, 128, None) == 2                     # workspace too small
 
 
 def test_mx_entry_points_check_their_arguments(lib):

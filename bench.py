@@ -48,13 +48,23 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # one ncu capture of the sources with these hashes; reported only while they
 # match (the captures' commands sit beside their summaries).
 GMM_TRAFFIC = [
-    {"workload": "layer_train_t16384", "bytes_per_launch": 2.701e9,
-     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "gmm_pair.cu": "274989130d60d1fcc7540ca26e4e372dceef60f3dc8f492e4bcafdbe26f04593",
-                 "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5", "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
-    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.912e9,
-     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5"}},
+    {"workload": "layer_train_t16384", "bytes_per_launch": 2.708e9,
+     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12",
+                 "gmm_pair.cu": "7acdcaeb39a20463640220649c863932e342290ca1dae165d40bfcb594943a1f",
+                 "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157",
+                 "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
+    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.908e9,
+     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
     {"workload": "layer_decode_t64", "bytes_per_launch": 1.4125e9,
-     "sources": {"gmm.cu": "cf1371048c54995b7c8dc0a146ef31f83eef451bf8ef0331a67e52b0e8cf07c0", "common.cuh": "876ba6d6126a3b24d3e5690281095f720c512ce24de8de2b44d0a71936bf7cd5"}},
+     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
+    {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 3.106e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
+    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.896e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
+    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 2.927e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
+    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 1.894e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
 ]
 
 

@@ -930,6 +930,8 @@ def measure(name, step, inp, args, steps, warmup, world, dev, peaks, with_e2e=Tr
         peak = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
+                # also against the sustained (power-capped, seconds-long) cuBLAS rate
+                "frac_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "traffic": measured_gmm_traffic(name) if args.tokens is None else None,
                 "kernel": "gmm_pair_kernel / gmm_kernel (all %d GMM launches of a step)" % gmm_launches,
                 "timing": "the step's timed region (every launch is a GMM)" if gmm_only else

@@ -327,6 +327,11 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
 }
+// The same under an L2 cache policy (createpolicy).
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "l"(pol)
+               : "memory");
+}
 
 // Atomic add with release (this thread's earlier writes are visible GPU-wide
 // first) and acquire (writes released before the values it read are visible

@@ -49,22 +49,22 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # match (the captures' commands sit beside their summaries).
 GMM_TRAFFIC = [
     {"workload": "layer_train_t16384", "bytes_per_launch": 2.708e9,
-     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12",
+     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c",
                  "gmm_pair.cu": "7acdcaeb39a20463640220649c863932e342290ca1dae165d40bfcb594943a1f",
-                 "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157",
+                 "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba",
                  "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
-    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.908e9,
-     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
-    {"workload": "layer_decode_t64", "bytes_per_launch": 1.4125e9,
-     "sources": {"gmm.cu": "b29e31c4903f9af10b402b28f40c50671734a30380cbf48b4ef61e28bf5c9d12", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
-    {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 3.106e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
-    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.896e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
-    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 2.927e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
-    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 1.894e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "70f06e98425a4a2f1f8a6a03ad43c70ac67a18081955bbf499df2d869127e157"}},
+    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.833e9,
+     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_decode_t64", "bytes_per_launch": 1.4126e9,
+     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 3.108e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.898e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 2.925e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 1.895e8,
+     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
 ]
 
 

@@ -161,6 +161,10 @@ SMALL = [
     LayerWorkload("small_a", 31, T=200, H=256, E=8, k=2, I=128, clip=0.0, hot_bias=0.0, backward=True),
     LayerWorkload("small_b", 32, T=333, H=384, E=16, k=4, I=256, clip=7.0, hot_bias=2.0, backward=True),
     LayerWorkload("small_c", 33, T=64, H=512, E=64, k=8, I=128, clip=0.5, hot_bias=0.0, backward=True),
+    # the most experts the library takes: 1280 routed slots (the multi-block
+    # index pass) over 1024 experts leave about 29% of them empty, whose dW1 and
+    # dW2 must come out zero; H=192 is a partial 128-column tile of the down GMM
+    LayerWorkload("small_e1024", 34, T=160, H=192, E=1024, k=8, I=128, clip=0.0, hot_bias=0.0, backward=True),
 ]
 
 

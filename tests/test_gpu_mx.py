@@ -259,9 +259,22 @@ def gpu_mx_chain(inp, wts, wl, fmt, act, wfmt=None):
 
 @pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e2m1"), ("e2m1", "e2m1")])
 def test_layer_mx_small(fmt, wfmt):
+    check_layer_mx(fmt, wfmt, T=96, H=256, E=8, k=4, I=128)
+
+
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e4m3", "e2m1")])
+def test_layer_mx_max_experts(fmt, wfmt):
+    """1024 experts (the library's limit): 1280 routed slots take the
+    multi-block index pass and leave about 29% of the experts empty."""
+    check_layer_mx(fmt, wfmt, T=160, H=256, E=1024, k=8, I=128)
+
+
+def check_layer_mx(fmt, wfmt, **shape):
+    """moe_layer_forward_mx against the chain of single calls (bit-identical),
+    each step of the chain on its own input, and y end to end."""
     import moe_routed_expert_gb300 as M
     wl = WORKLOADS["layer_prefill_mx_t4096"]
-    wl = type(wl)(**{**wl.__dict__, "T": 96, "H": 256, "E": 8, "k": 4, "I": 128, "mx": fmt, "w_mx": wfmt})
+    wl = type(wl)(**{**wl.__dict__, **shape, "mx": fmt, "w_mx": wfmt})
     inp = layer_inputs(wl, with_weights=False)
     wts = mx_layer_weights(wl)
     act = ("swiglu", [7.0])

@@ -48,23 +48,23 @@ DEFAULT_WORKLOAD = "layer_train_t16384"
 # one ncu capture of the sources with these hashes; reported only while they
 # match (the captures' commands sit beside their summaries).
 GMM_TRAFFIC = [
-    {"workload": "layer_train_t16384", "bytes_per_launch": 2.708e9,
-     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c",
+    {"workload": "layer_train_t16384", "bytes_per_launch": 2.693e9,
+     "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f",
                  "gmm_pair.cu": "7acdcaeb39a20463640220649c863932e342290ca1dae165d40bfcb594943a1f",
-                 "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba",
+                 "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd",
                  "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
-    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.833e9,
-     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
-    {"workload": "layer_decode_t64", "bytes_per_launch": 1.4126e9,
-     "sources": {"gmm.cu": "5637d750a3054f768ba06f9652dd0d89aaa8530ba8a2827eb34818024670881c", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+    {"workload": "layer_prefill_t4096", "bytes_per_launch": 1.836e9,
+     "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "layer_decode_t64", "bytes_per_launch": 1.4158e9,
+     "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
     {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 3.108e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
-    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.898e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
-    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 2.925e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
-    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 1.895e8,
-     "sources": {"gmm_mx.cu": "69588cf720821351bbd579e5fbbeb6fd5b97f36babbf368d4b4508aa43eba8ca", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "f92606c55fcb2b95da83d38863cf26aa1e2b97d1f47b48d03fbb5e7e543e84ba"}},
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.928e8,
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "layer_prefill_a4w4_t4096", "bytes_per_launch": 2.927e8,
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "layer_decode_a4w4_t64", "bytes_per_launch": 1.926e8,
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
 ]
 
 

@@ -175,8 +175,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // Every kernel of the library is launched with programmatic stream
 // serialisation: it may start while the previous kernel on the stream drains.
 // pdl_wait() blocks until that kernel has finished and its writes are visible;
-// no kernel reads or writes global memory before it.  pdl_trigger() lets the
-// next kernel start launching.
+// no kernel reads or writes global memory before it (an L2 prefetch of an
+// input, which returns nothing and changes nothing, is the one exception).
+// pdl_trigger() lets the next kernel start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -364,6 +365,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // Bring the 128-byte line holding p into L2 (no value returned).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+// Bring [p, p + bytes) into L2 through the bulk-copy unit (no value returned).
+// p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
 // 16-byte load cached in L2 only (data another SM wrote during this kernel).

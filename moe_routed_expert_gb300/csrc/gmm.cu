@@ -732,6 +732,10 @@ moe_status_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const Gmm
 // tiles of the first stage are issued before that wait.  The signal warp also
 // frees each accumulator once the four epilogue warps stored its tile.
 constexpr int LAYER_THREADS = NUM_THREADS + 32 * GATHER_WARPS + 32;   // + gather warps + signal warp
+#ifndef MOE_W1_PREFETCH_MB
+#define MOE_W1_PREFETCH_MB 24
+#endif
+constexpr int kW1PrefetchMB = MOE_W1_PREFETCH_MB;
 
 struct LayerParams {
   const int64_t* group_list;
@@ -751,6 +755,8 @@ struct LayerParams {
   int32_t* ready;              // [row tiles]: phase-0 tiles stored (zero at launch)
   Act act;
   int w_evict_first;
+  const uint8_t* w1;           // gate_up weights, for the L2 prefetch before the wait
+  int64_t w1_prefetch;         // bytes of w1 to prefetch (a multiple of 16 per CTA share)
 };
 
 struct LTile {
@@ -814,6 +820,16 @@ expert_mlp_kernel(const __grid_constant__ CUtensorMap tmB1, const __grid_constan
     tma_prefetch_desc(&tmB1);
     tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 2 && p.w1_prefetch > 0) {
+    // While the index pass that writes group_list still runs, pull the first
+    // experts' gate_up weights into L2: the first wave of phase-0 tiles starts
+    // with the lowest experts.  CTA b takes the b-th share of the first
+    // w1_prefetch bytes, 16 KB a lane and copy.
+    const int64_t share = (p.w1_prefetch / gridDim.x) & ~int64_t(15);
+    const uint8_t* base = p.w1 + share * blockIdx.x;
+    for (int64_t off = static_cast<int64_t>(lane) * 16384; off < share; off += 32 * 16384)
+      prefetch_l2_bulk(base + off, static_cast<uint32_t>(share - off < 16384 ? share - off : 16384));
   }
   __syncthreads();
   pdl_wait();
@@ -1203,6 +1219,12 @@ moe_status_t launch_expert_mlp(const uint16_t* x, const int32_t* sorted_flat, co
   // rows per expert: 0.383 ms with the policy against 0.356 without; at a few
   // rows per expert 0.212 against 0.216)
   p.w_evict_first = (T * k < 64 * E) ? 1 : 0;
+  // the L2 prefetch before the wait: about what HBM delivers during the index
+  // pass (decode 8 us, prefill 14 us), at most all of w1
+  p.w1 = reinterpret_cast<const uint8_t*>(w1);
+  const int64_t w1_bytes = E * H * 2 * I * 2;
+  p.w1_prefetch = (static_cast<int64_t>(kW1PrefetchMB) << 20) < w1_bytes ? (static_cast<int64_t>(kW1PrefetchMB) << 20)
+                                                                           : w1_bytes;
   CUtensorMap tb1, ta2, tb2;
   if (!make_map_3d(&tb1, w1, E, H, 2 * I, 64) || !make_map_2d(&ta2, a, T * k, I, BM) ||
       !make_map_3d(&tb2, w2, E, I, H, 64))

@@ -87,6 +87,11 @@ static_assert(ACC_COLS + SF_SLOTS * SF_COLS <= TMEM_COLS, "TMEM budget");
 
 enum { MX_PLAIN = 0, MX_ACT = 1 };
 
+#ifndef MOE_MX_PREFETCH_MB
+#define MOE_MX_PREFETCH_MB 24
+#endif
+constexpr int kMxPrefetchMB = MOE_MX_PREFETCH_MB;   // weight bytes prefetched into L2 before the wait
+
 struct MxParams {
   const int64_t* group_list;
   const uint8_t* a_sf;   // [M, K/32]
@@ -109,6 +114,9 @@ struct MxParams {
   uint32_t tx_bytes;     // bytes a stage's A and B copies deliver: E2M1 operands count their packed size
   uint32_t w_evict_first;  // weight tiles loaded under an L2 evict-first policy
   uint32_t* status;
+  const uint8_t* b;      // the weight codes, for the L2 prefetch before the wait
+  int64_t b_prefetch;    // bytes of b to prefetch, and of b_sf
+  int64_t sf_prefetch;
 };
 
 struct __align__(16) MxSmem {
@@ -264,6 +272,17 @@ gmm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm->tmem_base), TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 2 && p.b_prefetch > 0) {
+    // While the launch before this one still runs, pull the first experts'
+    // weights and their scales into L2: the first wave of tiles starts with
+    // the lowest experts.  CTA b takes the b-th share, 16 KB a lane and copy.
+    const int64_t share = (p.b_prefetch / gridDim.x) & ~int64_t(15);
+    const uint8_t* base = p.b + share * blockIdx.x;
+    for (int64_t off = static_cast<int64_t>(lane) * 16384; off < share; off += 32 * 16384)
+      prefetch_l2_bulk(base + off, static_cast<uint32_t>(share - off < 16384 ? share - off : 16384));
+    const int64_t sshare = (p.sf_prefetch / gridDim.x) & ~int64_t(15);
+    if (lane == 0 && sshare > 0) prefetch_l2_bulk(p.b_sf + sshare * blockIdx.x, static_cast<uint32_t>(sshare));
   }
   tc_fence_before();
   __syncthreads();
@@ -564,6 +583,16 @@ moe_status_t launch_gmm_mx(const MxGmmArgs& x, uint32_t* status, cudaStream_t s)
   // tile is read once, while larger groups read it again from L2 for each of
   // their 128-row tiles
   p.w_evict_first = x.M < 64 * x.E ? 1u : 0u;
+  // the L2 prefetch before the wait (at most all of the weights), with the
+  // matching share of their scales (a scale byte per 32 elements)
+  {
+    const int64_t elems = x.E * x.N * x.K;
+    const int64_t b_bytes = x.b_fmt == MOE_FP4_E2M1 ? elems / 2 : elems;
+    const int64_t budget = static_cast<int64_t>(kMxPrefetchMB) << 20;
+    p.b = x.b;
+    p.b_prefetch = budget < b_bytes ? budget : b_bytes;
+    p.sf_prefetch = p.b_prefetch / (b_bytes / (elems / 32));
+  }
   p.group_list = x.group_list;
   p.a_sf = x.a_sf;
   p.b_sf = x.b_sf;

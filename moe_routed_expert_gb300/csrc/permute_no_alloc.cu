@@ -81,8 +81,8 @@ using namespace moe;
 extern "C" moe_status_t moe_permute_no_alloc(const moe_bf16* x, const int32_t* topk_ids, int64_t T, int64_t H,
                                              int64_t k, int64_t E, moe_bf16* x_perm, int64_t* group_list,
                                              int32_t* row_id_map, int32_t* sorted_flat, uint32_t* device_status,
-                                             moe_stream_t stream) {  MOE_TRACE_CALL();
-
+                                             moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_permute_args(x, topk_ids, T, H, k, E, x_perm, group_list, row_id_map, sorted_flat);
   if (st != MOE_OK) return st;
   if (reinterpret_cast<uintptr_t>(device_status) & 3u) return MOE_ERR_INVALID;  // an atomically updated word

@@ -174,6 +174,51 @@ def test_layer_small_every_output(wl):
     if wl.name == "small_b":    # unused slots and an expert nobody picks
         inp["topk_ids"][::5, -1] = -1
         inp["topk_ids"][inp["topk_ids"] == 3] = -1
+    check_layer_every_output(inp, wl)
+
+
+def _one_expert(ids):
+    ids[:] = 5
+
+
+def _one_routed_row(ids):
+    ids[:] = -1
+    ids[17, 2] = 6
+
+
+def _no_routed_row(ids):
+    ids[:] = -1
+
+
+EDGE = [
+    (LayerWorkload("edge_one_token", 35, T=1, H=256, E=4, k=1, I=128, clip=0.0, hot_bias=0.0, backward=True), None),
+    (LayerWorkload("edge_one_token_every_expert", 36, T=1, H=256, E=8, k=8, I=128, clip=7.0, hot_bias=0.0,
+                   backward=True), None),
+    (LayerWorkload("edge_one_expert_holds_all", 37, T=300, H=256, E=16, k=1, I=128, clip=0.0, hot_bias=0.0,
+                   backward=True), _one_expert),
+    (LayerWorkload("edge_one_routed_row", 38, T=50, H=256, E=8, k=4, I=128, clip=0.0, hot_bias=0.0,
+                   backward=True), _one_routed_row),
+    (LayerWorkload("edge_no_routed_row", 39, T=40, H=256, E=8, k=2, I=128, clip=0.0, hot_bias=0.0,
+                   backward=True), _no_routed_row),
+]
+
+
+@pytest.mark.parametrize("wl,edit", EDGE, ids=[w.name for w, _ in EDGE])
+def test_layer_edge_routings(wl, edit):
+    """Degenerate routings: a single token (one slot, or one slot per expert),
+    every row on one expert (the other 15 empty), a single routed row, and no
+    routed row at all (every slot unused: y, dx and dprobs zero, every weight
+    gradient zero)."""
+    inp = layer_inputs(wl)
+    if edit is not None:
+        edit(inp["topk_ids"])
+    check_layer_every_output(inp, wl)
+
+
+def check_layer_every_output(inp, wl):
+    """Every output of the layer forward and backward: integer outputs exact,
+    each step on the GPU's own input to it, the outputs end to end, and the
+    layer entry points equal to the chain of single calls."""
     g = gpu_layer(inp, wl, backward=True)
     gs = saved_to_host(g["saved"])
     o = oracle_layer(inp, wl, backward=True, gpu_saved=gs)

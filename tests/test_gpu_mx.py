@@ -269,6 +269,13 @@ def test_layer_mx_max_experts(fmt, wfmt):
     check_layer_mx(fmt, wfmt, T=160, H=256, E=1024, k=8, I=128)
 
 
+@pytest.mark.parametrize("fmt,wfmt", [("e4m3", "e4m3"), ("e4m3", "e2m1"), ("e2m1", "e2m1")])
+def test_layer_mx_one_token(fmt, wfmt):
+    """A single token routed to 8 of 8 experts: one row per expert, every tile
+    of both block-scaled matmuls holding one valid row."""
+    check_layer_mx(fmt, wfmt, T=1, H=256, E=8, k=8, I=128)
+
+
 def check_layer_mx(fmt, wfmt, **shape):
     """moe_layer_forward_mx against the chain of single calls (bit-identical),
     each step of the chain on its own input, and y end to end."""

@@ -57,6 +57,15 @@ GMM_TRAFFIC = [
      "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
     {"workload": "layer_decode_t64", "bytes_per_launch": 1.4158e9,
      "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "gmm_zipf_e8", "bytes_per_launch": 7.58e7,
+     "sources": {"gmm.cu": "4376a8c0af4fe31054a2e34448ac98ffc1291363faa2891dbfc3494167497b5f",
+                 "gmm_pair.cu": "7acdcaeb39a20463640220649c863932e342290ca1dae165d40bfcb594943a1f",
+                 "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd",
+                 "sched.cuh": "3e1e8e7b2a17ea21d2a8bff7550b0730d5170eabf1c4d36c95b442e3a7e89365"}},
+    {"workload": "layer_prefill_mx_t4096", "bytes_per_launch": 5.179e8,
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
+    {"workload": "layer_decode_mx_t64", "bytes_per_launch": 3.683e8,
+     "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
     {"workload": "layer_prefill_a8w4_t4096", "bytes_per_launch": 3.108e8,
      "sources": {"gmm_mx.cu": "72a42ef9d9137faeff13650d3ac3feb3baf11564ae897628e5f19e1c254733cc", "mx.cuh": "8184ef27c720621f7414f59e02aa9014a885853c33cc323bb1750e932d249ffd", "common.cuh": "0408a2178e2f80598505925f2d7a91553ba5aefc51b89e8a1bc927e9ee3fbfcd"}},
     {"workload": "layer_decode_a8w4_t64", "bytes_per_launch": 1.928e8,
